@@ -1,0 +1,147 @@
+"""CPU oracle for the Engram n-gram hash and the fp8 row lookup.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package. The product library never
+calls it, and it shares no code with the CUDA path.
+
+``engram_oracle.c`` is a plain restatement of the "DeepSeek V4.1" pages
+(blocks/stack-hashes page: the n-gram hash ``forward``; engram-first/lookup
+page: ``ParallelEngramEmbedding.forward``). This module compiles it with gcc and
+calls it through ctypes.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
+(brute force, closed forms, invariants, library reductions, the released table
+sizes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "engram_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+FLAG_BAD_START = 1
+FLAG_BAD_ID = 2
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
+    """Compile the oracle (portable C, no fast-math, no FMA contraction)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    cmd = ["gcc", "-std=c11", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared", "-o", out + ".tmp",
+           src, "-lm"]
+    subprocess.check_call(cmd)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    lib.oracle_fp8_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.oracle_fp8_e4m3_to_f32.restype = ctypes.c_float
+    lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
+    lib.oracle_bf16_rne.restype = ctypes.c_uint16
+    lib.oracle_floor_mod.argtypes = [_I, _I]
+    lib.oracle_floor_mod.restype = _I
+    lib.oracle_engram_hash.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _P, _P]
+    lib.oracle_engram_hash.restype = ctypes.c_int
+    lib.oracle_engram_lookup.argtypes = [_P, _I, _P, _P, _I, _I, _I, _P]
+    lib.oracle_engram_lookup.restype = ctypes.c_int
+    return lib
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = _bind(_LIB)
+    return _lib
+
+
+def load_variant(path: str):
+    """Bind another build of the same source (used to check that the pins catch planted mistakes)."""
+    return _bind(path)
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def fp8_e4m3_to_f32(code: int, L=None) -> float:
+    return (L or lib()).oracle_fp8_e4m3_to_f32(code)
+
+
+def bf16_rne(x: float, L=None) -> int:
+    return (L or lib()).oracle_bf16_rne(x)
+
+
+def floor_mod(x: int, p: int, L=None) -> int:
+    return (L or lib()).oracle_floor_mod(x, p)
+
+
+class OracleState:
+    """The hash module's parameters plus its compressed-token cache (int64, starts DEAD)."""
+
+    def __init__(self, n_layers, max_ngram, n_heads, token_map, multipliers, primes, offsets, dead, pad_id,
+                 max_batch, max_seq_len, L=None):
+        self.lib = L or lib()
+        self.n_layers, self.max_ngram, self.n_heads = int(n_layers), int(max_ngram), int(n_heads)
+        self.n_cols = (self.max_ngram - 1) * self.n_heads
+        self.token_map = np.ascontiguousarray(token_map, dtype=np.int64)
+        self.multipliers = np.ascontiguousarray(multipliers, dtype=np.int64).reshape(self.n_layers, self.max_ngram)
+        self.primes = np.ascontiguousarray(primes, dtype=np.int64).reshape(self.n_layers, self.max_ngram - 1,
+                                                                           self.n_heads)
+        self.offsets = np.ascontiguousarray(offsets, dtype=np.int64).reshape(self.n_layers, self.n_cols)
+        self.dead, self.pad_id = int(dead), int(pad_id)
+        self.max_batch, self.max_seq_len = int(max_batch), int(max_seq_len)
+        self.cache = np.full((self.max_batch, self.max_seq_len), self.dead, dtype=np.int64)
+
+    @classmethod
+    def from_layout(cls, lay, max_batch, max_seq_len, L=None):
+        return cls(lay.n_layers, lay.max_ngram, lay.n_heads, lay.token_map, lay.multipliers, lay.primes, lay.offsets,
+                   lay.dead, lay.pad_id, max_batch, max_seq_len, L)
+
+    def reset(self):
+        self.cache[:] = self.dead
+
+    def hash(self, ids, start_pos, mask=None):
+        """ids int64 [B, L]; start_pos int or [B]; mask bool [B, L] or None.
+        Returns (hashes int64 [B, L, n_layers, C], flags)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int64)
+        B, L = ids.shape
+        sp = np.ascontiguousarray(np.broadcast_to(np.asarray(start_pos, dtype=np.int64), (B,)))
+        m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+        out = np.empty((B, L, self.n_layers, self.n_cols), dtype=np.int64)
+        flags = ctypes.c_uint32(0)
+        rc = self.lib.oracle_engram_hash(
+            self.n_layers, self.max_ngram, self.n_heads, _ptr(self.token_map), self.token_map.size, self.dead,
+            self.pad_id, _ptr(self.multipliers), _ptr(self.primes), _ptr(self.offsets), _ptr(self.cache),
+            self.max_batch, self.max_seq_len, _ptr(ids), _ptr(m), _ptr(sp), B, L, _ptr(out), ctypes.byref(flags))
+        if rc != 0:
+            raise ValueError(f"oracle_engram_hash rejected its arguments ({rc})")
+        return out, flags.value
+
+
+def engram_lookup(idx, W, S, rows, D, block, L=None) -> np.ndarray:
+    """idx int64 [...]; W uint8 [rows, D]; S float32 [rows, D/block]. Returns bf16 bits uint16 [..., D]."""
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    S = np.ascontiguousarray(S, dtype=np.float32)
+    out = np.empty(idx.shape + (D,), dtype=np.uint16)
+    rc = (L or lib()).oracle_engram_lookup(_ptr(idx), idx.size, _ptr(W), _ptr(S), int(rows), int(D), int(block),
+                                           _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle_engram_lookup rejected its arguments ({rc})")
+    return out

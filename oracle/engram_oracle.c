@@ -1,0 +1,184 @@
+/*
+ * Engram n-gram hash + fp8 row lookup: plain CPU oracle.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
+ * baseline use this file. It shares no code, header or constant with the CUDA
+ * library and is deliberately slow: one loop per step of the pages, in their
+ * order, with no blocking, fusion or reordering.
+ *
+ * Sources (all on the "DeepSeek V4.1" pages):
+ *   - blocks/stack-hashes page, the n-gram hash `forward(input_ids, start_pos,
+ *     token_mask)`: token compression, masking, compressed-token cache,
+ *     lookback with cumulative blocking, multiply / rolling XOR, floored mod
+ *     by the bucket primes, column concatenation plus offsets.
+ *   - blocks/stack-hashes page, `Transformer.forward`: the engram mask is the
+ *     negated image mask.
+ *   - engram-first/lookup page, `ParallelEngramEmbedding.forward`: out-of-range
+ *     rows are read as row 0 and then zeroed; fp8 values are widened to fp32,
+ *     multiplied block-wise by the fp32 scale, and converted to bf16.
+ *
+ * Precision: the pages fix it (`.float()` on both operands, one multiply,
+ * `.to(torch.bfloat16)`), so the dequant is one fp32 round-to-nearest multiply
+ * followed by round-to-nearest-even to bf16. Build with -ffp-contract=off and
+ * without fast-math so no FMA or flush-to-zero can creep in.
+ *
+ * Readings where the pages are silent (documented with the build):
+ *   - the cache starts out (and is reset to) DEAD;
+ *   - start_pos is a per-row value; rows never interact;
+ *   - int64 products wrap mod 2^64 and `%` is floored (torch semantics);
+ *   - an id outside [0, raw_vocab) is treated as a masked (DEAD) token and
+ *     flagged; a row whose start position does not fit the cache writes
+ *     nothing, gets hash -1 everywhere, and is flagged.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL (-1)
+
+#define ORACLE_FLAG_BAD_START 1u
+#define ORACLE_FLAG_BAD_ID 2u
+
+/* ---------------------------------------------------------------- scalar definitions */
+
+/* OCP 8-bit E4M3 ("fn" variant): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa
+ * bits; exponent 0 is subnormal (m * 2^-9); S.1111.111 is NaN; no infinities. */
+float oracle_fp8_e4m3_to_f32(uint8_t code) {
+  const int sign = (code >> 7) & 1;
+  const int e = (code >> 3) & 0xF;
+  const int m = code & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)m, -9);
+  } else {
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  }
+  return (float)(sign ? -v : v);
+}
+
+/* bf16 = the upper half of an IEEE binary32, rounded to nearest, ties to even.
+ * NaNs stay NaN (quiet bit set). */
+uint16_t oracle_bf16_rne(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u) {
+    return (uint16_t)((u >> 16) | 0x0040u);
+  }
+  const uint32_t lower = u & 0xFFFFu;
+  uint32_t upper = u >> 16;
+  if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) {
+    upper += 1u; /* carries into the exponent (and to infinity) as rounding requires */
+  }
+  return (uint16_t)upper;
+}
+
+/* Floored modulo: the result has the sign of p (p > 0 here), like torch's `%`. */
+int64_t oracle_floor_mod(int64_t x, int64_t p) {
+  int64_t r = x % p; /* C: truncated toward zero, |r| < p */
+  if (r != 0 && ((r < 0) != (p < 0))) r += p;
+  return r;
+}
+
+/* ---------------------------------------------------------------- n-gram hash */
+
+/* hashes[B][L][n_layers][C], C = (max_ngram - 1) * n_heads.
+ * cache[cache_rows][cache_len] int64 holds compressed tokens across calls.
+ * multipliers[n_layers][max_ngram], primes[n_layers][max_ngram-1][n_heads],
+ * offsets[n_layers][C]. mask may be NULL (every token takes part). */
+int oracle_engram_hash(int64_t n_layers, int64_t max_ngram, int64_t n_heads,
+                       const int64_t* token_map, int64_t raw_vocab, int64_t dead, int64_t pad_id,
+                       const int64_t* multipliers, const int64_t* primes, const int64_t* offsets,
+                       int64_t* cache, int64_t cache_rows, int64_t cache_len,
+                       const int64_t* ids, const uint8_t* mask, const int64_t* start_pos,
+                       int64_t B, int64_t L, int64_t* hashes, uint32_t* flags) {
+  if (n_layers < 1 || max_ngram < 2 || max_ngram > 64 || n_heads < 1 || B < 0 || L < 0) return ORACLE_EINVAL;
+  if (B > cache_rows) return ORACLE_EINVAL;
+  const int64_t C = (max_ngram - 1) * n_heads;
+  uint32_t fl = 0;
+
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t s = start_pos[b];
+    const int row_ok = (s >= 0 && s <= cache_len - L);
+    if (!row_ok) {
+      fl |= ORACLE_FLAG_BAD_START;
+      for (int64_t t = 0; t < L; ++t)
+        for (int64_t j = 0; j < n_layers * C; ++j) hashes[(b * L + t) * n_layers * C + j] = -1;
+      continue;
+    }
+
+    /* compressed = token_map[input_ids]; masked tokens become DEAD */
+    /* cache[b, s : s + L] = compressed */
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t id = ids[b * L + t];
+      int64_t c;
+      if (id < 0 || id >= raw_vocab) {
+        fl |= ORACLE_FLAG_BAD_ID;
+        c = dead;
+      } else {
+        c = token_map[id];
+      }
+      if (mask != NULL && !mask[b * L + t]) c = dead;
+      cache[b * cache_len + s + t] = c;
+    }
+
+    /* one token at a time: lookback with cumulative blocking, then the hash */
+    for (int64_t t = 0; t < L; ++t) {
+      const int64_t pos = s + t;
+      int64_t tokens[64];
+      int blocked = 0;
+      for (int64_t shift = 0; shift < max_ngram; ++shift) {
+        const int64_t src_pos = pos - shift < 0 ? 0 : pos - shift; /* clamp_min(0) */
+        const int64_t source = cache[b * cache_len + src_pos];
+        blocked = blocked || (pos < shift) || (source == dead);
+        tokens[shift] = blocked ? pad_id : source;
+      }
+      for (int64_t l = 0; l < n_layers; ++l) {
+        /* products = tokens * multipliers (int64, wrapping) */
+        uint64_t products[64];
+        for (int64_t k = 0; k < max_ngram; ++k)
+          products[k] = (uint64_t)tokens[k] * (uint64_t)multipliers[l * max_ngram + k];
+        uint64_t rolling = products[0];
+        for (int64_t i = 1; i < max_ngram; ++i) {
+          rolling ^= products[i];
+          for (int64_t h = 0; h < n_heads; ++h) {
+            const int64_t p = primes[(l * (max_ngram - 1) + (i - 1)) * n_heads + h];
+            const int64_t col = (i - 1) * n_heads + h;
+            const int64_t x = (int64_t)rolling; /* two's complement reinterpretation */
+            hashes[((b * L + t) * n_layers + l) * C + col] = oracle_floor_mod(x, p) + offsets[l * C + col];
+          }
+        }
+      }
+    }
+  }
+  if (flags) *flags |= fl;
+  return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- fp8 row lookup */
+
+/* out[n_idx][D] bf16 bits. W[rows][D] E4M3 codes, S[rows][D / block] fp32.
+ * An index outside [0, rows) gives a row of +0. */
+int oracle_engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
+                         int64_t D, int64_t block, uint16_t* out) {
+  if (n_idx < 0 || D < 1 || block < 1 || D % block != 0) return ORACLE_EINVAL;
+  const int64_t n_scales = D / block;
+  for (int64_t i = 0; i < n_idx; ++i) {
+    const int64_t r = idx[i];
+    const int out_of_range = (r < 0 || r >= rows);
+    const int64_t local = out_of_range ? 0 : r; /* masked_fill(mask, 0) */
+    for (int64_t k = 0; k < D; ++k) {
+      uint16_t y = 0;
+      if (!out_of_range) {
+        const float value = oracle_fp8_e4m3_to_f32(W[local * D + k]);
+        const float scale = S[local * n_scales + k / block];
+        const float prod = value * scale; /* one fp32 multiply, round to nearest */
+        y = oracle_bf16_rne(prod);
+      }
+      out[i * D + k] = y; /* masked rows: +0 */
+    }
+  }
+  return ORACLE_OK;
+}

@@ -1,0 +1,289 @@
+"""Pins for the CPU oracle: each function checks the oracle (given as a bound
+library, so planted-mistake builds can be checked too) against something other
+than itself, and raises AssertionError on the first mismatch.
+
+What pins what:
+  - floored mod            <- Python's floored ``%`` on big integers
+  - fp8 E4M3 decode        <- hand values of the E4M3 definition + torch's float8_e4m3fn cast
+  - bf16 rounding          <- torch's float32 -> bfloat16 conversion (RNE)
+  - lookup                 <- the same library calls the engram-first/lookup page makes
+                              (F.embedding, .float(), block multiply, .to(bfloat16), masked_fill),
+                              run on torch CPU
+  - n-gram hash            <- big-integer brute force from explicit n-gram tuples (tests/brute.py),
+                              closed forms for one-hot multipliers, and invariants
+                              (bucket range, chunked == one-shot, locality, masked == all-pad)
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+from tests import brute
+
+# ----------------------------------------------------------------------------- scalars
+
+
+def pin_floor_mod(L=None):
+    rng = np.random.default_rng(7)
+    xs = [0, 1, -1, 2 ** 63 - 1, -(2 ** 63), 123456789, -123456789, -7]
+    xs += [int(v) for v in rng.integers(-(2 ** 63), 2 ** 63 - 1, size=400, dtype=np.int64)]
+    ps = [1, 2, 3, 5, 997, 2003, 1_000_003, 16_000_057, 2 ** 31 - 1]
+    for x in xs:
+        for p in ps:
+            got = oracle.floor_mod(x, p, L)
+            assert got == x % p, (x, p, got, x % p)
+
+
+def pin_fp8_decode(L=None):
+    import torch
+
+    # hand values from the E4M3 definition (bias 7, 3 mantissa bits, exponent 0 subnormal)
+    hand = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x7E: 448.0, 0xFE: -448.0, 0x01: 2.0 ** -9,
+            0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0xB8: -1.0, 0x30: 0.5, 0x77: 240.0}
+    for code, val in hand.items():
+        assert oracle.fp8_e4m3_to_f32(code, L) == val, (hex(code), val)
+    assert np.signbit(oracle.fp8_e4m3_to_f32(0x80, L)) and oracle.fp8_e4m3_to_f32(0x80, L) == 0.0
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for code in range(256):
+        got = np.float32(oracle.fp8_e4m3_to_f32(code, L))
+        if np.isnan(ref[code]):
+            assert np.isnan(got), hex(code)
+        else:
+            assert got.view(np.uint32) == ref[code].view(np.uint32), (hex(code), got, ref[code])
+
+
+def _bf16_torch(x: np.ndarray) -> np.ndarray:
+    import torch
+
+    return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_bf16(L=None):
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2 ** 32, size=4000, dtype=np.uint64).astype(np.uint32)
+    special = np.array([0x00000000, 0x80000000, 0x3F808000, 0x3F818000, 0x3F808001, 0x3F80FFFF, 0x7F7FFFFF,
+                        0x7F7F8000, 0x7F7F7FFF, 0x7F800000, 0xFF800000, 0x00000001, 0x00008000, 0x00018000,
+                        0x0000FFFF, 0x807F8000, 0x007FFFFF], dtype=np.uint32)
+    bits = np.concatenate([special, bits])
+    x = bits.view(np.float32)
+    ref = _bf16_torch(x)
+    for xi, r in zip(x, ref):
+        got = oracle.bf16_rne(float(xi), L)
+        if np.isnan(xi):
+            assert (got & 0x7F80) == 0x7F80 and (got & 0x7F) != 0
+        else:
+            assert got == r, (hex(np.float32(xi).view(np.uint32)), hex(got), hex(r))
+
+
+# ----------------------------------------------------------------------------- lookup
+
+
+def torch_lookup(idx: np.ndarray, W: np.ndarray, S: np.ndarray, D: int, block: int) -> np.ndarray:
+    """The engram-first/lookup page's `ParallelEngramEmbedding.forward` at world size 1,
+    executed with the same torch library calls on the CPU. Returns bf16 bits."""
+    import torch
+    import torch.nn.functional as F
+
+    rows = W.shape[0]
+    indices = torch.from_numpy(idx.astype(np.int64))
+    weight = torch.from_numpy(W.copy()).view(torch.float8_e4m3fn)
+    scale = torch.from_numpy(S.copy())
+    mask = (indices < 0) | (indices >= rows)
+    local = indices.masked_fill(mask, 0)
+    values = F.embedding(local, weight)
+    scales = F.embedding(local, scale)
+    values = values.float().unflatten(-1, (-1, block)) * scales.float().unsqueeze(-1)
+    values = values.flatten(-2).to(torch.bfloat16)
+    values = values.masked_fill(mask.unsqueeze(-1), 0)
+    return values.view(torch.int16).numpy().view(np.uint16)
+
+
+def _cmp_bf16(got: np.ndarray, ref: np.ndarray):
+    g, r = got.reshape(-1), ref.reshape(-1)
+    nan_g = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
+    nan_r = ((r & 0x7F80) == 0x7F80) & ((r & 0x7F) != 0)
+    assert np.array_equal(nan_g, nan_r), "NaN positions differ"
+    ok = nan_g | (g == r)
+    if not ok.all():
+        i = int(np.argmin(ok))
+        raise AssertionError(f"bf16 mismatch at {i}: {hex(g[i])} vs {hex(r[i])} ({int((~ok).sum())} total)")
+
+
+def pin_lookup_vs_torch(L=None):
+    rng = np.random.default_rng(3)
+    for D, block in ((32, 32), (128, 128), (256, 128), (64, 16)):
+        nsc = D // block
+        rows = 256 // D * 8 + 40
+        W = rng.integers(0, 256, size=(rows, D), dtype=np.uint8)
+        W[: 256 // D].reshape(-1)[:] = np.arange(256, dtype=np.uint8)  # every code, NaNs included
+        S = rng.uniform(0.01, 1.0, size=(rows, nsc)).astype(np.float32)
+        S[0, 0] = 1e-40          # subnormal scale
+        S[1 % rows, -1] = 3.0e38  # overflow to inf for big codes
+        S[2 % rows, 0] = 2.0 ** -130
+        S[3 % rows, 0] = -0.75    # negative scale
+        idx = np.concatenate([np.arange(rows), rng.integers(-5, rows + 5, size=300), [-1, rows, -(2 ** 62), 2 ** 62]])
+        got = oracle.engram_lookup(idx, W, S, rows, D, block, L)
+        ref = torch_lookup(idx, W, S, D, block)
+        _cmp_bf16(got, ref)
+    # hand check: code 0x38 (1.0) times 0.5 is 0.5 = bf16 0x3F00; 0x7E (448) times 1.0 = 0x43E0
+    W = np.array([[0x38] * 16, [0x7E] * 16], dtype=np.uint8)
+    S = np.array([[0.5], [1.0]], dtype=np.float32)
+    out = oracle.engram_lookup(np.array([0, 1, 2]), W, S, 2, 16, 16, L)
+    assert (out[0] == 0x3F00).all() and (out[1] == 0x43E0).all() and (out[2] == 0).all()
+
+
+# ----------------------------------------------------------------------------- hash
+
+
+def _history_rows(seqs_ids, seqs_mask, lay):
+    """Compressed history per row from the raw sequences (brute-force side)."""
+    hist = []
+    for ids, msk in zip(seqs_ids, seqs_mask):
+        hist.append({q: brute.compress(int(ids[q]), bool(msk[q]), lay.token_map, lay.dead) for q in range(len(ids))})
+    return hist
+
+
+def _tiny_layouts():
+    lays = []
+    for full64 in (False, True):
+        lays.append(synth.make_layout("tiny", 99 + full64, full64=full64))
+    # a wider tiny layout: 2 layers, N=5, 3 heads, full 64-bit multipliers
+    primes = synth.distinct_primes_in(5, 997, 2003, (2, 4, 3))
+    lay = synth.Layout(2, 5, 3, 32, 32, 300, 50, synth.uniform_int(5, synth.TAG_TOKEN_MAP, 300, 0, 50),
+                       synth.multipliers(5, 2, 5, full64=True), primes, synth.column_offsets(primes))
+    lays.append(lay)
+    return lays
+
+
+def pin_brute_force(L=None):
+    for li, lay in enumerate(_tiny_layouts()):
+        B, total = 3, 48
+        ids = synth.uniform_int(17 + li, synth.TAG_IDS, B * total, -2, lay.raw_vocab + 2).reshape(B, total)
+        ids[:, ::11] = 0  # some repeats
+        ids[0, 5], ids[1, 7], ids[2, 9] = -1, lay.raw_vocab, -2  # invalid ids: treated as masked, flagged
+        mask = synth.uniform_int(18 + li, synth.TAG_IDS, B * total, 0, 5).reshape(B, total) > 0
+        hist = _history_rows(ids, mask, lay)
+        # one-shot
+        st = oracle.OracleState.from_layout(lay, B, 64, L)
+        got, flags = st.hash(ids, 0, mask)
+        assert flags & oracle.FLAG_BAD_ID  # the ids include -2, -1, vocab, vocab+1
+        for b in range(B):
+            for t in range(total):
+                exp = brute.hashes_at(hist[b], t, lay)
+                assert got[b, t].tolist() == exp, (li, b, t, got[b, t].tolist(), exp)
+        # chunked with per-row start positions: rows advance by different chunk sizes
+        st.reset()
+        pos = [0] * B
+        sizes = [5, 1, 7, 13, 2, 20]
+        for L_c in sizes:
+            sp = np.array(pos, dtype=np.int64)
+            chunk_ids = np.stack([ids[b, pos[b]:pos[b] + L_c] for b in range(B)])
+            chunk_mask = np.stack([mask[b, pos[b]:pos[b] + L_c] for b in range(B)])
+            got, _ = st.hash(chunk_ids, sp, chunk_mask)
+            for b in range(B):
+                for t in range(L_c):
+                    exp = brute.hashes_at(hist[b], pos[b] + t, lay)
+                    assert got[b, t].tolist() == exp, ("chunked", li, b, pos[b] + t)
+            pos = [p + L_c for p in pos]
+        # rows at different start positions in one call (decode-like)
+        st.reset()
+        st.hash(ids[:, :40], 0, mask[:, :40])
+        sp = np.array([3, 17, 40], dtype=np.int64)
+        one = np.stack([ids[b, sp[b]:sp[b] + 1] for b in range(B)])
+        onem = np.stack([mask[b, sp[b]:sp[b] + 1] for b in range(B)])
+        got, _ = st.hash(one, sp, onem)
+        for b in range(B):
+            h = {q: v for q, v in hist[b].items() if q <= sp[b]}
+            assert got[b, 0].tolist() == brute.hashes_at(h, int(sp[b]), lay), ("decode", li, b)
+
+
+def pin_closed_forms(L=None):
+    """One-hot multipliers turn the hash into a plain function of one lookback slot.
+
+    N=2, one head, prime P above the compressed vocab, offset O:
+      M = [1, 0]  ->  hash[t] = O + (c_t, or pad if c_t is DEAD)
+      M = [0, 1]  ->  hash[t] = O + (c_{t-1}, or pad if t == 0 or c_t or c_{t-1} is DEAD)
+    and with N=3, M = [0, 0, 1], column 1 (trigram) gives c_{t-2} under the same blocking."""
+    rng = np.random.default_rng(5)
+    V, CV, P, O, pad, dead = 40, 30, 1009, 77, 2, -1
+    tmap = rng.integers(0, CV, size=V)
+    T = 200
+    ids = rng.integers(0, V, size=(1, T))
+    keep = rng.random((1, T)) > 0.2
+    c = np.where(keep[0], tmap[ids[0]], dead)
+    for mult, shift in (([1, 0], 0), ([0, 1], 1)):
+        st = oracle.OracleState(1, 2, 1, tmap, np.array([mult]), np.array([[[P]]]), np.array([[O]]), dead, pad, 1, T, L)
+        got, _ = st.hash(ids, 0, keep)
+        for t in range(T):
+            blocked = any(t - s < 0 or c[t - s] == dead for s in range(shift + 1))
+            exp = O + (pad if blocked else int(c[t - shift]))
+            assert got[0, t, 0, 0] == exp, (mult, t, got[0, t, 0, 0], exp)
+    # N=3 (columns: bigram h0, trigram h0): M=[0,0,1] -> bigram column hashes 0 -> O0, trigram -> c_{t-2}
+    primes = np.array([[[1013], [1019]]])
+    offs = np.array([[5, 5 + 1013]])
+    st = oracle.OracleState(1, 3, 1, tmap, np.array([[0, 0, 1]]), primes, offs, dead, pad, 1, T, L)
+    got, _ = st.hash(ids, 0, keep)
+    for t in range(T):
+        assert got[0, t, 0, 0] == 5
+        blocked = any(t - s < 0 or c[t - s] == dead for s in range(3))
+        assert got[0, t, 0, 1] == 5 + 1013 + (pad if blocked else int(c[t - 2])), t
+    # a negative multiplier: rolling value is negative, the floored mod lands in [0, P)
+    st = oracle.OracleState(1, 2, 1, tmap, np.array([[-3, 0]]), np.array([[[P]]]), np.array([[0]]), dead, pad, 1, T, L)
+    got, _ = st.hash(ids, 0, None)
+    for t in range(T):
+        assert got[0, t, 0, 0] == (-3 * int(tmap[ids[0, t]])) % P
+
+
+def pin_invariants(L=None):
+    lay = synth.make_layout("tiny", 31, full64=True)
+    B, T = 2, 256
+    ids = synth.zipf_ids(31, B * T, vocab=lay.raw_vocab, s=1.3).reshape(B, T)  # repeats n-grams
+    mask = np.stack([synth.image_span_mask(31, T, 0.15, lo=8, hi=24, stream=b) for b in range(B)])
+    st = oracle.OracleState.from_layout(lay, B, T, L)
+    one, _ = st.hash(ids, 0, mask)
+    c0 = lay.token_map[ids[:, 0]]
+    P = lay.primes.reshape(lay.n_layers, -1)
+    O = lay.offsets
+    # range: every hash is inside its column's bucket range
+    assert ((one >= O[None, None]) & (one < (O + P)[None, None])).all()
+    # masked positions hash like the all-pad n-gram
+    pad_hash = np.array(brute.hashes_at({}, 10, lay))  # empty history = every slot blocked
+    assert (one[~mask] == pad_hash[None]).all()
+    # position 0: every n-gram is (c_0, pad, pad, ...), so it depends on c_0 alone
+    for b in range(B):
+        if mask[b, 0]:
+            assert one[b, 0].tolist() == brute.hashes_at({0: int(c0[b])}, 0, lay)
+    # locality: equal (n-1)-token lookbacks give equal hashes for n-gram size n
+    H = lay.n_heads
+    c = np.where(mask, lay.token_map[np.clip(ids, 0, lay.raw_vocab - 1)], lay.dead)
+    seen = {}
+    hits = 0
+    for b in range(B):
+        for t in range(lay.max_ngram - 1, T):
+            window = tuple(c[b, t - lay.max_ngram + 1:t + 1])
+            if lay.dead in window:
+                continue
+            key = window
+            if key in seen:
+                hits += 1
+                assert (one[b, t] == one[seen[key]]).all()
+            else:
+                seen[key] = (b, t)
+    assert hits > 0, "Zipf input should repeat a 4-gram"
+    # chunked prefill == one-shot
+    st.reset()
+    parts = []
+    for s0, s1 in ((0, 1), (1, 3), (3, 100), (100, 101), (101, 256)):
+        h, _ = st.hash(ids[:, s0:s1], s0, mask[:, s0:s1])
+        parts.append(h)
+    assert np.array_equal(np.concatenate(parts, axis=1), one)
+    # a row that does not fit the cache is rejected: hash -1, no cache write, flagged
+    snap = st.cache.copy()
+    h, fl = st.hash(ids[:, :10], np.array([T - 5, 0]), mask[:, :10])
+    assert fl & oracle.FLAG_BAD_START and (h[0] == -1).all() and (h[1] >= 0).all()
+    assert np.array_equal(st.cache[0], snap[0])
+
+
+ALL_PINS = [pin_floor_mod, pin_fp8_decode, pin_bf16, pin_lookup_vs_torch, pin_brute_force, pin_closed_forms,
+            pin_invariants]

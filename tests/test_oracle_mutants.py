@@ -1,0 +1,85 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case copies the oracle's C source to a temporary directory, plants one
+mistake (a dropped term, a wrong sign or index, a transposed operand),
+compiles it, and checks that at least one pin fails on that build. Mistakes
+are planted only in these CPU copies.
+"""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "engram_oracle.c")
+
+MUTANTS = {
+    "lookback_forward": ("pos - shift < 0 ? 0 : pos - shift", "pos + shift"),
+    "no_position_block": ("blocked || (pos < shift) || (source == dead)", "blocked || (source == dead)"),
+    "no_dead_block": ("blocked || (pos < shift) || (source == dead)", "blocked || (pos < shift)"),
+    "non_cumulative_block": ("blocked = blocked || (pos < shift)", "blocked = (pos < shift)"),
+    "pad_swapped": ("tokens[shift] = blocked ? pad_id : source;", "tokens[shift] = blocked ? source : pad_id;"),
+    "mask_to_pad": ("if (mask != NULL && !mask[b * L + t]) c = dead;", "if (mask != NULL && !mask[b * L + t]) c = pad_id;"),
+    "mask_ignored": ("if (mask != NULL && !mask[b * L + t]) c = dead;", ""),
+    "xor_as_add": ("rolling ^= products[i];", "rolling += products[i];"),
+    "first_product_dropped": ("uint64_t rolling = products[0];", "uint64_t rolling = 0;"),
+    "multiplier_index": ("multipliers[l * max_ngram + k]", "multipliers[k]"),
+    "prime_head_dropped": ("primes[(l * (max_ngram - 1) + (i - 1)) * n_heads + h]",
+                           "primes[(l * (max_ngram - 1) + (i - 1)) * n_heads]"),
+    "column_transposed": ("const int64_t col = (i - 1) * n_heads + h;", "const int64_t col = h * (max_ngram - 1) + (i - 1);"),
+    "offset_dropped": ("oracle_floor_mod(x, p) + offsets[l * C + col]", "oracle_floor_mod(x, p)"),
+    "truncated_mod": ("if (r != 0 && ((r < 0) != (p < 0))) r += p;", ""),
+    "mod_sign_flipped": ("if (r != 0 && ((r < 0) != (p < 0))) r += p;", "if (r != 0 && ((r < 0) != (p < 0))) r -= p;"),
+    "unsigned_mod": ("const int64_t x = (int64_t)rolling;", "const int64_t x = (int64_t)(rolling >> 1);"),
+    "cache_write_shift": ("cache[b * cache_len + s + t] = c;", "cache[b * cache_len + t] = c;"),
+    "fp8_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "fp8_subnormal": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "fp8_mantissa": ("1.0 + (double)m / 8.0", "1.0 + (double)m / 16.0"),
+    "fp8_sign": ("return (float)(sign ? -v : v);", "return (float)v;"),
+    "bf16_truncate": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) {", "if (0) {"),
+    "bf16_ties_away": ("(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
+    "scale_block_index": ("S[local * n_scales + k / block]", "S[local * n_scales + k % n_scales]"),
+    "scale_row_index": ("S[local * n_scales + k / block]", "S[k / block]"),
+    "masked_rows_read": ("const int64_t local = out_of_range ? 0 : r;", "const int64_t local = out_of_range ? 0 : r;\n    const int dummy_ = out_of_range; (void)dummy_;"),
+}
+# the last one is a no-op control: it must *survive* (proves the harness can pass)
+CONTROL = "masked_rows_read"
+
+
+def _build_variant(name, old, new, tmp):
+    src = open(SRC).read()
+    assert old in src, f"mutation {name}: pattern not found"
+    path = os.path.join(tmp, f"{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new, 1))
+    return oracle.load_variant(oracle.build(force=True, src=path, out=os.path.join(tmp, f"lib{name}.so")))
+
+
+def _pins_fail(L):
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(L)
+        except (AssertionError, ValueError, IndexError, OverflowError):
+            return pin.__name__
+    return None
+
+
+@pytest.fixture(scope="module")
+def tmpdir_mut():
+    d = tempfile.mkdtemp(prefix="oracle_mut_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmpdir_mut):
+    old, new = MUTANTS[name]
+    L = _build_variant(name, old, new, tmpdir_mut)
+    caught = _pins_fail(L)
+    if name == CONTROL:
+        assert caught is None, f"control build failed pin {caught}"
+    else:
+        assert caught is not None, f"planted mistake {name} passed every pin"
