@@ -1,0 +1,265 @@
+"""Engram n-gram hash + fp8 row lookup on GB300 (sm_103a): thin Python binding.
+
+The work is done by ``libengram.so`` (CUDA kernels behind the C ABI declared in
+``include/engram.h``). This module only marshals torch tensors into pointers,
+sizes and the current CUDA stream; it has no compute path of its own and no
+fallback: if the library is missing, every call raises.
+
+Functions carry the C names: :func:`engram_state_create`,
+:func:`engram_state_destroy`, :func:`engram_cache_reset`,
+:func:`engram_state_status`, :func:`engram_hash`, :func:`engram_lookup`,
+:func:`engram_hash_lookup`. :class:`EngramHash` bundles a state with them.
+
+Method: the "DeepSeek V4.1" pages -- blocks/stack-hashes page (the n-gram hash
+``forward``) and engram-first/lookup page (``ParallelEngramEmbedding.forward``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from ._build import LIB as _LIB_PATH
+from ._build import build
+
+__all__ = [
+    "EngramError", "EngramHash", "build", "engram_state_create", "engram_state_destroy", "engram_cache_reset",
+    "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_strerror",
+    "STATUS_BAD_START", "STATUS_BAD_ID", "library_path",
+]
+
+OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
+STATUS_BAD_START = 1
+STATUS_BAD_ID = 2
+MAX_LAYERS = 8
+
+
+class EngramError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {engram_strerror(code)} ({code})")
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("max_ngram", ctypes.c_int32), ("n_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("max_seq_len", ctypes.c_int64), ("raw_vocab", ctypes.c_int64), ("dead", ctypes.c_int64),
+                ("pad_id", ctypes.c_int64)]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_lib_handle = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _lib():
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libengram.so is not built ({_LIB_PATH}); run gram_hash_embedding_gb300.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        L.engram_state_create.argtypes = [ctypes.POINTER(_Layout), _P, _P, _P, _P, _P, ctypes.POINTER(_P)]
+        L.engram_state_destroy.argtypes = [_P]
+        L.engram_cache_reset.argtypes = [_P, _P]
+        L.engram_state_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+        L.engram_hash.argtypes = [_P, _P, _P, _P, _I32, _I64, _P, _P]
+        L.engram_lookup.argtypes = [_P, _I64, _P, _P, _I64, _I32, _I32, _P, _P]
+        L.engram_hash_lookup.argtypes = [_P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _P, _P]
+        L.engram_state_layout.argtypes = [_P, ctypes.POINTER(_Layout)]
+        L.engram_strerror.argtypes = [ctypes.c_int]
+        L.engram_strerror.restype = ctypes.c_char_p
+        for name in ("engram_state_create", "engram_state_destroy", "engram_cache_reset", "engram_state_status",
+                     "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib_handle = L
+    return _lib_handle
+
+
+def engram_strerror(code: int) -> str:
+    return _lib().engram_strerror(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != OK:
+        raise EngramError(rc, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _host_i64(a, n: int, name: str):
+    t = torch.as_tensor(a, dtype=torch.int64).reshape(-1).contiguous()
+    if t.numel() != n:
+        raise ValueError(f"{name}: expected {n} values, got {t.numel()}")
+    return t
+
+
+# ----------------------------------------------------------------------------- C-named functions
+def engram_state_create(*, n_layers, max_ngram, n_heads, head_dim, block, max_batch, max_seq_len, token_map,
+                        multipliers, primes, offsets, dead=-1, pad_id=2, stream=None) -> int:
+    """Create a state; returns the opaque handle (an int). Host arrays: token_map [raw_vocab],
+    multipliers [n_layers, max_ngram], primes [n_layers, max_ngram-1, n_heads], offsets [n_layers, C]."""
+    tm = torch.as_tensor(token_map, dtype=torch.int64).reshape(-1).contiguous()
+    C = (max_ngram - 1) * n_heads
+    mu = _host_i64(multipliers, n_layers * max_ngram, "multipliers")
+    pr = _host_i64(primes, n_layers * C, "primes")
+    of = _host_i64(offsets, n_layers * C, "offsets")
+    lay = _Layout(n_layers, max_ngram, n_heads, head_dim, block, max_batch, max_seq_len, tm.numel(), dead, pad_id)
+    h = _P()
+    _check(_lib().engram_state_create(ctypes.byref(lay), tm.data_ptr(), mu.data_ptr(), pr.data_ptr(), of.data_ptr(),
+                                      _stream(stream), ctypes.byref(h)), "engram_state_create")
+    return h.value
+
+
+def engram_state_destroy(state: int) -> None:
+    _check(_lib().engram_state_destroy(state), "engram_state_destroy")
+
+
+def engram_cache_reset(state: int, stream=None) -> None:
+    _check(_lib().engram_cache_reset(state, _stream(stream)), "engram_cache_reset")
+
+
+def engram_state_status(state: int, clear: bool = True, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(_lib().engram_state_status(state, _stream(stream), ctypes.byref(v), int(bool(clear))),
+           "engram_state_status")
+    return v.value
+
+
+def engram_state_layout(state: int) -> dict:
+    lay = _Layout()
+    _check(_lib().engram_state_layout(state, ctypes.byref(lay)), "engram_state_layout")
+    return {f: getattr(lay, f) for f, _ in _Layout._fields_}
+
+
+def _start_tensor(start_pos, B: int, device) -> torch.Tensor:
+    if isinstance(start_pos, torch.Tensor):
+        return start_pos
+    return torch.full((B,), int(start_pos), dtype=torch.int32, device=device)
+
+
+def engram_hash(state: int, ids: torch.Tensor, start_pos, mask: torch.Tensor | None = None,
+                hashes: torch.Tensor | None = None, n_layers: int | None = None, n_cols: int | None = None,
+                stream=None) -> torch.Tensor:
+    """ids int64 [B, L] (CUDA); start_pos int or int32 [B]; mask bool/uint8 [B, L] or None.
+    Returns (or fills) int64 hash ids [B, L, n_layers, C]."""
+    B, L = ids.shape
+    if hashes is None:
+        lay = engram_state_layout(state)
+        hashes = torch.empty((B, L, lay["n_layers"], (lay["max_ngram"] - 1) * lay["n_heads"]), dtype=torch.int64,
+                             device=ids.device)
+    sp = _start_tensor(start_pos, B, ids.device)
+    m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+    _check(_lib().engram_hash(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"), B, L,
+                              _dev(hashes, torch.int64, "hashes"), _stream(stream)), "engram_hash")
+    return hashes
+
+
+def _as_u8(mask: torch.Tensor) -> torch.Tensor:
+    return mask.view(torch.uint8) if mask.dtype == torch.bool else mask
+
+
+def engram_lookup(idx: torch.Tensor, W: torch.Tensor, S: torch.Tensor, block: int, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """idx int64 [...]; W fp8 (float8_e4m3fn or uint8) [rows, D]; S float32 [rows, D/block].
+    Returns (or fills) bf16 [..., D]."""
+    rows, D = W.shape
+    if out is None:
+        out = torch.empty(tuple(idx.shape) + (D,), dtype=torch.bfloat16, device=idx.device)
+    Wu = W.view(torch.uint8)
+    _check(_lib().engram_lookup(_dev(idx, torch.int64, "idx"), idx.numel(), _dev(Wu, torch.uint8, "W"),
+                                _dev(S, torch.float32, "S"), rows, D, int(block), _dev(out, torch.bfloat16, "out"),
+                                _stream(stream)), "engram_lookup")
+    return out
+
+
+def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: list, mask: torch.Tensor | None = None,
+                       out: list | None = None, hashes: torch.Tensor | None = None, stream=None) -> list:
+    """Hash + per-layer lookup in one launch. W/S: per-layer tables. Returns (or fills) the
+    per-layer bf16 outputs [B, L, C, D]."""
+    B, L = ids.shape
+    n = len(W)
+    if n != len(S) or n > MAX_LAYERS:
+        raise ValueError("W and S need one entry per engram layer")
+    D = W[0].shape[1]
+    if out is None:
+        lay = engram_state_layout(state)
+        C = (lay["max_ngram"] - 1) * lay["n_heads"]
+        out = [torch.empty((B, L, C, D), dtype=torch.bfloat16, device=ids.device) for _ in range(n)]
+    sp = _start_tensor(start_pos, B, ids.device)
+    m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+    Wp = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
+    Sp = (_P * n)(*[_dev(s, torch.float32, "S") for s in S])
+    Rp = (_I64 * n)(*[w.shape[0] for w in W])
+    Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
+    hp = None if hashes is None else _dev(hashes, torch.int64, "hashes")
+    _check(_lib().engram_hash_lookup(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"), B,
+                                     L, Wp, Sp, Rp, Op, hp, _stream(stream)), "engram_hash_lookup")
+    return out
+
+
+# ----------------------------------------------------------------------------- convenience object
+class EngramHash:
+    """A state plus the calls that use it (the hash module of the model, with its cache)."""
+
+    def __init__(self, *, n_layers, max_ngram, n_heads, head_dim, block, max_batch, max_seq_len, token_map,
+                 multipliers, primes, offsets, dead=-1, pad_id=2):
+        self.n_layers, self.max_ngram, self.n_heads = n_layers, max_ngram, n_heads
+        self.n_cols = (max_ngram - 1) * n_heads
+        self.head_dim, self.block = head_dim, block
+        self.handle = engram_state_create(n_layers=n_layers, max_ngram=max_ngram, n_heads=n_heads, head_dim=head_dim,
+                                          block=block, max_batch=max_batch, max_seq_len=max_seq_len,
+                                          token_map=token_map, multipliers=multipliers, primes=primes,
+                                          offsets=offsets, dead=dead, pad_id=pad_id)
+
+    def close(self):
+        if self.handle:
+            engram_state_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self):
+        engram_cache_reset(self.handle)
+
+    def status(self, clear=True) -> int:
+        return engram_state_status(self.handle, clear)
+
+    def hash(self, ids, start_pos=0, mask=None, hashes=None):
+        if hashes is None:
+            B, L = ids.shape
+            hashes = torch.empty((B, L, self.n_layers, self.n_cols), dtype=torch.int64, device=ids.device)
+        return engram_hash(self.handle, ids, start_pos, mask, hashes)
+
+    def hash_lookup(self, ids, W, S, start_pos=0, mask=None, out=None, hashes=None):
+        if out is None:
+            B, L = ids.shape
+            out = [torch.empty((B, L, self.n_cols, self.head_dim), dtype=torch.bfloat16, device=ids.device)
+                   for _ in range(len(W))]
+        return engram_hash_lookup(self.handle, ids, start_pos, W, S, mask, out, hashes)
+
+    def lookup(self, idx, W, S, out=None):
+        return engram_lookup(idx, W, S, self.block, out)

@@ -1,0 +1,268 @@
+// C ABI of libengram: state management, host-side argument checks, launches.
+// Declarations and the contract of every entry point are in include/engram.h.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "engram_internal.cuh"
+
+struct engram_state {
+  engram_layout lay;
+  int device;
+  int32_t* d_token_map;
+  uint64_t* d_mult;
+  engram::ColParam* d_cols;
+  int32_t* d_cache;
+  unsigned int* d_status;
+};
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline bool head_dim_ok(int32_t D, int32_t block) {
+  const bool pow2 = D == 16 || D == 32 || D == 64 || D == 128 || D == 256 || D == 512;
+  return pow2 && block >= 8 && block % 8 == 0 && D % block == 0;
+}
+
+int cols_total(const engram_layout& l) { return l.n_layers * (l.max_ngram - 1) * l.n_heads; }
+
+int check_layout(const engram_layout* l) {
+  if (l == nullptr) return ENGRAM_ERR_INVALID;
+  if (l->n_layers < 1 || l->max_ngram < 2 || l->n_heads < 1 || l->max_batch < 1 || l->max_seq_len < 1 ||
+      l->raw_vocab < 1)
+    return ENGRAM_ERR_INVALID;
+  if (l->n_layers > ENGRAM_MAX_LAYERS || l->max_ngram > ENGRAM_MAX_NGRAM) return ENGRAM_ERR_UNSUPPORTED;
+  if ((int64_t)l->n_layers * (l->max_ngram - 1) * l->n_heads > ENGRAM_MAX_COLS_TOTAL) return ENGRAM_ERR_UNSUPPORTED;
+  if (l->max_batch > 65535 || l->max_seq_len > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
+  if (l->dead < INT32_MIN || l->dead > INT32_MAX) return ENGRAM_ERR_INVALID;
+  if (!head_dim_ok(l->head_dim, l->block)) return ENGRAM_ERR_UNSUPPORTED;
+  return ENGRAM_OK;
+}
+
+engram::StateView view(const engram_state* st) {
+  engram::StateView v;
+  v.token_map = st->d_token_map;
+  v.mult = st->d_mult;
+  v.cols = st->d_cols;
+  v.cache = st->d_cache;
+  v.status = st->d_status;
+  v.raw_vocab = st->lay.raw_vocab;
+  v.max_seq_len = st->lay.max_seq_len;
+  v.pad_id = st->lay.pad_id;
+  v.dead = (int32_t)st->lay.dead;
+  v.n_layers = st->lay.n_layers;
+  v.max_ngram = st->lay.max_ngram;
+  v.n_heads = st->lay.n_heads;
+  v.n_cols = (st->lay.max_ngram - 1) * st->lay.n_heads;
+  return v;
+}
+
+bool on_state_device(const engram_state* st) {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == st->device;
+}
+
+void free_state(engram_state* st) {
+  if (st == nullptr) return;
+  cudaFree(st->d_token_map);
+  cudaFree(st->d_mult);
+  cudaFree(st->d_cols);
+  cudaFree(st->d_cache);
+  cudaFree(st->d_status);
+  delete st;
+}
+
+// common checks of engram_hash / engram_hash_lookup
+int check_call(const engram_state* st, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos, int32_t B,
+               int64_t L) {
+  (void)mask;
+  if (st == nullptr || B < 0 || L < 0) return ENGRAM_ERR_INVALID;
+  if (B == 0 || L == 0) return ENGRAM_OK;
+  if (ids == nullptr || start_pos == nullptr || !aligned(ids, 8) || !aligned(start_pos, 4)) return ENGRAM_ERR_INVALID;
+  if (B > st->lay.max_batch || L > st->lay.max_seq_len) return ENGRAM_ERR_RANGE;
+  if ((int64_t)B * L > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
+  if (!on_state_device(st)) return ENGRAM_ERR_INVALID;
+  return ENGRAM_OK;
+}
+
+engram::CallArgs call_args(const engram_state* st, const int64_t* ids, const uint8_t* mask,
+                           const int32_t* start_pos, int32_t B, int64_t L, int64_t* hashes) {
+  engram::CallArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.ids = ids;
+  a.mask = mask;
+  a.start_pos = start_pos;
+  a.hashes = hashes;
+  a.L = L;
+  a.B = B;
+  a.head_dim = st->lay.head_dim;
+  a.block = st->lay.block;
+  return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int engram_state_create(const engram_layout* layout, const int64_t* token_map, const int64_t* multipliers,
+                        const int64_t* primes, const int64_t* offsets, engram_stream_t stream, engram_state** out) {
+  if (out == nullptr) return ENGRAM_ERR_INVALID;
+  *out = nullptr;
+  int rc = check_layout(layout);
+  if (rc != ENGRAM_OK) return rc;
+  if (token_map == nullptr || multipliers == nullptr || primes == nullptr || offsets == nullptr)
+    return ENGRAM_ERR_INVALID;
+  const engram_layout& l = *layout;
+  const int C = (l.max_ngram - 1) * l.n_heads;
+  const int NC = cols_total(l);
+
+  std::vector<int32_t> tm(l.raw_vocab);
+  for (int64_t i = 0; i < l.raw_vocab; ++i) {
+    if (token_map[i] < INT32_MIN || token_map[i] > INT32_MAX) return ENGRAM_ERR_INVALID;
+    tm[i] = (int32_t)token_map[i];
+  }
+  std::vector<uint64_t> mult(l.n_layers * l.max_ngram);
+  for (size_t i = 0; i < mult.size(); ++i) mult[i] = (uint64_t)multipliers[i];
+  // column j = (n-2)*n_heads + h of layer ll uses primes[ll][n-2][h]: the same flat order
+  std::vector<engram::ColParam> cols(NC);
+  for (int ll = 0; ll < l.n_layers; ++ll) {
+    for (int j = 0; j < C; ++j) {
+      const int64_t p = primes[ll * C + j];
+      const int64_t o = offsets[ll * C + j];
+      if (p < 1 || p >= ((int64_t)1 << 62)) return ENGRAM_ERR_INVALID;
+      if (o > INT64_MAX - (p - 1) || o < INT64_MIN + 1) return ENGRAM_ERR_INVALID;
+      engram::ColParam& cp = cols[ll * C + j];
+      cp.prime = (uint64_t)p;
+      cp.magic = UINT64_MAX / (uint64_t)p;
+      cp.wrap = (UINT64_MAX % (uint64_t)p + 1u) % (uint64_t)p;
+      cp.offset = o;
+    }
+  }
+
+  engram_state* st = new engram_state;
+  std::memset(st, 0, sizeof *st);
+  st->lay = l;
+  if (cudaGetDevice(&st->device) != cudaSuccess) {
+    delete st;
+    return ENGRAM_ERR_CUDA;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t cache_n = (int64_t)l.max_batch * l.max_seq_len;
+  if (cudaMalloc(&st->d_token_map, tm.size() * sizeof(int32_t)) != cudaSuccess ||
+      cudaMalloc(&st->d_mult, mult.size() * sizeof(uint64_t)) != cudaSuccess ||
+      cudaMalloc(&st->d_cols, cols.size() * sizeof(engram::ColParam)) != cudaSuccess ||
+      cudaMalloc(&st->d_cache, cache_n * sizeof(int32_t)) != cudaSuccess ||
+      cudaMalloc(&st->d_status, sizeof(unsigned int)) != cudaSuccess) {
+    cudaGetLastError();
+    free_state(st);
+    return ENGRAM_ERR_NOMEM;
+  }
+  cudaError_t e = cudaMemcpyAsync(st->d_token_map, tm.data(), tm.size() * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(st->d_mult, mult.data(), mult.size() * sizeof(uint64_t), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(st->d_cols, cols.data(), cols.size() * sizeof(engram::ColParam), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->d_status, 0, sizeof(unsigned int), s);
+  if (e == cudaSuccess) e = engram::launch_fill_i32(st->d_cache, cache_n, (int32_t)l.dead, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // host staging vectors go out of scope
+  if (e != cudaSuccess) {
+    free_state(st);
+    return ENGRAM_ERR_CUDA;
+  }
+  *out = st;
+  return ENGRAM_OK;
+}
+
+int engram_state_destroy(engram_state* state) {
+  if (state == nullptr) return ENGRAM_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != state->device) cudaSetDevice(state->device);
+  cudaDeviceSynchronize();
+  free_state(state);
+  if (prev >= 0 && prev != state->device) cudaSetDevice(prev);
+  return ENGRAM_OK;
+}
+
+int engram_cache_reset(engram_state* state, engram_stream_t stream) {
+  if (state == nullptr || !on_state_device(state)) return ENGRAM_ERR_INVALID;
+  cudaError_t e = engram::launch_fill_i32(state->d_cache, (int64_t)state->lay.max_batch * state->lay.max_seq_len,
+                                          (int32_t)state->lay.dead, (cudaStream_t)stream);
+  return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* flags, int clear) {
+  if (state == nullptr || flags == nullptr || !on_state_device(state)) return ENGRAM_ERR_INVALID;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, state->d_status, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) e = cudaMemsetAsync(state->d_status, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+  *flags = v;
+  return ENGRAM_OK;
+}
+
+int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos, int32_t B,
+                int64_t L, int64_t* hashes, engram_stream_t stream) {
+  int rc = check_call(state, ids, mask, start_pos, B, L);
+  if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
+  if (hashes == nullptr || !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
+  engram::CallArgs a = call_args(state, ids, mask, start_pos, B, L, hashes);
+  return engram::launch_hash(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
+                  int32_t head_dim, int32_t block, uint16_t* out, engram_stream_t stream) {
+  if (n_idx < 0 || rows < 0) return ENGRAM_ERR_INVALID;
+  if (!head_dim_ok(head_dim, block)) return ENGRAM_ERR_UNSUPPORTED;
+  if (n_idx == 0) return ENGRAM_OK;
+  if (idx == nullptr || out == nullptr || !aligned(idx, 8) || !aligned(out, 16)) return ENGRAM_ERR_INVALID;
+  if (rows > 0 && (W == nullptr || S == nullptr || !aligned(W, 16) || !aligned(S, 4))) return ENGRAM_ERR_INVALID;
+  if (n_idx > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
+  cudaError_t e = engram::launch_lookup(idx, n_idx, W, S, rows, head_dim, block, out, (cudaStream_t)stream);
+  return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
+                       int32_t B, int64_t L, const uint8_t* const* W, const float* const* S, const int64_t* rows,
+                       uint16_t* const* out, int64_t* hashes, engram_stream_t stream) {
+  int rc = check_call(state, ids, mask, start_pos, B, L);
+  if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
+  if (W == nullptr || S == nullptr || rows == nullptr || out == nullptr) return ENGRAM_ERR_INVALID;
+  if (hashes != nullptr && !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
+  engram::CallArgs a = call_args(state, ids, mask, start_pos, B, L, hashes);
+  for (int l = 0; l < state->lay.n_layers; ++l) {
+    if (rows[l] < 0 || out[l] == nullptr || !aligned(out[l], 16)) return ENGRAM_ERR_INVALID;
+    if (rows[l] > 0 && (W[l] == nullptr || S[l] == nullptr || !aligned(W[l], 16) || !aligned(S[l], 4)))
+      return ENGRAM_ERR_INVALID;
+    a.W[l] = W[l];
+    a.S[l] = S[l];
+    a.rows[l] = rows[l];
+    a.out[l] = out[l];
+  }
+  return engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK
+                                                                                          : ENGRAM_ERR_CUDA;
+}
+
+int engram_state_layout(const engram_state* state, engram_layout* layout) {
+  if (state == nullptr || layout == nullptr) return ENGRAM_ERR_INVALID;
+  *layout = state->lay;
+  return ENGRAM_OK;
+}
+
+const char* engram_strerror(int code) {
+  switch (code) {
+    case ENGRAM_OK: return "ok";
+    case ENGRAM_ERR_INVALID: return "invalid argument (null or misaligned pointer, negative size, bad layout value)";
+    case ENGRAM_ERR_RANGE: return "out of range (B > max_batch or L > max_seq_len)";
+    case ENGRAM_ERR_CUDA: return "CUDA runtime or launch error";
+    case ENGRAM_ERR_NOMEM: return "device allocation failed";
+    case ENGRAM_ERR_UNSUPPORTED: return "size beyond the library limits (head_dim, block, layers, n-gram size)";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

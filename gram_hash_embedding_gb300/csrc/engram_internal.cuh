@@ -1,0 +1,55 @@
+// Internal declarations shared by the kernels and the C-ABI layer of libengram.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/engram.h"
+
+namespace engram {
+
+// One hash column (layer l, n-gram size n, head h) as the kernels use it.
+struct ColParam {
+  uint64_t prime;   // P, 1 <= P < 2^62
+  uint64_t magic;   // floor((2^64 - 1) / P): quotient estimate that is exact or one short
+  uint64_t wrap;    // 2^64 mod P: corrects the unsigned residue of a negative int64
+  int64_t offset;   // the column's first row in the layer's table
+};
+
+// Device-resident view of a state, passed by value to the kernels.
+struct StateView {
+  const int32_t* token_map;  // [raw_vocab]
+  const uint64_t* mult;      // [n_layers][max_ngram]
+  const ColParam* cols;      // [n_layers][C]
+  int32_t* cache;            // [max_batch][max_seq_len]
+  unsigned int* status;      // ENGRAM_STATUS_* bits
+  int64_t raw_vocab;
+  int64_t max_seq_len;
+  int64_t pad_id;
+  int32_t dead;
+  int32_t n_layers, max_ngram, n_heads, n_cols;
+};
+
+// Per-call arguments of the hash / fused kernels.
+struct CallArgs {
+  const int64_t* ids;
+  const uint8_t* mask;        // may be null
+  const int32_t* start_pos;
+  int64_t* hashes;            // may be null (fused)
+  int64_t L;
+  int32_t B;
+  int32_t head_dim, block;
+  const uint8_t* W[ENGRAM_MAX_LAYERS];
+  const float* S[ENGRAM_MAX_LAYERS];
+  int64_t rows[ENGRAM_MAX_LAYERS];
+  uint16_t* out[ENGRAM_MAX_LAYERS];
+};
+
+// Launchers (kernels.cu). Return cudaGetLastError() of the launch.
+cudaError_t launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s);
+cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s);
+cudaError_t launch_hash_lookup(const StateView& sv, const CallArgs& a, cudaStream_t s);
+cudaError_t launch_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
+                          int32_t head_dim, int32_t block, uint16_t* out, cudaStream_t s);
+
+}  // namespace engram

@@ -1,0 +1,151 @@
+/*
+ * engram.h -- C ABI of the Engram n-gram hash + fp8 row lookup library (sm_103a).
+ *
+ * The operation is the Engram front end of the DeepSeek V4.1 block stack, as
+ * printed on the "DeepSeek V4.1" pages:
+ *   - blocks/stack-hashes page, the n-gram hash `forward(input_ids, start_pos,
+ *     token_mask)`: compress raw ids through `token_map`, replace masked tokens
+ *     by DEAD, store them in a per-batch cache at [start_pos, start_pos+L), look
+ *     back max_ngram-1 positions with cumulative blocking (positions before 0
+ *     and DEAD tokens turn that slot and every later slot into pad_id),
+ *     multiply the slots by per-layer int64 multipliers, XOR them one lookback
+ *     at a time, reduce each running value with a floored mod by per-(n-gram
+ *     size, head) primes, and add per-column offsets. Result: int64 hash ids
+ *     [B, L, n_layers, C] with C = (max_ngram-1) * n_heads.
+ *   - engram-first/lookup page, `ParallelEngramEmbedding.forward` (world size
+ *     1): gather fp8 E4M3 rows of a [rows, head_dim] table and their fp32
+ *     per-block scales, multiply in fp32, round to bf16 (nearest-even); an index
+ *     outside [0, rows) yields a row of +0.
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" must be CUDA device (or managed) memory of the
+ *     current device; "host" pointers are ordinary host memory.
+ *   - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream), allocates nothing, and never synchronises.
+ *   - Arguments are checked on the host before anything is launched; on a
+ *     non-zero return nothing was enqueued.
+ *   - The library never reads beyond the sizes it is given and never faults on
+ *     data values: out-of-range ids, start positions and table indices are
+ *     handled as documented below and recorded in the state's status word.
+ *   - Caller-owned buffers stay caller-owned; the library only reads inputs and
+ *     tables and writes the outputs it is given.
+ */
+#ifndef ENGRAM_H
+#define ENGRAM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* engram_stream_t;
+
+/* Opaque state: device copies of the layout, token_map and the compressed-token cache. */
+typedef struct engram_state engram_state;
+
+/* Return codes. */
+#define ENGRAM_OK 0
+#define ENGRAM_ERR_INVALID (-1)     /* null or misaligned pointer, negative size, inconsistent layout value */
+#define ENGRAM_ERR_RANGE (-2)       /* B > max_batch, L > max_seq_len, layer out of range */
+#define ENGRAM_ERR_CUDA (-3)        /* a CUDA runtime call or kernel launch failed */
+#define ENGRAM_ERR_NOMEM (-4)       /* device allocation failed (engram_state_create only) */
+#define ENGRAM_ERR_UNSUPPORTED (-5) /* a size beyond the library limits below */
+
+/* Status flags accumulated on the device (read with engram_state_status). */
+#define ENGRAM_STATUS_BAD_START 1u /* a row's start_pos was < 0 or start_pos + L > max_seq_len: that row wrote
+                                      nothing to the cache, its hash ids are -1 and its looked-up rows are +0 */
+#define ENGRAM_STATUS_BAD_ID 2u    /* an input id outside [0, raw_vocab): that token was treated as masked (DEAD) */
+
+/* Library limits. */
+#define ENGRAM_MAX_LAYERS 8       /* n_layers */
+#define ENGRAM_MAX_NGRAM 8        /* max_ngram (>= 2) */
+#define ENGRAM_MAX_COLS_TOTAL 512 /* n_layers * (max_ngram - 1) * n_heads */
+/* head_dim must be one of 16, 32, 64, 128, 256, 512; block must divide head_dim and be a multiple of 8. */
+
+typedef struct engram_layout {
+  int32_t n_layers;    /* engram layers hashed per call (the config's engram_layer_ids count) */
+  int32_t max_ngram;   /* engram_max_ngram_size: n-gram sizes 2..max_ngram are hashed */
+  int32_t n_heads;     /* engram_n_heads: one prime per (n-gram size, head) */
+  int32_t head_dim;    /* fp8 values per table row (engram_head_dim) */
+  int32_t block;       /* fp8 values per fp32 scale (fp8 block size) */
+  int32_t max_batch;   /* cache rows: calls take B <= max_batch */
+  int64_t max_seq_len; /* cache positions per row */
+  int64_t raw_vocab;   /* entries of token_map (the tokenizer vocabulary) */
+  int64_t dead;        /* DEAD sentinel stored for masked tokens; must fit int32 */
+  int64_t pad_id;      /* token that fills blocked n-gram slots (engram_pad_id) */
+} engram_layout;
+
+/*
+ * Create a state. All table-independent parameters of the hash module are
+ * copied to the device; the cache [max_batch, max_seq_len] is allocated and
+ * filled with DEAD (so history that was never written reads as blocked).
+ *   token_map   host int64 [raw_vocab]; every value and `dead` must fit in int32
+ *   multipliers host int64 [n_layers][max_ngram]
+ *   primes      host int64 [n_layers][max_ngram-1][n_heads]; each in [1, 2^62)
+ *   offsets     host int64 [n_layers][C], column = (n-2)*n_heads + head for n-gram size n;
+ *               offset + prime - 1 must not overflow int64
+ * On success *out receives the state; the call synchronises `stream` once.
+ * Errors: ENGRAM_ERR_INVALID / _UNSUPPORTED for bad layout values, _NOMEM, _CUDA.
+ */
+int engram_state_create(const engram_layout* layout, const int64_t* token_map, const int64_t* multipliers,
+                        const int64_t* primes, const int64_t* offsets, engram_stream_t stream, engram_state** out);
+
+/* Free the state's device memory (synchronises the device first). NULL is accepted. */
+int engram_state_destroy(engram_state* state);
+
+/* Refill the whole cache with DEAD (asynchronous on stream). */
+int engram_cache_reset(engram_state* state, engram_stream_t stream);
+
+/* Read the accumulated ENGRAM_STATUS_* flags into *flags (synchronises stream);
+ * clears them when `clear` is non-zero. */
+int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* flags, int clear);
+
+/*
+ * The n-gram hash (blocks/stack-hashes page, hash `forward`).
+ *   ids        device int64 [B][L] raw token ids
+ *   mask       device uint8 [B][L] (non-zero = token takes part) or NULL (all take part)
+ *   start_pos  device int32 [B]: position of ids[b][0] in cache row b (a scalar start is a filled array)
+ *   hashes     device int64 [B][L][n_layers][C], written
+ * Writes cache[b][start_pos[b] + t] for every valid row. Rows never interact.
+ * B == 0 or L == 0 is a no-op. Errors: _INVALID (null, misaligned), _RANGE (B > max_batch, L > max_seq_len).
+ */
+int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos, int32_t B,
+                int64_t L, int64_t* hashes, engram_stream_t stream);
+
+/*
+ * The fp8 row lookup of one table (engram-first/lookup page, `ParallelEngramEmbedding.forward`, world size 1).
+ *   idx   device int64 [n_idx] row indices; an index outside [0, rows) gives a row of +0
+ *   W     device fp8 E4M3 codes [rows][head_dim], 16-byte aligned
+ *   S     device fp32 [rows][head_dim / block], 4-byte aligned
+ *   out   device bf16 bits [n_idx][head_dim], 16-byte aligned, written
+ * out[i][k] = bf16_rne(fp32(W[idx[i]][k]) * S[idx[i]][k / block]) (one fp32 round-to-nearest multiply).
+ * n_idx == 0 is a no-op. Errors: _INVALID, _UNSUPPORTED (head_dim / block).
+ */
+int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
+                  int32_t head_dim, int32_t block, uint16_t* out, engram_stream_t stream);
+
+/*
+ * Hash and lookup in one launch: the hash of engram_hash (same cache update), then for every layer l the
+ * lookup of its C columns in table l, as the model does for each engram layer.
+ *   W, S, rows, out  host arrays of n_layers entries: per layer the device table, scales, row count
+ *                    (as engram_lookup) and a device bf16 output [B][L][C][head_dim]
+ *   hashes           device int64 [B][L][n_layers][C] to also receive the hash ids, or NULL
+ * Errors: as engram_hash and engram_lookup.
+ */
+int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
+                       int32_t B, int64_t L, const uint8_t* const* W, const float* const* S, const int64_t* rows,
+                       uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
+
+/* Layout the state was created with (host copy). */
+int engram_state_layout(const engram_state* state, engram_layout* layout);
+
+/* Static text for a return code. */
+const char* engram_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_H */

@@ -439,7 +439,8 @@ def make_workload(cfg: int, seed: int = MASTER_SEED, full64: bool = False) -> Wo
         pre = zipf_ids(s, B * P).reshape(B, P)
         start = uniform_int(s, TAG_START, B, 1, P + 1).astype(np.int32)
         ids = zipf_ids(s, B, offset=B * P).reshape(B, 1)
-        return Workload("decode B256xL1", lay, B, 1, ids, None, start, s, B, P + 1, prefill_ids=pre)
+        # same tables as the prefill configuration (24M rows per layer)
+        return Workload("decode B256xL1", lay, B, 1, ids, None, start, seed + 1, B, P + 1, prefill_ids=pre)
     if cfg == 3:
         lay = make_layout("full", s, full64)
         B, L = 8, 8192
@@ -453,6 +454,7 @@ def make_workload(cfg: int, seed: int = MASTER_SEED, full64: bool = False) -> Wo
         mask = np.ones(total, dtype=bool)
         mask[:Lc] = image_span_mask(s, Lc, 0.15)
         ids = np.where(mask, ids, IMAGE_TOKEN_ID)
+        # same full-scale tables as configuration 3
         return Workload("long chunked B1x65536 (8x8192)", lay, 1, Lc, ids.reshape(1, total), mask.reshape(1, total),
-                        np.zeros(1, np.int32), s, 1, total, chunks=chunks)
+                        np.zeros(1, np.int32), seed + 3, 1, total, chunks=chunks)
     raise ValueError(cfg)

@@ -1,0 +1,87 @@
+"""The C ABI without a GPU: the header compiles as plain C, the library loads and
+exports every function the header declares, argument checks that need no device
+answer with the documented codes, and the product path fails loudly when the
+library is missing."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gram_hash_embedding_gb300 as geng
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "engram.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(engram_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    geng.build()
+    return ctypes.CDLL(geng.library_path())
+
+
+def test_header_is_plain_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "engram.h"\nint main(void){engram_layout l; (void)l; return 0;}\n')
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.dirname(HEADER),
+                           str(src)])
+
+
+def test_every_declared_function_is_exported(lib):
+    names = declared_functions()
+    assert {"engram_state_create", "engram_state_destroy", "engram_hash", "engram_lookup",
+            "engram_hash_lookup", "engram_cache_reset", "engram_state_status", "engram_strerror"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in engram.h but not exported"
+
+
+def test_host_side_checks_need_no_gpu(lib):
+    lib.engram_strerror.restype = ctypes.c_char_p
+    assert lib.engram_strerror(0) == b"ok"
+    assert b"invalid" in lib.engram_strerror(-1)
+    # null out pointer / null layout
+    assert lib.engram_state_create(None, None, None, None, None, None, None) == geng.ERR_INVALID
+    out = ctypes.c_void_p()
+    assert lib.engram_state_create(None, None, None, None, None, None, ctypes.byref(out)) == geng.ERR_INVALID
+    lay = geng._Layout(1, 4, 2, 48, 16, 1, 8, 10, -1, 2)  # head_dim 48 unsupported
+    tm = (ctypes.c_int64 * 10)()
+    arr = (ctypes.c_int64 * 16)()
+    assert lib.engram_state_create(ctypes.byref(lay), tm, arr, arr, arr, None, ctypes.byref(out)) == geng.ERR_UNSUPPORTED
+    lay = geng._Layout(1, 1, 2, 32, 32, 1, 8, 10, -1, 2)  # max_ngram 1
+    assert lib.engram_state_create(ctypes.byref(lay), tm, arr, arr, arr, None, ctypes.byref(out)) == geng.ERR_INVALID
+    lay = geng._Layout(9, 4, 2, 32, 32, 1, 8, 10, -1, 2)  # too many layers
+    assert lib.engram_state_create(ctypes.byref(lay), tm, arr, arr, arr, None, ctypes.byref(out)) == geng.ERR_UNSUPPORTED
+    lay = geng._Layout(1, 4, 2, 32, 32, 1, 8, 10, 1 << 40, 2)  # DEAD beyond int32
+    assert lib.engram_state_create(ctypes.byref(lay), tm, arr, arr, arr, None, ctypes.byref(out)) == geng.ERR_INVALID
+    # lookup: unsupported head_dim / block, and an empty call, need no device
+    L = lib
+    L.engram_lookup.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.engram_lookup(None, 5, None, None, 4, 48, 16, None, None) == geng.ERR_UNSUPPORTED
+    assert L.engram_lookup(None, 5, None, None, 4, 128, 12, None, None) == geng.ERR_UNSUPPORTED
+    assert L.engram_lookup(None, 0, None, None, 4, 128, 128, None, None) == geng.OK
+    assert L.engram_lookup(None, -1, None, None, 4, 128, 128, None, None) == geng.ERR_INVALID
+    assert lib.engram_state_destroy(None) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(geng, "_LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(geng, "_lib_handle", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        geng.engram_strerror(0)
+
+
+def test_oracle_is_not_referenced_by_the_product():
+    pkg = os.path.join(ROOT, "gram_hash_embedding_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read().lower()
+                assert "oracle" not in text, f"{f} mentions the oracle"

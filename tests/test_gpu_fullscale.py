@@ -1,0 +1,93 @@
+"""Full-scale tables (384,006,168 and 384,016,682 rows x 128 fp8, ~98 GB on the device):
+the launch configuration the benchmark times, checked against the oracle on every hash id
+and on sampled output rows (GPU only)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def full_tables():
+    H.build_all()
+    wl = synth.make_workload(3)
+    assert wl.layout.rows == [384_006_168, 384_016_682]
+    Ws, Ss = H.device_tables(wl)
+    yield Ws, Ss
+    del Ws, Ss
+    torch.cuda.empty_cache()
+
+
+def _sample_positions(rng, B, L, n_layers, C, n):
+    b = rng.integers(0, B, n)
+    t = rng.integers(0, L, n)
+    # tile edges and sequence ends
+    edge_t = np.array([0, 1, 15, 16, 17, L - 1])
+    b = np.concatenate([b, np.repeat(np.arange(B), len(edge_t))])
+    t = np.concatenate([t, np.tile(edge_t, B)])
+    l = rng.integers(0, n_layers, b.size)
+    c = rng.integers(0, C, b.size)
+    return b, t, l, c
+
+
+def _check_sampled_rows(wl, outs, exp_h, rng, n=20000, tag=""):
+    B, L = exp_h.shape[:2]
+    b, t, l, c = _sample_positions(rng, B, L, 2, 24, n)
+    for layer in range(2):
+        sel = l == layer
+        bi, ti, ci = (torch.from_numpy(x[sel]).cuda() for x in (b, t, c))
+        got = H.bf16_bits(outs[layer][bi, ti, ci])
+        exp = H.oracle_lookup_rows(wl, layer, exp_h[b[sel], t[sel], layer, c[sel]])
+        H.assert_bits_equal(got, exp, f"{tag} sampled rows layer {layer}")
+
+
+def test_full_scale_hash_lookup(full_tables):
+    Ws, Ss = full_tables
+    wl = synth.make_workload(3)
+    st, orc = H.make_state(wl), H.make_oracle(wl)
+    hashes = torch.empty((wl.B, wl.L, 2, 24), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(wl.ids), Ws, Ss, start_pos=0, hashes=hashes)
+    exp_h, _ = orc.hash(wl.ids, 0)
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "full-scale hashes")
+    P = wl.layout.primes.reshape(2, -1)
+    O = wl.layout.offsets
+    assert ((exp_h >= O) & (exp_h < O + P)).all()
+    _check_sampled_rows(wl, outs, exp_h, np.random.default_rng(3), tag="full-scale")
+    # the rows of a whole sequence end (last 8 tokens of the last row), every column
+    for layer in range(2):
+        got = H.bf16_bits(outs[layer][-1, -8:])
+        H.assert_bits_equal(got, H.oracle_lookup_rows(wl, layer, exp_h[-1, -8:, layer, :]), "sequence tail")
+    assert st.status() == 0
+
+
+def test_long_chunked_equals_one_shot(full_tables):
+    Ws, Ss = full_tables
+    wl = synth.make_workload(4)
+    total = wl.ids.shape[1]
+    Lc = wl.L
+    chunked, one = H.make_state(wl), H.make_state(wl)
+    ids, mask = H.to_dev(wl.ids), H.to_dev(wl.mask)
+    h_chunks, outs_chunks = [], []
+    for k in range(wl.chunks):
+        hk = torch.empty((1, Lc, 2, 24), dtype=torch.int64, device="cuda")
+        o = chunked.hash_lookup(ids[:, k * Lc:(k + 1) * Lc].contiguous(), Ws, Ss, start_pos=k * Lc,
+                                mask=mask[:, k * Lc:(k + 1) * Lc].contiguous(), hashes=hk)
+        h_chunks.append(hk)
+        outs_chunks.append(o)
+    h_one = torch.empty((1, total, 2, 24), dtype=torch.int64, device="cuda")
+    outs_one = one.hash_lookup(ids, Ws, Ss, start_pos=0, mask=mask, hashes=h_one)
+    h_cat = torch.cat(h_chunks, dim=1)
+    assert torch.equal(h_cat, h_one), "chunked prefill differs from one-shot hashing"
+    for layer in range(2):
+        cat = torch.cat([o[layer] for o in outs_chunks], dim=1)
+        assert torch.equal(cat.view(torch.int16), outs_one[layer].view(torch.int16))
+    orc = H.make_oracle(wl)
+    exp_h, _ = orc.hash(wl.ids, 0, wl.mask)
+    H.assert_bits_equal(h_one.cpu().numpy(), exp_h, "long one-shot hashes")
+    _check_sampled_rows(wl, outs_one, exp_h, np.random.default_rng(4), tag="long")
+    # repeated n-grams (Zipf ids) repeat their hash ids
+    assert np.unique(exp_h[0, :, 0, -1]).size < total

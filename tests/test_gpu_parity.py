@@ -1,0 +1,207 @@
+"""CUDA path vs the CPU oracle, bit for bit, through the C ABI (GPU only).
+
+Hash ids are integers: bit-exact. Looked-up rows are one fp32 round-to-nearest
+multiply then round-to-nearest-even to bf16 on both sides: bit-exact (0 ulp).
+The seeded tables never hold the NaN codes, so no NaN payload is compared;
+the all-codes test compares NaN positions only.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gram_hash_embedding_gb300 as geng
+import oracle
+import synth
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    H.build_all()
+    yield
+
+
+# ----------------------------------------------------------------------------- lookup alone
+@pytest.mark.parametrize("D,block", [(16, 16), (32, 32), (64, 16), (128, 128), (128, 32), (256, 128), (512, 256)])
+@pytest.mark.parametrize("n_idx", [1, 7, 1000, 4099])
+def test_lookup_all_codes(D, block, n_idx):
+    rng = np.random.default_rng(D * 7 + n_idx)
+    nsc = D // block
+    rows = max(256 // D, 1) + 61
+    W = rng.integers(0, 256, size=(rows, D), dtype=np.uint8)
+    W.reshape(-1)[:256] = np.arange(256, dtype=np.uint8)  # every code, NaN codes included
+    S = rng.uniform(0.01, 1.0, size=(rows, nsc)).astype(np.float32)
+    S[0, 0], S[1, -1], S[2, 0], S[3, 0] = 1e-40, 3.0e38, 2.0 ** -130, -0.75
+    idx = rng.integers(-3, rows + 3, size=n_idx).astype(np.int64)
+    idx[: min(n_idx, 4)] = np.arange(min(n_idx, 4))
+    if n_idx > 10:
+        idx[-1], idx[-2] = -(2 ** 62), 2 ** 62
+    exp = oracle.engram_lookup(idx, W, S, rows, D, block)
+    out = geng.engram_lookup(H.to_dev(idx), H.to_dev(W), H.to_dev(S), block)
+    torch.cuda.synchronize()
+    got = H.bf16_bits(out)
+    nan_e = ((exp & 0x7F80) == 0x7F80) & ((exp & 0x7F) != 0)
+    nan_g = ((got & 0x7F80) == 0x7F80) & ((got & 0x7F) != 0)
+    assert np.array_equal(nan_e, nan_g)
+    H.assert_bits_equal(np.where(nan_e, 0, got), np.where(nan_e, 0, exp), f"lookup D={D} block={block}")
+
+
+def test_lookup_empty_and_errors():
+    W = torch.zeros((4, 128), dtype=torch.uint8, device="cuda")
+    S = torch.ones((4, 1), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((0,), dtype=torch.int64, device="cuda")
+    out = geng.engram_lookup(idx, W, S, 128)
+    assert out.shape == (0, 128)
+    with pytest.raises(geng.EngramError) as e:
+        geng.engram_lookup(torch.zeros(3, dtype=torch.int64, device="cuda"), W[:, :48].contiguous(), S, 48)
+    assert e.value.code == geng.ERR_UNSUPPORTED
+    # misaligned output pointer
+    big = torch.empty((3 * 128 + 8,), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(geng.EngramError) as e:
+        geng.engram_lookup(torch.zeros(3, dtype=torch.int64, device="cuda"), W, S, 128, out=big[1:1 + 3 * 128].view(3, 128))
+    assert e.value.code == geng.ERR_INVALID
+
+
+# ----------------------------------------------------------------------------- tiny configuration
+@pytest.mark.parametrize("full64", [False, True])
+def test_tiny_hash_and_lookup(full64):
+    wl = synth.make_workload(0, full64=full64)
+    st, orc = H.make_state(wl), H.make_oracle(wl)
+    Ws, Ss = H.device_tables(wl)
+    ids = H.to_dev(wl.ids)
+    hashes = torch.empty((1, 64, 1, 6), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(ids, Ws, Ss, start_pos=0, hashes=hashes)
+    exp_h, _ = orc.hash(wl.ids, 0)
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "tiny hashes")
+    exp_rows = H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :])
+    H.assert_bits_equal(H.bf16_bits(outs[0]), exp_rows, "tiny rows")
+    # hash-only entry point, fresh cache
+    st.reset()
+    h2 = st.hash(ids, 0)
+    H.assert_bits_equal(h2.cpu().numpy(), exp_h, "tiny hash-only")
+    # the full tiny table on the host: oracle on the real table, not a compact one
+    Wh = Ws[0].cpu().numpy()
+    Sh = Ss[0].cpu().numpy()
+    H.assert_bits_equal(oracle.engram_lookup(exp_h[:, :, 0, :], Wh, Sh, Wh.shape[0], 32, 32), exp_rows, "compact table")
+    assert st.status() == 0
+
+
+def test_device_fill_matches_host_generator():
+    wl = synth.make_workload(0)
+    Ws, Ss = H.device_tables(wl)
+    rows = wl.layout.rows[0]
+    H.assert_bits_equal(Ws[0].cpu().numpy(), synth.table_rows(wl.table_seed, 0, np.arange(rows), 32), "fp8 fill")
+    H.assert_bits_equal(Ss[0].cpu().numpy().view(np.uint32),
+                        synth.table_scales(wl.table_seed, 0, np.arange(rows), 1).view(np.uint32), "scale fill")
+
+
+# ----------------------------------------------------------------------------- ragged tiles, chunks, starts
+@pytest.mark.parametrize("L", [1, 2, 3, 15, 16, 17, 63, 64, 65, 1000])
+def test_ragged_lengths_and_row_starts(L):
+    wl = synth.make_workload(0, full64=True)
+    lay = wl.layout
+    B, T = 3, 1200
+    ids = synth.uniform_int(L, synth.TAG_IDS, B * T, 0, lay.raw_vocab).reshape(B, T)
+    mask = synth.uniform_int(L + 1, synth.TAG_IDS, B * T, 0, 6).reshape(B, T) > 0
+    st, orc = H.make_state(wl, B, 4096), H.make_oracle(wl, B, 4096)
+    Ws, Ss = H.device_tables(wl)
+    starts = np.array([0, 5, 2], dtype=np.int32)
+    # history first (prefill each row up to its start), then an L-token call at per-row starts
+    pre = ids[:, :8]
+    st.hash(H.to_dev(pre), 0, H.to_dev(mask[:, :8]))
+    orc.hash(pre, 0, mask[:, :8])
+    chunk = np.stack([ids[b, starts[b]:starts[b] + L] for b in range(B)])
+    cmask = np.stack([mask[b, starts[b]:starts[b] + L] for b in range(B)])
+    hashes = torch.empty((B, L, 1, 6), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(chunk), Ws, Ss, start_pos=H.to_dev(starts), mask=H.to_dev(cmask), hashes=hashes)
+    exp_h, _ = orc.hash(chunk, starts.astype(np.int64), cmask)
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, f"hashes L={L}")
+    H.assert_bits_equal(H.bf16_bits(outs[0]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]), f"rows L={L}")
+
+
+def test_bad_start_and_bad_ids_are_flagged_not_faulted():
+    wl = synth.make_workload(0)
+    st, orc = H.make_state(wl, 2, 64), H.make_oracle(wl, 2, 64)
+    Ws, Ss = H.device_tables(wl)
+    ids = np.array([[1, 2, 3, 4], [5, -7, 999, 1000]], dtype=np.int64)
+    starts = np.array([62, 0], dtype=np.int32)  # row 0: 62 + 4 > 64
+    hashes = torch.empty((2, 4, 1, 6), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(ids), Ws, Ss, start_pos=H.to_dev(starts), hashes=hashes)
+    flags = st.status()
+    assert flags == geng.STATUS_BAD_START | geng.STATUS_BAD_ID
+    exp_h, eflags = orc.hash(ids, starts.astype(np.int64))
+    assert eflags == flags
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "flagged hashes")
+    assert (exp_h[0] == -1).all()
+    assert (H.bf16_bits(outs[0])[0] == 0).all()
+    H.assert_bits_equal(H.bf16_bits(outs[0]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]), "flagged rows")
+    assert st.status() == 0  # cleared
+
+
+def test_argument_errors():
+    wl = synth.make_workload(0)
+    st = H.make_state(wl, 2, 64)
+    ids = torch.zeros((3, 4), dtype=torch.int64, device="cuda")
+    with pytest.raises(geng.EngramError) as e:
+        st.hash(ids, 0)  # B > max_batch
+    assert e.value.code == geng.ERR_RANGE
+    with pytest.raises(geng.EngramError) as e:
+        st.hash(torch.zeros((1, 65), dtype=torch.int64, device="cuda"), 0)  # L > max_seq_len
+    assert e.value.code == geng.ERR_RANGE
+    # empty calls are no-ops
+    assert st.hash(torch.zeros((0, 4), dtype=torch.int64, device="cuda"), 0).shape == (0, 4, 1, 6)
+    assert st.hash(torch.zeros((2, 0), dtype=torch.int64, device="cuda"), 0).shape == (2, 0, 1, 6)
+    with pytest.raises(geng.EngramError) as e:
+        geng.engram_state_create(n_layers=1, max_ngram=4, n_heads=2, head_dim=32, block=32, max_batch=1,
+                                 max_seq_len=8, token_map=[0, 1], multipliers=[1, 1, 1, 1], primes=[0] * 6,
+                                 offsets=[0] * 6)
+    assert e.value.code == geng.ERR_INVALID  # prime 0
+
+
+# ----------------------------------------------------------------------------- prefill configuration
+@pytest.fixture(scope="module")
+def prefill_tables():
+    wl = synth.make_workload(1)
+    Ws, Ss = H.device_tables(wl)
+    yield wl, Ws, Ss
+    del Ws, Ss
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("full64", [False, True])
+def test_prefill_with_image_spans(prefill_tables, full64):
+    wl1, Ws, Ss = prefill_tables
+    wl = synth.make_workload(1, full64=full64) if full64 else wl1
+    st, orc = H.make_state(wl), H.make_oracle(wl)
+    hashes = torch.empty((wl.B, wl.L, 2, 24), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(wl.ids), Ws, Ss, start_pos=0, mask=H.to_dev(wl.mask), hashes=hashes)
+    exp_h, fl = orc.hash(wl.ids, 0, wl.mask)
+    assert fl == 0 and st.status() == 0
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "prefill hashes")
+    for l in range(2):
+        H.assert_bits_equal(H.bf16_bits(outs[l]), H.oracle_lookup_rows(wl1, l, exp_h[:, :, l, :]), f"prefill rows l{l}")
+
+
+def test_decode_per_row_start(prefill_tables):
+    _, Ws, Ss = prefill_tables
+    wl = synth.make_workload(2)
+    st, orc = H.make_state(wl), H.make_oracle(wl)
+    # prefill every row with 8192 Zipf tokens, then one decode step at each row's own start
+    h_pre = st.hash(H.to_dev(wl.prefill_ids), 0)
+    e_pre, _ = orc.hash(wl.prefill_ids, 0)
+    H.assert_bits_equal(h_pre.cpu().numpy(), e_pre, "decode prefill hashes")
+    hashes = torch.empty((wl.B, 1, 2, 24), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(wl.ids), Ws, Ss, start_pos=H.to_dev(wl.start_pos), hashes=hashes)
+    exp_h, _ = orc.hash(wl.ids, wl.start_pos.astype(np.int64))
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "decode hashes")
+    for l in range(2):
+        H.assert_bits_equal(H.bf16_bits(outs[l]), H.oracle_lookup_rows(wl, l, exp_h[:, :, l, :]), f"decode rows l{l}")
+    # a decode step equals the same row prefilled in one shot through its new token
+    b = int(np.argmax(wl.start_pos))
+    s = int(wl.start_pos[b])
+    one = H.make_state(wl, 1, wl.max_seq_len)
+    seq = np.concatenate([wl.prefill_ids[b, :s], wl.ids[b]])[None]
+    h_one = one.hash(H.to_dev(seq), 0)
+    assert (h_one[0, -1] == hashes[b, 0]).all()
