@@ -1,0 +1,566 @@
+#!/usr/bin/env python
+"""Benchmark of the fused Engram n-gram hash + fp8 row lookup on GB300.
+
+One step = one pass of the whole hot path over one batch: the n-gram hash
+(token_map compression, cache write, lookback with blocking, multiply/XOR,
+floored mod by primes, offsets) fused with the gather of 2 x 24 fp8 rows per
+token from the two full-scale tables (384,006,168 and 384,016,682 rows x 128,
+~98 GB) and their fp32 scales, dequantised to bf16 -- one kernel launch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--cfg 3] [--impl ours|reference]
+
+Prints one JSON line (rank 0). `value` is tokens/s over all ranks with inputs
+resident in HBM; `e2e` adds the host->device copy of the step's ids and the
+device->host copy of its bf16 rows from/to pinned host memory; `roofline`
+relates the fused kernel's algorithmic bytes (fp8 row + fp32 scale read +
+bf16 row written, 18,624 B per token) to the measured HBM copy bandwidth;
+`cpu_baseline` times the CPU oracle on the same workload.
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent
+replica on its own batch (weak scaling): the path has no exchange step.
+`--impl reference` times the CPU oracle alone (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+ALGO_BYTES_PER_ROW = None  # set from the layout: head_dim + 4*head_dim/block + 2*head_dim
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_fullscale_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "gram_hash_embedding_gb300", "csrc", f) for f in
+                  ("kernels.cu", "engram_internal.cuh")]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--cfg", type=int, default=3, choices=[1, 2, 3, 4, 5],
+                   help="1 prefill B4xL4096, 2 decode B256xL1, 3 full-scale B8xL8192 (default), 4 long chunked, "
+                        "5 profiling case (prefill shapes, 1 GB tables)")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end loop (default min(K, 100))")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29533")
+        dist.init_process_group(backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each replica hashes its own batch (different ids); the tables are the same."""
+    return base + 1000 * rank
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = self._smi_id(gpu_index)
+        self.proc = None
+        self.lines = []
+
+    @staticmethod
+    def _smi_id(local: int) -> str:
+        """nvidia-smi id of the device this process uses (CUDA_VISIBLE_DEVICES may renumber it)."""
+        try:
+            import torch
+
+            u = str(torch.cuda.get_device_properties(local).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            parts = [v for v in vis.split(",") if v.strip()]
+            return parts[local].strip() if local < len(parts) else str(local)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self, max_mhz_default=None):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": max_mhz_default, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(cfg: int):
+    """DRAM bytes per launch of the fused kernel from a committed ncu summary, or None when the
+    kernel sources changed since the counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    if d.get("source_sha256") != kernel_source_hash() or int(d.get("cfg", -1)) != cfg:
+        return None
+    return float(d["dram_bytes_per_launch"])
+
+
+def algo_bytes_per_token(lay) -> int:
+    D, nsc = lay.head_dim, lay.head_dim // lay.block
+    return lay.n_layers * lay.n_cols * (D + 4 * nsc + 2 * D)
+
+
+# ----------------------------------------------------------------------------- our arm
+class Runner:
+    """Device-resident workload and one step of the fused path for configuration `cfg`."""
+
+    def __init__(self, cfg: int, rank: int, device):
+        import numpy as np
+        import torch
+
+        import gram_hash_embedding_gb300 as geng
+        import synth
+
+        self.torch, self.np, self.geng, self.synth = torch, np, geng, synth
+        self.cfg = cfg
+        self.device = device
+        wl = synth.make_workload(cfg)
+        self.wl = wl
+        lay = wl.layout
+        self.lay = lay
+        # tables: one replica per GPU, filled by the seeded generator
+        self.W, self.S = [], []
+        for l, rows in enumerate(lay.rows):
+            W = torch.empty((rows, lay.head_dim), dtype=torch.uint8, device=device)
+            S = torch.empty((rows, lay.n_scales), dtype=torch.float32, device=device)
+            synth.fill_table_device(W, S, wl.table_seed, l)
+            self.W.append(W)
+            self.S.append(S)
+        self.state = geng.EngramHash(n_layers=lay.n_layers, max_ngram=lay.max_ngram, n_heads=lay.n_heads,
+                                     head_dim=lay.head_dim, block=lay.block, max_batch=wl.max_batch,
+                                     max_seq_len=wl.max_seq_len, token_map=lay.token_map,
+                                     multipliers=lay.multipliers, primes=lay.primes, offsets=lay.offsets,
+                                     dead=lay.dead, pad_id=lay.pad_id)
+        seed = rank_seed(synth.MASTER_SEED + 17, rank)
+        # batches: distinct id sets cycled step to step
+        if cfg == 4:
+            total = wl.ids.shape[1]
+            ids = [wl.ids if rank == 0 else synth.zipf_ids(seed, total).reshape(1, total)]
+            masks = [wl.mask]
+            self.chunks = [(k * wl.L, (k + 1) * wl.L) for k in range(wl.chunks)]
+            self.B, self.L = 1, total
+        else:
+            n_batches = 4 if cfg != 2 else 1
+            ids = [wl.ids if (k == 0 and rank == 0) else
+                   synth.uniform_ids(seed + k, wl.B * wl.L).reshape(wl.B, wl.L) for k in range(n_batches)]
+            if cfg == 2:
+                ids = [wl.ids]
+            masks = [wl.mask] * len(ids)
+            self.chunks = [(0, wl.L)]
+            self.B, self.L = wl.B, wl.L
+        self.ids_host = ids
+        self.ids = [torch.from_numpy(np.ascontiguousarray(a)).to(device) for a in ids]
+        self.masks = [None if m is None else torch.from_numpy(np.ascontiguousarray(m)).to(device) for m in masks]
+        self.start = torch.from_numpy(np.ascontiguousarray(wl.start_pos.astype(np.int32))).to(device)
+        if cfg == 2:  # decode: history first
+            self.state.hash(torch.from_numpy(wl.prefill_ids).to(device), 0)
+        Lc = self.chunks[0][1] - self.chunks[0][0]
+        self.out = [torch.empty((self.B, Lc, lay.n_cols, lay.head_dim), dtype=torch.bfloat16, device=device)
+                    for _ in range(lay.n_layers)]
+        self.tokens_per_step = self.B * self.L
+        self.launches_per_step = len(self.chunks)
+        torch.cuda.synchronize(device)
+
+    def step(self, k: int, ids=None, mask=None):
+        """Enqueue one step; returns the launches' (start, end) event pairs when timing."""
+        ids = self.ids[k % len(self.ids)] if ids is None else ids
+        mask = self.masks[k % len(self.masks)] if mask is None else mask
+        for c0, c1 in self.chunks:
+            if len(self.chunks) == 1:
+                ii, mm, sp = ids, mask, self.start
+            else:
+                ii = ids[:, c0:c1]
+                mm = None if mask is None else mask[:, c0:c1]
+                sp = c0
+            self.geng.engram_hash_lookup(self.state.handle, ii if ii.is_contiguous() else ii.contiguous(), sp,
+                                         self.W, self.S, mm if (mm is None or mm.is_contiguous()) else mm.contiguous(),
+                                         self.out)
+
+    def e2e_buffers(self):
+        torch = self.torch
+        self.ids_pinned = [torch.from_numpy(self.np.ascontiguousarray(a)).pin_memory() for a in self.ids_host]
+        self.mask_pinned = [None if m is None else m.cpu().pin_memory() for m in self.masks]
+        self.start_pinned = self.start.cpu().pin_memory()
+        self.ids_dev = torch.empty_like(self.ids[0])
+        self.mask_dev = None if self.masks[0] is None else torch.empty_like(self.masks[0])
+        self.start_dev = torch.empty_like(self.start)
+        self.out_pinned = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.out]
+
+    def e2e_step(self, k: int):
+        """Host ids -> device, fused hash + lookup through the C ABI, bf16 rows -> host."""
+        j = k % len(self.ids_pinned)
+        self.ids_dev.copy_(self.ids_pinned[j], non_blocking=True)
+        if self.mask_dev is not None:
+            self.mask_dev.copy_(self.mask_pinned[j % len(self.mask_pinned)], non_blocking=True)
+        self.start_dev.copy_(self.start_pinned, non_blocking=True)
+        saved = self.start
+        self.start = self.start_dev
+        try:
+            if len(self.chunks) == 1:
+                self.step(k, self.ids_dev, self.mask_dev)
+                for o, h in zip(self.out, self.out_pinned):
+                    h.copy_(o, non_blocking=True)
+            else:  # chunked: copy each chunk's rows out after its launch
+                for c0, c1 in self.chunks:
+                    mm = None if self.mask_dev is None else self.mask_dev[:, c0:c1].contiguous()
+                    self.geng.engram_hash_lookup(self.state.handle, self.ids_dev[:, c0:c1].contiguous(), c0, self.W,
+                                                 self.S, mm, self.out)
+                    for o, h in zip(self.out, self.out_pinned):
+                        h.copy_(o, non_blocking=True)
+        finally:
+            self.start = saved
+
+    def e2e_bytes(self):
+        h2d = self.ids_pinned[0].numel() * 8 + self.start_pinned.numel() * 4
+        if self.mask_dev is not None:
+            h2d += self.mask_dev.numel()
+        d2h = sum(o.numel() * 2 for o in self.out) * len(self.chunks)
+        return h2d, d2h
+
+
+def time_region(torch, dist, dev_index, fn, steps, stream, per_launch_events=False, n_launch=1):
+    """Run `fn(k)` `steps` times between barriers and synchronisations; returns (total seconds, mean
+    seconds between the per-step events) from CUDA events on `stream`."""
+    torch.cuda.synchronize()
+    barrier(dist, dev_index)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    pairs = []
+    start.record(stream)
+    for k in range(steps):
+        if per_launch_events:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn(k)
+            b.record(stream)
+            pairs.append((a, b))
+        else:
+            fn(k)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, dev_index)
+    total = start.elapsed_time(end) / 1e3
+    mean = statistics.mean(a.elapsed_time(b) for a, b in pairs) / 1e3 if pairs else None
+    return total, mean
+
+
+def cpu_baseline_oracle(runner, n_tokens: int):
+    """Time the CPU oracle (single thread, as it stands) on the first n_tokens of the workload:
+    hash of those tokens, then the lookup of every row they touch. The touched rows are copied
+    out of the generator-filled device tables into a compact host table (not timed)."""
+    import numpy as np
+
+    import oracle
+
+    torch = runner.torch
+    wl, lay = runner.wl, runner.lay
+    ids = runner.ids_host[0]
+    B, L = ids.shape
+    rows_used = max(1, min(B, -(-n_tokens // L)))
+    cut = min(L, n_tokens)
+    sub = np.ascontiguousarray(ids[:rows_used, :cut])
+    mask = None if wl.mask is None else np.ascontiguousarray(wl.mask[:rows_used, :cut])
+    orc = oracle.OracleState.from_layout(lay, rows_used, max(cut, 1))
+    t0 = time.perf_counter()
+    hashes, _ = orc.hash(sub, 0, mask)
+    t_hash = time.perf_counter() - t0
+    t_lookup = 0.0
+    for l in range(lay.n_layers):
+        flat = hashes[:, :, l, :].reshape(-1)
+        uniq, inv = np.unique(flat, return_inverse=True)
+        sel = torch.from_numpy(uniq).to(runner.device)
+        Wc = runner.W[l][sel].cpu().numpy()
+        Sc = runner.S[l][sel].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.engram_lookup(inv.astype(np.int64), Wc, Sc, uniq.size, lay.head_dim, lay.block)
+        t_lookup += time.perf_counter() - t0
+    tokens = sub.size
+    return {"value": tokens / (t_hash + t_lookup), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {tokens} tokens of the same workload ({rows_used} sequence(s) x {cut}); hash + lookup "
+                      f"of their {tokens * lay.n_layers * lay.n_cols} rows; single-threaded C; "
+                      f"hash {t_hash:.3f} s + lookup {t_lookup:.3f} s"}
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    if rank == 0:
+        import __graft_entry__
+
+        __graft_entry__.build()
+    barrier(dist, local)
+    import gram_hash_embedding_gb300 as geng
+
+    geng._lib()
+    runner = Runner(args.cfg, rank, device)
+    stream = torch.cuda.current_stream(device)
+    K, W = args.steps, args.warmup
+    for k in range(W):
+        runner.step(k)
+    torch.cuda.synchronize()
+    flags = runner.state.status()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    total, mean_launch = time_region(torch, dist, local, runner.step, K, stream, per_launch_events=True)
+    clocks.stop()
+    total_max = max_over_ranks(dist, total, device)
+    tokens = runner.tokens_per_step * K * world
+    value = tokens / total_max
+
+    # end to end: host ids in, host bf16 rows out, every step
+    runner.e2e_buffers()
+    Ke = args.e2e_steps or max(3, min(K, 100))
+    for k in range(3):
+        runner.e2e_step(k)
+    e_total, _ = time_region(torch, dist, local, runner.e2e_step, Ke, stream)
+    e_total = max_over_ranks(dist, e_total, device)
+    e_value = runner.tokens_per_step * Ke * world / e_total
+    h2d, d2h = runner.e2e_bytes()
+
+    lay = runner.lay
+    bpt = algo_bytes_per_token(lay)
+    per_launch_tokens = runner.tokens_per_step // runner.launches_per_step
+    algo_bytes = per_launch_tokens * bpt
+    launch_s = mean_launch / runner.launches_per_step
+    peak, peak_kind = measured_peaks()
+    achieved = algo_bytes / launch_s / 1e9
+    traffic = recorded_traffic(args.cfg)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_oracle(runner, runner.tokens_per_step if args.cfg != 2 else runner.tokens_per_step)
+    csum = clocks.summary()
+    wl = runner.wl
+    line = {
+        "metric": "Engram hash+fp8-gather tokens/s (B8×L8192); gathered HBM GB/s vs peak",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": total_max / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name,
+            "cfg": args.cfg,
+            "B": runner.B,
+            "L": runner.L,
+            "engram_layers": lay.n_layers,
+            "hash_cols": lay.n_cols,
+            "head_dim": lay.head_dim,
+            "fp8_block": lay.block,
+            "table_rows": lay.rows,
+            "arithmetic": "hash int64 (wrapping multiply, XOR, floored mod); fp8 E4M3 x fp32 scale in fp32, RNE to bf16",
+            "parallelism": f"replicas x{world} (no exchange step)",
+            "l2": "inputs larger than L2: ~98 GB of tables read at random, 805 MB of bf16 written per step; "
+                  f"{len(runner.ids)} distinct id batches cycled",
+            "status_flags_after_warmup": flags,
+        },
+        "gathered_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": algo_bytes, "launch_us": launch_s * 1e6,
+                     "kernel": "hash_kernel<GATHER=true> (fused hash + gather + dequant)"},
+        "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": Ke, "ms_per_step": e_total / Ke * 1e3},
+        "gpu_launches": K * runner.launches_per_step,
+        "clocks": csum,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as it stands, timed on the host cores: each step hashes a bounded sample of
+    the workload (the first T tokens of one of its sequences, in turn) and looks up every row
+    those tokens touch."""
+    import numpy as np
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import synth
+
+    oracle.build()
+    wl = synth.make_workload(args.cfg)
+    lay = wl.layout
+    K, W = args.steps, args.warmup
+    # size each step so the whole run stays within about two minutes of oracle time
+    est_tok_s = 6000.0
+    T = int(max(8, min(wl.L if args.cfg != 4 else 8192, est_tok_s * 120.0 / max(1, K + W))))
+    ids_all = wl.ids
+    B = ids_all.shape[0]
+    samples = []
+    for b in range(min(B, 8)):
+        sub = np.ascontiguousarray(ids_all[b:b + 1, :T])
+        msk = None if wl.mask is None else np.ascontiguousarray(wl.mask[b:b + 1, :T])
+        orc = oracle.OracleState.from_layout(lay, 1, T)
+        h, _ = orc.hash(sub, 0, msk)
+        tabs = []
+        for l in range(lay.n_layers):
+            flat = h[:, :, l, :].reshape(-1)
+            uniq, inv = np.unique(flat, return_inverse=True)
+            Wc = synth.table_rows(wl.table_seed, l, uniq, lay.head_dim)
+            Sc = synth.table_scales(wl.table_seed, l, uniq, lay.n_scales)
+            tabs.append((uniq, Wc, Sc))
+        samples.append((sub, msk, orc, tabs))
+
+    def one(k):
+        sub, msk, orc, tabs = samples[k % len(samples)]
+        orc.reset()
+        t0 = time.perf_counter()
+        h, _ = orc.hash(sub, 0, msk)
+        el = time.perf_counter() - t0
+        for l, (uniq, Wc, Sc) in enumerate(tabs):
+            local_idx = np.searchsorted(uniq, h[:, :, l, :].reshape(-1))
+            t0 = time.perf_counter()
+            oracle.engram_lookup(local_idx, Wc, Sc, uniq.size, lay.head_dim, lay.block)
+            el += time.perf_counter() - t0
+        return el
+
+    for k in range(W):
+        one(k)
+    total = sum(one(k) for k in range(K))
+    value = T * K / total
+    sample = (f"each step: the first {T} tokens of one sequence of the workload (cycling over {len(samples)}), "
+              f"hash + lookup of their {T * lay.n_layers * lay.n_cols} rows from compact host tables; "
+              "single-threaded C oracle")
+    line = {
+        "impl": "reference",
+        "metric": "Engram hash+fp8-gather tokens/s (B8×L8192); gathered HBM GB/s vs peak",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": total / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "cfg": args.cfg, "sample_tokens_per_step": T},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -282,10 +282,9 @@ def table_rows(seed: int, layer: int, rows, D: int) -> np.ndarray:
     ctr = (rows[:, None] * np.uint64(wpr) + np.arange(wpr, dtype=np.uint64)[None, :]).reshape(-1)
     w = words(seed, TAG_TABLE + layer, ctr)
     lut = fp8_normal_lut()
-    out = np.empty((w.size, 4), dtype=np.uint8)
-    for j in range(4):
-        out[:, j] = lut[((w >> np.uint64(16 * j)) & np.uint64(0xFFFF)).astype(np.int64)]
-    return out.reshape(rows.size, D)
+    # piece j of a word is bits [16j, 16j+16): on a little-endian host, uint16 element j of its view
+    pieces = w.astype("<u8", copy=False).view("<u2")
+    return lut[pieces].reshape(rows.size, D)
 
 
 def table_scales(seed: int, layer: int, rows, n_scales: int) -> np.ndarray:
@@ -413,6 +412,8 @@ def make_layout(kind: str, seed: int, full64: bool = False) -> Layout:
         primes = layered_primes(1_000_000, 2, 4, 8)
     elif kind == "full":    # the released table sizes
         primes = layered_primes(FULL_SCALE_PRIME_START, 2, 4, 8)
+    elif kind == "profile":  # same shapes, ~0.5 GB per layer: small enough for a full ncu capture
+        primes = layered_primes(160_000, 2, 4, 8)
     else:
         raise ValueError(kind)
     return Layout(2, 4, 8, 128, 128, RAW_VOCAB, COMPRESSED_VOCAB, token_map(seed), multipliers(seed, 2, 4, full64),
@@ -457,4 +458,9 @@ def make_workload(cfg: int, seed: int = MASTER_SEED, full64: bool = False) -> Wo
         # same full-scale tables as configuration 3
         return Workload("long chunked B1x65536 (8x8192)", lay, 1, Lc, ids.reshape(1, total), mask.reshape(1, total),
                         np.zeros(1, np.int32), seed + 3, 1, total, chunks=chunks)
+    if cfg == 5:  # profiling case: prefill shapes on ~1 GB of tables (still far above L2)
+        lay = make_layout("profile", s, full64)
+        B, L = 4, 4096
+        ids = uniform_ids(s, B * L).reshape(B, L)
+        return Workload("profile B4xL4096 (1 GB tables)", lay, B, L, ids, None, np.zeros(B, np.int32), s, B, L)
     raise ValueError(cfg)
