@@ -34,8 +34,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-ALGO_BYTES_PER_ROW = None  # set from the layout: head_dim + 4*head_dim/block + 2*head_dim
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_fullscale_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_fullscale_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "gram_hash_embedding_gb300", "csrc", f) for f in
                   ("kernels.cu", "engram_internal.cuh")]
 
@@ -182,12 +181,17 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(cfg: int):
-    """DRAM bytes per launch of the fused kernel from a committed ncu summary, or None when the
-    kernel sources changed since the counters were taken."""
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary ("key: value" lines),
+    or None when the kernel sources changed since the counters were taken or the workload differs."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
+    d = {}
     with open(TRAFFIC_FILE) as f:
-        d = json.load(f)
+        for line in f:
+            if line.startswith("#") or ":" not in line:
+                continue
+            k, v = line.split(":", 1)
+            d[k.strip()] = v.strip()
     if d.get("source_sha256") != kernel_source_hash() or int(d.get("cfg", -1)) != cfg:
         return None
     return float(d["dram_bytes_per_launch"])
@@ -257,6 +261,7 @@ class Runner:
                     for _ in range(lay.n_layers)]
         self.tokens_per_step = self.B * self.L
         self.launches_per_step = len(self.chunks)
+        self.kernel_name = f"hash_kernel<GATHER=true, D={lay.head_dim}> (hash + gather + dequant)"
         torch.cuda.synchronize(device)
 
     def step(self, k: int, ids=None, mask=None):
@@ -471,7 +476,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": algo_bytes, "launch_us": launch_s * 1e6,
-                     "kernel": "hash_kernel<GATHER=true> (fused hash + gather + dequant)"},
+                     "kernel": runner.kernel_name},
         "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke, "ms_per_step": e_total / Ke * 1e3},
         "gpu_launches": K * runner.launches_per_step,

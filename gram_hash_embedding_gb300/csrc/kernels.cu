@@ -10,9 +10,17 @@
 // of its bytes); there is no dense contraction, so no tensor cores. A CTA owns a tile of
 // consecutive tokens of one sequence: it stages the tile's compressed tokens plus the
 // (max_ngram-1)-token halo in shared memory, computes every hash id of the tile there, and then
-// all its threads stream the tile's rows. For one layer the tile's output rows are contiguous,
-// so each warp store covers whole 32-byte sectors: lane q of a row's D/16-lane group converts
-// codes [8q, 8q+8) and [D/2+8q, D/2+8q+8) and writes 16 bytes into each half of the output row.
+// all its threads stream the tile's rows through registers, several rows in flight per thread.
+// For one layer the tile's output rows are contiguous, so each warp store covers whole 32-byte
+// sectors: lane q of a row's D/16-lane group converts codes [8q, 8q+8) and [D/2+8q, D/2+8q+8) and
+// writes 16 bytes into each half of the output row.
+//
+// On this GPU every random read of 4 to 128 bytes costs one 128-byte DRAM access, so a row
+// (128 B of codes) and its 4-byte scale cost two; with the 256-byte bf16 write that is 512 DRAM
+// bytes per row for 388 algorithmic bytes. A variant that landed rows and scales in shared memory
+// with bulk copies (TMA engine) and per-warp mbarrier pipelines was built and measured slower at
+// every shape tried (its shared-memory slots cap the SM at ~1000 rows in flight and leave 8-16
+// warps to convert), so the register path is the one kept.
 #include <cstdint>
 
 #include "engram_internal.cuh"
@@ -20,10 +28,24 @@
 namespace engram {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kUnroll = 4;          // independent rows in flight per thread
-constexpr int kFusedTile = 16;      // tokens per CTA, fused kernel
-constexpr int kHashTile = 64;       // tokens per CTA, hash-only kernel
+#ifndef ENGRAM_THREADS
+#define ENGRAM_THREADS 256
+#endif
+#ifndef ENGRAM_UNROLL
+#define ENGRAM_UNROLL 4
+#endif
+#ifndef ENGRAM_FUSED_TILE
+#define ENGRAM_FUSED_TILE 16
+#endif
+#ifndef ENGRAM_MIN_BLOCKS
+#define ENGRAM_MIN_BLOCKS 4
+#endif
+
+constexpr int kThreads = ENGRAM_THREADS;
+constexpr int kUnroll = ENGRAM_UNROLL;          // independent row pieces in flight per thread
+constexpr int kFusedTile = ENGRAM_FUSED_TILE;   // tokens per CTA, fused kernel
+constexpr int kHashTile = 64;                   // tokens per CTA, hash-only kernel
+constexpr int kMinBlocks = ENGRAM_MIN_BLOCKS;   // occupancy hint for the fused kernel
 
 // ------------------------------------------------------------------------------------------------
 // integer helpers
@@ -96,6 +118,8 @@ __device__ __forceinline__ void st_out_v4(void* p, uint4 v) {
                : "memory");
 }
 
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
+
 // One lane's share of one output row: codes [8q, 8q+8) and [D/2+8q, D/2+8q+8) of table row `row`.
 struct RowPiece {
   uint2 v0, v1;
@@ -103,22 +127,27 @@ struct RowPiece {
   bool valid;
 };
 
+// D (head_dim) is a compile-time power of two, so row offsets are shifts; the scale block is a
+// power of two too (it divides D), passed as its log2. `one_block`: the row has a single scale
+// (block >= D), so both halves share one scale load.
+template <int D, bool ONE>
 __device__ __forceinline__ void piece_load(RowPiece& pc, const uint8_t* W, const float* S, int64_t rows, int64_t row,
-                                           int q, int D, int block, int nsc) {
+                                           int q, int blk_shift) {
   pc.valid = (row >= 0) && (row < rows);
   if (pc.valid) {
-    const uint8_t* base = W + row * (int64_t)D;
+    const uint8_t* base = W + (row << ilog2(D));
     const int k0 = 8 * q, k1 = (D >> 1) + 8 * q;
     pc.v0 = ld_rows_v2(base + k0);
     pc.v1 = ld_rows_v2(base + k1);
-    const float* srow = S + row * (int64_t)nsc;
-    pc.s0 = ld_scale(srow + k0 / block);
-    pc.s1 = ld_scale(srow + k1 / block);
+    const float* srow = S + (row << (ilog2(D) - blk_shift));
+    pc.s0 = ld_scale(srow + (k0 >> blk_shift));
+    pc.s1 = ONE ? pc.s0 : ld_scale(srow + (k1 >> blk_shift));
   }
 }
 
 // out_row: bf16 row of D values (2*D bytes)
-__device__ __forceinline__ void piece_store(const RowPiece& pc, uint16_t* out_row, int q, int D) {
+template <int D>
+__device__ __forceinline__ void piece_store(const RowPiece& pc, uint16_t* out_row, int q) {
   uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;  // masked rows are +0
   if (pc.valid) {
     a = dequant8(pc.v0, pc.s0);
@@ -129,7 +158,7 @@ __device__ __forceinline__ void piece_store(const RowPiece& pc, uint16_t* out_ro
 }
 
 // ------------------------------------------------------------------------------------------------
-// shared-memory plan of the hash / fused kernels
+// shared-memory plan of the hash phase (all kernels that hash a token tile)
 
 struct SmemPlan {
   int cols_off, mult_off, roll_off, rowidx_off, tok_off, bytes;
@@ -150,49 +179,42 @@ __host__ __device__ inline SmemPlan smem_plan(int n_layers, int max_ngram, int n
 }
 
 // ------------------------------------------------------------------------------------------------
-// hash (+ gather) kernel. grid = (ceil(L / tile), B); one CTA = `tile` consecutive tokens of row b.
-//
-// G = head_dim / 16 lanes per output row (power of two); unused when GATHER is false.
-template <bool GATHER, int G>
-__global__ void __launch_bounds__(kThreads) hash_kernel(const StateView sv, const CallArgs a, const int tile) {
-  extern __shared__ __align__(16) unsigned char smem[];
+// hash phase of one tile: `ntok` consecutive tokens starting at t0 of sequence b. Called by every
+// thread of the CTA (contains barriers). Fills rowidx (layer-major: [l][t][col]) when given, and the
+// optional int64 hash output. Returns whether the row's start position fits the cache.
+__device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a, unsigned char* smem,
+                                          const SmemPlan& plan, const int tile, const int b, const int64_t t0,
+                                          const int ntok, const bool want_rowidx, unsigned int* flags_s) {
   const int N = sv.max_ngram, NL = sv.n_layers, C = sv.n_cols, H = sv.n_heads;
   const int NC = NL * C;
-  const SmemPlan plan = smem_plan(NL, N, C, tile, GATHER);
   ColParam* cols_s = reinterpret_cast<ColParam*>(smem + plan.cols_off);
   uint64_t* mult_s = reinterpret_cast<uint64_t*>(smem + plan.mult_off);
   uint64_t* roll_s = reinterpret_cast<uint64_t*>(smem + plan.roll_off);
   int64_t* rowidx_s = reinterpret_cast<int64_t*>(smem + plan.rowidx_off);
   int32_t* tok_s = reinterpret_cast<int32_t*>(smem + plan.tok_off);
-  __shared__ unsigned int flags_s;
-
-  const int tid = threadIdx.x;
-  const int b = blockIdx.y;
+  const int tid = threadIdx.x, nthr = blockDim.x;
   const int64_t L = a.L;
-  const int64_t t0 = (int64_t)blockIdx.x * tile;
-  const int ntok = (int)min((int64_t)tile, L - t0);
   const int64_t s_b = (int64_t)a.start_pos[b];
   const bool row_ok = (s_b >= 0) && (s_b <= sv.max_seq_len - L);
   const int32_t dead = sv.dead;
   int32_t* cache_row = sv.cache + (int64_t)b * sv.max_seq_len;
 
-  if (tid == 0) flags_s = row_ok ? 0u : ENGRAM_STATUS_BAD_START;
-  for (int i = tid; i < NC; i += kThreads) cols_s[i] = sv.cols[i];
-  for (int i = tid; i < NL * N; i += kThreads) mult_s[i] = sv.mult[i];
-  __syncthreads();
+  if (tid == 0 && !row_ok) atomicOr(flags_s, ENGRAM_STATUS_BAD_START);
+  for (int i = tid; i < NC; i += nthr) cols_s[i] = sv.cols[i];
+  for (int i = tid; i < NL * N; i += nthr) mult_s[i] = sv.mult[i];
 
   // 1. compressed tokens of the tile and its halo: tok_s[j] holds position t0 - (N-1) + j.
   //    In-chunk tokens come from ids (token_map, mask); earlier positions come from the cache,
   //    which this launch never writes below start_pos, so reads and writes are disjoint.
   if (row_ok) {
-    for (int j = tid; j < ntok + N - 1; j += kThreads) {
+    for (int j = tid; j < ntok + N - 1; j += nthr) {
       const int64_t t = t0 - (N - 1) + j;
       int32_t c;
       if (t >= 0) {
         const int64_t id = a.ids[(int64_t)b * L + t];
         if (id < 0 || id >= sv.raw_vocab) {
           c = dead;
-          atomicOr(&flags_s, ENGRAM_STATUS_BAD_ID);
+          atomicOr(flags_s, ENGRAM_STATUS_BAD_ID);
         } else {
           c = sv.token_map[id];
         }
@@ -208,7 +230,7 @@ __global__ void __launch_bounds__(kThreads) hash_kernel(const StateView sv, cons
 
   // 2. cache write, lookback with cumulative blocking, products and rolling XOR per layer
   if (row_ok) {
-    for (int t = tid; t < ntok; t += kThreads) {
+    for (int t = tid; t < ntok; t += nthr) {
       const int32_t cur = tok_s[t + N - 1];
       const int64_t pos = s_b + t0 + t;
       cache_row[pos] = cur;
@@ -236,55 +258,90 @@ __global__ void __launch_bounds__(kThreads) hash_kernel(const StateView sv, cons
   }
   __syncthreads();
 
-  // 3. hash ids: floored mod by the column's prime plus its offset; (t, layer, column) order
-  //    so the optional int64 write is contiguous
-  for (int e = tid; e < ntok * NC; e += kThreads) {
-    const int t = e / NC;
-    const int j = e - t * NC;
-    const int l = j / C;
-    const int col = j - l * C;
-    int64_t h = -1;
-    if (row_ok) {
+  // 3. hash ids: floored mod by the column's prime plus its offset. Thread -> (column j, token t)
+  //    with j fixed per thread, so consecutive threads write consecutive int64 of the optional
+  //    [B, L, layer, column] output; rowidx is compact and layer-major ([l][t][col]), i.e. in the
+  //    order of each layer's contiguous output rows.
+  if (NC <= nthr) {
+    const int j = tid % NC;
+    const int tstep = nthr / NC;
+    if (tid < tstep * NC) {
+      const int l = j / C;
+      const int col = j - l * C;
+      const int i = col / H;
       const ColParam cp = cols_s[j];
-      h = floored_mod(roll_s[(t * NL + l) * (N - 1) + col / H], cp) + cp.offset;
+      for (int t = tid / NC; t < ntok; t += tstep) {
+        int64_t h = -1;
+        if (row_ok) h = floored_mod(roll_s[(t * NL + l) * (N - 1) + i], cp) + cp.offset;
+        if (a.hashes != nullptr) a.hashes[((int64_t)b * L + t0 + t) * NC + j] = h;
+        if (want_rowidx) rowidx_s[(l * ntok + t) * C + col] = h;
+      }
     }
-    if (a.hashes != nullptr) a.hashes[((int64_t)b * L + t0 + t) * NC + j] = h;
-    if (GATHER) rowidx_s[(l * tile + t) * C + col] = h;
+  } else {
+    for (int e = tid; e < ntok * NC; e += nthr) {
+      const int t = e / NC;
+      const int j = e - t * NC;
+      const int l = j / C;
+      const int col = j - l * C;
+      int64_t h = -1;
+      if (row_ok) {
+        const ColParam cp = cols_s[j];
+        h = floored_mod(roll_s[(t * NL + l) * (N - 1) + col / H], cp) + cp.offset;
+      }
+      if (a.hashes != nullptr) a.hashes[((int64_t)b * L + t0 + t) * NC + j] = h;
+      if (want_rowidx) rowidx_s[(l * ntok + t) * C + col] = h;
+    }
   }
+  return row_ok;
+}
+
+// ------------------------------------------------------------------------------------------------
+// fused kernel: hash a tile, then (GATHER) stream its rows through registers.
+// grid = (ceil(L / tile), B); one CTA = `tile` consecutive tokens of sequence b.
+// D = head_dim (compile time); G = D / 16 lanes per output row. Unused when GATHER is false.
+template <bool GATHER, int D, bool ONE>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateView sv, const CallArgs a, const int tile) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ unsigned int flags_s;
+  const int NL = sv.n_layers, C = sv.n_cols;
+  const SmemPlan plan = smem_plan(NL, sv.max_ngram, C, tile, GATHER);
+  const int64_t* rowidx_s = reinterpret_cast<const int64_t*>(smem + plan.rowidx_off);
+  const int tid = threadIdx.x;
+  const int b = blockIdx.y;
+  const int64_t L = a.L;
+  const int64_t t0 = (int64_t)blockIdx.x * tile;
+  const int ntok = (int)min((int64_t)tile, L - t0);
+  if (tid == 0) flags_s = 0u;
+  __syncthreads();
+  hash_tile(sv, a, smem, plan, tile, b, t0, ntok, GATHER, &flags_s);
 
   if (GATHER) {
     __syncthreads();
-    // 4. gather + dequant: for each layer the tile's ntok*C output rows are contiguous
-    const int D = a.head_dim, blk = a.block, nsc = D / blk;
-    const int rows_per_layer = ntok * C;
-    const int units = NL * rows_per_layer * G;
+    // 4. gather + dequant, one layer at a time: the tile's ntok*C rows of a layer are contiguous in
+    //    its output, in the same order as rowidx, so unit u = (row u/G, lane piece u%G) needs no
+    //    division beyond shifts.
+    constexpr int G = D / 16;
+    const int blk_shift = __ffs(a.block) - 1;
+    const int rpl = ntok * C;
+    const int units = rpl * G;
     const int64_t out_base_row = ((int64_t)b * L + t0) * C;
-    for (int base = tid; base < units; base += kThreads * kUnroll) {
-      RowPiece pc[kUnroll];
-      int ls[kUnroll], rems[kUnroll];
+    for (int l = 0; l < NL; ++l) {
+      const uint8_t* Wl = a.W[l];
+      const float* Sl = a.S[l];
+      const int64_t rows_l = a.rows[l];
+      uint16_t* out_l = a.out[l] + out_base_row * D;
+      const int64_t* rid = rowidx_s + l * rpl;
+      for (int base = tid; base < units; base += kThreads * kUnroll) {
+        RowPiece pc[kUnroll];
 #pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        const int u = base + k * kThreads;
-        ls[k] = -1;
-        if (u < units) {
-          const int v = u / G;
-          const int q = u % G;
-          const int l = v / rows_per_layer;
-          const int rem = v - l * rows_per_layer;
-          const int t = rem / C;
-          const int col = rem - t * C;
-          ls[k] = l;
-          rems[k] = rem;
-          piece_load(pc[k], a.W[l], a.S[l], a.rows[l], rowidx_s[(l * tile + t) * C + col], q, D, blk, nsc);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kUnroll; ++k) {
-        if (ls[k] >= 0) {
+        for (int k = 0; k < kUnroll; ++k) {
           const int u = base + k * kThreads;
-          const int q = u % G;
-          uint16_t* orow = a.out[ls[k]] + (out_base_row + rems[k]) * (int64_t)D;
-          piece_store(pc[k], orow, q, D);
+          if (u < units) piece_load<D, ONE>(pc[k], Wl, Sl, rows_l, rid[u / G], u % G, blk_shift);
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+          const int u = base + k * kThreads;
+          if (u < units) piece_store<D>(pc[k], out_l + (int64_t)(u / G) * D, u % G);
         }
       }
     }
@@ -297,32 +354,25 @@ __global__ void __launch_bounds__(kThreads) hash_kernel(const StateView sv, cons
 // ------------------------------------------------------------------------------------------------
 // standalone lookup: grid-stride over (index, lane) units
 
-template <int G>
+template <int D, bool ONE>
 __global__ void __launch_bounds__(kThreads) lookup_kernel(const int64_t* __restrict__ idx, const int64_t n_idx,
                                                           const uint8_t* __restrict__ W,
                                                           const float* __restrict__ S, const int64_t rows,
-                                                          const int D, const int blk, uint16_t* __restrict__ out) {
-  const int nsc = D / blk;
+                                                          const int blk_shift, uint16_t* __restrict__ out) {
+  constexpr int G = D / 16;
   const int64_t units = n_idx * G;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < units; base += stride * kUnroll) {
     RowPiece pc[kUnroll];
-    int64_t rowid[kUnroll];
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
       const int64_t u = base + k * stride;
-      rowid[k] = -1;
-      if (u < units) {
-        rowid[k] = u / G;
-        piece_load(pc[k], W, S, rows, __ldg(idx + rowid[k]), (int)(u % G), D, blk, nsc);
-      }
+      if (u < units) piece_load<D, ONE>(pc[k], W, S, rows, __ldg(idx + u / G), (int)(u % G), blk_shift);
     }
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
-      if (rowid[k] >= 0) {
-        const int64_t u = base + k * stride;
-        piece_store(pc[k], out + rowid[k] * (int64_t)D, (int)(u % G), D);
-      }
+      const int64_t u = base + k * stride;
+      if (u < units) piece_store<D>(pc[k], out + (u / G) * D, (int)(u % G));
     }
   }
 }
@@ -343,10 +393,10 @@ int sm_count() {
   return n;
 }
 
-template <bool GATHER, int G>
-cudaError_t launch_hash_g(const StateView& sv, const CallArgs& a, int tile, cudaStream_t s) {
+template <bool GATHER, int D, bool ONE>
+cudaError_t launch_hash_k(const StateView& sv, const CallArgs& a, int tile, cudaStream_t s) {
   const SmemPlan plan = smem_plan(sv.n_layers, sv.max_ngram, sv.n_cols, tile, GATHER);
-  auto kern = hash_kernel<GATHER, G>;
+  auto kern = hash_kernel<GATHER, D, ONE>;
   if (plan.bytes > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.bytes);
     if (e != cudaSuccess) return e;
@@ -356,15 +406,27 @@ cudaError_t launch_hash_g(const StateView& sv, const CallArgs& a, int tile, cuda
   return cudaGetLastError();
 }
 
-template <int G>
-cudaError_t launch_lookup_g(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows, int D,
+// a row with a single scale block (block >= head_dim) loads its scale once
+template <bool GATHER, int D>
+cudaError_t launch_hash_g(const StateView& sv, const CallArgs& a, int tile, cudaStream_t s) {
+  if (GATHER && a.block >= D) return launch_hash_k<GATHER, D, true>(sv, a, tile, s);
+  return launch_hash_k<GATHER, D, false>(sv, a, tile, s);
+}
+
+template <int D>
+cudaError_t launch_lookup_g(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
                             int blk, uint16_t* out, cudaStream_t s) {
+  constexpr int G = D / 16;
   const int64_t units = n_idx * G;
   int64_t blocks = (units + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
   const int64_t cap = (int64_t)sm_count() * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  lookup_kernel<G><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, D, blk, out);
+  const int blk_shift = ilog2(blk);
+  if (blk >= D)
+    lookup_kernel<D, true><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
+  else
+    lookup_kernel<D, false><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
   return cudaGetLastError();
 }
 
@@ -379,30 +441,30 @@ cudaError_t launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s
 }
 
 cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s) {
-  return launch_hash_g<false, 1>(sv, a, kHashTile, s);
+  return launch_hash_g<false, 16>(sv, a, kHashTile, s);
 }
 
 cudaError_t launch_hash_lookup(const StateView& sv, const CallArgs& a, cudaStream_t s) {
-  switch (a.head_dim / 16) {
-    case 1: return launch_hash_g<true, 1>(sv, a, kFusedTile, s);
-    case 2: return launch_hash_g<true, 2>(sv, a, kFusedTile, s);
-    case 4: return launch_hash_g<true, 4>(sv, a, kFusedTile, s);
-    case 8: return launch_hash_g<true, 8>(sv, a, kFusedTile, s);
+  switch (a.head_dim) {
     case 16: return launch_hash_g<true, 16>(sv, a, kFusedTile, s);
     case 32: return launch_hash_g<true, 32>(sv, a, kFusedTile, s);
+    case 64: return launch_hash_g<true, 64>(sv, a, kFusedTile, s);
+    case 128: return launch_hash_g<true, 128>(sv, a, kFusedTile, s);
+    case 256: return launch_hash_g<true, 256>(sv, a, kFusedTile, s);
+    case 512: return launch_hash_g<true, 512>(sv, a, kFusedTile, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
                           int32_t head_dim, int32_t block, uint16_t* out, cudaStream_t s) {
-  switch (head_dim / 16) {
-    case 1: return launch_lookup_g<1>(idx, n_idx, W, S, rows, head_dim, block, out, s);
-    case 2: return launch_lookup_g<2>(idx, n_idx, W, S, rows, head_dim, block, out, s);
-    case 4: return launch_lookup_g<4>(idx, n_idx, W, S, rows, head_dim, block, out, s);
-    case 8: return launch_lookup_g<8>(idx, n_idx, W, S, rows, head_dim, block, out, s);
-    case 16: return launch_lookup_g<16>(idx, n_idx, W, S, rows, head_dim, block, out, s);
-    case 32: return launch_lookup_g<32>(idx, n_idx, W, S, rows, head_dim, block, out, s);
+  switch (head_dim) {
+    case 16: return launch_lookup_g<16>(idx, n_idx, W, S, rows, block, out, s);
+    case 32: return launch_lookup_g<32>(idx, n_idx, W, S, rows, block, out, s);
+    case 64: return launch_lookup_g<64>(idx, n_idx, W, S, rows, block, out, s);
+    case 128: return launch_lookup_g<128>(idx, n_idx, W, S, rows, block, out, s);
+    case 256: return launch_lookup_g<256>(idx, n_idx, W, S, rows, block, out, s);
+    case 512: return launch_lookup_g<512>(idx, n_idx, W, S, rows, block, out, s);
     default: return cudaErrorInvalidValue;
   }
 }

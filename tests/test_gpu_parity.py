@@ -205,3 +205,62 @@ def test_decode_per_row_start(prefill_tables):
     seq = np.concatenate([wl.prefill_ids[b, :s], wl.ids[b]])[None]
     h_one = one.hash(H.to_dev(seq), 0)
     assert (h_one[0, -1] == hashes[b, 0]).all()
+
+
+# ----------------------------------------------------------------------------- both fused paths
+def _custom_layout(seed, n_layers, max_ngram, n_heads, D, block, primes=None, vocab=300, cvocab=50):
+    if primes is None:
+        primes = synth.distinct_primes_in(seed, 997, 2003, (n_layers, max_ngram - 1, n_heads))
+    primes = np.asarray(primes, dtype=np.int64).reshape(n_layers, max_ngram - 1, n_heads)
+    return synth.Layout(n_layers, max_ngram, n_heads, D, block, vocab, cvocab,
+                        synth.uniform_int(seed, synth.TAG_TOKEN_MAP, vocab, 0, cvocab),
+                        synth.multipliers(seed, n_layers, max_ngram, full64=True), primes,
+                        synth.column_offsets(primes))
+
+
+def _run_fused_vs_oracle(lay, B, L, rows_override=None, seed=0, with_mask=True):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, lay.raw_vocab, size=(B, L)).astype(np.int64)
+    mask = (rng.random((B, L)) > 0.1) if with_mask else None
+    st = geng.EngramHash(n_layers=lay.n_layers, max_ngram=lay.max_ngram, n_heads=lay.n_heads, head_dim=lay.head_dim,
+                         block=lay.block, max_batch=B, max_seq_len=L, token_map=lay.token_map,
+                         multipliers=lay.multipliers, primes=lay.primes, offsets=lay.offsets)
+    orc = oracle.OracleState.from_layout(lay, B, L)
+    Wh, Sh, Wd, Sd = [], [], [], []
+    for l in range(lay.n_layers):
+        rows = lay.rows[l] if rows_override is None else rows_override[l]
+        W = rng.integers(0, 256, size=(rows, lay.head_dim), dtype=np.uint8)
+        W[W == 0x7F] = 0x7E
+        W[W == 0xFF] = 0xFE
+        S = rng.uniform(0.01, 2.0, size=(rows, lay.head_dim // lay.block)).astype(np.float32)
+        Wh.append(W); Sh.append(S); Wd.append(H.to_dev(W)); Sd.append(H.to_dev(S))
+    hashes = torch.empty((B, L, lay.n_layers, lay.n_cols), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(ids), Wd, Sd, start_pos=0, mask=None if mask is None else H.to_dev(mask),
+                          hashes=hashes)
+    exp_h, _ = orc.hash(ids, 0, mask)
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "fused hashes")
+    for l in range(lay.n_layers):
+        exp = oracle.engram_lookup(exp_h[:, :, l, :], Wh[l], Sh[l], Wh[l].shape[0], lay.head_dim, lay.block)
+        H.assert_bits_equal(H.bf16_bits(outs[l]), exp, f"fused rows layer {l}")
+    assert st.status() == 0
+
+
+@pytest.mark.parametrize("D,block", [(16, 16), (32, 32), (64, 16), (128, 128), (128, 64), (128, 32), (256, 128),
+                                     (512, 128), (512, 64), (128, 8), (256, 16)])
+@pytest.mark.parametrize("L", [1, 33, 100])
+def test_fused_paths_all_shapes(D, block, L):
+    """1, 2 or 4 scales per row take the bulk-copy path; 8 or 16 take the register path."""
+    lay = _custom_layout(D + block, 2, 4, 3, D, block)
+    _run_fused_vs_oracle(lay, 3, L, seed=D * 1000 + block + L)
+
+
+@pytest.mark.parametrize("D,block", [(128, 128), (256, 128), (64, 16), (512, 64)])
+def test_fused_small_tables_edge_rows(D, block):
+    """Bucket ranges of 5 and 7 rows: every row is hit, including the last ones, whose 16-byte scale
+    chunk would run past the scale array; passing tables with fewer rows than the hash range makes
+    the top hash ids out of range (+0 rows)."""
+    lay = _custom_layout(3, 1, 2, 2, D, block, primes=[[[5, 7]]])
+    assert lay.rows == [12]
+    _run_fused_vs_oracle(lay, 2, 200, seed=D)
+    _run_fused_vs_oracle(lay, 2, 200, rows_override=[9], seed=D + 1)
+    _run_fused_vs_oracle(lay, 2, 200, rows_override=[1], seed=D + 2, with_mask=False)
