@@ -44,12 +44,15 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--cfg", type=int, default=3, choices=[1, 2, 3, 4, 5],
+    p.add_argument("--cfg", type=int, default=3, choices=[1, 2, 3, 4, 5, 6],
                    help="1 prefill B4xL4096, 2 decode B256xL1, 3 full-scale B8xL8192 (default), 4 long chunked, "
-                        "5 profiling case (prefill shapes, 1 GB tables)")
+                        "5 profiling case (prefill shapes, 1 GB tables), 6 full-scale with head_dim 256")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end loop (default min(K, 100))")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--graph", action="store_true",
+                   help="capture the steps in a CUDA graph and replay it (removes host launch overhead; for the "
+                        "small decode / chunk launches)")
     return p.parse_args(argv)
 
 
@@ -412,9 +415,26 @@ def run_ours(args):
     flags = runner.state.status()
 
     clocks = ClockSampler(local)
-    clocks.start()
-    total, mean_launch = time_region(torch, dist, local, runner.step, K, stream, per_launch_events=True)
-    clocks.stop()
+    if args.graph:
+        # one graph holds one step per distinct id batch; a replay runs them all
+        per_graph = len(runner.ids)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for k in range(per_graph):
+                runner.step(k)
+        for _ in range(3):
+            graph.replay()
+        replays = max(1, -(-K // per_graph))
+        K = replays * per_graph
+        stream = torch.cuda.current_stream(device)
+        clocks.start()
+        total, _ = time_region(torch, dist, local, lambda k: graph.replay(), replays, stream)
+        clocks.stop()
+        mean_launch = total / K
+    else:
+        clocks.start()
+        total, mean_launch = time_region(torch, dist, local, runner.step, K, stream, per_launch_events=True)
+        clocks.stop()
     total_max = max_over_ranks(dist, total, device)
     tokens = runner.tokens_per_step * K * world
     value = tokens / total_max
@@ -471,6 +491,7 @@ def run_ours(args):
             "l2": "inputs larger than L2: ~98 GB of tables read at random, 805 MB of bf16 written per step; "
                   f"{len(runner.ids)} distinct id batches cycled",
             "status_flags_after_warmup": flags,
+            "launch": "CUDA graph replay" if args.graph else "eager launches from Python",
         },
         "gathered_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

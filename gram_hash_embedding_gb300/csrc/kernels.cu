@@ -43,7 +43,13 @@ namespace {
 
 constexpr int kThreads = ENGRAM_THREADS;
 constexpr int kUnroll = ENGRAM_UNROLL;          // independent row pieces in flight per thread
-constexpr int kFusedTile = ENGRAM_FUSED_TILE;   // tokens per CTA, fused kernel
+#ifndef ENGRAM_TARGET_CTAS
+#define ENGRAM_TARGET_CTAS 1216
+#endif
+
+constexpr int kFusedTile = ENGRAM_FUSED_TILE;   // largest tile (tokens per CTA) of the fused kernel
+constexpr int kTargetCtas = ENGRAM_TARGET_CTAS; // fused grid size the tile choice aims for (2 waves)
+constexpr int kMinFusedTile = 4;                // below 4 tokens the halo and hash phase dominate
 constexpr int kHashTile = 64;                   // tokens per CTA, hash-only kernel
 constexpr int kMinBlocks = ENGRAM_MIN_BLOCKS;   // occupancy hint for the fused kernel
 
@@ -317,32 +323,38 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
 
   if (GATHER) {
     __syncthreads();
-    // 4. gather + dequant, one layer at a time: the tile's ntok*C rows of a layer are contiguous in
-    //    its output, in the same order as rowidx, so unit u = (row u/G, lane piece u%G) needs no
-    //    division beyond shifts.
+    // 4. gather + dequant. Units run over all layers at once (so a short tile, e.g. one decode
+    //    token, issues every layer's row loads in one batch); within a layer the tile's ntok*C rows
+    //    are contiguous in its output and in rowidx, so unit u = (row u/G, piece u%G) needs only
+    //    shifts, and its layer is found by comparison.
     constexpr int G = D / 16;
     const int blk_shift = __ffs(a.block) - 1;
     const int rpl = ntok * C;
-    const int units = rpl * G;
+    const int upl = rpl * G;  // units per layer
+    const int units = NL * upl;
     const int64_t out_base_row = ((int64_t)b * L + t0) * C;
-    for (int l = 0; l < NL; ++l) {
-      const uint8_t* Wl = a.W[l];
-      const float* Sl = a.S[l];
-      const int64_t rows_l = a.rows[l];
-      uint16_t* out_l = a.out[l] + out_base_row * D;
-      const int64_t* rid = rowidx_s + l * rpl;
-      for (int base = tid; base < units; base += kThreads * kUnroll) {
-        RowPiece pc[kUnroll];
+    for (int base = tid; base < units; base += kThreads * kUnroll) {
+      RowPiece pc[kUnroll];
+      uint16_t* orow[kUnroll];
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-          const int u = base + k * kThreads;
-          if (u < units) piece_load<D, ONE>(pc[k], Wl, Sl, rows_l, rid[u / G], u % G, blk_shift);
+      for (int k = 0; k < kUnroll; ++k) {
+        int u = base + k * kThreads;
+        orow[k] = nullptr;
+        if (u < units) {
+          int l = 0;
+          while (u >= upl) {
+            u -= upl;
+            ++l;
+          }
+          const int r = u / G;
+          orow[k] = a.out[l] + (out_base_row + r) * D;
+          piece_load<D, ONE>(pc[k], a.W[l], a.S[l], a.rows[l], rowidx_s[l * rpl + r], u % G, blk_shift);
         }
+      }
 #pragma unroll
-        for (int k = 0; k < kUnroll; ++k) {
-          const int u = base + k * kThreads;
-          if (u < units) piece_store<D>(pc[k], out_l + (int64_t)(u / G) * D, u % G);
-        }
+      for (int k = 0; k < kUnroll; ++k) {
+        const int u = base + k * kThreads;
+        if (orow[k] != nullptr) piece_store<D>(pc[k], orow[k], u % G);
       }
     }
   }
@@ -444,14 +456,27 @@ cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s) 
   return launch_hash_g<false, 16>(sv, a, kHashTile, s);
 }
 
+// Tokens per CTA of the fused kernel: the largest power of two in [kMinFusedTile, kFusedTile] that
+// still gives about kTargetCtas CTAs, so small launches (one 8K-token chunk, a 16K-token prefill) fill several
+// waves instead of leaving SMs idle; a smaller tile only re-reads a (max_ngram-1)-token halo more.
+int fused_tile(const CallArgs& a) {
+#ifdef ENGRAM_FIXED_TILE
+  return ENGRAM_FIXED_TILE;
+#endif
+  int tile = kFusedTile;
+  while (tile > kMinFusedTile && (int64_t)a.B * ((a.L + tile - 1) / tile) < kTargetCtas) tile >>= 1;
+  return tile;
+}
+
 cudaError_t launch_hash_lookup(const StateView& sv, const CallArgs& a, cudaStream_t s) {
+  const int tile = fused_tile(a);
   switch (a.head_dim) {
-    case 16: return launch_hash_g<true, 16>(sv, a, kFusedTile, s);
-    case 32: return launch_hash_g<true, 32>(sv, a, kFusedTile, s);
-    case 64: return launch_hash_g<true, 64>(sv, a, kFusedTile, s);
-    case 128: return launch_hash_g<true, 128>(sv, a, kFusedTile, s);
-    case 256: return launch_hash_g<true, 256>(sv, a, kFusedTile, s);
-    case 512: return launch_hash_g<true, 512>(sv, a, kFusedTile, s);
+    case 16: return launch_hash_g<true, 16>(sv, a, tile, s);
+    case 32: return launch_hash_g<true, 32>(sv, a, tile, s);
+    case 64: return launch_hash_g<true, 64>(sv, a, tile, s);
+    case 128: return launch_hash_g<true, 128>(sv, a, tile, s);
+    case 256: return launch_hash_g<true, 256>(sv, a, tile, s);
+    case 512: return launch_hash_g<true, 512>(sv, a, tile, s);
     default: return cudaErrorInvalidValue;
   }
 }

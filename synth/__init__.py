@@ -414,6 +414,10 @@ def make_layout(kind: str, seed: int, full64: bool = False) -> Layout:
         primes = layered_primes(FULL_SCALE_PRIME_START, 2, 4, 8)
     elif kind == "profile":  # same shapes, ~0.5 GB per layer: small enough for a full ncu capture
         primes = layered_primes(160_000, 2, 4, 8)
+    elif kind == "full256":  # the released table sizes and head_dim (2 fp32 scales per row)
+        primes = layered_primes(FULL_SCALE_PRIME_START, 2, 4, 8)
+        return Layout(2, 4, 8, 256, 128, RAW_VOCAB, COMPRESSED_VOCAB, token_map(seed), multipliers(seed, 2, 4, full64),
+                      primes, column_offsets(primes))
     else:
         raise ValueError(kind)
     return Layout(2, 4, 8, 128, 128, RAW_VOCAB, COMPRESSED_VOCAB, token_map(seed), multipliers(seed, 2, 4, full64),
@@ -458,6 +462,11 @@ def make_workload(cfg: int, seed: int = MASTER_SEED, full64: bool = False) -> Wo
         # same full-scale tables as configuration 3
         return Workload("long chunked B1x65536 (8x8192)", lay, 1, Lc, ids.reshape(1, total), mask.reshape(1, total),
                         np.zeros(1, np.int32), seed + 3, 1, total, chunks=chunks)
+    if cfg == 6:  # released head_dim: full-scale tables of 256 fp8 values per row (~197 GB + 6 GB of scales)
+        lay = make_layout("full256", s, full64)
+        B, L = 8, 8192
+        ids = uniform_ids(s, B * L).reshape(B, L)
+        return Workload("full-scale head_dim 256 B8xL8192", lay, B, L, ids, None, np.zeros(B, np.int32), s, B, L)
     if cfg == 5:  # profiling case: prefill shapes on ~1 GB of tables (still far above L2)
         lay = make_layout("profile", s, full64)
         B, L = 4, 4096

@@ -264,3 +264,29 @@ def test_fused_small_tables_edge_rows(D, block):
     _run_fused_vs_oracle(lay, 2, 200, seed=D)
     _run_fused_vs_oracle(lay, 2, 200, rows_override=[9], seed=D + 1)
     _run_fused_vs_oracle(lay, 2, 200, rows_override=[1], seed=D + 2, with_mask=False)
+
+
+def test_fused_call_replays_from_a_cuda_graph():
+    """The fused call allocates nothing and never synchronises, so it can be captured once and
+    replayed; the replay recomputes the same cache writes, hash ids and rows."""
+    wl = synth.make_workload(0, full64=True)
+    st, orc = H.make_state(wl), H.make_oracle(wl)
+    Ws, Ss = H.device_tables(wl)
+    ids = H.to_dev(wl.ids)
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hashes = torch.full((1, 64, 1, 6), -7, dtype=torch.int64, device="cuda")
+    outs = [torch.zeros((1, 64, 6, 32), dtype=torch.bfloat16, device="cuda")]
+    st.hash_lookup(ids, Ws, Ss, start_pos=start, out=outs, hashes=hashes)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st.hash_lookup(ids, Ws, Ss, start_pos=start, out=outs, hashes=hashes)
+    hashes.fill_(-7)
+    outs[0].zero_()
+    st.reset()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    exp_h, _ = orc.hash(wl.ids, 0)
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "graph hashes")
+    H.assert_bits_equal(H.bf16_bits(outs[0]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]), "graph rows")
