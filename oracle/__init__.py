@@ -54,6 +54,9 @@ def _bind(path: str):
     lib.oracle_floor_mod.restype = _I
     lib.oracle_engram_hash.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _P, _P]
     lib.oracle_engram_hash.restype = ctypes.c_int
+    lib.oracle_engram_hash_varlen.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I,
+                                              _P, _P]
+    lib.oracle_engram_hash_varlen.restype = ctypes.c_int
     lib.oracle_engram_lookup.argtypes = [_P, _I, _P, _P, _I, _I, _I, _P]
     lib.oracle_engram_lookup.restype = ctypes.c_int
     return lib
@@ -131,6 +134,26 @@ class OracleState:
             self.max_batch, self.max_seq_len, _ptr(ids), _ptr(m), _ptr(sp), B, L, _ptr(out), ctypes.byref(flags))
         if rc != 0:
             raise ValueError(f"oracle_engram_hash rejected its arguments ({rc})")
+        return out, flags.value
+
+
+    def hash_varlen(self, ids, cu_seqlens, start_pos, mask=None):
+        """Packed sequences: ids int64 [T]; cu_seqlens [B+1]; start_pos [B]; mask bool [T] or None.
+        Sequence b uses cache row b. Returns (hashes int64 [T, n_layers, C], flags)."""
+        ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
+        cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64).reshape(-1)
+        B = cu.size - 1
+        sp = np.ascontiguousarray(np.broadcast_to(np.asarray(start_pos, dtype=np.int64), (B,)))
+        m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
+        out = np.empty((ids.size, self.n_layers, self.n_cols), dtype=np.int64)
+        flags = ctypes.c_uint32(0)
+        rc = self.lib.oracle_engram_hash_varlen(
+            self.n_layers, self.max_ngram, self.n_heads, _ptr(self.token_map), self.token_map.size, self.dead,
+            self.pad_id, _ptr(self.multipliers), _ptr(self.primes), _ptr(self.offsets), _ptr(self.cache),
+            self.max_batch, self.max_seq_len, _ptr(ids), _ptr(m), _ptr(cu), _ptr(sp), B, _ptr(out),
+            ctypes.byref(flags))
+        if rc != 0:
+            raise ValueError(f"oracle_engram_hash_varlen rejected its arguments ({rc})")
         return out, flags.value
 
 

@@ -84,8 +84,70 @@ int64_t oracle_floor_mod(int64_t x, int64_t p) {
 
 /* ---------------------------------------------------------------- n-gram hash */
 
+/* One sequence: L tokens that sit at positions s .. s+L-1 of the cache row `cache_row`
+ * (cache_len positions). ids/mask/hashes point at the sequence's first token; hashes is
+ * [L][n_layers][C]. Returns the status flags it raised. */
+static uint32_t hash_sequence(int64_t n_layers, int64_t max_ngram, int64_t n_heads, const int64_t* token_map,
+                              int64_t raw_vocab, int64_t dead, int64_t pad_id, const int64_t* multipliers,
+                              const int64_t* primes, const int64_t* offsets, int64_t* cache_row, int64_t cache_len,
+                              const int64_t* ids, const uint8_t* mask, int64_t s, int64_t L, int64_t* hashes) {
+  const int64_t C = (max_ngram - 1) * n_heads;
+  uint32_t fl = 0;
+  const int row_ok = (s >= 0 && s <= cache_len - L);
+  if (!row_ok) {
+    for (int64_t t = 0; t < L; ++t)
+      for (int64_t j = 0; j < n_layers * C; ++j) hashes[t * n_layers * C + j] = -1;
+    return ORACLE_FLAG_BAD_START;
+  }
+
+  /* compressed = token_map[input_ids]; masked tokens become DEAD */
+  /* cache[b, s : s + L] = compressed */
+  for (int64_t t = 0; t < L; ++t) {
+    const int64_t id = ids[t];
+    int64_t c;
+    if (id < 0 || id >= raw_vocab) {
+      fl |= ORACLE_FLAG_BAD_ID;
+      c = dead;
+    } else {
+      c = token_map[id];
+    }
+    if (mask != NULL && !mask[t]) c = dead;
+    cache_row[s + t] = c;
+  }
+
+  /* one token at a time: lookback with cumulative blocking, then the hash */
+  for (int64_t t = 0; t < L; ++t) {
+    const int64_t pos = s + t;
+    int64_t tokens[64];
+    int blocked = 0;
+    for (int64_t shift = 0; shift < max_ngram; ++shift) {
+      const int64_t src_pos = pos - shift < 0 ? 0 : pos - shift; /* clamp_min(0) */
+      const int64_t source = cache_row[src_pos];
+      blocked = blocked || (pos < shift) || (source == dead);
+      tokens[shift] = blocked ? pad_id : source;
+    }
+    for (int64_t l = 0; l < n_layers; ++l) {
+      /* products = tokens * multipliers (int64, wrapping) */
+      uint64_t products[64];
+      for (int64_t k = 0; k < max_ngram; ++k)
+        products[k] = (uint64_t)tokens[k] * (uint64_t)multipliers[l * max_ngram + k];
+      uint64_t rolling = products[0];
+      for (int64_t i = 1; i < max_ngram; ++i) {
+        rolling ^= products[i];
+        for (int64_t h = 0; h < n_heads; ++h) {
+          const int64_t p = primes[(l * (max_ngram - 1) + (i - 1)) * n_heads + h];
+          const int64_t col = (i - 1) * n_heads + h;
+          const int64_t x = (int64_t)rolling; /* two's complement reinterpretation */
+          hashes[(t * n_layers + l) * C + col] = oracle_floor_mod(x, p) + offsets[l * C + col];
+        }
+      }
+    }
+  }
+  return fl;
+}
+
 /* hashes[B][L][n_layers][C], C = (max_ngram - 1) * n_heads.
- * cache[cache_rows][cache_len] int64 holds compressed tokens across calls.
+ * cache[cache_rows][cache_len] int64 holds compressed tokens across calls; sequence b uses row b.
  * multipliers[n_layers][max_ngram], primes[n_layers][max_ngram-1][n_heads],
  * offsets[n_layers][C]. mask may be NULL (every token takes part). */
 int oracle_engram_hash(int64_t n_layers, int64_t max_ngram, int64_t n_heads,
@@ -98,60 +160,33 @@ int oracle_engram_hash(int64_t n_layers, int64_t max_ngram, int64_t n_heads,
   if (B > cache_rows) return ORACLE_EINVAL;
   const int64_t C = (max_ngram - 1) * n_heads;
   uint32_t fl = 0;
-
   for (int64_t b = 0; b < B; ++b) {
-    const int64_t s = start_pos[b];
-    const int row_ok = (s >= 0 && s <= cache_len - L);
-    if (!row_ok) {
-      fl |= ORACLE_FLAG_BAD_START;
-      for (int64_t t = 0; t < L; ++t)
-        for (int64_t j = 0; j < n_layers * C; ++j) hashes[(b * L + t) * n_layers * C + j] = -1;
-      continue;
-    }
+    fl |= hash_sequence(n_layers, max_ngram, n_heads, token_map, raw_vocab, dead, pad_id, multipliers, primes,
+                        offsets, cache + b * cache_len, cache_len, ids + b * L, mask ? mask + b * L : NULL,
+                        start_pos[b], L, hashes + b * L * n_layers * C);
+  }
+  if (flags) *flags |= fl;
+  return ORACLE_OK;
+}
 
-    /* compressed = token_map[input_ids]; masked tokens become DEAD */
-    /* cache[b, s : s + L] = compressed */
-    for (int64_t t = 0; t < L; ++t) {
-      const int64_t id = ids[b * L + t];
-      int64_t c;
-      if (id < 0 || id >= raw_vocab) {
-        fl |= ORACLE_FLAG_BAD_ID;
-        c = dead;
-      } else {
-        c = token_map[id];
-      }
-      if (mask != NULL && !mask[b * L + t]) c = dead;
-      cache[b * cache_len + s + t] = c;
-    }
-
-    /* one token at a time: lookback with cumulative blocking, then the hash */
-    for (int64_t t = 0; t < L; ++t) {
-      const int64_t pos = s + t;
-      int64_t tokens[64];
-      int blocked = 0;
-      for (int64_t shift = 0; shift < max_ngram; ++shift) {
-        const int64_t src_pos = pos - shift < 0 ? 0 : pos - shift; /* clamp_min(0) */
-        const int64_t source = cache[b * cache_len + src_pos];
-        blocked = blocked || (pos < shift) || (source == dead);
-        tokens[shift] = blocked ? pad_id : source;
-      }
-      for (int64_t l = 0; l < n_layers; ++l) {
-        /* products = tokens * multipliers (int64, wrapping) */
-        uint64_t products[64];
-        for (int64_t k = 0; k < max_ngram; ++k)
-          products[k] = (uint64_t)tokens[k] * (uint64_t)multipliers[l * max_ngram + k];
-        uint64_t rolling = products[0];
-        for (int64_t i = 1; i < max_ngram; ++i) {
-          rolling ^= products[i];
-          for (int64_t h = 0; h < n_heads; ++h) {
-            const int64_t p = primes[(l * (max_ngram - 1) + (i - 1)) * n_heads + h];
-            const int64_t col = (i - 1) * n_heads + h;
-            const int64_t x = (int64_t)rolling; /* two's complement reinterpretation */
-            hashes[((b * L + t) * n_layers + l) * C + col] = oracle_floor_mod(x, p) + offsets[l * C + col];
-          }
-        }
-      }
-    }
+/* Packed sequences: sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of ids/mask/hashes
+ * (hashes [T][n_layers][C]) and uses cache row b from position start_pos[b]. */
+int oracle_engram_hash_varlen(int64_t n_layers, int64_t max_ngram, int64_t n_heads,
+                              const int64_t* token_map, int64_t raw_vocab, int64_t dead, int64_t pad_id,
+                              const int64_t* multipliers, const int64_t* primes, const int64_t* offsets,
+                              int64_t* cache, int64_t cache_rows, int64_t cache_len,
+                              const int64_t* ids, const uint8_t* mask, const int64_t* cu_seqlens,
+                              const int64_t* start_pos, int64_t B, int64_t* hashes, uint32_t* flags) {
+  if (n_layers < 1 || max_ngram < 2 || max_ngram > 64 || n_heads < 1 || B < 0) return ORACLE_EINVAL;
+  if (B > cache_rows) return ORACLE_EINVAL;
+  const int64_t C = (max_ngram - 1) * n_heads;
+  uint32_t fl = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t begin = cu_seqlens[b], L = cu_seqlens[b + 1] - cu_seqlens[b];
+    if (L < 0) return ORACLE_EINVAL;
+    fl |= hash_sequence(n_layers, max_ngram, n_heads, token_map, raw_vocab, dead, pad_id, multipliers, primes,
+                        offsets, cache + b * cache_len, cache_len, ids + begin, mask ? mask + begin : NULL,
+                        start_pos[b], L, hashes + begin * n_layers * C);
   }
   if (flags) *flags |= fl;
   return ORACLE_OK;

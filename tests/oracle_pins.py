@@ -285,5 +285,38 @@ def pin_invariants(L=None):
     assert np.array_equal(st.cache[0], snap[0])
 
 
+def pin_varlen(L=None):
+    """Packed ragged sequences (lengths 0, 1, 5, 17, 40 at different starts) against the brute
+    force, and equal-length packs against the dense call."""
+    lay = synth.make_layout("tiny", 41, full64=True)
+    lens = [5, 0, 17, 1, 40]
+    starts = [0, 3, 6, 9, 2]
+    B = len(lens)
+    rng = np.random.default_rng(41)
+    total = 60
+    full_ids = rng.integers(0, lay.raw_vocab, size=(B, total))
+    full_mask = rng.random((B, total)) > 0.15
+    hist = _history_rows(full_ids, full_mask, lay)
+    st = oracle.OracleState.from_layout(lay, B, 64, L)
+    # history before each start, written with the dense call
+    st.hash(full_ids[:, :max(starts)], 0, full_mask[:, :max(starts)])
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    ids = np.concatenate([full_ids[b, starts[b]:starts[b] + lens[b]] for b in range(B)])
+    mask = np.concatenate([full_mask[b, starts[b]:starts[b] + lens[b]] for b in range(B)])
+    got, _ = st.hash_varlen(ids, cu, starts, mask)
+    for b in range(B):
+        h = {q: v for q, v in hist[b].items() if q < starts[b] + lens[b]}
+        for t in range(lens[b]):
+            assert got[cu[b] + t].tolist() == brute.hashes_at(h, starts[b] + t, lay), ("varlen", b, t)
+    # equal lengths: the packed call equals the dense call
+    d1 = oracle.OracleState.from_layout(lay, 3, 64, L)
+    d2 = oracle.OracleState.from_layout(lay, 3, 64, L)
+    dense, _ = d1.hash(full_ids[:3, :20], [0, 4, 7], full_mask[:3, :20])
+    packed, _ = d2.hash_varlen(full_ids[:3, :20].reshape(-1), [0, 20, 40, 60], [0, 4, 7],
+                               full_mask[:3, :20].reshape(-1))
+    assert np.array_equal(dense.reshape(60, lay.n_layers, -1), packed)
+    assert np.array_equal(d1.cache, d2.cache)
+
+
 ALL_PINS = [pin_floor_mod, pin_fp8_decode, pin_bf16, pin_lookup_vs_torch, pin_brute_force, pin_closed_forms,
-            pin_invariants]
+            pin_invariants, pin_varlen]

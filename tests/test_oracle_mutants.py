@@ -22,8 +22,8 @@ MUTANTS = {
     "no_dead_block": ("blocked || (pos < shift) || (source == dead)", "blocked || (pos < shift)"),
     "non_cumulative_block": ("blocked = blocked || (pos < shift)", "blocked = (pos < shift)"),
     "pad_swapped": ("tokens[shift] = blocked ? pad_id : source;", "tokens[shift] = blocked ? source : pad_id;"),
-    "mask_to_pad": ("if (mask != NULL && !mask[b * L + t]) c = dead;", "if (mask != NULL && !mask[b * L + t]) c = pad_id;"),
-    "mask_ignored": ("if (mask != NULL && !mask[b * L + t]) c = dead;", ""),
+    "mask_to_pad": ("if (mask != NULL && !mask[t]) c = dead;", "if (mask != NULL && !mask[t]) c = pad_id;"),
+    "mask_ignored": ("if (mask != NULL && !mask[t]) c = dead;", ""),
     "xor_as_add": ("rolling ^= products[i];", "rolling += products[i];"),
     "first_product_dropped": ("uint64_t rolling = products[0];", "uint64_t rolling = 0;"),
     "multiplier_index": ("multipliers[l * max_ngram + k]", "multipliers[k]"),
@@ -34,7 +34,9 @@ MUTANTS = {
     "truncated_mod": ("if (r != 0 && ((r < 0) != (p < 0))) r += p;", ""),
     "mod_sign_flipped": ("if (r != 0 && ((r < 0) != (p < 0))) r += p;", "if (r != 0 && ((r < 0) != (p < 0))) r -= p;"),
     "unsigned_mod": ("const int64_t x = (int64_t)rolling;", "const int64_t x = (int64_t)(rolling >> 1);"),
-    "cache_write_shift": ("cache[b * cache_len + s + t] = c;", "cache[b * cache_len + t] = c;"),
+    "cache_write_shift": ("cache_row[s + t] = c;", "cache_row[t] = c;"),
+    "varlen_offset_dropped": ("ids + begin, mask ? mask + begin : NULL", "ids, mask"),
+    "varlen_cache_row": ("offsets, cache + b * cache_len, cache_len, ids + begin", "offsets, cache, cache_len, ids + begin"),
     "fp8_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "fp8_subnormal": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     "fp8_mantissa": ("1.0 + (double)m / 8.0", "1.0 + (double)m / 16.0"),
