@@ -25,13 +25,15 @@ from ._build import build
 
 __all__ = [
     "EngramError", "EngramHash", "build", "engram_state_create", "engram_state_destroy", "engram_cache_reset",
-    "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_strerror",
-    "STATUS_BAD_START", "STATUS_BAD_ID", "library_path",
+    "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
+    "engram_hash_lookup_varlen", "engram_strerror", "STATUS_BAD_START", "STATUS_BAD_ID", "STATUS_BAD_LENGTH",
+    "library_path",
 ]
 
 OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 STATUS_BAD_START = 1
 STATUS_BAD_ID = 2
+STATUS_BAD_LENGTH = 4
 MAX_LAYERS = 8
 
 
@@ -71,11 +73,14 @@ def _lib():
         L.engram_hash.argtypes = [_P, _P, _P, _P, _I32, _I64, _P, _P]
         L.engram_lookup.argtypes = [_P, _I64, _P, _P, _I64, _I32, _I32, _P, _P]
         L.engram_hash_lookup.argtypes = [_P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _P, _P]
+        L.engram_hash_varlen.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P]
+        L.engram_hash_lookup_varlen.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _P]
         L.engram_state_layout.argtypes = [_P, ctypes.POINTER(_Layout)]
         L.engram_strerror.argtypes = [ctypes.c_int]
         L.engram_strerror.restype = ctypes.c_char_p
         for name in ("engram_state_create", "engram_state_destroy", "engram_cache_reset", "engram_state_status",
-                     "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout"):
+                     "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout",
+                     "engram_hash_varlen", "engram_hash_lookup_varlen"):
             getattr(L, name).restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -217,6 +222,60 @@ def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: lis
     return out
 
 
+def _max_len(cu_seqlens: torch.Tensor, max_len) -> int:
+    if max_len is not None:
+        return int(max_len)
+    # convenience only: reads the extents back (a device-to-host copy); pass max_len to avoid it
+    return int((cu_seqlens[1:] - cu_seqlens[:-1]).max().item()) if cu_seqlens.numel() > 1 else 0
+
+
+def engram_hash_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, start_pos: torch.Tensor,
+                       mask: torch.Tensor | None = None, hashes: torch.Tensor | None = None, max_len: int | None = None,
+                       stream=None) -> torch.Tensor:
+    """Packed sequences: ids int64 [T]; cu_seqlens int32 [B+1]; start_pos int32 [B]; mask [T] or None.
+    Returns (or fills) int64 hash ids [T, n_layers, C]."""
+    T = ids.numel()
+    B = cu_seqlens.numel() - 1
+    if hashes is None:
+        lay = engram_state_layout(state)
+        hashes = torch.empty((T, lay["n_layers"], (lay["max_ngram"] - 1) * lay["n_heads"]), dtype=torch.int64,
+                             device=ids.device)
+    m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+    _check(_lib().engram_hash_varlen(state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"),
+                                     _dev(start_pos, torch.int32, "start_pos"), B, T, _max_len(cu_seqlens, max_len),
+                                     _dev(hashes, torch.int64, "hashes"), _stream(stream)), "engram_hash_varlen")
+    return hashes
+
+
+def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, start_pos: torch.Tensor,
+                              W: list, S: list, mask: torch.Tensor | None = None, out: list | None = None,
+                              hashes: torch.Tensor | None = None, max_len: int | None = None, stream=None) -> list:
+    """Packed sequences, hash + per-layer lookup in one launch. Returns (or fills) per-layer bf16
+    outputs [T, C, D]."""
+    T = ids.numel()
+    B = cu_seqlens.numel() - 1
+    n = len(W)
+    if n != len(S) or n > MAX_LAYERS:
+        raise ValueError("W and S need one entry per engram layer")
+    D = W[0].shape[1]
+    if out is None:
+        lay = engram_state_layout(state)
+        C = (lay["max_ngram"] - 1) * lay["n_heads"]
+        out = [torch.empty((T, C, D), dtype=torch.bfloat16, device=ids.device) for _ in range(n)]
+    m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+    Wp = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
+    Sp = (_P * n)(*[_dev(x, torch.float32, "S") for x in S])
+    Rp = (_I64 * n)(*[w.shape[0] for w in W])
+    Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
+    hp = None if hashes is None else _dev(hashes, torch.int64, "hashes")
+    _check(_lib().engram_hash_lookup_varlen(state, _dev(ids, torch.int64, "ids"), m,
+                                            _dev(cu_seqlens, torch.int32, "cu_seqlens"),
+                                            _dev(start_pos, torch.int32, "start_pos"), B, T,
+                                            _max_len(cu_seqlens, max_len), Wp, Sp, Rp, Op, hp, _stream(stream)),
+           "engram_hash_lookup_varlen")
+    return out
+
+
 # ----------------------------------------------------------------------------- convenience object
 class EngramHash:
     """A state plus the calls that use it (the hash module of the model, with its cache)."""
@@ -260,6 +319,12 @@ class EngramHash:
             out = [torch.empty((B, L, self.n_cols, self.head_dim), dtype=torch.bfloat16, device=ids.device)
                    for _ in range(len(W))]
         return engram_hash_lookup(self.handle, ids, start_pos, W, S, mask, out, hashes)
+
+    def hash_varlen(self, ids, cu_seqlens, start_pos, mask=None, hashes=None, max_len=None):
+        return engram_hash_varlen(self.handle, ids, cu_seqlens, start_pos, mask, hashes, max_len)
+
+    def hash_lookup_varlen(self, ids, cu_seqlens, start_pos, W, S, mask=None, out=None, hashes=None, max_len=None):
+        return engram_hash_lookup_varlen(self.handle, ids, cu_seqlens, start_pos, W, S, mask, out, hashes, max_len)
 
     def lookup(self, idx, W, S, out=None):
         return engram_lookup(idx, W, S, self.block, out)

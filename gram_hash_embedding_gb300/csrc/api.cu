@@ -95,11 +95,29 @@ engram::CallArgs call_args(const engram_state* st, const int64_t* ids, const uin
   a.mask = mask;
   a.start_pos = start_pos;
   a.hashes = hashes;
+  a.cu_seqlens = nullptr;
   a.L = L;
+  a.total = (int64_t)B * L;
   a.B = B;
   a.head_dim = st->lay.head_dim;
   a.block = st->lay.block;
   return a;
+}
+
+// per-layer tables and outputs of a fused call (host arrays of n_layers device pointers)
+int fill_tables(const engram_state* st, const uint8_t* const* W, const float* const* S, const int64_t* rows,
+                uint16_t* const* out, engram::CallArgs* a) {
+  if (W == nullptr || S == nullptr || rows == nullptr || out == nullptr) return ENGRAM_ERR_INVALID;
+  for (int l = 0; l < st->lay.n_layers; ++l) {
+    if (rows[l] < 0 || out[l] == nullptr || !aligned(out[l], 16)) return ENGRAM_ERR_INVALID;
+    if (rows[l] > 0 && (W[l] == nullptr || S[l] == nullptr || !aligned(W[l], 16) || !aligned(S[l], 4)))
+      return ENGRAM_ERR_INVALID;
+    a->W[l] = W[l];
+    a->S[l] = S[l];
+    a->rows[l] = rows[l];
+    a->out[l] = out[l];
+  }
+  return ENGRAM_OK;
 }
 
 }  // namespace
@@ -231,18 +249,56 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
                        uint16_t* const* out, int64_t* hashes, engram_stream_t stream) {
   int rc = check_call(state, ids, mask, start_pos, B, L);
   if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
-  if (W == nullptr || S == nullptr || rows == nullptr || out == nullptr) return ENGRAM_ERR_INVALID;
   if (hashes != nullptr && !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
   engram::CallArgs a = call_args(state, ids, mask, start_pos, B, L, hashes);
-  for (int l = 0; l < state->lay.n_layers; ++l) {
-    if (rows[l] < 0 || out[l] == nullptr || !aligned(out[l], 16)) return ENGRAM_ERR_INVALID;
-    if (rows[l] > 0 && (W[l] == nullptr || S[l] == nullptr || !aligned(W[l], 16) || !aligned(S[l], 4)))
-      return ENGRAM_ERR_INVALID;
-    a.W[l] = W[l];
-    a.S[l] = S[l];
-    a.rows[l] = rows[l];
-    a.out[l] = out[l];
-  }
+  rc = fill_tables(state, W, S, rows, out, &a);
+  if (rc != ENGRAM_OK) return rc;
+  return engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK
+                                                                                          : ENGRAM_ERR_CUDA;
+}
+
+namespace {
+
+// common checks of the packed calls; on success fills *a (without tables)
+int packed_call(const engram_state* st, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
+                const int32_t* start_pos, int32_t B, int64_t T, int64_t max_len, int64_t* hashes,
+                engram::CallArgs* a) {
+  if (st == nullptr || B < 0 || T < 0 || max_len < 0) return ENGRAM_ERR_INVALID;
+  if (B == 0 || T == 0 || max_len == 0) return ENGRAM_OK;
+  if (ids == nullptr || cu_seqlens == nullptr || start_pos == nullptr || !aligned(ids, 8) ||
+      !aligned(cu_seqlens, 4) || !aligned(start_pos, 4))
+    return ENGRAM_ERR_INVALID;
+  if (hashes != nullptr && !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
+  if (B > st->lay.max_batch || max_len > st->lay.max_seq_len) return ENGRAM_ERR_RANGE;
+  if (T > ((int64_t)1 << 31) - 1) return ENGRAM_ERR_UNSUPPORTED;  // int32 extents
+  if (!on_state_device(st)) return ENGRAM_ERR_INVALID;
+  *a = call_args(st, ids, mask, start_pos, B, max_len, hashes);
+  a->cu_seqlens = cu_seqlens;
+  a->total = T;
+  return ENGRAM_OK;
+}
+
+}  // namespace
+
+int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
+                       const int32_t* start_pos, int32_t B, int64_t T, int64_t max_len, int64_t* hashes,
+                       engram_stream_t stream) {
+  if (hashes == nullptr && state != nullptr && B > 0 && T > 0 && max_len > 0) return ENGRAM_ERR_INVALID;
+  engram::CallArgs a;
+  int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, B, T, max_len, hashes, &a);
+  if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
+  return engram::launch_hash(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
+                              const int32_t* cu_seqlens, const int32_t* start_pos, int32_t B, int64_t T,
+                              int64_t max_len, const uint8_t* const* W, const float* const* S, const int64_t* rows,
+                              uint16_t* const* out, int64_t* hashes, engram_stream_t stream) {
+  engram::CallArgs a;
+  int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, B, T, max_len, hashes, &a);
+  if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
+  rc = fill_tables(state, W, S, rows, out, &a);
+  if (rc != ENGRAM_OK) return rc;
   return engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK
                                                                                           : ENGRAM_ERR_CUDA;
 }

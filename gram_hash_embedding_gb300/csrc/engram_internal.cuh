@@ -36,7 +36,9 @@ struct CallArgs {
   const uint8_t* mask;        // may be null
   const int32_t* start_pos;
   int64_t* hashes;            // may be null (fused)
-  int64_t L;
+  const int32_t* cu_seqlens;  // packed calls: [B+1] sequence extents in ids; null for dense [B, L] calls
+  int64_t L;                  // dense: tokens per row; packed: the longest sequence (grid bound)
+  int64_t total;              // packed: tokens in ids (T); dense: B * L
   int32_t B;
   int32_t head_dim, block;
   const uint8_t* W[ENGRAM_MAX_LAYERS];

@@ -185,12 +185,14 @@ __host__ __device__ inline SmemPlan smem_plan(int n_layers, int max_ngram, int n
 }
 
 // ------------------------------------------------------------------------------------------------
-// hash phase of one tile: `ntok` consecutive tokens starting at t0 of sequence b. Called by every
-// thread of the CTA (contains barriers). Fills rowidx (layer-major: [l][t][col]) when given, and the
-// optional int64 hash output. Returns whether the row's start position fits the cache.
+// hash phase of one tile: `ntok` consecutive tokens starting at t0 of sequence b, whose Lb tokens
+// start at element seq_off of ids / mask / hashes and use cache row b. Called by every thread of
+// the CTA (contains barriers). Fills rowidx (layer-major: [l][t][col]) when given, and the optional
+// int64 hash output. Returns whether the sequence's start position fits the cache.
 __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a, unsigned char* smem,
-                                          const SmemPlan& plan, const int tile, const int b, const int64_t t0,
-                                          const int ntok, const bool want_rowidx, unsigned int* flags_s) {
+                                          const SmemPlan& plan, const int tile, const int b, const int64_t seq_off,
+                                          const int64_t Lb, const int64_t t0, const int ntok, const bool want_rowidx,
+                                          unsigned int* flags_s) {
   const int N = sv.max_ngram, NL = sv.n_layers, C = sv.n_cols, H = sv.n_heads;
   const int NC = NL * C;
   ColParam* cols_s = reinterpret_cast<ColParam*>(smem + plan.cols_off);
@@ -199,9 +201,8 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
   int64_t* rowidx_s = reinterpret_cast<int64_t*>(smem + plan.rowidx_off);
   int32_t* tok_s = reinterpret_cast<int32_t*>(smem + plan.tok_off);
   const int tid = threadIdx.x, nthr = blockDim.x;
-  const int64_t L = a.L;
   const int64_t s_b = (int64_t)a.start_pos[b];
-  const bool row_ok = (s_b >= 0) && (s_b <= sv.max_seq_len - L);
+  const bool row_ok = (s_b >= 0) && (s_b <= sv.max_seq_len - Lb);
   const int32_t dead = sv.dead;
   int32_t* cache_row = sv.cache + (int64_t)b * sv.max_seq_len;
 
@@ -217,14 +218,14 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
       const int64_t t = t0 - (N - 1) + j;
       int32_t c;
       if (t >= 0) {
-        const int64_t id = a.ids[(int64_t)b * L + t];
+        const int64_t id = a.ids[seq_off + t];
         if (id < 0 || id >= sv.raw_vocab) {
           c = dead;
           atomicOr(flags_s, ENGRAM_STATUS_BAD_ID);
         } else {
           c = sv.token_map[id];
         }
-        if (a.mask != nullptr && a.mask[(int64_t)b * L + t] == 0) c = dead;
+        if (a.mask != nullptr && a.mask[seq_off + t] == 0) c = dead;
       } else {
         const int64_t p = s_b + t;
         c = (p >= 0) ? cache_row[p] : dead;
@@ -279,7 +280,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
       for (int t = tid / NC; t < ntok; t += tstep) {
         int64_t h = -1;
         if (row_ok) h = floored_mod(roll_s[(t * NL + l) * (N - 1) + i], cp) + cp.offset;
-        if (a.hashes != nullptr) a.hashes[((int64_t)b * L + t0 + t) * NC + j] = h;
+        if (a.hashes != nullptr) a.hashes[(seq_off + t0 + t) * NC + j] = h;
         if (want_rowidx) rowidx_s[(l * ntok + t) * C + col] = h;
       }
     }
@@ -294,7 +295,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
         const ColParam cp = cols_s[j];
         h = floored_mod(roll_s[(t * NL + l) * (N - 1) + col / H], cp) + cp.offset;
       }
-      if (a.hashes != nullptr) a.hashes[((int64_t)b * L + t0 + t) * NC + j] = h;
+      if (a.hashes != nullptr) a.hashes[(seq_off + t0 + t) * NC + j] = h;
       if (want_rowidx) rowidx_s[(l * ntok + t) * C + col] = h;
     }
   }
@@ -314,12 +315,26 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
   const int64_t* rowidx_s = reinterpret_cast<const int64_t*>(smem + plan.rowidx_off);
   const int tid = threadIdx.x;
   const int b = blockIdx.y;
-  const int64_t L = a.L;
+  // sequence b: dense calls hold L tokens per row; packed calls read its extent from cu_seqlens
+  int64_t seq_off, Lb;
+  if (a.cu_seqlens != nullptr) {
+    seq_off = a.cu_seqlens[b];
+    const int64_t end = a.cu_seqlens[b + 1];
+    Lb = end - seq_off;
+    if (seq_off < 0 || end > a.total || Lb < 0 || Lb > a.L) {  // inconsistent extent: nothing is done
+      if (blockIdx.x == 0 && tid == 0) atomicOr(sv.status, ENGRAM_STATUS_BAD_LENGTH);
+      return;
+    }
+  } else {
+    seq_off = (int64_t)b * a.L;
+    Lb = a.L;
+  }
   const int64_t t0 = (int64_t)blockIdx.x * tile;
-  const int ntok = (int)min((int64_t)tile, L - t0);
+  if (t0 >= Lb) return;  // past this sequence's end (packed calls size the grid for the longest)
+  const int ntok = (int)min((int64_t)tile, Lb - t0);
   if (tid == 0) flags_s = 0u;
   __syncthreads();
-  hash_tile(sv, a, smem, plan, tile, b, t0, ntok, GATHER, &flags_s);
+  hash_tile(sv, a, smem, plan, tile, b, seq_off, Lb, t0, ntok, GATHER, &flags_s);
 
   if (GATHER) {
     __syncthreads();
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
     const int rpl = ntok * C;
     const int upl = rpl * G;  // units per layer
     const int units = NL * upl;
-    const int64_t out_base_row = ((int64_t)b * L + t0) * C;
+    const int64_t out_base_row = (seq_off + t0) * C;
     for (int base = tid; base < units; base += kThreads * kUnroll) {
       RowPiece pc[kUnroll];
       uint16_t* orow[kUnroll];
@@ -464,7 +479,11 @@ int fused_tile(const CallArgs& a) {
   return ENGRAM_FIXED_TILE;
 #endif
   int tile = kFusedTile;
-  while (tile > kMinFusedTile && (int64_t)a.B * ((a.L + tile - 1) / tile) < kTargetCtas) tile >>= 1;
+  // CTAs that do work: every row's tiles (dense), or about total/tile + one partial tile per sequence
+  auto active = [&](int t) {
+    return a.cu_seqlens != nullptr ? a.total / t + a.B : (int64_t)a.B * ((a.L + t - 1) / t);
+  };
+  while (tile > kMinFusedTile && active(tile) < kTargetCtas) tile >>= 1;
   return tile;
 }
 

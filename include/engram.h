@@ -57,6 +57,9 @@ typedef struct engram_state engram_state;
 #define ENGRAM_STATUS_BAD_START 1u /* a row's start_pos was < 0 or start_pos + L > max_seq_len: that row wrote
                                       nothing to the cache, its hash ids are -1 and its looked-up rows are +0 */
 #define ENGRAM_STATUS_BAD_ID 2u    /* an input id outside [0, raw_vocab): that token was treated as masked (DEAD) */
+#define ENGRAM_STATUS_BAD_LENGTH 4u /* packed calls: a sequence's extent from cu_seqlens was negative, outside
+                                       [0, T] or longer than max_len: that sequence was skipped entirely (no cache
+                                       write, its hash ids and rows left unwritten) */
 
 /* Library limits. */
 #define ENGRAM_MAX_LAYERS 8       /* n_layers */
@@ -137,6 +140,36 @@ int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const flo
 int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
                        int32_t B, int64_t L, const uint8_t* const* W, const float* const* S, const int64_t* rows,
                        uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
+
+/*
+ * Packed (variable-length) sequences, for continuous batching: B sequences of different lengths are
+ * concatenated into one token array. Sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1,
+ * sits at positions start_pos[b] .. of cache row b, and is hashed exactly as engram_hash would hash
+ * it alone (blocks/stack-hashes page, hash `forward`, applied per sequence).
+ *   ids         device int64 [T] raw token ids
+ *   mask        device uint8 [T] or NULL
+ *   cu_seqlens  device int32 [B+1], non-decreasing, cu_seqlens[0] = 0 and cu_seqlens[B] = T expected
+ *   start_pos   device int32 [B]
+ *   max_len     host: an upper bound on every sequence's length (sizes the grid; max_len <= max_seq_len)
+ *   hashes      device int64 [T][n_layers][C]
+ * A sequence whose extent is inconsistent is skipped and flagged (ENGRAM_STATUS_BAD_LENGTH); a start
+ * position that does not fit is handled as in engram_hash. Extents must not overlap (tokens shared by
+ * two sequences would be written twice). B == 0, T == 0 or max_len == 0 is a no-op.
+ * Errors: _INVALID (null, misaligned, negative sizes), _RANGE (B > max_batch, max_len > max_seq_len).
+ */
+int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
+                       const int32_t* start_pos, int32_t B, int64_t T, int64_t max_len, int64_t* hashes,
+                       engram_stream_t stream);
+
+/*
+ * Packed sequences, hash and lookup in one launch (as engram_hash_lookup): out[l] is device bf16
+ * [T][C][head_dim] for layer l, hashes ([T][n_layers][C]) may be NULL. Other arguments and errors as
+ * engram_hash_varlen and engram_hash_lookup.
+ */
+int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
+                              const int32_t* cu_seqlens, const int32_t* start_pos, int32_t B, int64_t T,
+                              int64_t max_len, const uint8_t* const* W, const float* const* S, const int64_t* rows,
+                              uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
 
 /* Layout the state was created with (host copy). */
 int engram_state_layout(const engram_state* state, engram_layout* layout);

@@ -1,0 +1,97 @@
+"""Packed variable-length sequences (continuous batching) vs the oracle (GPU only)."""
+import numpy as np
+import pytest
+import torch
+
+import gram_hash_embedding_gb300 as geng
+import synth
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    H.build_all()
+    yield
+
+
+def _pack(full_ids, full_mask, lens, starts):
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ids = np.concatenate([full_ids[b, starts[b]:starts[b] + lens[b]] for b in range(len(lens))]).astype(np.int64)
+    mask = np.concatenate([full_mask[b, starts[b]:starts[b] + lens[b]] for b in range(len(lens))])
+    return cu, ids, mask
+
+
+@pytest.mark.parametrize("lens", [[1] * 8, [5, 0, 17, 1, 40, 3, 16, 33], [0, 0, 0, 7], [100, 1, 1, 1, 64, 65, 15, 2]])
+def test_packed_matches_oracle(lens):
+    wl = synth.make_workload(0, full64=True)
+    lay = wl.layout
+    B = len(lens)
+    rng = np.random.default_rng(sum(lens) + B)
+    total = 256
+    full_ids = rng.integers(0, lay.raw_vocab, size=(B, total))
+    full_mask = rng.random((B, total)) > 0.1
+    starts = rng.integers(0, 40, size=B).astype(np.int32)
+    st, orc = H.make_state(wl, B, 512), H.make_oracle(wl, B, 512)
+    Ws, Ss = H.device_tables(wl)
+    # history: every row prefilled up to its start with the dense call
+    pre = int(starts.max())
+    if pre > 0:
+        st.hash(H.to_dev(full_ids[:, :pre]), 0, H.to_dev(full_mask[:, :pre]))
+        orc.hash(full_ids[:, :pre], 0, full_mask[:, :pre])
+    cu, ids, mask = _pack(full_ids, full_mask, lens, starts)
+    T = ids.size
+    hashes = torch.full((T, 1, 6), -9, dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup_varlen(H.to_dev(ids), H.to_dev(cu), H.to_dev(starts), Ws, Ss, mask=H.to_dev(mask),
+                                 hashes=hashes, max_len=max(lens))
+    exp_h, fl = orc.hash_varlen(ids, cu, starts, mask)
+    assert fl == 0 and st.status() == 0
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "packed hashes")
+    H.assert_bits_equal(H.bf16_bits(outs[0]), H.oracle_lookup_rows(wl, 0, exp_h[:, 0, :]), "packed rows")
+    # the hash-only packed call, after a second state replays the same history
+    st2 = H.make_state(wl, B, 512)
+    if pre > 0:
+        st2.hash(H.to_dev(full_ids[:, :pre]), 0, H.to_dev(full_mask[:, :pre]))
+    h2 = st2.hash_varlen(H.to_dev(ids), H.to_dev(cu), H.to_dev(starts), mask=H.to_dev(mask))  # max_len derived
+    H.assert_bits_equal(h2.cpu().numpy(), exp_h, "packed hash-only")
+
+
+def test_packed_equals_dense_for_equal_lengths():
+    wl = synth.make_workload(0)
+    B, L = 4, 48
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, wl.layout.raw_vocab, size=(B, L)).astype(np.int64)
+    starts = np.array([0, 2, 5, 1], dtype=np.int32)
+    a, b = H.make_state(wl, B, 128), H.make_state(wl, B, 128)
+    Ws, Ss = H.device_tables(wl)
+    hd = torch.empty((B, L, 1, 6), dtype=torch.int64, device="cuda")
+    od = a.hash_lookup(H.to_dev(ids), Ws, Ss, start_pos=H.to_dev(starts), hashes=hd)
+    cu = (np.arange(B + 1) * L).astype(np.int32)
+    hp = torch.empty((B * L, 1, 6), dtype=torch.int64, device="cuda")
+    op = b.hash_lookup_varlen(H.to_dev(ids.reshape(-1)), H.to_dev(cu), H.to_dev(starts), Ws, Ss, hashes=hp, max_len=L)
+    assert torch.equal(hd.view(-1), hp.view(-1))
+    assert torch.equal(od[0].view(torch.int16).reshape(-1), op[0].view(torch.int16).reshape(-1))
+
+
+def test_inconsistent_extent_is_skipped_and_flagged():
+    wl = synth.make_workload(0)
+    st = H.make_state(wl, 3, 64)
+    Ws, Ss = H.device_tables(wl)
+    ids = torch.arange(10, dtype=torch.int64, device="cuda")
+    cu = torch.tensor([0, 4, 4, 12], dtype=torch.int32, device="cuda")  # sequence 2 runs past T = 10
+    starts = torch.zeros(3, dtype=torch.int32, device="cuda")
+    hashes = torch.full((10, 1, 6), -9, dtype=torch.int64, device="cuda")
+    st.hash_lookup_varlen(ids, cu, starts, Ws, Ss, hashes=hashes, max_len=8)
+    assert st.status() == geng.STATUS_BAD_LENGTH
+    h = hashes.cpu().numpy()
+    assert (h[:4] >= 0).all() and (h[4:] == -9).all()  # sequence 0 done, empty sequence 1, sequence 2 skipped
+    # longer than max_len: skipped too
+    cu = torch.tensor([0, 2, 4, 10], dtype=torch.int32, device="cuda")
+    hashes.fill_(-9)
+    st.hash_lookup_varlen(ids, cu, starts, Ws, Ss, hashes=hashes, max_len=4)
+    assert st.status() == geng.STATUS_BAD_LENGTH
+    assert (hashes.cpu().numpy()[4:] == -9).all()
+    with pytest.raises(geng.EngramError) as e:
+        st.hash_lookup_varlen(ids, cu, starts, Ws, Ss, max_len=65)  # max_len > max_seq_len
+    assert e.value.code == geng.ERR_RANGE
