@@ -44,9 +44,10 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--cfg", type=int, default=3, choices=[1, 2, 3, 4, 5, 6],
+    p.add_argument("--cfg", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7],
                    help="1 prefill B4xL4096, 2 decode B256xL1, 3 full-scale B8xL8192 (default), 4 long chunked, "
-                        "5 profiling case (prefill shapes, 1 GB tables), 6 full-scale with head_dim 256")
+                        "5 profiling case (prefill shapes, 1 GB tables), 6 full-scale with head_dim 256, "
+                        "7 continuous batching (packed decode + prefill sequences)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end loop (default min(K, 100))")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -237,8 +238,15 @@ class Runner:
                                      multipliers=lay.multipliers, primes=lay.primes, offsets=lay.offsets,
                                      dead=lay.dead, pad_id=lay.pad_id)
         seed = rank_seed(synth.MASTER_SEED + 17, rank)
+        self.varlen = cfg == 7
         # batches: distinct id sets cycled step to step
-        if cfg == 4:
+        if cfg == 7:
+            ids = [wl.ids]
+            masks = [None]
+            self.chunks = [(0, wl.ids.size)]
+            self.B, self.L = wl.B, wl.L
+            self.cu = torch.from_numpy(wl.extra["cu_seqlens"]).to(device)
+        elif cfg == 4:
             total = wl.ids.shape[1]
             ids = [wl.ids if rank == 0 else synth.zipf_ids(seed, total).reshape(1, total)]
             masks = [wl.mask]
@@ -257,12 +265,12 @@ class Runner:
         self.ids = [torch.from_numpy(np.ascontiguousarray(a)).to(device) for a in ids]
         self.masks = [None if m is None else torch.from_numpy(np.ascontiguousarray(m)).to(device) for m in masks]
         self.start = torch.from_numpy(np.ascontiguousarray(wl.start_pos.astype(np.int32))).to(device)
-        if cfg == 2:  # decode: history first
+        if wl.prefill_ids is not None:  # decode / continuous batching: history first
             self.state.hash(torch.from_numpy(wl.prefill_ids).to(device), 0)
         Lc = self.chunks[0][1] - self.chunks[0][0]
-        self.out = [torch.empty((self.B, Lc, lay.n_cols, lay.head_dim), dtype=torch.bfloat16, device=device)
-                    for _ in range(lay.n_layers)]
-        self.tokens_per_step = self.B * self.L
+        out_shape = (wl.ids.size, lay.n_cols, lay.head_dim) if self.varlen else (self.B, Lc, lay.n_cols, lay.head_dim)
+        self.out = [torch.empty(out_shape, dtype=torch.bfloat16, device=device) for _ in range(lay.n_layers)]
+        self.tokens_per_step = wl.ids.size if self.varlen else self.B * self.L
         self.launches_per_step = len(self.chunks)
         self.kernel_name = f"hash_kernel<GATHER=true, D={lay.head_dim}> (hash + gather + dequant)"
         torch.cuda.synchronize(device)
@@ -271,6 +279,10 @@ class Runner:
         """Enqueue one step; returns the launches' (start, end) event pairs when timing."""
         ids = self.ids[k % len(self.ids)] if ids is None else ids
         mask = self.masks[k % len(self.masks)] if mask is None else mask
+        if self.varlen:
+            self.geng.engram_hash_lookup_varlen(self.state.handle, ids, self.cu, self.start, self.W, self.S, mask,
+                                                self.out, max_len=self.L)
+            return
         for c0, c1 in self.chunks:
             if len(self.chunks) == 1:
                 ii, mm, sp = ids, mask, self.start
@@ -291,6 +303,9 @@ class Runner:
         self.mask_dev = None if self.masks[0] is None else torch.empty_like(self.masks[0])
         self.start_dev = torch.empty_like(self.start)
         self.out_pinned = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.out]
+        if self.varlen:
+            self.cu_pinned = self.cu.cpu().pin_memory()
+            self.cu_dev = torch.empty_like(self.cu)
 
     def e2e_step(self, k: int):
         """Host ids -> device, fused hash + lookup through the C ABI, bf16 rows -> host."""
@@ -299,10 +314,13 @@ class Runner:
         if self.mask_dev is not None:
             self.mask_dev.copy_(self.mask_pinned[j % len(self.mask_pinned)], non_blocking=True)
         self.start_dev.copy_(self.start_pinned, non_blocking=True)
-        saved = self.start
+        saved, saved_cu = self.start, getattr(self, "cu", None)
         self.start = self.start_dev
+        if self.varlen:
+            self.cu_dev.copy_(self.cu_pinned, non_blocking=True)
+            self.cu = self.cu_dev
         try:
-            if len(self.chunks) == 1:
+            if self.varlen or len(self.chunks) == 1:
                 self.step(k, self.ids_dev, self.mask_dev)
                 for o, h in zip(self.out, self.out_pinned):
                     h.copy_(o, non_blocking=True)
@@ -315,9 +333,11 @@ class Runner:
                         h.copy_(o, non_blocking=True)
         finally:
             self.start = saved
+            if self.varlen:
+                self.cu = saved_cu
 
     def e2e_bytes(self):
-        h2d = self.ids_pinned[0].numel() * 8 + self.start_pinned.numel() * 4
+        h2d = self.ids_pinned[0].numel() * 8 + self.start_pinned.numel() * 4 + (4 * self.cu.numel() if self.varlen else 0)
         if self.mask_dev is not None:
             h2d += self.mask_dev.numel()
         d2h = sum(o.numel() * 2 for o in self.out) * len(self.chunks)
@@ -459,7 +479,7 @@ def run_ours(args):
     traffic = recorded_traffic(args.cfg)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not runner.varlen:
         cpu = cpu_baseline_oracle(runner, runner.tokens_per_step if args.cfg != 2 else runner.tokens_per_step)
     csum = clocks.summary()
     wl = runner.wl

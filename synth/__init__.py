@@ -467,6 +467,20 @@ def make_workload(cfg: int, seed: int = MASTER_SEED, full64: bool = False) -> Wo
         B, L = 8, 8192
         ids = uniform_ids(s, B * L).reshape(B, L)
         return Workload("full-scale head_dim 256 B8xL8192", lay, B, L, ids, None, np.zeros(B, np.int32), s, B, L)
+    if cfg == 7:  # continuous batching on the full-scale tables: 192 decode steps + 64 prefill chunks
+        lay = make_layout("full", s, full64)
+        B, P = 256, 8192
+        is_prefill = np.zeros(B, dtype=bool)
+        is_prefill[np.argsort(words(s, TAG_SAMPLE, np.arange(B, dtype=np.uint64)), kind="stable")[:64]] = True
+        lens = np.where(is_prefill, uniform_int(s, TAG_SAMPLE, B, 64, 513, offset=100), 1).astype(np.int64)
+        start = np.array([int(uniform_int(s, TAG_START, 1, 1, P - int(n) + 1, offset=b)[0]) for b, n in enumerate(lens)],
+                         dtype=np.int32)
+        ids = zipf_ids(s, int(lens.sum()), offset=B * P)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        pre = zipf_ids(s, B * P).reshape(B, P)
+        return Workload("continuous batching 192 decode + 64 prefill (64-512) on full-scale tables", lay, B,
+                        int(lens.max()), ids, None, start, seed + 3, B, P + 512, prefill_ids=pre,
+                        extra={"cu_seqlens": cu, "lens": lens})
     if cfg == 5:  # profiling case: prefill shapes on ~1 GB of tables (still far above L2)
         lay = make_layout("profile", s, full64)
         B, L = 4, 4096
