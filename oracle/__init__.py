@@ -7,7 +7,9 @@ calls it, and it shares no code with the CUDA path.
 ``engram_oracle.c`` is a plain restatement of the "DeepSeek V4.1" pages
 (blocks/stack-hashes page: the n-gram hash ``forward``; engram-first/lookup
 page: ``ParallelEngramEmbedding.forward``). This module compiles it with gcc and
-calls it through ctypes.
+calls it through ctypes. The ``Engram`` gate and its ``wkv`` projection
+(blocks/stack-hashes page, ``Engram.forward``) are restated below in numpy,
+in float64.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 (brute force, closed forms, invariants, library reductions, the released table
@@ -168,3 +170,56 @@ def engram_lookup(idx, W, S, rows, D, block, L=None) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"oracle_engram_lookup rejected its arguments ({rc})")
     return out
+
+
+# ----------------------------------------------------------------------------- Engram gate (float64)
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> exact float64 values."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def f64_to_bf16_bits(x) -> np.ndarray:
+    """Round float64 values to bf16 (nearest, ties to even), straight from float64 (no float32 step).
+    Finite inputs only; values beyond the bf16 range become infinities."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros(x.shape, dtype=np.uint16)
+    sign = np.signbit(x)
+    a = np.abs(x)
+    nz = a > 0
+    m, e = np.frexp(np.where(nz, a, 1.0))  # a = m * 2^e, m in [0.5, 1)
+    # bf16 keeps 8 significant bits; below the normal range (2^-126) the step is fixed at 2^-133
+    q = np.where(e - 1 >= -126, np.ldexp(np.rint(np.ldexp(m, 8)), e - 8), np.ldexp(np.rint(np.ldexp(a, 133)), -133))
+    q = np.where(nz, q, 0.0)
+    f = q.astype(np.float32)  # exact: q has at most 8 significant bits (or overflows to inf)
+    bits = (f.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    out[...] = np.where(sign, bits | np.uint16(0x8000), bits)
+    return out
+
+
+def engram_linear(emb_bits, w_bits) -> np.ndarray:
+    """The `wkv` projection of the Engram block on bf16 inputs: exact float64 products and sums,
+    rounded once to bf16. emb [T, K], w [N, K] (bf16 bits) -> kv bits [T, N]."""
+    e = bf16_bits_to_f64(emb_bits)
+    w = bf16_bits_to_f64(w_bits)
+    return f64_to_bf16_bits(e @ w.T)
+
+
+def engram_gate(x_bits, kv_bits, qw_bits, kw_bits, mask=None, eps=1e-20, clamp=1e-6) -> np.ndarray:
+    """`Engram.forward` after the projection (blocks/stack-hashes page), in float64:
+    x [T, hc, dim] (the residual copies), kv [T, (hc+1)*dim] = hc keys then one shared value,
+    q_weight / k_weight [hc, dim], mask [T] (False closes the gate). Returns the float64 result
+    h + gate * value, [T, hc, dim], before its conversion to x's dtype."""
+    h = bf16_bits_to_f64(x_bits)
+    T, hc, dim = h.shape
+    kv = bf16_bits_to_f64(kv_bits).reshape(T, hc + 1, dim)
+    key, value = kv[:, :hc, :], kv[:, hc, :]
+    weight = bf16_bits_to_f64(qw_bits) * bf16_bits_to_f64(kw_bits)            # [hc, dim]
+    # normalized per (token, hc copy) over dim
+    rstd = 1.0 / np.sqrt((h * h).mean(-1) + eps) / np.sqrt((key * key).mean(-1) + eps)
+    dot = (h * weight[None] * key).sum(-1) * rstd * dim ** -0.5              # [T, hc]
+    signed_sqrt = np.copysign(np.sqrt(np.maximum(np.abs(dot), clamp)), dot)
+    gate = 1.0 / (1.0 + np.exp(-signed_sqrt))
+    if mask is not None:
+        gate = np.where(np.asarray(mask, dtype=bool)[:, None], gate, 0.0)
+    return h + gate[..., None] * value[:, None, :]

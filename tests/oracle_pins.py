@@ -318,5 +318,88 @@ def pin_varlen(L=None):
     assert np.array_equal(d1.cache, d2.cache)
 
 
+# ----------------------------------------------------------------------------- Engram gate
+
+
+def _bf16(x):
+    import torch
+
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_bf16_from_f64():
+    # exact ties and near-ties that a float32 intermediate would round twice
+    one = 1.0
+    cases = {one + 2 ** -8: 0x3F80, one + 2 ** -8 + 2 ** -40: 0x3F81, one + 3 * 2 ** -8: 0x3F82,
+             -(one + 2 ** -8 + 2 ** -40): 0xBF81, 2.0 ** -133: 0x0001, 2.0 ** -134: 0x0000, 0.0: 0x0000}
+    for v, bits in cases.items():
+        got = int(oracle.f64_to_bf16_bits(np.array([v]))[0])
+        assert got == bits, (v, hex(got), hex(bits))
+
+
+def pin_linear():
+    rng = np.random.default_rng(1)
+    emb = _bf16(rng.standard_normal((5, 12)))
+    # one-hot weight rows pick single input columns: exact
+    w = np.zeros((4, 12), dtype=np.float32)
+    w[[0, 1, 2, 3], [0, 5, 11, 7]] = 1.0
+    kv = oracle.engram_linear(emb, _bf16(w))
+    assert np.array_equal(kv, emb[:, [0, 5, 11, 7]])
+    # small integers: every product and sum is exact in float32 and bf16
+    a = _bf16(rng.integers(-4, 5, size=(3, 6)))
+    b = _bf16(rng.integers(-4, 5, size=(2, 6)))
+    exp = oracle.bf16_bits_to_f64(a) @ oracle.bf16_bits_to_f64(b).T
+    assert np.array_equal(oracle.bf16_bits_to_f64(oracle.engram_linear(a, b)), exp)
+
+
+def pin_gate(gate=None):
+    import torch
+
+    gate = gate or oracle.engram_gate
+    rng = np.random.default_rng(2)
+    T, hc, dim = 6, 4, 64
+    x = _bf16(rng.standard_normal((T, hc, dim)))
+    ones = _bf16(np.ones((hc, dim)))
+    h = oracle.bf16_bits_to_f64(x)
+    # closed form: key = c*h, unit weights -> dot = sign(c) * sqrt(dim) -> gate = sigmoid(sign(c) * dim^(1/4))
+    for c in (2.0, -0.5):
+        kv = np.concatenate([c * h, rng.standard_normal((T, 1, dim))], axis=1)
+        kvb = _bf16(kv.reshape(T, -1))
+        out = gate(x, kvb, ones, ones)
+        value = oracle.bf16_bits_to_f64(kvb).reshape(T, hc + 1, dim)[:, hc, :]
+        g = 1.0 / (1.0 + np.exp(-np.sign(c) * dim ** 0.25))
+        assert np.allclose(out, h + g * value[:, None, :], rtol=1e-12, atol=1e-12)
+    # a closed gate passes the residual through unchanged
+    kvb = _bf16(rng.standard_normal((T, (hc + 1) * dim)))
+    mask = np.array([True, False, True, False, False, True])
+    out = gate(x, kvb, ones, ones, mask)
+    assert np.array_equal(out[~mask], h[~mask])
+    # a key orthogonal to h: dot is +0, clamped to 1e-6 -> gate = sigmoid(+1e-3)
+    h2 = np.zeros((1, 1, dim))
+    h2[0, 0, 0] = 1.0
+    k2 = np.zeros((1, 2, dim))
+    k2[0, 0, 1] = 1.0
+    out = gate(_bf16(h2), _bf16(k2.reshape(1, -1)), _bf16(np.ones((1, dim))), _bf16(np.ones((1, dim))))
+    assert out[0, 0, 0] == 1.0  # value row is zero; only the residual remains
+    # the page's own code, run in float32 on torch CPU, agrees to float32 accuracy
+    qw = _bf16(rng.uniform(0.5, 1.5, (hc, dim)))
+    kw = _bf16(rng.uniform(0.5, 1.5, (hc, dim)))
+    mask = rng.random(T) > 0.3
+    ref = gate(x, kvb, qw, kw, mask)
+    tx = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    tkv = torch.from_numpy(kvb.view(np.int16)).view(torch.bfloat16)
+    key, value = tkv.split([hc * dim, dim], dim=-1)
+    key = key.float().unflatten(-1, (hc, dim))
+    weight = torch.from_numpy(qw.view(np.int16)).view(torch.bfloat16).float() * \
+        torch.from_numpy(kw.view(np.int16)).view(torch.bfloat16).float()
+    hh = tx.float()
+    rstd = torch.rsqrt(hh.square().mean(-1) + 1e-20) * torch.rsqrt(key.square().mean(-1) + 1e-20)
+    dot = (hh * weight * key).sum(-1) * rstd * dim ** -0.5
+    gate = torch.sigmoid(torch.copysign(dot.abs().clamp_min(1e-6).sqrt(), dot))
+    gate = gate.masked_fill(~torch.from_numpy(mask).unsqueeze(-1), 0)
+    t32 = (hh + gate.unsqueeze(-1) * value.float().unsqueeze(-2)).numpy().astype(np.float64)
+    assert np.allclose(t32, ref, rtol=1e-5, atol=1e-5)
+
+
 ALL_PINS = [pin_floor_mod, pin_fp8_decode, pin_bf16, pin_lookup_vs_torch, pin_brute_force, pin_closed_forms,
             pin_invariants, pin_varlen]

@@ -85,3 +85,32 @@ def test_planted_mistake_is_caught(name, tmpdir_mut):
         assert caught is None, f"control build failed pin {caught}"
     else:
         assert caught is not None, f"planted mistake {name} passed every pin"
+
+
+# ----------------------------------------------------------------------------- the float64 gate oracle
+GATE_MUTANTS = {
+    "norm_over_copies": ("(h * h).mean(-1)", "(h * h).mean(-2, keepdims=True).squeeze(-2)[:, None].repeat(h.shape[1], 1)"),
+    "weight_dropped": ("(h * weight[None] * key)", "(h * key)"),
+    "no_dim_scale": (" * rstd * dim ** -0.5", " * rstd"),
+    "sign_lost": ("np.copysign(np.sqrt(np.maximum(np.abs(dot), clamp)), dot)", "np.sqrt(np.maximum(np.abs(dot), clamp))"),
+    "sigmoid_flipped": ("1.0 / (1.0 + np.exp(-signed_sqrt))", "1.0 / (1.0 + np.exp(signed_sqrt))"),
+    "mask_inverted": ("np.where(np.asarray(mask, dtype=bool)[:, None], gate, 0.0)",
+                      "np.where(np.asarray(mask, dtype=bool)[:, None], 0.0, gate)"),
+    "value_per_copy": ("h + gate[..., None] * value[:, None, :]", "h + gate[..., None] * key"),
+    "key_shifted": ("key, value = kv[:, :hc, :], kv[:, hc, :]", "key, value = kv[:, 1:, :], kv[:, 0, :]"),
+    "sqrt_dropped": ("np.sqrt(np.maximum(np.abs(dot), clamp))", "np.maximum(np.abs(dot), clamp)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GATE_MUTANTS))
+def test_planted_gate_mistake_is_caught(name):
+    import inspect
+
+    src = inspect.getsource(oracle.engram_gate)
+    old, new = GATE_MUTANTS[name]
+    assert old in src, f"gate mutation {name}: pattern not found"
+    ns = dict(vars(oracle))
+    exec(src.replace(old, new, 1), ns)
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        oracle_pins.pin_gate(ns["engram_gate"])
+    oracle_pins.pin_gate(oracle.engram_gate)  # the real one passes

@@ -37,3 +37,9 @@ def test_oracle_hash_rejects_bad_shapes():
     st = oracle.OracleState.from_layout(lay, 1, 8)
     with pytest.raises(ValueError):
         st.hash(np.zeros((2, 4), np.int64), 0)  # B > cache rows
+
+
+@pytest.mark.parametrize("pin", [oracle_pins.pin_bf16_from_f64, oracle_pins.pin_linear, oracle_pins.pin_gate],
+                         ids=lambda f: f.__name__)
+def test_gate_pin(pin):
+    pin()
