@@ -51,6 +51,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end loop (default min(K, 100))")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--block", action="store_true",
+                   help="time the whole Engram block per step: hash + lookup, then per layer the wkv projection "
+                        "(cuBLAS bf16 GEMM) and the gate kernel, at the released width (dim 5120, 4 copies)")
     p.add_argument("--graph", action="store_true",
                    help="capture the steps in a CUDA graph and replay it (removes host launch overhead; for the "
                         "small decode / chunk launches)")
@@ -530,6 +533,95 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- the whole Engram block
+def run_block(args):
+    """Engram block per step on workload args.cfg: the fused hash + lookup, then for each engram layer
+    kv = rows @ wkv^T (a plain cuBLAS bf16 GEMM) and the gate kernel (in place on the residual copies).
+    Weights are seeded synthetic values; dims are the released model's (dim 5120, hc_mult 4)."""
+    import numpy as np
+    import torch
+
+    import gram_hash_embedding_gb300 as geng
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        import __graft_entry__
+
+        __graft_entry__.build()
+    runner = Runner(args.cfg, rank, device)
+    lay = runner.lay
+    T = runner.tokens_per_step
+    dim, hc = 5120, 4
+    K = lay.n_cols * lay.head_dim
+    g = torch.Generator(device="cpu").manual_seed(20261202)
+    wkv = [(torch.randn((dim * (hc + 1), K), generator=g) * K ** -0.5).to(torch.bfloat16).to(device)
+           for _ in range(lay.n_layers)]
+    qw = [torch.rand((hc, dim), generator=g).add_(0.5).to(torch.bfloat16).to(device) for _ in range(lay.n_layers)]
+    kw = [torch.rand((hc, dim), generator=g).add_(0.5).to(torch.bfloat16).to(device) for _ in range(lay.n_layers)]
+    x = torch.randn((T, hc, dim), generator=g).to(torch.bfloat16).to(device)
+    kv = torch.empty((T, dim * (hc + 1)), dtype=torch.bfloat16, device=device)
+    mask = None if runner.masks[0] is None else runner.masks[0].reshape(-1)
+    stream = torch.cuda.current_stream(device)
+    names = ["hash+lookup"] + [f"{n}{l}" for l in range(lay.n_layers) for n in ("wkv", "gate")]
+
+    def step(k, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        runner.step(k)
+        i = 1
+        for l in range(lay.n_layers):
+            if ev is not None:
+                ev[i].record(stream)
+            torch.matmul(runner.out[l].view(T, K), wkv[l].t(), out=kv)
+            if ev is not None:
+                ev[i + 1].record(stream)
+            geng.engram_gate(x, kv, qw[l], kw[l], mask, out=x)
+            i += 2
+        if ev is not None:
+            ev[i].record(stream)
+
+    for k in range(max(3, args.warmup // 10)):
+        step(k)
+    torch.cuda.synchronize()
+    K_steps = max(3, min(args.steps, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K_steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K_steps):
+        step(k, evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    total = t0.elapsed_time(t1) / 1e3
+    comp = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) * 1e3 for i, n in enumerate(names)}
+    peak_hbm, _ = measured_peaks()
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        peaks = json.load(f)
+    gemm_flops = 2.0 * T * K * dim * (hc + 1)
+    gate_bytes = T * 2.0 * dim * (3 * hc + 1)
+    lookup_bytes = T * algo_bytes_per_token(lay)
+    roof = {"hash+lookup": {"bound": "hbm", "achieved": lookup_bytes / comp["hash+lookup"] / 1e3, "peak": peak_hbm,
+                            "unit": "GB/s"}}
+    for l in range(lay.n_layers):
+        roof[f"wkv{l}"] = {"bound": "tensor", "achieved": gemm_flops / comp[f"wkv{l}"] / 1e6,
+                           "peak": float(peaks["bf16_tflops_sustained"]), "unit": "TFLOP/s",
+                           "kernel": "cuBLAS bf16 GEMM (library)"}
+        roof[f"gate{l}"] = {"bound": "hbm", "achieved": gate_bytes / comp[f"gate{l}"] / 1e3, "peak": peak_hbm,
+                            "unit": "GB/s"}
+    for r in roof.values():
+        r["frac"] = r["achieved"] / r["peak"]
+    line = {
+        "metric": "Engram block (hash + fp8 lookup + wkv projection + gate) tokens/s",
+        "value": T * K_steps / total, "unit": "tokens/s", "n_gpus": 1, "steps": K_steps,
+        "ms_per_step": total / K_steps * 1e3, "higher_is_better": True, "dtype": "bf16/f32", "data": "synthetic",
+        "config": {"workload": runner.wl.name, "dim": dim, "hc_mult": hc, "wkv": [dim * (hc + 1), K]},
+        "component_us": comp, "roofline": roof,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """The CPU oracle as it stands, timed on the host cores: each step hashes a bounded sample of
@@ -604,6 +696,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.block:
+        run_block(args)
     else:
         run_ours(args)
 

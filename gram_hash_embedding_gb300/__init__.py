@@ -26,7 +26,7 @@ from ._build import build
 __all__ = [
     "EngramError", "EngramHash", "build", "engram_state_create", "engram_state_destroy", "engram_cache_reset",
     "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
-    "engram_hash_lookup_varlen", "engram_strerror", "STATUS_BAD_START", "STATUS_BAD_ID", "STATUS_BAD_LENGTH",
+    "engram_hash_lookup_varlen", "engram_gate", "engram_strerror", "STATUS_BAD_START", "STATUS_BAD_ID", "STATUS_BAD_LENGTH",
     "library_path",
 ]
 
@@ -76,11 +76,12 @@ def _lib():
         L.engram_hash_varlen.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P]
         L.engram_hash_lookup_varlen.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _P]
         L.engram_state_layout.argtypes = [_P, ctypes.POINTER(_Layout)]
+        L.engram_gate.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _I32, ctypes.c_float, _P, _P]
         L.engram_strerror.argtypes = [ctypes.c_int]
         L.engram_strerror.restype = ctypes.c_char_p
         for name in ("engram_state_create", "engram_state_destroy", "engram_cache_reset", "engram_state_status",
                      "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout",
-                     "engram_hash_varlen", "engram_hash_lookup_varlen"):
+                     "engram_hash_varlen", "engram_hash_lookup_varlen", "engram_gate"):
             getattr(L, name).restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -273,6 +274,23 @@ def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.T
                                             _dev(start_pos, torch.int32, "start_pos"), B, T,
                                             _max_len(cu_seqlens, max_len), Wp, Sp, Rp, Op, hp, _stream(stream)),
            "engram_hash_lookup_varlen")
+    return out
+
+
+def engram_gate(x: torch.Tensor, kv: torch.Tensor, q_weight: torch.Tensor, k_weight: torch.Tensor,
+                mask: torch.Tensor | None = None, eps: float = 1e-20, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """The Engram gate on bf16 tensors: x [T, hc, dim] (or [..., hc, dim]), kv [..., (hc+1)*dim],
+    q_weight / k_weight [hc, dim], mask [...] bool or None. Returns (or fills; may be x) bf16 [..., hc, dim]."""
+    hc, dim = x.shape[-2], x.shape[-1]
+    T = x.numel() // (hc * dim)
+    if out is None:
+        out = torch.empty_like(x)
+    m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+    _check(_lib().engram_gate(_dev(x, torch.bfloat16, "x"), _dev(kv, torch.bfloat16, "kv"),
+                              _dev(q_weight, torch.bfloat16, "q_weight"), _dev(k_weight, torch.bfloat16, "k_weight"),
+                              m, T, hc, dim, float(eps), _dev(out, torch.bfloat16, "out"), _stream(stream)),
+           "engram_gate")
     return out
 
 

@@ -303,6 +303,21 @@ int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uin
                                                                                           : ENGRAM_ERR_CUDA;
 }
 
+int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight, const uint16_t* k_weight,
+                const uint8_t* mask, int64_t T, int32_t hc, int32_t dim, float eps, uint16_t* out,
+                engram_stream_t stream) {
+  if (T < 0) return ENGRAM_ERR_INVALID;
+  if (!(hc == 1 || hc == 2 || hc == 4 || hc == 8) || dim < 8 || dim % 8 != 0) return ENGRAM_ERR_UNSUPPORTED;
+  if (T == 0) return ENGRAM_OK;
+  if (T > ((int64_t)1 << 31) - 1) return ENGRAM_ERR_UNSUPPORTED;
+  if (x == nullptr || kv == nullptr || q_weight == nullptr || k_weight == nullptr || out == nullptr)
+    return ENGRAM_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(kv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) || !aligned(out, 16))
+    return ENGRAM_ERR_INVALID;
+  cudaError_t e = engram::launch_gate(x, kv, q_weight, k_weight, mask, T, hc, dim, eps, out, (cudaStream_t)stream);
+  return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
 int engram_state_layout(const engram_state* state, engram_layout* layout) {
   if (state == nullptr || layout == nullptr) return ENGRAM_ERR_INVALID;
   *layout = state->lay;

@@ -51,6 +51,8 @@ struct CallArgs {
 cudaError_t launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s);
 cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s);
 cudaError_t launch_hash_lookup(const StateView& sv, const CallArgs& a, cudaStream_t s);
+cudaError_t launch_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* qw, const uint16_t* kw,
+                        const uint8_t* mask, int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s);
 cudaError_t launch_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
                           int32_t head_dim, int32_t block, uint16_t* out, cudaStream_t s);
 

@@ -1,0 +1,152 @@
+// The Engram gate (sm_103a): "DeepSeek V4.1" pages, blocks/stack-hashes page, `Engram.forward`,
+// the part after the `wkv` projection. For every token and residual copy i:
+//   rstd  = rsqrt(mean(h_i^2) + eps) * rsqrt(mean(key_i^2) + eps)
+//   dot   = sum(h_i * q_weight_i * k_weight_i * key_i) * rstd * dim^-0.5
+//   gate  = sigmoid(copysign(sqrt(max(|dot|, 1e-6)), dot)), 0 where the token is masked
+//   out_i = bf16(h_i + gate * value)          (value is shared by the copies)
+// in fp32, as the page computes it.
+//
+// Design: memory-bound (per token: read hc*dim residual values and (hc+1)*dim projections, write
+// hc*dim), so one CTA per token reads each input once with 16-byte loads, keeps the 3*hc partial
+// sums of every copy in registers, reduces them across the block, and then writes the outputs;
+// the second read of h and value hits L1/L2 (the token's inputs were just read). The page's
+// PyTorch code instead makes ~15 full passes over fp32 temporaries.
+#include <cstdint>
+
+#include "engram_internal.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kGateMaxCopies = ENGRAM_GATE_MAX_COPIES;  // largest hc the reduction buffers hold
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// grid = T CTAs; HC residual copies known at compile time (the partial sums live in registers)
+template <int HC>
+// x and out may be the same buffer: each thread reads a vector of x before it writes the same
+// vector of out, and no other thread touches it, so neither pointer is marked __restrict__.
+__global__ void __launch_bounds__(256) gate_kernel(const uint16_t* x, const uint16_t* __restrict__ kv,
+                                                   const uint16_t* __restrict__ qw, const uint16_t* __restrict__ kw,
+                                                   const uint8_t* __restrict__ mask, const int dim, const float eps,
+                                                   const float inv_sqrt_dim, uint16_t* out) {
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int nvec = dim >> 3;  // 8 bf16 per 16-byte vector
+  const uint16_t* xt = x + t * (int64_t)HC * dim;
+  const uint16_t* kvt = kv + t * (int64_t)(HC + 1) * dim;
+  __shared__ float red[3 * kGateMaxCopies][32];
+  __shared__ float gate_s[kGateMaxCopies];
+
+  float sh[HC], sk[HC], sd[HC];
+#pragma unroll
+  for (int i = 0; i < HC; ++i) sh[i] = sk[i] = sd[i] = 0.f;
+  for (int v = tid; v < nvec; v += nthr) {
+#pragma unroll
+    for (int i = 0; i < HC; ++i) {
+      float h[8], k[8], q[8], w[8];
+      bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v), h);
+      bf16x8_to_f32(ld16(kvt + (int64_t)i * dim + 8 * v), k);
+      bf16x8_to_f32(ld16(qw + (int64_t)i * dim + 8 * v), q);
+      bf16x8_to_f32(ld16(kw + (int64_t)i * dim + 8 * v), w);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sh[i] = fmaf(h[e], h[e], sh[i]);
+        sk[i] = fmaf(k[e], k[e], sk[i]);
+        sd[i] = fmaf(h[e] * (q[e] * w[e]), k[e], sd[i]);
+      }
+    }
+  }
+  // block reduction of the 3*HC sums: warp shuffles, then one value per warp in shared memory
+  const int lane = tid & 31, warp = tid >> 5, nwarp = (nthr + 31) >> 5;
+#pragma unroll
+  for (int i = 0; i < HC; ++i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sh[i] += __shfl_xor_sync(0xffffffffu, sh[i], o);
+      sk[i] += __shfl_xor_sync(0xffffffffu, sk[i], o);
+      sd[i] += __shfl_xor_sync(0xffffffffu, sd[i], o);
+    }
+    if (lane == 0) {
+      red[3 * i][warp] = sh[i];
+      red[3 * i + 1][warp] = sk[i];
+      red[3 * i + 2][warp] = sd[i];
+    }
+  }
+  __syncthreads();
+  if (tid < HC) {
+    float a = 0.f, b = 0.f, c = 0.f;
+    for (int w = 0; w < nwarp; ++w) {
+      a += red[3 * tid][w];
+      b += red[3 * tid + 1][w];
+      c += red[3 * tid + 2][w];
+    }
+    const float rd = 1.0f / (float)dim;
+    const float rstd = (1.0f / sqrtf(a * rd + eps)) * (1.0f / sqrtf(b * rd + eps));
+    const float dot = c * rstd * inv_sqrt_dim;
+    const float z = copysignf(sqrtf(fmaxf(fabsf(dot), 1e-6f)), dot);
+    float g = 1.0f / (1.0f + expf(-z));
+    if (mask != nullptr && mask[t] == 0) g = 0.f;
+    gate_s[tid] = g;
+  }
+  __syncthreads();
+  // out = h + gate * value (the value row is shared by the HC copies)
+  const uint16_t* vt = kvt + (int64_t)HC * dim;
+  uint16_t* ot = out + t * (int64_t)HC * dim;
+  for (int v = tid; v < nvec; v += nthr) {
+    float val[8];
+    bf16x8_to_f32(ld16(vt + 8 * v), val);
+#pragma unroll
+    for (int i = 0; i < HC; ++i) {
+      float h[8];
+      bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v), h);
+      const float g = gate_s[i];
+      uint4 o;
+      o.x = f32x2_to_bf16x2(h[0] + g * val[0], h[1] + g * val[1]);
+      o.y = f32x2_to_bf16x2(h[2] + g * val[2], h[3] + g * val[3]);
+      o.z = f32x2_to_bf16x2(h[4] + g * val[4], h[5] + g * val[5]);
+      o.w = f32x2_to_bf16x2(h[6] + g * val[6], h[7] + g * val[7]);
+      *reinterpret_cast<uint4*>(ot + (int64_t)i * dim + 8 * v) = o;
+    }
+  }
+}
+
+template <int HC>
+cudaError_t launch_gate_hc(const uint16_t* x, const uint16_t* kv, const uint16_t* qw, const uint16_t* kw,
+                           const uint8_t* mask, int64_t T, int dim, float eps, uint16_t* out, cudaStream_t s) {
+  int threads = dim / 8;
+  threads = threads < 32 ? 32 : (threads > 256 ? 256 : ((threads + 31) / 32) * 32);
+  const float inv_sqrt_dim = (float)(1.0 / sqrt((double)dim));
+  gate_kernel<HC><<<(unsigned)T, threads, 0, s>>>(x, kv, qw, kw, mask, dim, eps, inv_sqrt_dim, out);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* qw, const uint16_t* kw,
+                        const uint8_t* mask, int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s) {
+  switch (hc) {
+    case 1: return launch_gate_hc<1>(x, kv, qw, kw, mask, T, dim, eps, out, s);
+    case 2: return launch_gate_hc<2>(x, kv, qw, kw, mask, T, dim, eps, out, s);
+    case 4: return launch_gate_hc<4>(x, kv, qw, kw, mask, T, dim, eps, out, s);
+    case 8: return launch_gate_hc<8>(x, kv, qw, kw, mask, T, dim, eps, out, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace engram

@@ -66,6 +66,7 @@ typedef struct engram_state engram_state;
 #define ENGRAM_MAX_NGRAM 8        /* max_ngram (>= 2) */
 #define ENGRAM_MAX_COLS_TOTAL 512 /* n_layers * (max_ngram - 1) * n_heads */
 /* head_dim must be one of 16, 32, 64, 128, 256, 512; block must divide head_dim and be a multiple of 8. */
+#define ENGRAM_GATE_MAX_COPIES 8  /* engram_gate: residual copies hc in {1, 2, 4, 8}; dim a multiple of 8 */
 
 typedef struct engram_layout {
   int32_t n_layers;    /* engram layers hashed per call (the config's engram_layer_ids count) */
@@ -170,6 +171,24 @@ int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uin
                               const int32_t* cu_seqlens, const int32_t* start_pos, int32_t B, int64_t T,
                               int64_t max_len, const uint8_t* const* W, const float* const* S, const int64_t* rows,
                               uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
+
+/*
+ * The Engram gate (blocks/stack-hashes page, `Engram.forward`, after the `wkv` projection), in fp32:
+ * for every token t and residual copy i,
+ *   rstd = rsqrt(mean(h^2) + eps) * rsqrt(mean(key_i^2) + eps),  h = x[t][i]
+ *   dot  = sum(h * q_weight[i] * k_weight[i] * key_i) * rstd * dim^-0.5
+ *   gate = sigmoid(copysign(sqrt(max(|dot|, 1e-6)), dot)), and 0 where mask[t] == 0
+ *   out[t][i] = bf16_rne(h + gate * value)
+ *   x        device bf16 [T][hc][dim] (the residual copies)
+ *   kv       device bf16 [T][(hc+1)*dim]: the projection output, hc keys then one shared value
+ *   q_weight, k_weight  device bf16 [hc][dim]
+ *   mask     device uint8 [T] (non-zero = the token's gate is open) or NULL
+ *   out      device bf16 [T][hc][dim]; may be the same buffer as x
+ * All bf16 pointers 16-byte aligned. T == 0 is a no-op. Errors: _INVALID, _UNSUPPORTED (hc, dim).
+ */
+int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight, const uint16_t* k_weight,
+                const uint8_t* mask, int64_t T, int32_t hc, int32_t dim, float eps, uint16_t* out,
+                engram_stream_t stream);
 
 /* Layout the state was created with (host copy). */
 int engram_state_layout(const engram_state* state, engram_layout* layout);
