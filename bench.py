@@ -51,6 +51,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end loop (default min(K, 100))")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--mode", choices=["fused", "hash", "lookup"], default="fused",
+                   help="fused: engram_hash_lookup (default); hash: engram_hash alone (int64 ids out); "
+                        "lookup: engram_lookup alone on the workload's row ids, one launch per layer")
     p.add_argument("--block", action="store_true",
                    help="time the whole Engram block per step: hash + lookup, then per layer the wkv projection "
                         "(cuBLAS bf16 GEMM) and the gate kernel, at the released width (dim 5120, 4 copies)")
@@ -297,6 +300,45 @@ class Runner:
                                          self.W, self.S, mm if (mm is None or mm.is_contiguous()) else mm.contiguous(),
                                          self.out)
 
+    def setup_mode(self, mode: str):
+        """Buffers of the hash-only and lookup-only measurements."""
+        torch = self.torch
+        lay = self.lay
+        self.mode = mode
+        if mode == "fused":
+            return
+        self.hash_out = torch.empty((self.B, self.L, lay.n_layers, lay.n_cols), dtype=torch.int64, device=self.device)
+        if mode == "lookup":
+            # the row ids this workload hashes to, one flat list per layer
+            self.geng.engram_hash(self.state.handle, self.ids[0], self.start, self.masks[0], self.hash_out)
+            self.idx = [self.hash_out[:, :, l, :].contiguous().view(-1) for l in range(lay.n_layers)]
+            self.lookup_out = [torch.empty((self.idx[l].numel(), lay.head_dim), dtype=torch.bfloat16,
+                                           device=self.device) for l in range(lay.n_layers)]
+            self.launches_per_step = lay.n_layers
+            self.kernel_name = f"lookup_kernel<D={lay.head_dim}>"
+        else:
+            self.kernel_name = "hash_kernel<GATHER=false>"
+        torch.cuda.synchronize(self.device)
+
+    def step_mode(self, k: int):
+        if self.mode == "hash":
+            ids = self.ids[k % len(self.ids)]
+            mask = self.masks[k % len(self.masks)]
+            self.geng.engram_hash(self.state.handle, ids, self.start, mask, self.hash_out)
+        elif self.mode == "lookup":
+            for l in range(self.lay.n_layers):
+                self.geng.engram_lookup(self.idx[l], self.W[l], self.S[l], self.lay.block, self.lookup_out[l])
+        else:
+            self.step(k)
+
+    def mode_bytes_per_token(self) -> int:
+        lay = self.lay
+        if self.mode == "hash":  # ids in, cache entry out, int64 hash ids out (mask byte if any)
+            return 8 + 4 + 8 * lay.n_layers * lay.n_cols + (1 if self.masks[0] is not None else 0)
+        if self.mode == "lookup":  # the fused bytes plus the int64 row id read per row
+            return algo_bytes_per_token(lay) + 8 * lay.n_layers * lay.n_cols
+        return algo_bytes_per_token(lay)
+
     def e2e_buffers(self):
         torch = self.torch
         self.ids_pinned = [torch.from_numpy(self.np.ascontiguousarray(a)).pin_memory() for a in self.ids_host]
@@ -430,10 +472,11 @@ def run_ours(args):
 
     geng._lib()
     runner = Runner(args.cfg, rank, device)
+    runner.setup_mode(args.mode)
     stream = torch.cuda.current_stream(device)
     K, W = args.steps, args.warmup
     for k in range(W):
-        runner.step(k)
+        runner.step_mode(k)
     torch.cuda.synchronize()
     flags = runner.state.status()
 
@@ -444,7 +487,7 @@ def run_ours(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for k in range(per_graph):
-                runner.step(k)
+                runner.step_mode(k)
         for _ in range(3):
             graph.replay()
         replays = max(1, -(-K // per_graph))
@@ -456,13 +499,13 @@ def run_ours(args):
         mean_launch = total / K
     else:
         clocks.start()
-        total, mean_launch = time_region(torch, dist, local, runner.step, K, stream, per_launch_events=True)
+        total, mean_launch = time_region(torch, dist, local, runner.step_mode, K, stream, per_launch_events=True)
         clocks.stop()
     total_max = max_over_ranks(dist, total, device)
     tokens = runner.tokens_per_step * K * world
     value = tokens / total_max
 
-    # end to end: host ids in, host bf16 rows out, every step
+    # end to end: host ids in, host bf16 rows out, every step (the fused call)
     runner.e2e_buffers()
     Ke = args.e2e_steps or max(3, min(K, 100))
     for k in range(3):
@@ -473,21 +516,22 @@ def run_ours(args):
     h2d, d2h = runner.e2e_bytes()
 
     lay = runner.lay
-    bpt = algo_bytes_per_token(lay)
+    bpt = runner.mode_bytes_per_token()
     per_launch_tokens = runner.tokens_per_step // runner.launches_per_step
     algo_bytes = per_launch_tokens * bpt
     launch_s = mean_launch / runner.launches_per_step
     peak, peak_kind = measured_peaks()
     achieved = algo_bytes / launch_s / 1e9
-    traffic = recorded_traffic(args.cfg)
+    traffic = recorded_traffic(args.cfg) if args.mode == "fused" else None
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not runner.varlen:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not runner.varlen and args.mode == "fused":
         cpu = cpu_baseline_oracle(runner, runner.tokens_per_step if args.cfg != 2 else runner.tokens_per_step)
     csum = clocks.summary()
     wl = runner.wl
     line = {
-        "metric": "Engram hash+fp8-gather tokens/s (B8×L8192); gathered HBM GB/s vs peak",
+        "metric": "Engram hash+fp8-gather tokens/s (B8×L8192); gathered HBM GB/s vs peak" if args.mode == "fused"
+        else f"Engram {args.mode}-only tokens/s (entry point engram_{args.mode})",
         "value": value,
         "unit": "tokens/s",
         "n_gpus": world,
@@ -522,7 +566,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": algo_bytes, "launch_us": launch_s * 1e6,
                      "kernel": runner.kernel_name},
         "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": Ke, "ms_per_step": e_total / Ke * 1e3},
+                "steps": Ke, "ms_per_step": e_total / Ke * 1e3, "call": "engram_hash_lookup"},
         "gpu_launches": K * runner.launches_per_step,
         "clocks": csum,
         "cpu_baseline": cpu,
@@ -681,7 +725,8 @@ def run_reference(args):
               "single-threaded C oracle")
     line = {
         "impl": "reference",
-        "metric": "Engram hash+fp8-gather tokens/s (B8×L8192); gathered HBM GB/s vs peak",
+        "metric": "Engram hash+fp8-gather tokens/s (B8×L8192); gathered HBM GB/s vs peak" if args.mode == "fused"
+        else f"Engram {args.mode}-only tokens/s (entry point engram_{args.mode})",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": total / K * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",

@@ -50,7 +50,10 @@ constexpr int kUnroll = ENGRAM_UNROLL;          // independent row pieces in fli
 constexpr int kFusedTile = ENGRAM_FUSED_TILE;   // largest tile (tokens per CTA) of the fused kernel
 constexpr int kTargetCtas = ENGRAM_TARGET_CTAS; // fused grid size the tile choice aims for (2 waves)
 constexpr int kMinFusedTile = 4;                // below 4 tokens the halo and hash phase dominate
-constexpr int kHashTile = 64;                   // tokens per CTA, hash-only kernel
+#ifndef ENGRAM_HASH_TILE
+#define ENGRAM_HASH_TILE 64
+#endif
+constexpr int kHashTile = ENGRAM_HASH_TILE;     // tokens per CTA, hash-only kernel
 constexpr int kMinBlocks = ENGRAM_MIN_BLOCKS;   // occupancy hint for the fused kernel
 
 // ------------------------------------------------------------------------------------------------
