@@ -290,3 +290,39 @@ def test_fused_call_replays_from_a_cuda_graph():
     exp_h, _ = orc.hash(wl.ids, 0)
     H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "graph hashes")
     H.assert_bits_equal(H.bf16_bits(outs[0]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]), "graph rows")
+
+
+def test_layout_at_the_library_limits():
+    """8 layers, n-gram size 8, 9 heads: 504 hash columns per token (limit 512). The fused kernel's
+    shared memory (column constants, rolling values, row ids of a 16-token tile) then exceeds 48 KB
+    and is requested explicitly; the hash-only kernel stays below it."""
+    n_layers, max_ngram, n_heads = 8, 8, 9
+    primes = synth.distinct_primes_in(77, 2, 4000, (n_layers, max_ngram - 1, n_heads))
+    lay = synth.Layout(n_layers, max_ngram, n_heads, 32, 32, 500, 90, synth.uniform_int(77, synth.TAG_TOKEN_MAP, 500, 0, 90),
+                       synth.multipliers(77, n_layers, max_ngram, full64=True), primes, synth.column_offsets(primes))
+    assert n_layers * lay.n_cols == 504
+    rng = np.random.default_rng(77)
+    B, L = 2, 40
+    ids = rng.integers(0, 500, size=(B, L)).astype(np.int64)
+    mask = rng.random((B, L)) > 0.1
+    st = geng.EngramHash(n_layers=n_layers, max_ngram=max_ngram, n_heads=n_heads, head_dim=32, block=32,
+                         max_batch=B, max_seq_len=64, token_map=lay.token_map, multipliers=lay.multipliers,
+                         primes=lay.primes, offsets=lay.offsets)
+    orc = oracle.OracleState.from_layout(lay, B, 64)
+    Wh = [rng.integers(0, 0x7E, size=(r, 32), dtype=np.uint8) for r in lay.rows]
+    Sh = [rng.uniform(0.1, 1.0, size=(r, 1)).astype(np.float32) for r in lay.rows]
+    hashes = torch.empty((B, L, n_layers, lay.n_cols), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(ids), [H.to_dev(w) for w in Wh], [H.to_dev(x) for x in Sh], start_pos=0,
+                          mask=H.to_dev(mask), hashes=hashes)
+    exp_h, _ = orc.hash(ids, 0, mask)
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "limit-layout hashes")
+    for l in range(n_layers):
+        exp = oracle.engram_lookup(exp_h[:, :, l, :], Wh[l], Sh[l], lay.rows[l], 32, 32)
+        H.assert_bits_equal(H.bf16_bits(outs[l]), exp, f"limit-layout rows layer {l}")
+    st.reset()
+    H.assert_bits_equal(st.hash(H.to_dev(ids), 0, H.to_dev(mask)).cpu().numpy(), exp_h, "limit-layout hash-only")
+    with pytest.raises(geng.EngramError) as e:  # one more head: 8 x 7 x 10 = 560 columns
+        geng.engram_state_create(n_layers=8, max_ngram=8, n_heads=10, head_dim=32, block=32, max_batch=1,
+                                 max_seq_len=8, token_map=[0], multipliers=[1] * 64, primes=[3] * 560,
+                                 offsets=[0] * 560)
+    assert e.value.code == geng.ERR_UNSUPPORTED
