@@ -214,27 +214,25 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
   for (int i = tid; i < NL * N; i += nthr) mult_s[i] = sv.mult[i];
 
   // 1. compressed tokens of the tile and its halo: tok_s[j] holds position t0 - (N-1) + j.
-  //    In-chunk tokens come from ids (token_map, mask); earlier positions come from the cache,
-  //    which this launch never writes below start_pos, so reads and writes are disjoint.
-  if (row_ok) {
-    for (int j = tid; j < ntok + N - 1; j += nthr) {
-      const int64_t t = t0 - (N - 1) + j;
-      int32_t c;
-      if (t >= 0) {
-        const int64_t id = a.ids[seq_off + t];
-        if (id < 0 || id >= sv.raw_vocab) {
-          c = dead;
-          atomicOr(flags_s, ENGRAM_STATUS_BAD_ID);
-        } else {
-          c = sv.token_map[id];
-        }
-        if (a.mask != nullptr && a.mask[seq_off + t] == 0) c = dead;
+  //    In-chunk tokens come from ids (token_map, mask) and do not wait for the start position;
+  //    earlier positions come from the cache, which this launch never writes below start_pos, so
+  //    reads and writes are disjoint.
+  for (int j = tid; j < ntok + N - 1; j += nthr) {
+    const int64_t t = t0 - (N - 1) + j;
+    int32_t c = dead;
+    if (t >= 0) {
+      const int64_t id = a.ids[seq_off + t];
+      if (id < 0 || id >= sv.raw_vocab) {
+        if (row_ok) atomicOr(flags_s, ENGRAM_STATUS_BAD_ID);
       } else {
-        const int64_t p = s_b + t;
-        c = (p >= 0) ? cache_row[p] : dead;
+        c = sv.token_map[id];
       }
-      tok_s[j] = c;
+      if (a.mask != nullptr && a.mask[seq_off + t] == 0) c = dead;
+    } else if (row_ok) {
+      const int64_t p = s_b + t;
+      c = (p >= 0) ? cache_row[p] : dead;
     }
+    tok_s[j] = c;
   }
   __syncthreads();
 
