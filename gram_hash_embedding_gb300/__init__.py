@@ -26,7 +26,7 @@ from ._build import build
 __all__ = [
     "EngramError", "EngramHash", "build", "engram_state_create", "engram_state_destroy", "engram_cache_reset",
     "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
-    "engram_hash_lookup_varlen", "engram_gate", "engram_strerror", "STATUS_BAD_START", "STATUS_BAD_ID", "STATUS_BAD_LENGTH",
+    "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START", "STATUS_BAD_ID", "STATUS_BAD_LENGTH",
     "library_path",
 ]
 
@@ -294,6 +294,46 @@ def engram_gate(x: torch.Tensor, kv: torch.Tensor, q_weight: torch.Tensor, k_wei
     return out
 
 
+class PreparedHashLookup:
+    """A fused hash + lookup call whose arguments are checked and marshalled once, for serving loops
+    that call it many times on the same buffers (refill `ids` / `start_pos` / `mask` in place between
+    calls). Calling it only enqueues the kernel, without rebuilding pointer arrays or re-checking
+    tensors. It runs on the stream given here, or else on the stream current at each call (so it
+    also works inside a CUDA-graph capture)."""
+
+    def __init__(self, state: int, ids: torch.Tensor, start_pos: torch.Tensor, W: list, S: list,
+                 out: list, mask: torch.Tensor | None = None, hashes: torch.Tensor | None = None,
+                 cu_seqlens: torch.Tensor | None = None, max_len: int | None = None, stream=None):
+        n = len(W)
+        if n != len(S) or n != len(out) or n > MAX_LAYERS:
+            raise ValueError("W, S and out need one entry per engram layer")
+        self._keep = (ids, start_pos, W, S, out, mask, hashes, cu_seqlens)  # the buffers stay alive
+        self._W = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
+        self._S = (_P * n)(*[_dev(x, torch.float32, "S") for x in S])
+        self._R = (_I64 * n)(*[w.shape[0] for w in W])
+        self._O = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
+        m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+        h = None if hashes is None else _dev(hashes, torch.int64, "hashes")
+        sp = _dev(start_pos, torch.int32, "start_pos")
+        self._stream = None if stream is None else _stream(stream)
+        L = _lib()
+        if cu_seqlens is None:
+            B, T = ids.shape
+            self._fn = L.engram_hash_lookup
+            self._args = (state, _dev(ids, torch.int64, "ids"), m, sp, B, T, self._W, self._S, self._R, self._O, h)
+        else:
+            B = cu_seqlens.numel() - 1
+            self._fn = L.engram_hash_lookup_varlen
+            self._args = (state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"), sp, B,
+                          ids.numel(), _max_len(cu_seqlens, max_len), self._W, self._S, self._R, self._O, h)
+
+    def __call__(self) -> None:
+        st = self._stream if self._stream is not None else torch.cuda.current_stream().cuda_stream
+        rc = self._fn(*self._args, st)
+        if rc != OK:
+            raise EngramError(rc, "prepared engram_hash_lookup")
+
+
 # ----------------------------------------------------------------------------- convenience object
 class EngramHash:
     """A state plus the calls that use it (the hash module of the model, with its cache)."""
@@ -343,6 +383,10 @@ class EngramHash:
 
     def hash_lookup_varlen(self, ids, cu_seqlens, start_pos, W, S, mask=None, out=None, hashes=None, max_len=None):
         return engram_hash_lookup_varlen(self.handle, ids, cu_seqlens, start_pos, W, S, mask, out, hashes, max_len)
+
+    def prepare_hash_lookup(self, ids, start_pos, W, S, out, mask=None, hashes=None, cu_seqlens=None, max_len=None,
+                            stream=None) -> PreparedHashLookup:
+        return PreparedHashLookup(self.handle, ids, start_pos, W, S, out, mask, hashes, cu_seqlens, max_len, stream)
 
     def lookup(self, idx, W, S, out=None):
         return engram_lookup(idx, W, S, self.block, out)

@@ -29,6 +29,9 @@
  *     handled as documented below and recorded in the state's status word.
  *   - Caller-owned buffers stay caller-owned; the library only reads inputs and
  *     tables and writes the outputs it is given.
+ *   - A state's cache and status word are shared by every call on that state:
+ *     calls that may run at the same time (on different streams) must not use
+ *     the same cache rows; the library does not order them.
  */
 #ifndef ENGRAM_H
 #define ENGRAM_H

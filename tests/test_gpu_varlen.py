@@ -95,3 +95,26 @@ def test_inconsistent_extent_is_skipped_and_flagged():
     with pytest.raises(geng.EngramError) as e:
         st.hash_lookup_varlen(ids, cu, starts, Ws, Ss, max_len=65)  # max_len > max_seq_len
     assert e.value.code == geng.ERR_RANGE
+
+
+def test_prepared_call_matches_the_plain_call():
+    wl = synth.make_workload(0, full64=True)
+    B, L = 3, 20
+    rng = np.random.default_rng(11)
+    ids = torch.from_numpy(rng.integers(0, wl.layout.raw_vocab, size=(B, L)).astype(np.int64)).cuda()
+    start = torch.tensor([0, 3, 7], dtype=torch.int32, device="cuda")
+    a, b = H.make_state(wl, B, 128), H.make_state(wl, B, 128)
+    Ws, Ss = H.device_tables(wl)
+    out_a = [torch.empty((B, L, 6, 32), dtype=torch.bfloat16, device="cuda")]
+    out_b = [torch.empty((B, L, 6, 32), dtype=torch.bfloat16, device="cuda")]
+    ha = torch.empty((B, L, 1, 6), dtype=torch.int64, device="cuda")
+    hb = torch.empty_like(ha)
+    call = b.prepare_hash_lookup(ids, start, Ws, Ss, out_b, hashes=hb)
+    for step in range(3):  # refill the same buffers in place, as a serving loop would
+        ids.copy_(torch.from_numpy(rng.integers(0, wl.layout.raw_vocab, size=(B, L)).astype(np.int64)))
+        start += L
+        a.hash_lookup(ids, Ws, Ss, start_pos=start, out=out_a, hashes=ha)
+        call()
+        torch.cuda.synchronize()
+        assert (ha >= 0).all() and a.status() == 0 and b.status() == 0
+        assert torch.equal(ha, hb) and torch.equal(out_a[0].view(torch.int16), out_b[0].view(torch.int16))
