@@ -53,7 +53,11 @@ constexpr int kMinFusedTile = 4;                // below 4 tokens the halo and h
 #ifndef ENGRAM_HASH_TILE
 #define ENGRAM_HASH_TILE 64
 #endif
+#ifndef ENGRAM_HASH_THREADS
+#define ENGRAM_HASH_THREADS 128
+#endif
 constexpr int kHashTile = ENGRAM_HASH_TILE;     // tokens per CTA, hash-only kernel
+constexpr int kHashThreads = ENGRAM_HASH_THREADS;  // threads per CTA, hash-only kernel (<= kThreads)
 constexpr int kMinBlocks = ENGRAM_MIN_BLOCKS;   // occupancy hint for the fused kernel
 
 // ------------------------------------------------------------------------------------------------
@@ -430,7 +434,7 @@ cudaError_t launch_hash_k(const StateView& sv, const CallArgs& a, int tile, cuda
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)((a.L + tile - 1) / tile), (unsigned)a.B);
-  kern<<<grid, kThreads, plan.bytes, s>>>(sv, a, tile);
+  kern<<<grid, GATHER ? kThreads : kHashThreads, plan.bytes, s>>>(sv, a, tile);
   return cudaGetLastError();
 }
 
