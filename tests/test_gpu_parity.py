@@ -326,3 +326,36 @@ def test_layout_at_the_library_limits():
                                  max_seq_len=8, token_map=[0], multipliers=[1] * 64, primes=[3] * 560,
                                  offsets=[0] * 560)
     assert e.value.code == geng.ERR_UNSUPPORTED
+
+
+def test_hash_moduli_at_the_extremes():
+    """The floored mod on the GPU (multiply-high by floor((2^64-1)/P), one correction, 2^64 mod P
+    for negative running values) against the oracle's plain int64 `%` for moduli 1, 2, 3, near
+    2^31, near 2^62 (the limit) and offsets near the int64 limit, with full 64-bit multipliers so the
+    running values cover both signs."""
+    moduli = np.array([[[1, 2, 3], [2 ** 31 - 1, 2 ** 31 + 11, 2 ** 40 + 15]],
+                       [[2 ** 62 - 1, 2 ** 62 - 57, 2 ** 61 + 1], [97, 2 ** 62 - 3, 5]]], dtype=np.int64)
+    offsets = np.zeros((2, 6), dtype=np.int64)
+    offsets[0, 1] = 2 ** 63 - 2          # + (P-1) = 1 -> fits exactly
+    offsets[1, 0] = -(2 ** 62)
+    offsets[1, 5] = 12345
+    lay = synth.Layout(2, 3, 3, 16, 16, 256, 200, synth.uniform_int(9, synth.TAG_TOKEN_MAP, 256, 0, 200),
+                       synth.multipliers(9, 2, 3, full64=True), moduli, offsets)
+    rng = np.random.default_rng(9)
+    B, L = 4, 300
+    ids = rng.integers(0, 256, size=(B, L)).astype(np.int64)
+    st = geng.EngramHash(n_layers=2, max_ngram=3, n_heads=3, head_dim=16, block=16, max_batch=B, max_seq_len=L,
+                         token_map=lay.token_map, multipliers=lay.multipliers, primes=lay.primes, offsets=offsets)
+    orc = oracle.OracleState.from_layout(lay, B, L)
+    got = st.hash(H.to_dev(ids), 0).cpu().numpy()
+    exp, _ = orc.hash(ids, 0)
+    H.assert_bits_equal(got, exp, "extreme moduli")
+    assert (got[:, :, 0, 0] == 0).all()  # modulus 1
+    assert len(np.unique(got[:, :, 1, 1])) > 100  # a modulus near 2^62 spreads the ids
+    with pytest.raises(geng.EngramError) as e:  # offset + P - 1 past int64
+        bad = offsets.copy()
+        bad[0, 1] = 2 ** 63 - 1
+        geng.engram_state_create(n_layers=2, max_ngram=3, n_heads=3, head_dim=16, block=16, max_batch=1,
+                                 max_seq_len=8, token_map=lay.token_map, multipliers=lay.multipliers,
+                                 primes=lay.primes, offsets=bad)
+    assert e.value.code == geng.ERR_INVALID
