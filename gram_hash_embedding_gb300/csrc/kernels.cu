@@ -28,37 +28,37 @@
 namespace engram {
 namespace {
 
+// Launch shapes (compile-time; each default is the value measured fastest on a GB300).
 #ifndef ENGRAM_THREADS
 #define ENGRAM_THREADS 256
 #endif
 #ifndef ENGRAM_UNROLL
 #define ENGRAM_UNROLL 4
 #endif
-#ifndef ENGRAM_FUSED_TILE
-#define ENGRAM_FUSED_TILE 16
-#endif
 #ifndef ENGRAM_MIN_BLOCKS
 #define ENGRAM_MIN_BLOCKS 4
 #endif
-
-constexpr int kThreads = ENGRAM_THREADS;
-constexpr int kUnroll = ENGRAM_UNROLL;          // independent row pieces in flight per thread
+#ifndef ENGRAM_FUSED_TILE
+#define ENGRAM_FUSED_TILE 16
+#endif
 #ifndef ENGRAM_TARGET_CTAS
 #define ENGRAM_TARGET_CTAS 1216
 #endif
-
-constexpr int kFusedTile = ENGRAM_FUSED_TILE;   // largest tile (tokens per CTA) of the fused kernel
-constexpr int kTargetCtas = ENGRAM_TARGET_CTAS; // fused grid size the tile choice aims for (2 waves)
-constexpr int kMinFusedTile = 4;                // below 4 tokens the halo and hash phase dominate
 #ifndef ENGRAM_HASH_TILE
 #define ENGRAM_HASH_TILE 64
 #endif
 #ifndef ENGRAM_HASH_THREADS
 #define ENGRAM_HASH_THREADS 128
 #endif
-constexpr int kHashTile = ENGRAM_HASH_TILE;     // tokens per CTA, hash-only kernel
+
+constexpr int kThreads = ENGRAM_THREADS;           // threads per CTA, fused and lookup kernels
+constexpr int kUnroll = ENGRAM_UNROLL;             // independent row pieces in flight per thread
+constexpr int kMinBlocks = ENGRAM_MIN_BLOCKS;      // fused kernel: 4 CTAs per SM, i.e. <= 64 registers
+constexpr int kFusedTile = ENGRAM_FUSED_TILE;      // largest tile (tokens per CTA) of the fused kernel
+constexpr int kMinFusedTile = 4;                   // below 4 tokens the halo and hash phase dominate
+constexpr int kTargetCtas = ENGRAM_TARGET_CTAS;    // fused grid size the tile choice aims for (2 waves)
+constexpr int kHashTile = ENGRAM_HASH_TILE;        // tokens per CTA, hash-only kernel
 constexpr int kHashThreads = ENGRAM_HASH_THREADS;  // threads per CTA, hash-only kernel (<= kThreads)
-constexpr int kMinBlocks = ENGRAM_MIN_BLOCKS;   // occupancy hint for the fused kernel
 
 // ------------------------------------------------------------------------------------------------
 // integer helpers
