@@ -29,6 +29,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 
 FLAG_BAD_START = 1
 FLAG_BAD_ID = 2
+FLAG_BAD_ROW = 8
 
 
 def build(force: bool = False, src: str = _SRC, out: str = _LIB) -> str:
@@ -54,10 +55,11 @@ def _bind(path: str):
     lib.oracle_bf16_rne.restype = ctypes.c_uint16
     lib.oracle_floor_mod.argtypes = [_I, _I]
     lib.oracle_floor_mod.restype = _I
-    lib.oracle_engram_hash.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _I, _I, _P, _P]
+    lib.oracle_engram_hash.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I, _I, _P,
+                                       _P]
     lib.oracle_engram_hash.restype = ctypes.c_int
-    lib.oracle_engram_hash_varlen.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _I,
-                                              _P, _P]
+    lib.oracle_engram_hash_varlen.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P,
+                                              _I, _P, _P]
     lib.oracle_engram_hash_varlen.restype = ctypes.c_int
     lib.oracle_engram_lookup.argtypes = [_P, _I, _P, _P, _I, _I, _I, _P]
     lib.oracle_engram_lookup.restype = ctypes.c_int
@@ -121,38 +123,41 @@ class OracleState:
     def reset(self):
         self.cache[:] = self.dead
 
-    def hash(self, ids, start_pos, mask=None):
-        """ids int64 [B, L]; start_pos int or [B]; mask bool [B, L] or None.
-        Returns (hashes int64 [B, L, n_layers, C], flags)."""
+    def hash(self, ids, start_pos, mask=None, cache_rows=None):
+        """ids int64 [B, L]; start_pos int or [B]; mask bool [B, L] or None; cache_rows [B] or None
+        (row b uses cache row cache_rows[b], else b). Returns (hashes int64 [B, L, n_layers, C], flags)."""
         ids = np.ascontiguousarray(ids, dtype=np.int64)
         B, L = ids.shape
         sp = np.ascontiguousarray(np.broadcast_to(np.asarray(start_pos, dtype=np.int64), (B,)))
         m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8)
+        cr = None if cache_rows is None else np.ascontiguousarray(cache_rows, dtype=np.int64).reshape(B)
         out = np.empty((B, L, self.n_layers, self.n_cols), dtype=np.int64)
         flags = ctypes.c_uint32(0)
         rc = self.lib.oracle_engram_hash(
             self.n_layers, self.max_ngram, self.n_heads, _ptr(self.token_map), self.token_map.size, self.dead,
             self.pad_id, _ptr(self.multipliers), _ptr(self.primes), _ptr(self.offsets), _ptr(self.cache),
-            self.max_batch, self.max_seq_len, _ptr(ids), _ptr(m), _ptr(sp), B, L, _ptr(out), ctypes.byref(flags))
+            self.max_batch, self.max_seq_len, _ptr(ids), _ptr(m), _ptr(sp), _ptr(cr), B, L, _ptr(out),
+            ctypes.byref(flags))
         if rc != 0:
             raise ValueError(f"oracle_engram_hash rejected its arguments ({rc})")
         return out, flags.value
 
 
-    def hash_varlen(self, ids, cu_seqlens, start_pos, mask=None):
+    def hash_varlen(self, ids, cu_seqlens, start_pos, mask=None, cache_rows=None):
         """Packed sequences: ids int64 [T]; cu_seqlens [B+1]; start_pos [B]; mask bool [T] or None.
-        Sequence b uses cache row b. Returns (hashes int64 [T, n_layers, C], flags)."""
+        Sequence b uses cache row b (or cache_rows[b]). Returns (hashes int64 [T, n_layers, C], flags)."""
         ids = np.ascontiguousarray(ids, dtype=np.int64).reshape(-1)
         cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64).reshape(-1)
         B = cu.size - 1
         sp = np.ascontiguousarray(np.broadcast_to(np.asarray(start_pos, dtype=np.int64), (B,)))
         m = None if mask is None else np.ascontiguousarray(mask, dtype=np.uint8).reshape(-1)
+        cr = None if cache_rows is None else np.ascontiguousarray(cache_rows, dtype=np.int64).reshape(B)
         out = np.empty((ids.size, self.n_layers, self.n_cols), dtype=np.int64)
         flags = ctypes.c_uint32(0)
         rc = self.lib.oracle_engram_hash_varlen(
             self.n_layers, self.max_ngram, self.n_heads, _ptr(self.token_map), self.token_map.size, self.dead,
             self.pad_id, _ptr(self.multipliers), _ptr(self.primes), _ptr(self.offsets), _ptr(self.cache),
-            self.max_batch, self.max_seq_len, _ptr(ids), _ptr(m), _ptr(cu), _ptr(sp), B, _ptr(out),
+            self.max_batch, self.max_seq_len, _ptr(ids), _ptr(m), _ptr(cu), _ptr(sp), _ptr(cr), B, _ptr(out),
             ctypes.byref(flags))
         if rc != 0:
             raise ValueError(f"oracle_engram_hash_varlen rejected its arguments ({rc})")

@@ -29,6 +29,11 @@
  *   - an id outside [0, raw_vocab) is treated as a masked (DEAD) token and
  *     flagged; a row whose start position does not fit the cache writes
  *     nothing, gets hash -1 everywhere, and is flagged.
+ *   - call row b uses cache row b unless a cache-row map is given, in which
+ *     case it uses cache row cache_rows[b] (the pages index the cache by the
+ *     batch row; the map only renames rows, so each sequence is still hashed
+ *     exactly as the pages' `forward` hashes a batch row). A row mapped outside
+ *     the cache writes nothing, gets hash -1 everywhere, and is flagged.
  */
 #include <math.h>
 #include <stdint.h>
@@ -39,6 +44,7 @@
 
 #define ORACLE_FLAG_BAD_START 1u
 #define ORACLE_FLAG_BAD_ID 2u
+#define ORACLE_FLAG_BAD_ROW 8u
 
 /* ---------------------------------------------------------------- scalar definitions */
 
@@ -146,47 +152,71 @@ static uint32_t hash_sequence(int64_t n_layers, int64_t max_ngram, int64_t n_hea
   return fl;
 }
 
+/* The cache row of call row b: cache_rows[b] when a map is given, else b. A row outside
+ * [0, max_batch) gets hash -1 everywhere (L tokens from `hashes`) and returns -1. */
+static int64_t cache_row_of(const int64_t* cache_rows, int64_t b, int64_t max_batch, int64_t L, int64_t NC,
+                            int64_t* hashes) {
+  const int64_t r = cache_rows ? cache_rows[b] : b;
+  if (r >= 0 && r < max_batch) return r;
+  for (int64_t i = 0; i < L * NC; ++i) hashes[i] = -1;
+  return -1;
+}
+
 /* hashes[B][L][n_layers][C], C = (max_ngram - 1) * n_heads.
- * cache[cache_rows][cache_len] int64 holds compressed tokens across calls; sequence b uses row b.
+ * cache[max_batch][cache_len] int64 holds compressed tokens across calls; sequence b uses row b,
+ * or row cache_rows[b] when cache_rows is not NULL (rows of one call must differ).
  * multipliers[n_layers][max_ngram], primes[n_layers][max_ngram-1][n_heads],
  * offsets[n_layers][C]. mask may be NULL (every token takes part). */
 int oracle_engram_hash(int64_t n_layers, int64_t max_ngram, int64_t n_heads,
                        const int64_t* token_map, int64_t raw_vocab, int64_t dead, int64_t pad_id,
                        const int64_t* multipliers, const int64_t* primes, const int64_t* offsets,
-                       int64_t* cache, int64_t cache_rows, int64_t cache_len,
-                       const int64_t* ids, const uint8_t* mask, const int64_t* start_pos,
+                       int64_t* cache, int64_t max_batch, int64_t cache_len,
+                       const int64_t* ids, const uint8_t* mask, const int64_t* start_pos, const int64_t* cache_rows,
                        int64_t B, int64_t L, int64_t* hashes, uint32_t* flags) {
   if (n_layers < 1 || max_ngram < 2 || max_ngram > 64 || n_heads < 1 || B < 0 || L < 0) return ORACLE_EINVAL;
-  if (B > cache_rows) return ORACLE_EINVAL;
+  if (B > max_batch) return ORACLE_EINVAL;
   const int64_t C = (max_ngram - 1) * n_heads;
   uint32_t fl = 0;
   for (int64_t b = 0; b < B; ++b) {
+    int64_t* h = hashes + b * L * n_layers * C;
+    const int64_t r = cache_row_of(cache_rows, b, max_batch, L, n_layers * C, h);
+    if (r < 0) {
+      fl |= ORACLE_FLAG_BAD_ROW;
+      continue;
+    }
     fl |= hash_sequence(n_layers, max_ngram, n_heads, token_map, raw_vocab, dead, pad_id, multipliers, primes,
-                        offsets, cache + b * cache_len, cache_len, ids + b * L, mask ? mask + b * L : NULL,
-                        start_pos[b], L, hashes + b * L * n_layers * C);
+                        offsets, cache + r * cache_len, cache_len, ids + b * L, mask ? mask + b * L : NULL,
+                        start_pos[b], L, h);
   }
   if (flags) *flags |= fl;
   return ORACLE_OK;
 }
 
 /* Packed sequences: sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 of ids/mask/hashes
- * (hashes [T][n_layers][C]) and uses cache row b from position start_pos[b]. */
+ * (hashes [T][n_layers][C]) and uses cache row b (or cache_rows[b]) from position start_pos[b]. */
 int oracle_engram_hash_varlen(int64_t n_layers, int64_t max_ngram, int64_t n_heads,
                               const int64_t* token_map, int64_t raw_vocab, int64_t dead, int64_t pad_id,
                               const int64_t* multipliers, const int64_t* primes, const int64_t* offsets,
-                              int64_t* cache, int64_t cache_rows, int64_t cache_len,
+                              int64_t* cache, int64_t max_batch, int64_t cache_len,
                               const int64_t* ids, const uint8_t* mask, const int64_t* cu_seqlens,
-                              const int64_t* start_pos, int64_t B, int64_t* hashes, uint32_t* flags) {
+                              const int64_t* start_pos, const int64_t* cache_rows, int64_t B, int64_t* hashes,
+                              uint32_t* flags) {
   if (n_layers < 1 || max_ngram < 2 || max_ngram > 64 || n_heads < 1 || B < 0) return ORACLE_EINVAL;
-  if (B > cache_rows) return ORACLE_EINVAL;
+  if (B > max_batch) return ORACLE_EINVAL;
   const int64_t C = (max_ngram - 1) * n_heads;
   uint32_t fl = 0;
   for (int64_t b = 0; b < B; ++b) {
     const int64_t begin = cu_seqlens[b], L = cu_seqlens[b + 1] - cu_seqlens[b];
     if (L < 0) return ORACLE_EINVAL;
+    int64_t* h = hashes + begin * n_layers * C;
+    const int64_t r = cache_row_of(cache_rows, b, max_batch, L, n_layers * C, h);
+    if (r < 0) {
+      fl |= ORACLE_FLAG_BAD_ROW;
+      continue;
+    }
     fl |= hash_sequence(n_layers, max_ngram, n_heads, token_map, raw_vocab, dead, pad_id, multipliers, primes,
-                        offsets, cache + b * cache_len, cache_len, ids + begin, mask ? mask + begin : NULL,
-                        start_pos[b], L, hashes + begin * n_layers * C);
+                        offsets, cache + r * cache_len, cache_len, ids + begin, mask ? mask + begin : NULL,
+                        start_pos[b], L, h);
   }
   if (flags) *flags |= fl;
   return ORACLE_OK;

@@ -12,6 +12,7 @@ What pins what:
   - n-gram hash            <- big-integer brute force from explicit n-gram tuples (tests/brute.py),
                               closed forms for one-hot multipliers, and invariants
                               (bucket range, chunked == one-shot, locality, masked == all-pad)
+  - cache-row map          <- the same brute force on sequences that change call rows between calls
 """
 from __future__ import annotations
 
@@ -318,6 +319,63 @@ def pin_varlen(L=None):
     assert np.array_equal(d1.cache, d2.cache)
 
 
+def pin_cache_rows(L=None):
+    """A cache-row map (call row b uses cache row cache_rows[b]) only renames rows: sequences that
+    change call rows and call order between calls, each kept in its own cache row, hash like the
+    brute force on their own history; dense and packed calls alike."""
+    lay = _tiny_layouts()[2]
+    n_seq, total = 3, 60
+    rng = np.random.default_rng(61)
+    ids = rng.integers(0, lay.raw_vocab, size=(n_seq, total))
+    mask = rng.random((n_seq, total)) > 0.15
+    hist = _history_rows(ids, mask, lay)
+    slot = [4, 0, 2]  # sequence s lives in cache row slot[s] of a 5-row cache
+    st = oracle.OracleState.from_layout(lay, 5, 64, L)
+    pos = [0] * n_seq
+
+    def check(got_rows, order, lens):
+        for i, s in enumerate(order):
+            h = {q: v for q, v in hist[s].items() if q < pos[s] + lens[i]}
+            for t in range(lens[i]):
+                assert got_rows[i][t].tolist() == brute.hashes_at(h, pos[s] + t, lay), ("cache_rows", order, s, t)
+
+    for order, Lc in (([0, 1, 2], 7), ([2, 0], 5), ([1], 12), ([1, 2, 0], 3)):
+        cid = np.stack([ids[s, pos[s]:pos[s] + Lc] for s in order])
+        cm = np.stack([mask[s, pos[s]:pos[s] + Lc] for s in order])
+        got, fl = st.hash(cid, [pos[s] for s in order], cm, cache_rows=[slot[s] for s in order])
+        assert fl == 0
+        check(got, order, [Lc] * len(order))
+        for s in order:
+            pos[s] += Lc
+    # packed: sequences of different lengths (one empty), in yet another order
+    order, lens = [2, 1, 0], [4, 0, 6]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    pid = np.concatenate([ids[s, pos[s]:pos[s] + n] for s, n in zip(order, lens)])
+    pm = np.concatenate([mask[s, pos[s]:pos[s] + n] for s, n in zip(order, lens)])
+    got, fl = st.hash_varlen(pid, cu, [pos[s] for s in order], pm, cache_rows=[slot[s] for s in order])
+    assert fl == 0
+    check([got[cu[i]:cu[i + 1]] for i in range(len(order))], order, lens)
+    for s, n in zip(order, lens):
+        pos[s] += n
+    assert (st.cache[[1, 3]] == lay.dead).all()  # rows no sequence maps to are never written
+    # a row mapped outside the cache: hash -1, flagged, no write; the other row is unaffected
+    snap = st.cache.copy()
+    got, fl = st.hash(np.stack([ids[1, pos[1]:pos[1] + 4], ids[0, pos[0]:pos[0] + 4]]), [pos[1], pos[0]],
+                      np.stack([mask[1, pos[1]:pos[1] + 4], mask[0, pos[0]:pos[0] + 4]]), cache_rows=[5, slot[0]])
+    assert fl == oracle.FLAG_BAD_ROW and (got[0] == -1).all()
+    check(got[1:], [0], [4])
+    keep = [r for r in range(5) if r != slot[0]]
+    assert np.array_equal(st.cache[keep], snap[keep])
+    _, fl = st.hash(ids[:1, :2], [0], None, cache_rows=[-1])
+    assert fl == oracle.FLAG_BAD_ROW
+    # the identity map is the call without a map
+    a = oracle.OracleState.from_layout(lay, 3, 64, L)
+    b = oracle.OracleState.from_layout(lay, 3, 64, L)
+    ha, _ = a.hash(ids[:, :20], [0, 3, 9], mask[:, :20])
+    hb, _ = b.hash(ids[:, :20], [0, 3, 9], mask[:, :20], cache_rows=[0, 1, 2])
+    assert np.array_equal(ha, hb) and np.array_equal(a.cache, b.cache)
+
+
 # ----------------------------------------------------------------------------- Engram gate
 
 
@@ -402,4 +460,4 @@ def pin_gate(gate=None):
 
 
 ALL_PINS = [pin_floor_mod, pin_fp8_decode, pin_bf16, pin_lookup_vs_torch, pin_brute_force, pin_closed_forms,
-            pin_invariants, pin_varlen]
+            pin_invariants, pin_varlen, pin_cache_rows]

@@ -36,7 +36,10 @@ MUTANTS = {
     "unsigned_mod": ("const int64_t x = (int64_t)rolling;", "const int64_t x = (int64_t)(rolling >> 1);"),
     "cache_write_shift": ("cache_row[s + t] = c;", "cache_row[t] = c;"),
     "varlen_offset_dropped": ("ids + begin, mask ? mask + begin : NULL", "ids, mask"),
-    "varlen_cache_row": ("offsets, cache + b * cache_len, cache_len, ids + begin", "offsets, cache, cache_len, ids + begin"),
+    "varlen_cache_row": ("offsets, cache + r * cache_len, cache_len, ids + begin", "offsets, cache, cache_len, ids + begin"),
+    "dense_cache_row": ("offsets, cache + r * cache_len, cache_len, ids + b * L", "offsets, cache + b * cache_len, cache_len, ids + b * L"),
+    "cache_rows_ignored": ("const int64_t r = cache_rows ? cache_rows[b] : b;", "const int64_t r = b;"),
+    "bad_row_not_flagged": ("      fl |= ORACLE_FLAG_BAD_ROW;\n      continue;", "      continue;"),
     "fp8_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "fp8_subnormal": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     "fp8_mantissa": ("1.0 + (double)m / 8.0", "1.0 + (double)m / 16.0"),
