@@ -26,14 +26,15 @@ from ._build import build
 __all__ = [
     "EngramError", "EngramHash", "build", "engram_state_create", "engram_state_destroy", "engram_cache_reset",
     "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
-    "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START", "STATUS_BAD_ID", "STATUS_BAD_LENGTH",
-    "library_path",
+    "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START",
+    "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "library_path",
 ]
 
 OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
 STATUS_BAD_START = 1
 STATUS_BAD_ID = 2
 STATUS_BAD_LENGTH = 4
+STATUS_BAD_ROW = 8
 MAX_LAYERS = 8
 
 
@@ -70,11 +71,11 @@ def _lib():
         L.engram_state_destroy.argtypes = [_P]
         L.engram_cache_reset.argtypes = [_P, _P]
         L.engram_state_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
-        L.engram_hash.argtypes = [_P, _P, _P, _P, _I32, _I64, _P, _P]
+        L.engram_hash.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _P, _P]
         L.engram_lookup.argtypes = [_P, _I64, _P, _P, _I64, _I32, _I32, _P, _P]
-        L.engram_hash_lookup.argtypes = [_P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _P, _P]
-        L.engram_hash_varlen.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P]
-        L.engram_hash_lookup_varlen.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _P]
+        L.engram_hash_lookup.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _P, _P]
+        L.engram_hash_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P]
+        L.engram_hash_lookup_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _P]
         L.engram_state_layout.argtypes = [_P, ctypes.POINTER(_Layout)]
         L.engram_gate.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _I32, ctypes.c_float, _P, _P]
         L.engram_strerror.argtypes = [ctypes.c_int]
@@ -163,10 +164,15 @@ def _start_tensor(start_pos, B: int, device) -> torch.Tensor:
     return torch.full((B,), int(start_pos), dtype=torch.int32, device=device)
 
 
+def _rows_ptr(cache_rows):
+    return None if cache_rows is None else _dev(cache_rows, torch.int32, "cache_rows")
+
+
 def engram_hash(state: int, ids: torch.Tensor, start_pos, mask: torch.Tensor | None = None,
                 hashes: torch.Tensor | None = None, n_layers: int | None = None, n_cols: int | None = None,
-                stream=None) -> torch.Tensor:
-    """ids int64 [B, L] (CUDA); start_pos int or int32 [B]; mask bool/uint8 [B, L] or None.
+                stream=None, cache_rows: torch.Tensor | None = None) -> torch.Tensor:
+    """ids int64 [B, L] (CUDA); start_pos int or int32 [B]; mask bool/uint8 [B, L] or None;
+    cache_rows int32 [B] or None (row b uses cache row cache_rows[b], else b).
     Returns (or fills) int64 hash ids [B, L, n_layers, C]."""
     B, L = ids.shape
     if hashes is None:
@@ -175,8 +181,9 @@ def engram_hash(state: int, ids: torch.Tensor, start_pos, mask: torch.Tensor | N
                              device=ids.device)
     sp = _start_tensor(start_pos, B, ids.device)
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
-    _check(_lib().engram_hash(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"), B, L,
-                              _dev(hashes, torch.int64, "hashes"), _stream(stream)), "engram_hash")
+    _check(_lib().engram_hash(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"),
+                              _rows_ptr(cache_rows), B, L, _dev(hashes, torch.int64, "hashes"), _stream(stream)),
+           "engram_hash")
     return hashes
 
 
@@ -199,7 +206,8 @@ def engram_lookup(idx: torch.Tensor, W: torch.Tensor, S: torch.Tensor, block: in
 
 
 def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: list, mask: torch.Tensor | None = None,
-                       out: list | None = None, hashes: torch.Tensor | None = None, stream=None) -> list:
+                       out: list | None = None, hashes: torch.Tensor | None = None, stream=None,
+                       cache_rows: torch.Tensor | None = None) -> list:
     """Hash + per-layer lookup in one launch. W/S: per-layer tables. Returns (or fills) the
     per-layer bf16 outputs [B, L, C, D]."""
     B, L = ids.shape
@@ -218,8 +226,9 @@ def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: lis
     Rp = (_I64 * n)(*[w.shape[0] for w in W])
     Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
     hp = None if hashes is None else _dev(hashes, torch.int64, "hashes")
-    _check(_lib().engram_hash_lookup(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"), B,
-                                     L, Wp, Sp, Rp, Op, hp, _stream(stream)), "engram_hash_lookup")
+    _check(_lib().engram_hash_lookup(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"),
+                                     _rows_ptr(cache_rows), B, L, Wp, Sp, Rp, Op, hp, _stream(stream)),
+           "engram_hash_lookup")
     return out
 
 
@@ -232,7 +241,7 @@ def _max_len(cu_seqlens: torch.Tensor, max_len) -> int:
 
 def engram_hash_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, start_pos: torch.Tensor,
                        mask: torch.Tensor | None = None, hashes: torch.Tensor | None = None, max_len: int | None = None,
-                       stream=None) -> torch.Tensor:
+                       stream=None, cache_rows: torch.Tensor | None = None) -> torch.Tensor:
     """Packed sequences: ids int64 [T]; cu_seqlens int32 [B+1]; start_pos int32 [B]; mask [T] or None.
     Returns (or fills) int64 hash ids [T, n_layers, C]."""
     T = ids.numel()
@@ -243,14 +252,16 @@ def engram_hash_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, 
                              device=ids.device)
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     _check(_lib().engram_hash_varlen(state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"),
-                                     _dev(start_pos, torch.int32, "start_pos"), B, T, _max_len(cu_seqlens, max_len),
-                                     _dev(hashes, torch.int64, "hashes"), _stream(stream)), "engram_hash_varlen")
+                                     _dev(start_pos, torch.int32, "start_pos"), _rows_ptr(cache_rows), B, T,
+                                     _max_len(cu_seqlens, max_len), _dev(hashes, torch.int64, "hashes"),
+                                     _stream(stream)), "engram_hash_varlen")
     return hashes
 
 
 def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, start_pos: torch.Tensor,
                               W: list, S: list, mask: torch.Tensor | None = None, out: list | None = None,
-                              hashes: torch.Tensor | None = None, max_len: int | None = None, stream=None) -> list:
+                              hashes: torch.Tensor | None = None, max_len: int | None = None, stream=None,
+                              cache_rows: torch.Tensor | None = None) -> list:
     """Packed sequences, hash + per-layer lookup in one launch. Returns (or fills) per-layer bf16
     outputs [T, C, D]."""
     T = ids.numel()
@@ -271,7 +282,7 @@ def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.T
     hp = None if hashes is None else _dev(hashes, torch.int64, "hashes")
     _check(_lib().engram_hash_lookup_varlen(state, _dev(ids, torch.int64, "ids"), m,
                                             _dev(cu_seqlens, torch.int32, "cu_seqlens"),
-                                            _dev(start_pos, torch.int32, "start_pos"), B, T,
+                                            _dev(start_pos, torch.int32, "start_pos"), _rows_ptr(cache_rows), B, T,
                                             _max_len(cu_seqlens, max_len), Wp, Sp, Rp, Op, hp, _stream(stream)),
            "engram_hash_lookup_varlen")
     return out
@@ -303,11 +314,12 @@ class PreparedHashLookup:
 
     def __init__(self, state: int, ids: torch.Tensor, start_pos: torch.Tensor, W: list, S: list,
                  out: list, mask: torch.Tensor | None = None, hashes: torch.Tensor | None = None,
-                 cu_seqlens: torch.Tensor | None = None, max_len: int | None = None, stream=None):
+                 cu_seqlens: torch.Tensor | None = None, max_len: int | None = None, stream=None,
+                 cache_rows: torch.Tensor | None = None):
         n = len(W)
         if n != len(S) or n != len(out) or n > MAX_LAYERS:
             raise ValueError("W, S and out need one entry per engram layer")
-        self._keep = (ids, start_pos, W, S, out, mask, hashes, cu_seqlens)  # the buffers stay alive
+        self._keep = (ids, start_pos, W, S, out, mask, hashes, cu_seqlens, cache_rows)  # the buffers stay alive
         self._W = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
         self._S = (_P * n)(*[_dev(x, torch.float32, "S") for x in S])
         self._R = (_I64 * n)(*[w.shape[0] for w in W])
@@ -315,17 +327,18 @@ class PreparedHashLookup:
         m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
         h = None if hashes is None else _dev(hashes, torch.int64, "hashes")
         sp = _dev(start_pos, torch.int32, "start_pos")
+        cr = _rows_ptr(cache_rows)
         self._stream = None if stream is None else _stream(stream)
         L = _lib()
         if cu_seqlens is None:
             B, T = ids.shape
             self._fn = L.engram_hash_lookup
-            self._args = (state, _dev(ids, torch.int64, "ids"), m, sp, B, T, self._W, self._S, self._R, self._O, h)
+            self._args = (state, _dev(ids, torch.int64, "ids"), m, sp, cr, B, T, self._W, self._S, self._R, self._O, h)
         else:
             B = cu_seqlens.numel() - 1
             self._fn = L.engram_hash_lookup_varlen
-            self._args = (state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"), sp, B,
-                          ids.numel(), _max_len(cu_seqlens, max_len), self._W, self._S, self._R, self._O, h)
+            self._args = (state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"), sp, cr,
+                          B, ids.numel(), _max_len(cu_seqlens, max_len), self._W, self._S, self._R, self._O, h)
 
     def __call__(self) -> None:
         st = self._stream if self._stream is not None else torch.cuda.current_stream().cuda_stream
@@ -365,28 +378,32 @@ class EngramHash:
     def status(self, clear=True) -> int:
         return engram_state_status(self.handle, clear)
 
-    def hash(self, ids, start_pos=0, mask=None, hashes=None):
+    def hash(self, ids, start_pos=0, mask=None, hashes=None, cache_rows=None):
         if hashes is None:
             B, L = ids.shape
             hashes = torch.empty((B, L, self.n_layers, self.n_cols), dtype=torch.int64, device=ids.device)
-        return engram_hash(self.handle, ids, start_pos, mask, hashes)
+        return engram_hash(self.handle, ids, start_pos, mask, hashes, cache_rows=cache_rows)
 
-    def hash_lookup(self, ids, W, S, start_pos=0, mask=None, out=None, hashes=None):
+    def hash_lookup(self, ids, W, S, start_pos=0, mask=None, out=None, hashes=None, cache_rows=None):
         if out is None:
             B, L = ids.shape
             out = [torch.empty((B, L, self.n_cols, self.head_dim), dtype=torch.bfloat16, device=ids.device)
                    for _ in range(len(W))]
-        return engram_hash_lookup(self.handle, ids, start_pos, W, S, mask, out, hashes)
+        return engram_hash_lookup(self.handle, ids, start_pos, W, S, mask, out, hashes, cache_rows=cache_rows)
 
-    def hash_varlen(self, ids, cu_seqlens, start_pos, mask=None, hashes=None, max_len=None):
-        return engram_hash_varlen(self.handle, ids, cu_seqlens, start_pos, mask, hashes, max_len)
+    def hash_varlen(self, ids, cu_seqlens, start_pos, mask=None, hashes=None, max_len=None, cache_rows=None):
+        return engram_hash_varlen(self.handle, ids, cu_seqlens, start_pos, mask, hashes, max_len,
+                                  cache_rows=cache_rows)
 
-    def hash_lookup_varlen(self, ids, cu_seqlens, start_pos, W, S, mask=None, out=None, hashes=None, max_len=None):
-        return engram_hash_lookup_varlen(self.handle, ids, cu_seqlens, start_pos, W, S, mask, out, hashes, max_len)
+    def hash_lookup_varlen(self, ids, cu_seqlens, start_pos, W, S, mask=None, out=None, hashes=None, max_len=None,
+                           cache_rows=None):
+        return engram_hash_lookup_varlen(self.handle, ids, cu_seqlens, start_pos, W, S, mask, out, hashes, max_len,
+                                         cache_rows=cache_rows)
 
     def prepare_hash_lookup(self, ids, start_pos, W, S, out, mask=None, hashes=None, cu_seqlens=None, max_len=None,
-                            stream=None) -> PreparedHashLookup:
-        return PreparedHashLookup(self.handle, ids, start_pos, W, S, out, mask, hashes, cu_seqlens, max_len, stream)
+                            stream=None, cache_rows=None) -> PreparedHashLookup:
+        return PreparedHashLookup(self.handle, ids, start_pos, W, S, out, mask, hashes, cu_seqlens, max_len, stream,
+                                  cache_rows)
 
     def lookup(self, idx, W, S, out=None):
         return engram_lookup(idx, W, S, self.block, out)

@@ -52,6 +52,7 @@ engram::StateView view(const engram_state* st) {
   v.max_seq_len = st->lay.max_seq_len;
   v.pad_id = st->lay.pad_id;
   v.dead = (int32_t)st->lay.dead;
+  v.max_batch = st->lay.max_batch;
   v.n_layers = st->lay.n_layers;
   v.max_ngram = st->lay.max_ngram;
   v.n_heads = st->lay.n_heads;
@@ -75,12 +76,13 @@ void free_state(engram_state* st) {
 }
 
 // common checks of engram_hash / engram_hash_lookup
-int check_call(const engram_state* st, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos, int32_t B,
-               int64_t L) {
+int check_call(const engram_state* st, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
+               const int32_t* cache_rows, int32_t B, int64_t L) {
   (void)mask;
   if (st == nullptr || B < 0 || L < 0) return ENGRAM_ERR_INVALID;
   if (B == 0 || L == 0) return ENGRAM_OK;
   if (ids == nullptr || start_pos == nullptr || !aligned(ids, 8) || !aligned(start_pos, 4)) return ENGRAM_ERR_INVALID;
+  if (cache_rows != nullptr && !aligned(cache_rows, 4)) return ENGRAM_ERR_INVALID;
   if (B > st->lay.max_batch || L > st->lay.max_seq_len) return ENGRAM_ERR_RANGE;
   if ((int64_t)B * L > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
   if (!on_state_device(st)) return ENGRAM_ERR_INVALID;
@@ -88,12 +90,14 @@ int check_call(const engram_state* st, const int64_t* ids, const uint8_t* mask, 
 }
 
 engram::CallArgs call_args(const engram_state* st, const int64_t* ids, const uint8_t* mask,
-                           const int32_t* start_pos, int32_t B, int64_t L, int64_t* hashes) {
+                           const int32_t* start_pos, const int32_t* cache_rows, int32_t B, int64_t L,
+                           int64_t* hashes) {
   engram::CallArgs a;
   std::memset(&a, 0, sizeof a);
   a.ids = ids;
   a.mask = mask;
   a.start_pos = start_pos;
+  a.cache_rows = cache_rows;
   a.hashes = hashes;
   a.cu_seqlens = nullptr;
   a.L = L;
@@ -223,12 +227,12 @@ int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* f
   return ENGRAM_OK;
 }
 
-int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos, int32_t B,
-                int64_t L, int64_t* hashes, engram_stream_t stream) {
-  int rc = check_call(state, ids, mask, start_pos, B, L);
+int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
+                const int32_t* cache_rows, int32_t B, int64_t L, int64_t* hashes, engram_stream_t stream) {
+  int rc = check_call(state, ids, mask, start_pos, cache_rows, B, L);
   if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
   if (hashes == nullptr || !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
-  engram::CallArgs a = call_args(state, ids, mask, start_pos, B, L, hashes);
+  engram::CallArgs a = call_args(state, ids, mask, start_pos, cache_rows, B, L, hashes);
   return engram::launch_hash(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
 }
 
@@ -245,12 +249,13 @@ int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const flo
 }
 
 int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
-                       int32_t B, int64_t L, const uint8_t* const* W, const float* const* S, const int64_t* rows,
-                       uint16_t* const* out, int64_t* hashes, engram_stream_t stream) {
-  int rc = check_call(state, ids, mask, start_pos, B, L);
+                       const int32_t* cache_rows, int32_t B, int64_t L, const uint8_t* const* W,
+                       const float* const* S, const int64_t* rows, uint16_t* const* out, int64_t* hashes,
+                       engram_stream_t stream) {
+  int rc = check_call(state, ids, mask, start_pos, cache_rows, B, L);
   if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
   if (hashes != nullptr && !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
-  engram::CallArgs a = call_args(state, ids, mask, start_pos, B, L, hashes);
+  engram::CallArgs a = call_args(state, ids, mask, start_pos, cache_rows, B, L, hashes);
   rc = fill_tables(state, W, S, rows, out, &a);
   if (rc != ENGRAM_OK) return rc;
   return engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK
@@ -261,18 +266,19 @@ namespace {
 
 // common checks of the packed calls; on success fills *a (without tables)
 int packed_call(const engram_state* st, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
-                const int32_t* start_pos, int32_t B, int64_t T, int64_t max_len, int64_t* hashes,
-                engram::CallArgs* a) {
+                const int32_t* start_pos, const int32_t* cache_rows, int32_t B, int64_t T, int64_t max_len,
+                int64_t* hashes, engram::CallArgs* a) {
   if (st == nullptr || B < 0 || T < 0 || max_len < 0) return ENGRAM_ERR_INVALID;
   if (B == 0 || T == 0 || max_len == 0) return ENGRAM_OK;
   if (ids == nullptr || cu_seqlens == nullptr || start_pos == nullptr || !aligned(ids, 8) ||
       !aligned(cu_seqlens, 4) || !aligned(start_pos, 4))
     return ENGRAM_ERR_INVALID;
   if (hashes != nullptr && !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
+  if (cache_rows != nullptr && !aligned(cache_rows, 4)) return ENGRAM_ERR_INVALID;
   if (B > st->lay.max_batch || max_len > st->lay.max_seq_len) return ENGRAM_ERR_RANGE;
   if (T > ((int64_t)1 << 31) - 1) return ENGRAM_ERR_UNSUPPORTED;  // int32 extents
   if (!on_state_device(st)) return ENGRAM_ERR_INVALID;
-  *a = call_args(st, ids, mask, start_pos, B, max_len, hashes);
+  *a = call_args(st, ids, mask, start_pos, cache_rows, B, max_len, hashes);
   a->cu_seqlens = cu_seqlens;
   a->total = T;
   return ENGRAM_OK;
@@ -281,21 +287,21 @@ int packed_call(const engram_state* st, const int64_t* ids, const uint8_t* mask,
 }  // namespace
 
 int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
-                       const int32_t* start_pos, int32_t B, int64_t T, int64_t max_len, int64_t* hashes,
-                       engram_stream_t stream) {
+                       const int32_t* start_pos, const int32_t* cache_rows, int32_t B, int64_t T, int64_t max_len,
+                       int64_t* hashes, engram_stream_t stream) {
   if (hashes == nullptr && state != nullptr && B > 0 && T > 0 && max_len > 0) return ENGRAM_ERR_INVALID;
   engram::CallArgs a;
-  int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, B, T, max_len, hashes, &a);
+  int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, cache_rows, B, T, max_len, hashes, &a);
   if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
   return engram::launch_hash(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
 }
 
 int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
-                              const int32_t* cu_seqlens, const int32_t* start_pos, int32_t B, int64_t T,
-                              int64_t max_len, const uint8_t* const* W, const float* const* S, const int64_t* rows,
-                              uint16_t* const* out, int64_t* hashes, engram_stream_t stream) {
+                              const int32_t* cu_seqlens, const int32_t* start_pos, const int32_t* cache_rows,
+                              int32_t B, int64_t T, int64_t max_len, const uint8_t* const* W, const float* const* S,
+                              const int64_t* rows, uint16_t* const* out, int64_t* hashes, engram_stream_t stream) {
   engram::CallArgs a;
-  int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, B, T, max_len, hashes, &a);
+  int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, cache_rows, B, T, max_len, hashes, &a);
   if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
   rc = fill_tables(state, W, S, rows, out, &a);
   if (rc != ENGRAM_OK) return rc;

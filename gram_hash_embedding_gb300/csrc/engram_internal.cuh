@@ -27,6 +27,7 @@ struct StateView {
   int64_t max_seq_len;
   int64_t pad_id;
   int32_t dead;
+  int32_t max_batch;
   int32_t n_layers, max_ngram, n_heads, n_cols;
 };
 
@@ -35,6 +36,7 @@ struct CallArgs {
   const int64_t* ids;
   const uint8_t* mask;        // may be null
   const int32_t* start_pos;
+  const int32_t* cache_rows;  // [B] cache row of each call row; null: row b uses cache row b
   int64_t* hashes;            // may be null (fused)
   const int32_t* cu_seqlens;  // packed calls: [B+1] sequence extents in ids; null for dense [B, L] calls
   int64_t L;                  // dense: tokens per row; packed: the longest sequence (grid bound)

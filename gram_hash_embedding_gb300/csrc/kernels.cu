@@ -193,9 +193,10 @@ __host__ __device__ inline SmemPlan smem_plan(int n_layers, int max_ngram, int n
 
 // ------------------------------------------------------------------------------------------------
 // hash phase of one tile: `ntok` consecutive tokens starting at t0 of sequence b, whose Lb tokens
-// start at element seq_off of ids / mask / hashes and use cache row b. Called by every thread of
-// the CTA (contains barriers). Fills rowidx (layer-major: [l][t][col]) when given, and the optional
-// int64 hash output. Returns whether the sequence's start position fits the cache.
+// start at element seq_off of ids / mask / hashes and use cache row b (or cache_rows[b]). Called by
+// every thread of the CTA (contains barriers). Fills rowidx (layer-major: [l][t][col]) when given,
+// and the optional int64 hash output. Returns whether the sequence's cache row and start position
+// fit the cache.
 __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a, unsigned char* smem,
                                           const SmemPlan& plan, const int tile, const int b, const int64_t seq_off,
                                           const int64_t Lb, const int64_t t0, const int ntok, const bool want_rowidx,
@@ -209,11 +210,13 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
   int32_t* tok_s = reinterpret_cast<int32_t*>(smem + plan.tok_off);
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int64_t s_b = (int64_t)a.start_pos[b];
-  const bool row_ok = (s_b >= 0) && (s_b <= sv.max_seq_len - Lb);
+  const int64_t r_b = a.cache_rows != nullptr ? (int64_t)a.cache_rows[b] : (int64_t)b;
+  const bool slot_ok = (r_b >= 0) && (r_b < sv.max_batch);
+  const bool row_ok = slot_ok && (s_b >= 0) && (s_b <= sv.max_seq_len - Lb);
   const int32_t dead = sv.dead;
-  int32_t* cache_row = sv.cache + (int64_t)b * sv.max_seq_len;
+  int32_t* cache_row = sv.cache + (slot_ok ? r_b : 0) * sv.max_seq_len;  // dereferenced only when row_ok
 
-  if (tid == 0 && !row_ok) atomicOr(flags_s, ENGRAM_STATUS_BAD_START);
+  if (tid == 0 && !row_ok) atomicOr(flags_s, slot_ok ? ENGRAM_STATUS_BAD_START : ENGRAM_STATUS_BAD_ROW);
   for (int i = tid; i < NC; i += nthr) cols_s[i] = sv.cols[i];
   for (int i = tid; i < NL * N; i += nthr) mult_s[i] = sv.mult[i];
 

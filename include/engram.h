@@ -63,6 +63,8 @@ typedef struct engram_state engram_state;
 #define ENGRAM_STATUS_BAD_LENGTH 4u /* packed calls: a sequence's extent from cu_seqlens was negative, outside
                                        [0, T] or longer than max_len: that sequence was skipped entirely (no cache
                                        write, its hash ids and rows left unwritten) */
+#define ENGRAM_STATUS_BAD_ROW 8u   /* a cache_rows entry outside [0, max_batch): that row (sequence) wrote nothing to
+                                      the cache, its hash ids are -1 and its looked-up rows are +0 */
 
 /* Library limits. */
 #define ENGRAM_MAX_LAYERS 8       /* n_layers */
@@ -113,13 +115,18 @@ int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* f
  * The n-gram hash (blocks/stack-hashes page, hash `forward`).
  *   ids        device int64 [B][L] raw token ids
  *   mask       device uint8 [B][L] (non-zero = token takes part) or NULL (all take part)
- *   start_pos  device int32 [B]: position of ids[b][0] in cache row b (a scalar start is a filled array)
+ *   start_pos  device int32 [B]: position of ids[b][0] in row b's cache row (a scalar start is a filled array)
+ *   cache_rows device int32 [B] or NULL: row b reads and writes cache row cache_rows[b] (NULL: cache row b).
+ *              The pages index the cache by the batch row; the map only renames rows, so a serving loop can
+ *              keep each sequence in its own cache row whatever its place in the batch. The entries of one
+ *              call must differ (two rows on one cache row would race); an entry outside [0, max_batch) skips
+ *              that row and raises ENGRAM_STATUS_BAD_ROW.
  *   hashes     device int64 [B][L][n_layers][C], written
- * Writes cache[b][start_pos[b] + t] for every valid row. Rows never interact.
+ * Writes cache[r][start_pos[b] + t] (r = row b's cache row) for every valid row. Rows never interact.
  * B == 0 or L == 0 is a no-op. Errors: _INVALID (null, misaligned), _RANGE (B > max_batch, L > max_seq_len).
  */
-int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos, int32_t B,
-                int64_t L, int64_t* hashes, engram_stream_t stream);
+int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
+                const int32_t* cache_rows, int32_t B, int64_t L, int64_t* hashes, engram_stream_t stream);
 
 /*
  * The fp8 row lookup of one table (engram-first/lookup page, `ParallelEngramEmbedding.forward`, world size 1).
@@ -142,18 +149,20 @@ int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const flo
  * Errors: as engram_hash and engram_lookup.
  */
 int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
-                       int32_t B, int64_t L, const uint8_t* const* W, const float* const* S, const int64_t* rows,
-                       uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
+                       const int32_t* cache_rows, int32_t B, int64_t L, const uint8_t* const* W,
+                       const float* const* S, const int64_t* rows, uint16_t* const* out, int64_t* hashes,
+                       engram_stream_t stream);
 
 /*
  * Packed (variable-length) sequences, for continuous batching: B sequences of different lengths are
  * concatenated into one token array. Sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1,
- * sits at positions start_pos[b] .. of cache row b, and is hashed exactly as engram_hash would hash
- * it alone (blocks/stack-hashes page, hash `forward`, applied per sequence).
+ * sits at positions start_pos[b] .. of its cache row (b, or cache_rows[b]), and is hashed exactly as
+ * engram_hash would hash it alone (blocks/stack-hashes page, hash `forward`, applied per sequence).
  *   ids         device int64 [T] raw token ids
  *   mask        device uint8 [T] or NULL
  *   cu_seqlens  device int32 [B+1], non-decreasing, cu_seqlens[0] = 0 and cu_seqlens[B] = T expected
  *   start_pos   device int32 [B]
+ *   cache_rows  device int32 [B] or NULL: the cache row of sequence b, as in engram_hash
  *   max_len     host: an upper bound on every sequence's length (sizes the grid; max_len <= max_seq_len)
  *   hashes      device int64 [T][n_layers][C]
  * A sequence whose extent is inconsistent is skipped and flagged (ENGRAM_STATUS_BAD_LENGTH); a start
@@ -162,8 +171,8 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
  * Errors: _INVALID (null, misaligned, negative sizes), _RANGE (B > max_batch, max_len > max_seq_len).
  */
 int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
-                       const int32_t* start_pos, int32_t B, int64_t T, int64_t max_len, int64_t* hashes,
-                       engram_stream_t stream);
+                       const int32_t* start_pos, const int32_t* cache_rows, int32_t B, int64_t T, int64_t max_len,
+                       int64_t* hashes, engram_stream_t stream);
 
 /*
  * Packed sequences, hash and lookup in one launch (as engram_hash_lookup): out[l] is device bf16
@@ -171,9 +180,9 @@ int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* m
  * engram_hash_varlen and engram_hash_lookup.
  */
 int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
-                              const int32_t* cu_seqlens, const int32_t* start_pos, int32_t B, int64_t T,
-                              int64_t max_len, const uint8_t* const* W, const float* const* S, const int64_t* rows,
-                              uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
+                              const int32_t* cu_seqlens, const int32_t* start_pos, const int32_t* cache_rows,
+                              int32_t B, int64_t T, int64_t max_len, const uint8_t* const* W, const float* const* S,
+                              const int64_t* rows, uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
 
 /*
  * The Engram gate (blocks/stack-hashes page, `Engram.forward`, after the `wkv` projection), in fp32:

@@ -89,8 +89,13 @@ int main(int argc, char** argv) {
     Wl[l] = (const uint8_t*)d_W; Sl[l] = (const float*)d_S; Rl[l] = rows;
     CK(cudaMalloc((void**)&Ol[l], out_bytes));
   }
-  EK(engram_hash_lookup(st, (const int64_t*)d_ids, NULL, (const int32_t*)d_sp, B, L, Wl, Sl, Rl, Ol,
-                        (int64_t*)d_hash, NULL));
+  /* call row b uses cache row B-1-b: the reversed map must not change the hash ids */
+  int32_t* h_rows = (int32_t*)malloc((size_t)B * sizeof(int32_t));
+  for (int32_t b = 0; b < B; ++b) h_rows[b] = B - 1 - b;
+  void* d_rows = to_dev(h_rows, (size_t)B * sizeof(int32_t));
+  if (!d_rows) { fprintf(stderr, "device copy failed\n"); return 3; }
+  EK(engram_hash_lookup(st, (const int64_t*)d_ids, NULL, (const int32_t*)d_sp, (const int32_t*)d_rows, B, L, Wl, Sl,
+                        Rl, Ol, (int64_t*)d_hash, NULL));
   /* the standalone lookup of layer 0's hash ids must give layer 0's rows again */
   int64_t* h_hash = (int64_t*)malloc(hash_bytes);
   CK(cudaMemcpy(h_hash, d_hash, hash_bytes, cudaMemcpyDeviceToHost));

@@ -48,8 +48,8 @@ def test_plain_c_client(tmp_path):
     C = lay.n_cols
     hashes = np.fromfile(d / "hashes.out", dtype=np.int64).reshape(B, L, lay.n_layers, C)
     orc = oracle.OracleState.from_layout(lay, B, 64)
-    # the client's cache starts DEAD too, and its rows sit at per-row starts 0 and 3
-    exp_h, _ = orc.hash(ids, start.astype(np.int64))
+    # the client's cache starts DEAD too; its rows sit at per-row starts 0 and 3 of cache rows B-1-b
+    exp_h, _ = orc.hash(ids, start.astype(np.int64), cache_rows=np.arange(B)[::-1])
     assert np.array_equal(hashes, exp_h)
     exp_rows = oracle.engram_lookup(exp_h[:, :, 0, :], W, S, rows, lay.head_dim, lay.block)
     assert np.array_equal(np.fromfile(d / "rows0.out", dtype=np.uint16).reshape(exp_rows.shape), exp_rows)
