@@ -60,7 +60,24 @@ def parse_args(argv=None):
     p.add_argument("--graph", action="store_true",
                    help="capture the steps in a CUDA graph and replay it (removes host launch overhead; for the "
                         "small decode / chunk launches)")
+    p.add_argument("--probe", choices=["access", "gather", "layout"],
+                   help="run a DRAM measurement probe (bench_probe.cu) instead of the benchmark: access = DRAM "
+                        "bytes per random read size (under ncu), gather = the fused kernel's byte pattern without "
+                        "the hash, layout = scale placement next to the codes")
     return p.parse_args(argv)
+
+
+PROBE_SRC = os.path.join(ROOT, "bench_probe.cu")
+PROBE_BIN = os.path.join(ROOT, "_build", "bench_probe")
+
+
+def run_probe(mode: str) -> int:
+    """Compile bench_probe.cu for sm_103a (when stale) and run one of its modes."""
+    if not os.path.exists(PROBE_BIN) or os.path.getmtime(PROBE_BIN) < os.path.getmtime(PROBE_SRC):
+        os.makedirs(os.path.dirname(PROBE_BIN), exist_ok=True)
+        subprocess.check_call([os.environ.get("NVCC", "nvcc"), "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                               "-std=c++17", "-o", PROBE_BIN, PROBE_SRC])
+    return subprocess.call([PROBE_BIN, mode])
 
 
 # ----------------------------------------------------------------------------- distributed plumbing
@@ -783,6 +800,8 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.probe:
+        sys.exit(run_probe(args.probe))
     if args.impl == "reference":
         run_reference(args)
     elif args.block:

@@ -1,0 +1,264 @@
+// Measurement probes behind the fused kernel's roofline: what random row reads cost the DRAM on
+// this GPU, how fast the fused kernel's byte pattern can move at all, and whether placing a row's
+// fp32 scale next to its fp8 codes would change that. Timing and counting only: the regions are
+// uninitialised device memory, the outputs are meaningless, and nothing here is on the product
+// path. Built and run by `python bench.py --probe access|gather|layout`.
+//
+//   access  3,145,728 random reads of 4, 16, 32, 64 and 128 bytes (one kernel per size, named
+//           probe_read_<size>) into a 48 GB region; run it under ncu with dram__bytes_read.sum to
+//           see the DRAM bytes each access costs.
+//   gather  the fused kernel's bytes without the hash: per row a random 128-B code row and a random
+//           4-B scale read, 256 B written in order; 3,145,728 rows (one full-scale launch) out of
+//           768,022,850 (both full-scale tables), several launch shapes; read-only and write-only
+//           splits.
+//   layout  the same gather with the scale stored separately, not read, right after the codes
+//           (144-B and 256-B records) or in a block after every 32 rows.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#define CK(x)                                                                            \
+  do {                                                                                   \
+    cudaError_t e_ = (x);                                                                \
+    if (e_ != cudaSuccess) {                                                             \
+      std::printf("%s failed: %s\n", #x, cudaGetErrorString(e_));                        \
+      return 1;                                                                          \
+    }                                                                                    \
+  } while (0)
+
+namespace {
+
+constexpr int64_t kRowsFull = 768022850;  // 384,006,168 + 384,016,682 rows
+constexpr int64_t kN = 3145728;           // rows of one full-scale launch (65,536 tokens x 48)
+
+// splitmix64 finaliser: the row picked by access i of index set `seed`
+__device__ __forceinline__ uint64_t mix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__global__ void make_idx(int64_t* idx, int64_t n, int64_t rows, uint64_t seed) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i < n) idx[i] = (int64_t)(mix64(seed * 0x100000001ull + (uint64_t)i) % (uint64_t)rows);
+}
+
+// ---------------------------------------------------------------------------------------- access
+// One access of BYTES bytes at the start of a random 128-B slot: BYTES <= 16 is one lane's load,
+// larger sizes are BYTES/16 adjacent lanes loading 16 B each.
+template <int BYTES>
+__global__ void probe_read(const unsigned char* __restrict__ region, const int64_t* __restrict__ idx, int64_t n,
+                           uint32_t* __restrict__ sink) {
+  constexpr int LANES = BYTES >= 16 ? BYTES / 16 : 1;
+  const int64_t g = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / LANES;
+  const int lane = threadIdx.x % LANES;
+  if (g >= n) return;
+  const unsigned char* p = region + idx[g] * 128;
+  uint32_t v;
+  if (BYTES == 4) {
+    v = __ldg(reinterpret_cast<const uint32_t*>(p));
+  } else {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(p) + lane);
+    v = w.x ^ w.y ^ w.z ^ w.w;
+  }
+  if (v == 0x9E3779B9u) sink[0] = v;  // keeps the load; practically never taken
+}
+
+// ---------------------------------------------------------------------------------------- gather
+// LAYOUT 0: codes at base + 128 k, scale at sbase + 4 k (the pages' separate tensors)
+//        1: codes only (no scale read)
+//        2: records of STRIDE bytes: codes at STRIDE k, scale at STRIDE k + 128
+//        3: blocks of 32 rows: [32 x 128 B codes][32 x 4 B scales] (4,224 B)
+// MODE 0: read + write; 1: read only (a practically never taken store keeps the loads); 2: write only
+template <int U, int LAYOUT, int STRIDE, int MODE>
+__global__ void __launch_bounds__(256) probe_gather(const unsigned char* __restrict__ base,
+                                                    const float* __restrict__ sbase,
+                                                    const int64_t* __restrict__ idx, uint4* __restrict__ out,
+                                                    int64_t n_rows) {
+  const int lane8 = threadIdx.x & 7;
+  const int64_t groups = (int64_t)gridDim.x * (blockDim.x >> 3);
+  const int64_t g0 = blockIdx.x * (int64_t)(blockDim.x >> 3) + (threadIdx.x >> 3);
+  for (int64_t b0 = g0; b0 < n_rows; b0 += groups * U) {
+    uint4 v[U];
+    float s[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = b0 + (int64_t)u * groups;
+      v[u] = make_uint4((uint32_t)row, 1u, 2u, 3u);
+      s[u] = 1.f;
+      if (MODE != 2 && row < n_rows) {
+        const int64_t k = __ldg(idx + row);
+        const unsigned char* c;
+        const float* sp = nullptr;
+        if (LAYOUT == 0) {
+          c = base + k * 128;
+          sp = sbase + k;
+        } else if (LAYOUT == 1) {
+          c = base + k * 128;
+        } else if (LAYOUT == 2) {
+          c = base + k * STRIDE;
+          sp = reinterpret_cast<const float*>(c + 128);
+        } else {
+          const int64_t blk = k >> 5, j = k & 31;
+          c = base + blk * 4224 + j * 128;
+          sp = reinterpret_cast<const float*>(base + blk * 4224 + 4096 + j * 4);
+        }
+        v[u] = __ldg(reinterpret_cast<const uint4*>(c) + lane8);
+        if (LAYOUT != 1) s[u] = __ldg(sp);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = b0 + (int64_t)u * groups;
+      if (row >= n_rows) continue;
+      const uint32_t sb = __float_as_uint(s[u]);
+      const uint4 a = make_uint4(v[u].x ^ sb, v[u].y, v[u].z, v[u].w);
+      const uint4 b = make_uint4(v[u].x, v[u].y ^ sb, v[u].z, v[u].w);
+      uint4* o = out + row * 16;
+      if (MODE == 1) {
+        if ((a.x ^ b.y ^ a.z) == 0x12345678u) o[lane8] = a;
+      } else {
+        o[lane8] = a;
+        o[8 + lane8] = b;
+      }
+    }
+  }
+}
+
+struct Gather {
+  const unsigned char* base;
+  const float* sbase;
+  int64_t* idx[4];
+  uint4* out;
+  cudaEvent_t e0, e1;
+};
+
+template <int U, int LAYOUT, int STRIDE, int MODE>
+int time_gather(const Gather& g, const char* what, int blocks, int64_t* const* idx) {
+  const int reps = 200;
+  for (int w = 0; w < 3; ++w) probe_gather<U, LAYOUT, STRIDE, MODE><<<blocks, 256>>>(g.base, g.sbase, idx[w & 3], g.out, kN);
+  CK(cudaGetLastError());
+  CK(cudaDeviceSynchronize());
+  CK(cudaEventRecord(g.e0));
+  for (int i = 0; i < reps; ++i) probe_gather<U, LAYOUT, STRIDE, MODE><<<blocks, 256>>>(g.base, g.sbase, idx[i & 3], g.out, kN);
+  CK(cudaEventRecord(g.e1));
+  CK(cudaEventSynchronize(g.e1));
+  float ms = 0.f;
+  CK(cudaEventElapsedTime(&ms, g.e0, g.e1));
+  const double us = ms * 1e3 / reps;
+  const char* kind = MODE == 0 ? "read+write" : (MODE == 1 ? "read only" : "write only");
+  std::printf("%-44s %-10s grid %6d x 256, %d rows/thread-group pass: %7.1f us per launch\n", what, kind, blocks, U, us);
+  return 0;
+}
+
+int run_access(int64_t region_bytes) {
+  const int64_t slots = region_bytes / 128;
+  unsigned char* region;
+  int64_t* idx;
+  uint32_t* sink;
+  CK(cudaMalloc(&region, slots * 128));
+  CK(cudaMalloc(&idx, kN * 8));
+  CK(cudaMalloc(&sink, 4));
+  make_idx<<<(unsigned)((kN + 255) / 256), 256>>>(idx, kN, slots, 3);
+  CK(cudaDeviceSynchronize());
+  cudaEvent_t e0, e1;
+  CK(cudaEventCreate(&e0));
+  CK(cudaEventCreate(&e1));
+  std::printf("access probe: %lld random reads per launch into %.1f GB (one 128-B slot each)\n", (long long)kN,
+              slots * 128 / 1e9);
+  auto timed = [&](auto kernel, int bytes, int lanes) -> int {
+    const int64_t threads = kN * lanes;
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    for (int r = 0; r < 3; ++r) kernel<<<blocks, 256>>>(region, idx, kN, sink);
+    CK(cudaGetLastError());
+    CK(cudaEventRecord(e0));
+    kernel<<<blocks, 256>>>(region, idx, kN, sink);
+    CK(cudaEventRecord(e1));
+    CK(cudaEventSynchronize(e1));
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, e0, e1));
+    std::printf("probe_read_%d: %d-byte accesses, %7.1f us\n", bytes, bytes, ms * 1e3);
+    return 0;
+  };
+  int rc = 0;
+  rc |= timed(probe_read<4>, 4, 1);
+  rc |= timed(probe_read<16>, 16, 1);
+  rc |= timed(probe_read<32>, 32, 2);
+  rc |= timed(probe_read<64>, 64, 4);
+  rc |= timed(probe_read<128>, 128, 8);
+  return rc;
+}
+
+int run_gather(bool layout) {
+  const int64_t region = kRowsFull * 144;  // 110.6 GB: room for every layout
+  Gather g;
+  unsigned char* base;
+  CK(cudaMalloc(&base, region));
+  CK(cudaMalloc(&g.out, kN * 256));
+  int64_t* half[4];
+  for (int i = 0; i < 4; ++i) {
+    CK(cudaMalloc(&g.idx[i], kN * 8));
+    CK(cudaMalloc(&half[i], kN * 8));
+    make_idx<<<(unsigned)((kN + 255) / 256), 256>>>(g.idx[i], kN, kRowsFull, 11 + i);
+    make_idx<<<(unsigned)((kN + 255) / 256), 256>>>(half[i], kN, kRowsFull / 2, 21 + i);  // 256-B records
+  }
+  CK(cudaDeviceSynchronize());
+  g.base = base;
+  g.sbase = reinterpret_cast<const float*>(base + kRowsFull * 128);
+  CK(cudaEventCreate(&g.e0));
+  CK(cudaEventCreate(&g.e1));
+  int sms = 0;
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0));
+  const int short_ctas = (int)(kN / 128);  // 128 rows per CTA, one pass of 4 rows per thread group
+  int rc = 0;
+  std::printf("gather probe: %lld random rows per launch out of %lld (128-B codes + 4-B scale read, 256 B written)\n",
+              (long long)kN, (long long)kRowsFull);
+  if (!layout) {
+    rc |= time_gather<4, 0, 0, 0>(g, "separate scales, short CTAs", short_ctas, g.idx);
+    rc |= time_gather<1, 0, 0, 0>(g, "separate scales, one row per thread group", (int)(kN / 32), g.idx);
+    rc |= time_gather<4, 0, 0, 0>(g, "separate scales, persistent 4 CTAs/SM", sms * 4, g.idx);
+    rc |= time_gather<8, 0, 0, 0>(g, "separate scales, persistent 8 CTAs/SM", sms * 8, g.idx);
+    rc |= time_gather<4, 0, 0, 0>(g, "separate scales, 32 CTAs/SM", sms * 32, g.idx);
+    rc |= time_gather<4, 0, 0, 1>(g, "separate scales, short CTAs", short_ctas, g.idx);
+    rc |= time_gather<1, 0, 0, 1>(g, "separate scales, one row per thread group", (int)(kN / 32), g.idx);
+    rc |= time_gather<4, 0, 0, 2>(g, "separate scales, 8 CTAs/SM", sms * 8, g.idx);
+  } else {
+    for (int m = 0; m < 2; ++m) {
+      if (m == 0) {
+        rc |= time_gather<4, 0, 0, 0>(g, "separate scales", short_ctas, g.idx);
+        rc |= time_gather<4, 1, 0, 0>(g, "codes only (no scale read)", short_ctas, g.idx);
+        rc |= time_gather<4, 2, 144, 0>(g, "144-B records (scale after the codes)", short_ctas, g.idx);
+        rc |= time_gather<4, 2, 256, 0>(g, "256-B records (384M rows)", short_ctas, half);
+        rc |= time_gather<4, 3, 0, 0>(g, "blocks of 32 rows + their 32 scales", short_ctas, g.idx);
+      } else {
+        rc |= time_gather<4, 0, 0, 1>(g, "separate scales", short_ctas, g.idx);
+        rc |= time_gather<4, 1, 0, 1>(g, "codes only (no scale read)", short_ctas, g.idx);
+        rc |= time_gather<4, 2, 144, 1>(g, "144-B records (scale after the codes)", short_ctas, g.idx);
+        rc |= time_gather<4, 2, 256, 1>(g, "256-B records (384M rows)", short_ctas, half);
+        rc |= time_gather<4, 3, 0, 1>(g, "blocks of 32 rows + their 32 scales", short_ctas, g.idx);
+      }
+    }
+  }
+  return rc;
+}
+
+}  // namespace
+
+int main(int argc, char** argv) {
+  if (argc != 2 || (std::strcmp(argv[1], "access") && std::strcmp(argv[1], "gather") && std::strcmp(argv[1], "layout"))) {
+    std::printf("usage: %s access|gather|layout\n", argv[0]);
+    return 2;
+  }
+  size_t free_b = 0, total_b = 0;
+  CK(cudaMemGetInfo(&free_b, &total_b));
+  const bool access = !std::strcmp(argv[1], "access");
+  const int64_t need = access ? (int64_t)48e9 + kN * 8 : kRowsFull * 144 + kN * (256 + 64);
+  if ((int64_t)free_b < need + ((int64_t)2 << 30)) {
+    std::printf("probe needs %.1f GB of free device memory, %.1f GB free\n", need / 1e9, free_b / 1e9);
+    return 3;
+  }
+  return access ? run_access((int64_t)48e9) : run_gather(!std::strcmp(argv[1], "layout"));
+}

@@ -39,7 +39,7 @@ namespace {
 #define ENGRAM_MIN_BLOCKS 4
 #endif
 #ifndef ENGRAM_FUSED_TILE
-#define ENGRAM_FUSED_TILE 16
+#define ENGRAM_FUSED_TILE 8
 #endif
 #ifndef ENGRAM_TARGET_CTAS
 #define ENGRAM_TARGET_CTAS 1216
@@ -54,7 +54,9 @@ namespace {
 constexpr int kThreads = ENGRAM_THREADS;           // threads per CTA, fused and lookup kernels
 constexpr int kUnroll = ENGRAM_UNROLL;             // independent row pieces in flight per thread
 constexpr int kMinBlocks = ENGRAM_MIN_BLOCKS;      // fused kernel: 4 CTAs per SM, i.e. <= 64 registers
-constexpr int kFusedTile = ENGRAM_FUSED_TILE;      // largest tile (tokens per CTA) of the fused kernel
+constexpr int kFusedTile = ENGRAM_FUSED_TILE;      // largest tile (tokens per CTA) of the fused kernel: 8-token
+                                                   // tiles beat 16 at full scale (more, shorter CTAs keep more
+                                                   // row loads in flight; the hash phase is the same per token)
 constexpr int kMinFusedTile = 4;                   // below 4 tokens the halo and hash phase dominate
 constexpr int kTargetCtas = ENGRAM_TARGET_CTAS;    // fused grid size the tile choice aims for (2 waves)
 constexpr int kHashTile = ENGRAM_HASH_TILE;        // tokens per CTA, hash-only kernel

@@ -26,7 +26,7 @@ def _sample_positions(rng, B, L, n_layers, C, n):
     b = rng.integers(0, B, n)
     t = rng.integers(0, L, n)
     # tile edges and sequence ends
-    edge_t = np.array([0, 1, 15, 16, 17, L - 1])
+    edge_t = np.array([0, 1, 3, 4, 7, 8, 9, 15, 16, 17, L - 1])
     b = np.concatenate([b, np.repeat(np.arange(B), len(edge_t))])
     t = np.concatenate([t, np.tile(edge_t, B)])
     l = rng.integers(0, n_layers, b.size)

@@ -293,22 +293,23 @@ def test_fused_call_replays_from_a_cuda_graph():
 
 
 def test_layout_at_the_library_limits():
-    """8 layers, n-gram size 8, 9 heads: 504 hash columns per token (limit 512). The fused kernel's
-    shared memory (column constants, rolling values, row ids of a 16-token tile) then exceeds 48 KB
-    and is requested explicitly; the hash-only kernel stays below it."""
+    """8 layers, n-gram size 8, 9 heads: 504 hash columns per token (limit 512). At 1,216 tiles the
+    fused kernel keeps 8-token tiles, and its shared memory (column constants 16 KB, rolling values
+    3.5 KB, row ids 31.5 KB) exceeds 48 KB and is requested explicitly; the hash-only kernel stays
+    below it."""
     n_layers, max_ngram, n_heads = 8, 8, 9
     primes = synth.distinct_primes_in(77, 2, 4000, (n_layers, max_ngram - 1, n_heads))
     lay = synth.Layout(n_layers, max_ngram, n_heads, 32, 32, 500, 90, synth.uniform_int(77, synth.TAG_TOKEN_MAP, 500, 0, 90),
                        synth.multipliers(77, n_layers, max_ngram, full64=True), primes, synth.column_offsets(primes))
     assert n_layers * lay.n_cols == 504
     rng = np.random.default_rng(77)
-    B, L = 2, 40
+    B, L = 2, 608 * 8
     ids = rng.integers(0, 500, size=(B, L)).astype(np.int64)
     mask = rng.random((B, L)) > 0.1
     st = geng.EngramHash(n_layers=n_layers, max_ngram=max_ngram, n_heads=n_heads, head_dim=32, block=32,
-                         max_batch=B, max_seq_len=64, token_map=lay.token_map, multipliers=lay.multipliers,
+                         max_batch=B, max_seq_len=L, token_map=lay.token_map, multipliers=lay.multipliers,
                          primes=lay.primes, offsets=lay.offsets)
-    orc = oracle.OracleState.from_layout(lay, B, 64)
+    orc = oracle.OracleState.from_layout(lay, B, L)
     Wh = [rng.integers(0, 0x7E, size=(r, 32), dtype=np.uint8) for r in lay.rows]
     Sh = [rng.uniform(0.1, 1.0, size=(r, 1)).astype(np.float32) for r in lay.rows]
     hashes = torch.empty((B, L, n_layers, lay.n_cols), dtype=torch.int64, device="cuda")
