@@ -60,11 +60,44 @@ def parse_args(argv=None):
     p.add_argument("--graph", action="store_true",
                    help="capture the steps in a CUDA graph and replay it (removes host launch overhead; for the "
                         "small decode / chunk launches)")
+    p.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
+                   help="L2 between timed steps: flush = write 256 MB before every step and time the kernels "
+                        "alone; auto (default) = flush when the steps' rows fit in L2 (decode) and launches are "
+                        "eager; none = back to back")
     p.add_argument("--probe", choices=["access", "gather", "layout"],
                    help="run a DRAM measurement probe (bench_probe.cu) instead of the benchmark: access = DRAM "
                         "bytes per random read size (under ncu), gather = the fused kernel's byte pattern without "
                         "the hash, layout = scale placement next to the codes")
     return p.parse_args(argv)
+
+
+L2_BYTES = 129 * 1000 * 1000  # GB300 L2
+DECODE_STEPS = 128  # steps of the decode run (configuration 2)
+
+
+def l2_working_set(runner) -> int:
+    """DRAM bytes the timed steps touch across the cycled id batches: per row of every step a
+    128-byte atom for its codes (head_dim bytes, at least 128) and one for its scales, plus the
+    bf16 output (written to the same buffers every step)."""
+    lay = runner.lay
+    rows = runner.tokens_per_step * lay.n_layers * lay.n_cols
+    per_row_read = max(128, lay.head_dim) + 128
+    return rows * per_row_read * len(runner.ids) + rows * 2 * lay.head_dim
+
+
+def l2_note(runner, flushed: bool, fits: bool) -> str:
+    ws = l2_working_set(runner)
+    lay = runner.lay
+    tables = sum(lay.rows) * (lay.head_dim + 4 * lay.n_scales)
+    if flushed:
+        return (f"L2 flushed between timed steps (256 MB written outside the per-launch events; value from the "
+                f"event-timed kernels alone): the {len(runner.ids)} cycled id batches touch {ws / 1e6:.0f} MB, "
+                f"less than L2")
+    if fits:
+        return (f"warm: the {len(runner.ids)} cycled id batches touch {ws / 1e6:.0f} MB, which fits in the "
+                f"129 MB L2 (back-to-back steps, no flush)")
+    return (f"inputs larger than L2: {tables / 1e9:.1f} GB of tables read at random, {ws / 1e6:.0f} MB touched "
+            f"over the {len(runner.ids)} cycled id batches")
 
 
 PROBE_SRC = os.path.join(ROOT, "bench_probe.cu")
@@ -257,12 +290,14 @@ class Runner:
             self.S.append(S)
         self.state = geng.EngramHash(n_layers=lay.n_layers, max_ngram=lay.max_ngram, n_heads=lay.n_heads,
                                      head_dim=lay.head_dim, block=lay.block, max_batch=wl.max_batch,
-                                     max_seq_len=wl.max_seq_len, token_map=lay.token_map,
+                                     max_seq_len=wl.max_seq_len + (DECODE_STEPS if cfg == 2 else 0),
+                                     token_map=lay.token_map,
                                      multipliers=lay.multipliers, primes=lay.primes, offsets=lay.offsets,
                                      dead=lay.dead, pad_id=lay.pad_id)
         seed = rank_seed(synth.MASTER_SEED + 17, rank)
         self.varlen = cfg == 7
-        # batches: distinct id sets cycled step to step
+        # batches: distinct id sets (each with its start positions) cycled step to step
+        starts = None
         if cfg == 7:
             ids = [wl.ids]
             masks = [None]
@@ -275,19 +310,31 @@ class Runner:
             masks = [wl.mask]
             self.chunks = [(k * wl.L, (k + 1) * wl.L) for k in range(wl.chunks)]
             self.B, self.L = 1, total
+        elif cfg == 2:
+            # a decode run: step k gives every row its next Zipf token at position start + k, so the
+            # steps gather different rows (about 400 MB of row atoms over the run, three times L2);
+            # on rank 0 step 0 is the workload's own decode step
+            P = wl.prefill_ids.shape[1]
+            base = synth.MASTER_SEED + 2 if rank == 0 else seed
+            ids = [synth.zipf_ids(base, wl.B, offset=wl.B * P + k * wl.B).reshape(wl.B, 1) for k in range(DECODE_STEPS)]
+            assert rank != 0 or np.array_equal(ids[0], wl.ids)
+            starts = [wl.start_pos.astype(np.int32) + k for k in range(DECODE_STEPS)]
+            masks = [None] * len(ids)
+            self.chunks = [(0, 1)]
+            self.B, self.L = wl.B, 1
         else:
-            n_batches = 4 if cfg != 2 else 1
             ids = [wl.ids if (k == 0 and rank == 0) else
-                   synth.uniform_ids(seed + k, wl.B * wl.L).reshape(wl.B, wl.L) for k in range(n_batches)]
-            if cfg == 2:
-                ids = [wl.ids]
+                   synth.uniform_ids(seed + k, wl.B * wl.L).reshape(wl.B, wl.L) for k in range(4)]
             masks = [wl.mask] * len(ids)
             self.chunks = [(0, wl.L)]
             self.B, self.L = wl.B, wl.L
         self.ids_host = ids
         self.ids = [torch.from_numpy(np.ascontiguousarray(a)).to(device) for a in ids]
         self.masks = [None if m is None else torch.from_numpy(np.ascontiguousarray(m)).to(device) for m in masks]
-        self.start = torch.from_numpy(np.ascontiguousarray(wl.start_pos.astype(np.int32))).to(device)
+        if starts is None:
+            starts = [wl.start_pos.astype(np.int32)]
+        self.starts = [torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device) for a in starts]
+        self.start = self.starts[0]  # the start positions of explicit-ids steps (the end-to-end leg sets them)
         if wl.prefill_ids is not None:  # decode / continuous batching: history first
             self.state.hash(torch.from_numpy(wl.prefill_ids).to(device), 0)
         Lc = self.chunks[0][1] - self.chunks[0][0]
@@ -299,9 +346,9 @@ class Runner:
         self.calls = None
         if len(self.chunks) == 1:
             self.calls = [self.geng.PreparedHashLookup(
-                self.state.handle, i, self.start, self.W, self.S, self.out, mask=m,
+                self.state.handle, i, self.starts[j % len(self.starts)], self.W, self.S, self.out, mask=m,
                 cu_seqlens=self.cu if self.varlen else None, max_len=self.L if self.varlen else None)
-                for i, m in zip(self.ids, self.masks)]
+                for j, (i, m) in enumerate(zip(self.ids, self.masks))]
         self.kernel_name = f"hash_kernel<GATHER=true, D={lay.head_dim}> (hash + gather + dequant)"
         torch.cuda.synchronize(device)
 
@@ -310,15 +357,16 @@ class Runner:
         if ids is None and mask is None and self.calls is not None:
             self.calls[k % len(self.calls)]()
             return
+        start = self.starts[k % len(self.starts)] if ids is None else self.start
         ids = self.ids[k % len(self.ids)] if ids is None else ids
         mask = self.masks[k % len(self.masks)] if mask is None else mask
         if self.varlen:
-            self.geng.engram_hash_lookup_varlen(self.state.handle, ids, self.cu, self.start, self.W, self.S, mask,
+            self.geng.engram_hash_lookup_varlen(self.state.handle, ids, self.cu, start, self.W, self.S, mask,
                                                 self.out, max_len=self.L)
             return
         for c0, c1 in self.chunks:
             if len(self.chunks) == 1:
-                ii, mm, sp = ids, mask, self.start
+                ii, mm, sp = ids, mask, start
             else:
                 ii = ids[:, c0:c1]
                 mm = None if mask is None else mask[:, c0:c1]
@@ -351,7 +399,7 @@ class Runner:
         if self.mode == "hash":
             ids = self.ids[k % len(self.ids)]
             mask = self.masks[k % len(self.masks)]
-            self.geng.engram_hash(self.state.handle, ids, self.start, mask, self.hash_out)
+            self.geng.engram_hash(self.state.handle, ids, self.starts[k % len(self.starts)], mask, self.hash_out)
         elif self.mode == "lookup":
             for l in range(self.lay.n_layers):
                 self.geng.engram_lookup(self.idx[l], self.W[l], self.S[l], self.lay.block, self.lookup_out[l])
@@ -370,7 +418,7 @@ class Runner:
         torch = self.torch
         self.ids_pinned = [torch.from_numpy(self.np.ascontiguousarray(a)).pin_memory() for a in self.ids_host]
         self.mask_pinned = [None if m is None else m.cpu().pin_memory() for m in self.masks]
-        self.start_pinned = self.start.cpu().pin_memory()
+        self.start_pinned = [s.cpu().pin_memory() for s in self.starts]
         self.ids_dev = torch.empty_like(self.ids[0])
         self.mask_dev = None if self.masks[0] is None else torch.empty_like(self.masks[0])
         self.start_dev = torch.empty_like(self.start)
@@ -392,7 +440,7 @@ class Runner:
         self.ids_dev.copy_(self.ids_pinned[j], non_blocking=True)
         if self.mask_dev is not None:
             self.mask_dev.copy_(self.mask_pinned[j % len(self.mask_pinned)], non_blocking=True)
-        self.start_dev.copy_(self.start_pinned, non_blocking=True)
+        self.start_dev.copy_(self.start_pinned[j % len(self.start_pinned)], non_blocking=True)
         saved, saved_cu = self.start, getattr(self, "cu", None)
         self.start = self.start_dev
         if self.varlen:
@@ -437,16 +485,17 @@ class Runner:
         cur.wait_stream(self.copy_stream)
 
     def e2e_bytes(self):
-        h2d = self.ids_pinned[0].numel() * 8 + self.start_pinned.numel() * 4 + (4 * self.cu.numel() if self.varlen else 0)
+        h2d = self.ids_pinned[0].numel() * 8 + self.start_pinned[0].numel() * 4 + (4 * self.cu.numel() if self.varlen else 0)
         if self.mask_dev is not None:
             h2d += self.mask_dev.numel()
         d2h = sum(o.numel() * 2 for o in self.out) * len(self.chunks)
         return h2d, d2h
 
 
-def time_region(torch, dist, dev_index, fn, steps, stream, per_launch_events=False, n_launch=1):
-    """Run `fn(k)` `steps` times between barriers and synchronisations; returns (total seconds, mean
-    seconds between the per-step events) from CUDA events on `stream`."""
+def time_region(torch, dist, dev_index, fn, steps, stream, per_launch_events=False, between=None):
+    """Run `fn(k)` `steps` times between barriers and synchronisations; returns (total seconds, per-step
+    seconds between the events around each `fn(k)`, or None) from CUDA events on `stream`.
+    `between(k)`, when given, runs before each step outside its events (an L2 flush)."""
     torch.cuda.synchronize()
     barrier(dist, dev_index)
     torch.cuda.synchronize()
@@ -455,6 +504,8 @@ def time_region(torch, dist, dev_index, fn, steps, stream, per_launch_events=Fal
     pairs = []
     start.record(stream)
     for k in range(steps):
+        if between is not None:
+            between(k)
         if per_launch_events:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
@@ -468,8 +519,8 @@ def time_region(torch, dist, dev_index, fn, steps, stream, per_launch_events=Fal
     torch.cuda.synchronize()
     barrier(dist, dev_index)
     total = start.elapsed_time(end) / 1e3
-    mean = statistics.mean(a.elapsed_time(b) for a, b in pairs) / 1e3 if pairs else None
-    return total, mean
+    per_step = [a.elapsed_time(b) / 1e3 for a, b in pairs] if pairs else None
+    return total, per_step
 
 
 def cpu_baselines(runner, n_tokens: int):
@@ -673,6 +724,10 @@ def run_ours(args):
     runner.setup_mode(args.mode)
     stream = torch.cuda.current_stream(device)
     K, W = args.steps, args.warmup
+    fits_l2 = l2_working_set(runner) < L2_BYTES
+    flush_l2 = args.l2 == "flush" or (args.l2 == "auto" and fits_l2 and not args.graph)
+    if flush_l2 and args.graph:
+        raise SystemExit("--l2 flush times each kernel between flushes; use eager launches (no --graph)")
     for k in range(W):
         runner.step_mode(k)
     torch.cuda.synchronize()
@@ -696,11 +751,19 @@ def run_ours(args):
         clocks.start()
         total, _ = time_region(torch, dist, local, lambda k: graph.replay(), replays, stream)
         clocks.stop()
-        mean_launch = total / K
+        mean_launch = median_launch = total / K
     else:
+        flush = None
+        if flush_l2:
+            l2_scratch = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # twice the 129 MB L2
+            flush = lambda k: l2_scratch.fill_(k & 0xFF)  # noqa: E731
         clocks.start()
-        total, mean_launch = time_region(torch, dist, local, runner.step_mode, K, stream, per_launch_events=True)
+        total, per_step = time_region(torch, dist, local, runner.step_mode, K, stream, per_launch_events=True,
+                                      between=flush)
         clocks.stop()
+        mean_launch, median_launch = statistics.mean(per_step), statistics.median(per_step)
+        if flush_l2:  # the timed work is the kernels alone; the flushes between them are not counted
+            total = sum(per_step)
     total_max = max_over_ranks(dist, total, device)
     tokens = runner.tokens_per_step * K * world
     value = tokens / total_max
@@ -744,7 +807,7 @@ def run_ours(args):
         "dtype": "f32",
         "data": "synthetic",
         "config": {
-            "workload": wl.name,
+            "workload": wl.name if args.cfg != 2 else f"{wl.name}, a run of {DECODE_STEPS} consecutive steps",
             "cfg": args.cfg,
             "B": runner.B,
             "L": runner.L,
@@ -755,8 +818,7 @@ def run_ours(args):
             "table_rows": lay.rows,
             "arithmetic": "hash int64 (wrapping multiply, XOR, floored mod); fp8 E4M3 x fp32 scale in fp32, RNE to bf16",
             "parallelism": f"replicas x{world} (no exchange step)",
-            "l2": "inputs larger than L2: ~98 GB of tables read at random, 805 MB of bf16 written per step; "
-                  f"{len(runner.ids)} distinct id batches cycled",
+            "l2": l2_note(runner, flush_l2, fits_l2),
             "status_flags_after_warmup": flags,
             "launch": "CUDA graph replay" if args.graph else "eager launches from Python",
         },
@@ -764,6 +826,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": algo_bytes, "launch_us": launch_s * 1e6,
+                     "launch_us_median": median_launch / runner.launches_per_step * 1e6,
                      "kernel": runner.kernel_name},
         "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke, "ms_per_step": e_total / Ke * 1e3, "call": "engram_hash_lookup",

@@ -86,3 +86,17 @@ def test_all_cores_oracle_timing_runs():
     h, _ = oracle.OracleState.from_layout(lay, 2, 300).hash(ids, 0)
     th, tl, cores = bench.cpu_baseline_all_cores(lay, ids, None, _compact_tables(lay, h, 6))
     assert th > 0 and tl > 0 and cores >= 1
+
+
+def test_l2_working_set_decides_the_flush():
+    """Decode steps touch a few MB of rows (they fit in L2, so the bench flushes L2 between them by
+    default); the prefill and full-scale steps touch far more than L2."""
+    from types import SimpleNamespace
+
+    lay = synth.make_layout("prefill", 1)
+    decode = SimpleNamespace(lay=lay, tokens_per_step=256, ids=[0] * 4)
+    full = SimpleNamespace(lay=synth.make_layout("full", 1), tokens_per_step=65536, ids=[0] * 4)
+    assert bench.l2_working_set(decode) < bench.L2_BYTES < bench.l2_working_set(full)
+    assert "flushed" in bench.l2_note(decode, True, True) and "warm" in bench.l2_note(decode, False, True)
+    assert "larger than L2" in bench.l2_note(full, False, False)
+    assert bench.parse_args([]).l2 == "auto"
