@@ -456,7 +456,9 @@ cudaError_t launch_lookup_g(const int64_t* idx, int64_t n_idx, const uint8_t* W,
   constexpr int G = D / 16;
   const int64_t units = n_idx * G;
   int64_t blocks = (units + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
-  const int64_t cap = (int64_t)sm_count() * 8;
+  // many short CTAs beat a grid-stride loop over a few (146.4 -> 142.0 us for 1.57M rows at 32 per
+  // SM instead of 8); the cap only keeps huge calls inside the grid limit
+  const int64_t cap = (int64_t)sm_count() * 32;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const int blk_shift = ilog2(blk);
