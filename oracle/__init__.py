@@ -61,7 +61,11 @@ def _bind(path: str):
     lib.oracle_engram_hash_varlen.argtypes = [_I, _I, _I, _P, _I, _I, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P,
                                               _I, _P, _P]
     lib.oracle_engram_hash_varlen.restype = ctypes.c_int
-    lib.oracle_engram_lookup.argtypes = [_P, _I, _P, _P, _I, _I, _I, _P]
+    lib.oracle_engram_lookup.argtypes = [_P, _I, _P, _P, _I, _I, _I, _I, _P]
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = ctypes.c_float
+    lib.oracle_e8m0_to_f32.argtypes = [ctypes.c_uint8]
+    lib.oracle_e8m0_to_f32.restype = ctypes.c_float
     lib.oracle_engram_lookup.restype = ctypes.c_int
     return lib
 
@@ -164,14 +168,27 @@ class OracleState:
         return out, flags.value
 
 
-def engram_lookup(idx, W, S, rows, D, block, L=None) -> np.ndarray:
-    """idx int64 [...]; W uint8 [rows, D]; S float32 [rows, D/block]. Returns bf16 bits uint16 [..., D]."""
+SCALE_F32, SCALE_BF16, SCALE_E8M0, SCALE_E4M3 = 0, 1, 2, 3
+_SCALE_STORAGE = {SCALE_F32: np.float32, SCALE_BF16: np.uint16, SCALE_E8M0: np.uint8, SCALE_E4M3: np.uint8}
+
+
+def bf16_to_f32(h: int, L=None) -> float:
+    return (L or lib()).oracle_bf16_to_f32(h)
+
+
+def e8m0_to_f32(e: int, L=None) -> float:
+    return (L or lib()).oracle_e8m0_to_f32(e)
+
+
+def engram_lookup(idx, W, S, rows, D, block, L=None, scale_dtype=SCALE_F32) -> np.ndarray:
+    """idx int64 [...]; W uint8 [rows, D]; S [rows, D/block] stored as scale_dtype (float32 values, or
+    the uint16 bits of bf16, or the uint8 codes of UE8M0 / E4M3). Returns bf16 bits uint16 [..., D]."""
     idx = np.ascontiguousarray(idx, dtype=np.int64)
     W = np.ascontiguousarray(W, dtype=np.uint8)
-    S = np.ascontiguousarray(S, dtype=np.float32)
+    S = np.ascontiguousarray(S, dtype=_SCALE_STORAGE[scale_dtype])
     out = np.empty(idx.shape + (D,), dtype=np.uint16)
     rc = (L or lib()).oracle_engram_lookup(_ptr(idx), idx.size, _ptr(W), _ptr(S), int(rows), int(D), int(block),
-                                           _ptr(out))
+                                           int(scale_dtype), _ptr(out))
     if rc != 0:
         raise ValueError(f"oracle_engram_lookup rejected its arguments ({rc})")
     return out

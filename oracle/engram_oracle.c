@@ -15,7 +15,8 @@
  *     negated image mask.
  *   - engram-first/lookup page, `ParallelEngramEmbedding.forward`: out-of-range
  *     rows are read as row 0 and then zeroed; fp8 values are widened to fp32,
- *     multiplied block-wise by the fp32 scale, and converted to bf16.
+ *     multiplied block-wise by the scale widened to fp32 (`.float()`), and
+ *     converted to bf16.
  *
  * Precision: the pages fix it (`.float()` on both operands, one multiply,
  * `.to(torch.bfloat16)`), so the dequant is one fp32 round-to-nearest multiply
@@ -29,6 +30,9 @@
  *   - an id outside [0, raw_vocab) is treated as a masked (DEAD) token and
  *     flagged; a row whose start position does not fit the cache writes
  *     nothing, gets hash -1 everywhere, and is flagged.
+ *   - the scale dtype (`scale_dtype`, left open by the pages) is fp32, bf16,
+ *     UE8M0 or E4M3; each widens to fp32 exactly, as `.float()` does, before
+ *     the one fp32 multiply.
  *   - call row b uses cache row b unless a cache-row map is given, in which
  *     case it uses cache row cache_rows[b] (the pages index the cache by the
  *     batch row; the map only renames rows, so each sequence is still hashed
@@ -45,6 +49,11 @@
 #define ORACLE_FLAG_BAD_START 1u
 #define ORACLE_FLAG_BAD_ID 2u
 #define ORACLE_FLAG_BAD_ROW 8u
+
+#define ORACLE_SCALE_F32 0
+#define ORACLE_SCALE_BF16 1
+#define ORACLE_SCALE_E8M0 2
+#define ORACLE_SCALE_E4M3 3
 
 /* ---------------------------------------------------------------- scalar definitions */
 
@@ -63,6 +72,20 @@ float oracle_fp8_e4m3_to_f32(uint8_t code) {
     v = ldexp(1.0 + (double)m / 8.0, e - 7);
   }
   return (float)(sign ? -v : v);
+}
+
+/* bfloat16 is the upper half of an IEEE binary32: widening appends 16 zero bits (exact). */
+float oracle_bf16_to_f32(uint16_t h) {
+  const uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* OCP UE8M0: 8 exponent bits, no sign, no mantissa: 2^(e - 127); e = 255 is NaN. */
+float oracle_e8m0_to_f32(uint8_t e) {
+  if (e == 0xFF) return NAN;
+  return (float)ldexp(1.0, (int)e - 127); /* 2^-127 is an fp32 subnormal, still exact */
 }
 
 /* bf16 = the upper half of an IEEE binary32, rounded to nearest, ties to even.
@@ -224,11 +247,22 @@ int oracle_engram_hash_varlen(int64_t n_layers, int64_t max_ngram, int64_t n_hea
 
 /* ---------------------------------------------------------------- fp8 row lookup */
 
-/* out[n_idx][D] bf16 bits. W[rows][D] E4M3 codes, S[rows][D / block] fp32.
- * An index outside [0, rows) gives a row of +0. */
-int oracle_engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
-                         int64_t D, int64_t block, uint16_t* out) {
+/* Scale i of a scale tensor stored as `scale_dtype`, widened to fp32. */
+static float scale_at(const void* S, int64_t scale_dtype, int64_t i) {
+  switch (scale_dtype) {
+    case ORACLE_SCALE_BF16: return oracle_bf16_to_f32(((const uint16_t*)S)[i]);
+    case ORACLE_SCALE_E8M0: return oracle_e8m0_to_f32(((const uint8_t*)S)[i]);
+    case ORACLE_SCALE_E4M3: return oracle_fp8_e4m3_to_f32(((const uint8_t*)S)[i]);
+    default: return ((const float*)S)[i];
+  }
+}
+
+/* out[n_idx][D] bf16 bits. W[rows][D] E4M3 codes, S[rows][D / block] scales stored as
+ * scale_dtype (ORACLE_SCALE_*). An index outside [0, rows) gives a row of +0. */
+int oracle_engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
+                         int64_t D, int64_t block, int64_t scale_dtype, uint16_t* out) {
   if (n_idx < 0 || D < 1 || block < 1 || D % block != 0) return ORACLE_EINVAL;
+  if (scale_dtype < ORACLE_SCALE_F32 || scale_dtype > ORACLE_SCALE_E4M3) return ORACLE_EINVAL;
   const int64_t n_scales = D / block;
   for (int64_t i = 0; i < n_idx; ++i) {
     const int64_t r = idx[i];
@@ -238,7 +272,7 @@ int oracle_engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, co
       uint16_t y = 0;
       if (!out_of_range) {
         const float value = oracle_fp8_e4m3_to_f32(W[local * D + k]);
-        const float scale = S[local * n_scales + k / block];
+        const float scale = scale_at(S, scale_dtype, local * n_scales + k / block);
         const float prod = value * scale; /* one fp32 multiply, round to nearest */
         y = oracle_bf16_rne(prod);
       }

@@ -8,7 +8,8 @@ What pins what:
   - bf16 rounding          <- torch's float32 -> bfloat16 conversion (RNE)
   - lookup                 <- the same library calls the engram-first/lookup page makes
                               (F.embedding, .float(), block multiply, .to(bfloat16), masked_fill),
-                              run on torch CPU
+                              run on torch CPU, with fp32, bf16, UE8M0 and E4M3 scale tensors,
+                              plus hand values of each scale format
   - n-gram hash            <- big-integer brute force from explicit n-gram tuples (tests/brute.py),
                               closed forms for one-hot multipliers, and invariants
                               (bucket range, chunked == one-shot, locality, masked == all-pad)
@@ -80,16 +81,20 @@ def pin_bf16(L=None):
 # ----------------------------------------------------------------------------- lookup
 
 
-def torch_lookup(idx: np.ndarray, W: np.ndarray, S: np.ndarray, D: int, block: int) -> np.ndarray:
+def torch_lookup(idx: np.ndarray, W: np.ndarray, S: np.ndarray, D: int, block: int,
+                 scale_dtype: int = oracle.SCALE_F32) -> np.ndarray:
     """The engram-first/lookup page's `ParallelEngramEmbedding.forward` at world size 1,
-    executed with the same torch library calls on the CPU. Returns bf16 bits."""
+    executed with the same torch library calls on the CPU, with the scale tensor stored as
+    `scale_dtype` (float32 values, or the bits of bf16 / UE8M0 / E4M3). Returns bf16 bits."""
     import torch
     import torch.nn.functional as F
 
     rows = W.shape[0]
     indices = torch.from_numpy(idx.astype(np.int64))
     weight = torch.from_numpy(W.copy()).view(torch.float8_e4m3fn)
-    scale = torch.from_numpy(S.copy())
+    as_dtype = {oracle.SCALE_F32: torch.float32, oracle.SCALE_BF16: torch.bfloat16,
+                oracle.SCALE_E8M0: torch.float8_e8m0fnu, oracle.SCALE_E4M3: torch.float8_e4m3fn}[scale_dtype]
+    scale = torch.from_numpy(S.copy()).view(as_dtype)
     mask = (indices < 0) | (indices >= rows)
     local = indices.masked_fill(mask, 0)
     values = F.embedding(local, weight)
@@ -132,6 +137,37 @@ def pin_lookup_vs_torch(L=None):
     S = np.array([[0.5], [1.0]], dtype=np.float32)
     out = oracle.engram_lookup(np.array([0, 1, 2]), W, S, 2, 16, 16, L)
     assert (out[0] == 0x3F00).all() and (out[1] == 0x43E0).all() and (out[2] == 0).all()
+
+
+def pin_scale_dtypes(L=None):
+    """The other scale storage types widen exactly to fp32 (`.float()`) before the one fp32
+    multiply: every bf16 pattern class, all 256 UE8M0 and E4M3 codes, against the same torch
+    library calls, plus hand values of each format's definition."""
+    rng = np.random.default_rng(8)
+    # every UE8M0 exponent; every E4M3 scale code; bf16: normal, subnormal, zero, inf, NaN patterns
+    e8 = np.arange(256, dtype=np.uint8)
+    bf = np.concatenate([rng.integers(0, 1 << 16, size=250), [0x0000, 0x8000, 0x0001, 0x807F, 0x7F80, 0xFF80,
+                                                              0x7FC0, 0x3F80]]).astype(np.uint16)
+    for dtype, codes in ((oracle.SCALE_E8M0, e8), (oracle.SCALE_E4M3, e8), (oracle.SCALE_BF16, bf)):
+        for D, block in ((32, 32), (64, 16)):
+            nsc = D // block
+            rows = -(-codes.size // nsc)
+            S = np.resize(codes, rows * nsc).reshape(rows, nsc)
+            W = rng.integers(0, 256, size=(rows, D), dtype=np.uint8)
+            W[0, :16] = [0x00, 0x80, 0x01, 0x81, 0x08, 0x38, 0x7E, 0xFE, 0x7F, 0xFF, 0x30, 0x40, 0x77, 0x06, 0x3F, 0x47]
+            idx = np.concatenate([np.arange(rows), rng.integers(-3, rows + 3, size=100)])
+            got = oracle.engram_lookup(idx, W, S, rows, D, block, L, scale_dtype=dtype)
+            _cmp_bf16(got, torch_lookup(idx, W, S, D, block, dtype))
+    # hand values: UE8M0 127 is 1, 0 is 2^-127 (an fp32 subnormal), 130 is 8, 255 is NaN;
+    # bf16 0x3FC0 is 1.5; E4M3 scale 0x40 is 2
+    assert oracle.e8m0_to_f32(127, L) == 1.0 and oracle.e8m0_to_f32(130, L) == 8.0
+    assert oracle.e8m0_to_f32(0, L) == 2.0 ** -127 and np.isnan(oracle.e8m0_to_f32(255, L))
+    assert oracle.bf16_to_f32(0x3FC0, L) == 1.5 and oracle.bf16_to_f32(0x8000, L) == 0.0
+    W = np.array([[0x38] * 16], dtype=np.uint8)  # 1.0
+    for dtype, sc, want in ((oracle.SCALE_E8M0, [[126]], 0x3F00), (oracle.SCALE_BF16, [[0x3FC0]], 0x3FC0),
+                            (oracle.SCALE_E4M3, [[0x40]], 0x4000)):
+        out = oracle.engram_lookup(np.array([0]), W, np.array(sc), 1, 16, 16, L, scale_dtype=dtype)
+        assert (out == want).all(), (dtype, hex(int(out[0, 0])))
 
 
 # ----------------------------------------------------------------------------- hash
@@ -460,4 +496,4 @@ def pin_gate(gate=None):
 
 
 ALL_PINS = [pin_floor_mod, pin_fp8_decode, pin_bf16, pin_lookup_vs_torch, pin_brute_force, pin_closed_forms,
-            pin_invariants, pin_varlen, pin_cache_rows]
+            pin_invariants, pin_varlen, pin_cache_rows, pin_scale_dtypes]

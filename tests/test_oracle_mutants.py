@@ -41,13 +41,18 @@ MUTANTS = {
     "cache_rows_ignored": ("const int64_t r = cache_rows ? cache_rows[b] : b;", "const int64_t r = b;"),
     "bad_row_not_flagged": ("      fl |= ORACLE_FLAG_BAD_ROW;\n      continue;", "      continue;"),
     "fp8_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e8m0_bias": ("return (float)ldexp(1.0, (int)e - 127);", "return (float)ldexp(1.0, (int)e - 128);"),
+    "e8m0_nan_dropped": ("  if (e == 0xFF) return NAN;\n", ""),
+    "bf16_widen_shift": ("const uint32_t u = (uint32_t)h << 16;", "const uint32_t u = (uint32_t)h << 15;"),
+    "scale_dtype_ignored": ("    case ORACLE_SCALE_E8M0: return oracle_e8m0_to_f32(((const uint8_t*)S)[i]);\n", ""),
     "fp8_subnormal": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     "fp8_mantissa": ("1.0 + (double)m / 8.0", "1.0 + (double)m / 16.0"),
     "fp8_sign": ("return (float)(sign ? -v : v);", "return (float)v;"),
     "bf16_truncate": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) {", "if (0) {"),
     "bf16_ties_away": ("(lower == 0x8000u && (upper & 1u))", "(lower == 0x8000u)"),
-    "scale_block_index": ("S[local * n_scales + k / block]", "S[local * n_scales + k % n_scales]"),
-    "scale_row_index": ("S[local * n_scales + k / block]", "S[k / block]"),
+    "scale_block_index": ("scale_at(S, scale_dtype, local * n_scales + k / block)",
+                          "scale_at(S, scale_dtype, local * n_scales + k % n_scales)"),
+    "scale_row_index": ("scale_at(S, scale_dtype, local * n_scales + k / block)", "scale_at(S, scale_dtype, k / block)"),
     "masked_rows_read": ("const int64_t local = out_of_range ? 0 : r;", "const int64_t local = out_of_range ? 0 : r;\n    const int dummy_ = out_of_range; (void)dummy_;"),
 }
 # the last one is a no-op control: it must *survive* (proves the harness can pass)
