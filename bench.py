@@ -44,10 +44,11 @@ def parse_args(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--cfg", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7],
+    p.add_argument("--cfg", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8],
                    help="1 prefill B4xL4096, 2 decode B256xL1, 3 full-scale B8xL8192 (default), 4 long chunked, "
                         "5 profiling case (prefill shapes, 1 GB tables), 6 full-scale with head_dim 256, "
-                        "7 continuous batching (packed decode + prefill sequences)")
+                        "7 continuous batching (packed decode + prefill sequences), 8 full-scale with head_dim 256 "
+                        "and UE8M0 scales")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=0, help="steps of the end-to-end loop (default min(K, 100))")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -258,8 +259,23 @@ def recorded_traffic(cfg: int):
 
 
 def algo_bytes_per_token(lay) -> int:
+    """fp8 row + its scales (of the layout's storage width) read, bf16 row written, per hash column."""
     D, nsc = lay.head_dim, lay.head_dim // lay.block
-    return lay.n_layers * lay.n_cols * (D + 4 * nsc + 2 * D)
+    return lay.n_layers * lay.n_cols * (D + lay.scale_bytes * nsc + 2 * D)
+
+
+def scale_torch_dtype(torch, scale_dtype: int):
+    """torch dtype of a scale tensor of storage type `scale_dtype` (SCALE_F32, BF16, E8M0, E4M3)."""
+    return [torch.float32, torch.bfloat16, torch.float8_e8m0fnu, torch.float8_e4m3fn][scale_dtype]
+
+
+def scale_bits(torch, t):
+    """Host numpy copy of a device scale tensor: fp32 values, or the bits of the other storage types."""
+    if t.dtype == torch.float32:
+        return t.cpu().numpy()
+    if t.element_size() == 2:
+        return t.view(torch.int16).cpu().numpy().view("uint16")
+    return t.view(torch.uint8).cpu().numpy()
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -284,8 +300,8 @@ class Runner:
         self.W, self.S = [], []
         for l, rows in enumerate(lay.rows):
             W = torch.empty((rows, lay.head_dim), dtype=torch.uint8, device=device)
-            S = torch.empty((rows, lay.n_scales), dtype=torch.float32, device=device)
-            synth.fill_table_device(W, S, wl.table_seed, l)
+            S = torch.empty((rows, lay.n_scales), dtype=scale_torch_dtype(torch, lay.scale_dtype), device=device)
+            synth.fill_table_device(W, S, wl.table_seed, l, lay.scale_dtype)
             self.W.append(W)
             self.S.append(S)
         self.state = geng.EngramHash(n_layers=lay.n_layers, max_ngram=lay.max_ngram, n_heads=lay.n_heads,
@@ -293,7 +309,7 @@ class Runner:
                                      max_seq_len=wl.max_seq_len + (DECODE_STEPS if cfg == 2 else 0),
                                      token_map=lay.token_map,
                                      multipliers=lay.multipliers, primes=lay.primes, offsets=lay.offsets,
-                                     dead=lay.dead, pad_id=lay.pad_id)
+                                     dead=lay.dead, pad_id=lay.pad_id, scale_dtype=lay.scale_dtype)
         seed = rank_seed(synth.MASTER_SEED + 17, rank)
         self.varlen = cfg == 7
         # batches: distinct id sets (each with its start positions) cycled step to step
@@ -349,7 +365,9 @@ class Runner:
                 self.state.handle, i, self.starts[j % len(self.starts)], self.W, self.S, self.out, mask=m,
                 cu_seqlens=self.cu if self.varlen else None, max_len=self.L if self.varlen else None)
                 for j, (i, m) in enumerate(zip(self.ids, self.masks))]
-        self.kernel_name = f"hash_kernel<GATHER=true, D={lay.head_dim}> (hash + gather + dequant)"
+        sname = ["fp32", "bf16", "UE8M0", "E4M3"][lay.scale_dtype]
+        self.scale_name = sname
+        self.kernel_name = f"hash_kernel<GATHER=true, D={lay.head_dim}, {sname} scales> (hash + gather + dequant)"
         torch.cuda.synchronize(device)
 
     def step(self, k: int, ids=None, mask=None):
@@ -553,10 +571,10 @@ def cpu_baselines(runner, n_tokens: int):
         inv = inv.astype(np.int64)
         sel = torch.from_numpy(uniq).to(runner.device)
         Wc = runner.W[l][sel].cpu().numpy()
-        Sc = runner.S[l][sel].cpu().numpy()
+        Sc = scale_bits(torch, runner.S[l][sel])
         compact.append((inv, Wc, Sc, int(uniq.size)))
         t0 = time.perf_counter()
-        oracle.engram_lookup(inv, Wc, Sc, uniq.size, lay.head_dim, lay.block)
+        oracle.engram_lookup(inv, Wc, Sc, uniq.size, lay.head_dim, lay.block, scale_dtype=lay.scale_dtype)
         t_lookup += time.perf_counter() - t0
     tokens = sub.size
     what = (f"first {tokens} tokens of the same workload ({rows_used} sequence(s) x {cut}); hash + lookup of their "
@@ -602,11 +620,11 @@ def _oracle_task(task):
         t0 = time.perf_counter()
         orc.hash(ids, 0, mask)
         return time.perf_counter() - t0
-    _, _, l, a, b, n_uniq, D, block = task
+    _, _, l, a, b, n_uniq, D, block, sdt = task
     idx = np.ascontiguousarray(ld(f"inv{l}")[a:b])
     W, S = ld(f"W{l}"), ld(f"S{l}")
     t0 = time.perf_counter()
-    oracle.engram_lookup(idx, W, S, n_uniq, D, block)
+    oracle.engram_lookup(idx, W, S, n_uniq, D, block, scale_dtype=sdt)
     return time.perf_counter() - t0
 
 
@@ -639,7 +657,8 @@ def cpu_baseline_all_cores(lay, sub, mask, compact):
         tasks_l = []
         for l, (inv, _, _, n_uniq) in enumerate(compact):
             step = max(1, -(-inv.size // (4 * cores)))
-            tasks_l += [("lookup", d, l, a, min(inv.size, a + step), n_uniq, lay.head_dim, lay.block)
+            tasks_l += [("lookup", d, l, a, min(inv.size, a + step), n_uniq, lay.head_dim, lay.block,
+                         lay.scale_dtype)
                         for a in range(0, inv.size, step)]
         with mp.get_context("spawn").Pool(cores) as pool:
             pool.map(_oracle_task, [("warm", d)] * cores)
@@ -696,7 +715,10 @@ def torch_cpu_hash_lookup(torch, lay, ids, mask, tables):
     for inv, Wc, Sc in tables:
         it = torch.from_numpy(np.ascontiguousarray(inv, dtype=np.int64))
         w = torch.from_numpy(np.ascontiguousarray(Wc))[it].view(torch.float8_e4m3fn).float()  # gather codes, then widen
-        sc = torch.from_numpy(np.ascontiguousarray(Sc, dtype=np.float32))[it]
+        sc = torch.from_numpy(np.ascontiguousarray(Sc))[it]
+        if lay.scale_dtype != 0:  # the stored bits, widened as `.float()` widens them
+            sc = sc.view(scale_torch_dtype(torch, lay.scale_dtype))
+        sc = sc.float()
         D = w.shape[-1]
         blk = D // sc.shape[-1]
         rows.append((w.view(-1, sc.shape[-1], blk) * sc[:, :, None]).view(-1, D).to(torch.bfloat16))
@@ -816,7 +838,8 @@ def run_ours(args):
             "head_dim": lay.head_dim,
             "fp8_block": lay.block,
             "table_rows": lay.rows,
-            "arithmetic": "hash int64 (wrapping multiply, XOR, floored mod); fp8 E4M3 x fp32 scale in fp32, RNE to bf16",
+            "arithmetic": "hash int64 (wrapping multiply, XOR, floored mod); fp8 E4M3 x "
+                          f"{runner.scale_name} scale widened to fp32, one fp32 multiply, RNE to bf16",
             "parallelism": f"replicas x{world} (no exchange step)",
             "l2": l2_note(runner, flush_l2, fits_l2),
             "status_flags_after_warmup": flags,
@@ -968,7 +991,7 @@ def run_reference(args):
             flat = h[:, :, l, :].reshape(-1)
             uniq, inv = np.unique(flat, return_inverse=True)
             Wc = synth.table_rows(wl.table_seed, l, uniq, lay.head_dim)
-            Sc = synth.table_scales(wl.table_seed, l, uniq, lay.n_scales)
+            Sc = synth.table_scales(wl.table_seed, l, uniq, lay.n_scales, lay.scale_dtype)
             tabs.append((uniq, Wc, Sc))
         samples.append((sub, msk, orc, tabs))
 
@@ -981,7 +1004,7 @@ def run_reference(args):
         for l, (uniq, Wc, Sc) in enumerate(tabs):
             local_idx = np.searchsorted(uniq, h[:, :, l, :].reshape(-1))
             t0 = time.perf_counter()
-            oracle.engram_lookup(local_idx, Wc, Sc, uniq.size, lay.head_dim, lay.block)
+            oracle.engram_lookup(local_idx, Wc, Sc, uniq.size, lay.head_dim, lay.block, scale_dtype=lay.scale_dtype)
             el += time.perf_counter() - t0
         return el
 

@@ -27,7 +27,8 @@ __all__ = [
     "EngramError", "EngramHash", "build", "engram_state_create", "engram_state_destroy", "engram_cache_reset",
     "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
     "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START",
-    "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "library_path",
+    "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "SCALE_F32", "SCALE_BF16", "SCALE_E8M0", "SCALE_E4M3",
+    "library_path",
 ]
 
 OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
@@ -35,6 +36,12 @@ STATUS_BAD_START = 1
 STATUS_BAD_ID = 2
 STATUS_BAD_LENGTH = 4
 STATUS_BAD_ROW = 8
+# storage types of the scale tensors (ENGRAM_SCALE_*)
+SCALE_F32, SCALE_BF16, SCALE_E8M0, SCALE_E4M3 = 0, 1, 2, 3
+_SCALE_BYTES = {SCALE_F32: 4, SCALE_BF16: 2, SCALE_E8M0: 1, SCALE_E4M3: 1}
+_SCALE_OF_DTYPE = {torch.float32: SCALE_F32, torch.bfloat16: SCALE_BF16, torch.float8_e4m3fn: SCALE_E4M3}
+if hasattr(torch, "float8_e8m0fnu"):
+    _SCALE_OF_DTYPE[torch.float8_e8m0fnu] = SCALE_E8M0
 MAX_LAYERS = 8
 
 
@@ -48,7 +55,7 @@ class _Layout(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("max_ngram", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("max_seq_len", ctypes.c_int64), ("raw_vocab", ctypes.c_int64), ("dead", ctypes.c_int64),
-                ("pad_id", ctypes.c_int64)]
+                ("pad_id", ctypes.c_int64), ("scale_dtype", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -72,7 +79,7 @@ def _lib():
         L.engram_cache_reset.argtypes = [_P, _P]
         L.engram_state_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.engram_hash.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _P, _P]
-        L.engram_lookup.argtypes = [_P, _I64, _P, _P, _I64, _I32, _I32, _P, _P]
+        L.engram_lookup.argtypes = [_P, _I64, _P, _P, _I64, _I32, _I32, _I32, _P, _P]
         L.engram_hash_lookup.argtypes = [_P, _P, _P, _P, _P, _I32, _I64, _P, _P, _P, _P, _P, _P]
         L.engram_hash_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P]
         L.engram_hash_lookup_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _P]
@@ -122,15 +129,17 @@ def _host_i64(a, n: int, name: str):
 
 # ----------------------------------------------------------------------------- C-named functions
 def engram_state_create(*, n_layers, max_ngram, n_heads, head_dim, block, max_batch, max_seq_len, token_map,
-                        multipliers, primes, offsets, dead=-1, pad_id=2, stream=None) -> int:
+                        multipliers, primes, offsets, dead=-1, pad_id=2, stream=None, scale_dtype=SCALE_F32) -> int:
     """Create a state; returns the opaque handle (an int). Host arrays: token_map [raw_vocab],
-    multipliers [n_layers, max_ngram], primes [n_layers, max_ngram-1, n_heads], offsets [n_layers, C]."""
+    multipliers [n_layers, max_ngram], primes [n_layers, max_ngram-1, n_heads], offsets [n_layers, C].
+    scale_dtype: storage type of the tables' scales (SCALE_*)."""
     tm = torch.as_tensor(token_map, dtype=torch.int64).reshape(-1).contiguous()
     C = (max_ngram - 1) * n_heads
     mu = _host_i64(multipliers, n_layers * max_ngram, "multipliers")
     pr = _host_i64(primes, n_layers * C, "primes")
     of = _host_i64(offsets, n_layers * C, "offsets")
-    lay = _Layout(n_layers, max_ngram, n_heads, head_dim, block, max_batch, max_seq_len, tm.numel(), dead, pad_id)
+    lay = _Layout(n_layers, max_ngram, n_heads, head_dim, block, max_batch, max_seq_len, tm.numel(), dead, pad_id,
+                  int(scale_dtype))
     h = _P()
     _check(_lib().engram_state_create(ctypes.byref(lay), tm.data_ptr(), mu.data_ptr(), pr.data_ptr(), of.data_ptr(),
                                       _stream(stream), ctypes.byref(h)), "engram_state_create")
@@ -156,6 +165,28 @@ def engram_state_layout(state: int) -> dict:
     lay = _Layout()
     _check(_lib().engram_state_layout(state, ctypes.byref(lay)), "engram_state_layout")
     return {f: getattr(lay, f) for f, _ in _Layout._fields_}
+
+
+def _scale_dtype_of(S: torch.Tensor, scale_dtype=None) -> int:
+    """The storage type of a scale tensor: given explicitly (then S may hold the raw bits in any
+    dtype of that width), or read from S's dtype (float32, bfloat16, float8_e8m0fnu, float8_e4m3fn)."""
+    if scale_dtype is not None:
+        return int(scale_dtype)
+    if S.dtype not in _SCALE_OF_DTYPE:
+        raise TypeError(f"cannot tell the scale storage type of a {S.dtype} tensor; pass scale_dtype")
+    return _SCALE_OF_DTYPE[S.dtype]
+
+
+def _dev_scales(S: torch.Tensor, scale_dtype: int, name: str = "S") -> int:
+    if not isinstance(S, torch.Tensor) or not S.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if scale_dtype not in _SCALE_BYTES or S.element_size() != _SCALE_BYTES[scale_dtype]:
+        raise TypeError(f"{name}: {S.dtype} does not hold scales of storage type {scale_dtype}")
+    if S.dtype in _SCALE_OF_DTYPE and _SCALE_OF_DTYPE[S.dtype] != scale_dtype:
+        raise TypeError(f"{name} is {S.dtype} but the scales are stored as type {scale_dtype}")
+    if not S.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return S.data_ptr()
 
 
 def _start_tensor(start_pos, B: int, device) -> torch.Tensor:
@@ -192,15 +223,16 @@ def _as_u8(mask: torch.Tensor) -> torch.Tensor:
 
 
 def engram_lookup(idx: torch.Tensor, W: torch.Tensor, S: torch.Tensor, block: int, out: torch.Tensor | None = None,
-                  stream=None) -> torch.Tensor:
-    """idx int64 [...]; W fp8 (float8_e4m3fn or uint8) [rows, D]; S float32 [rows, D/block].
-    Returns (or fills) bf16 [..., D]."""
+                  stream=None, scale_dtype: int | None = None) -> torch.Tensor:
+    """idx int64 [...]; W fp8 (float8_e4m3fn or uint8) [rows, D]; S [rows, D/block] scales (float32,
+    bfloat16, float8_e8m0fnu or float8_e4m3fn; or raw bits with scale_dtype). Returns (or fills) bf16 [..., D]."""
+    sdt = _scale_dtype_of(S, scale_dtype)
     rows, D = W.shape
     if out is None:
         out = torch.empty(tuple(idx.shape) + (D,), dtype=torch.bfloat16, device=idx.device)
     Wu = W.view(torch.uint8)
     _check(_lib().engram_lookup(_dev(idx, torch.int64, "idx"), idx.numel(), _dev(Wu, torch.uint8, "W"),
-                                _dev(S, torch.float32, "S"), rows, D, int(block), _dev(out, torch.bfloat16, "out"),
+                                _dev_scales(S, sdt), rows, D, int(block), sdt, _dev(out, torch.bfloat16, "out"),
                                 _stream(stream)), "engram_lookup")
     return out
 
@@ -222,7 +254,8 @@ def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: lis
     sp = _start_tensor(start_pos, B, ids.device)
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     Wp = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
-    Sp = (_P * n)(*[_dev(s, torch.float32, "S") for s in S])
+    sdt = engram_state_layout(state)["scale_dtype"]
+    Sp = (_P * n)(*[_dev_scales(s, sdt) for s in S])
     Rp = (_I64 * n)(*[w.shape[0] for w in W])
     Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
     hp = None if hashes is None else _dev(hashes, torch.int64, "hashes")
@@ -276,7 +309,8 @@ def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.T
         out = [torch.empty((T, C, D), dtype=torch.bfloat16, device=ids.device) for _ in range(n)]
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     Wp = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
-    Sp = (_P * n)(*[_dev(x, torch.float32, "S") for x in S])
+    sdt = engram_state_layout(state)["scale_dtype"]
+    Sp = (_P * n)(*[_dev_scales(x, sdt) for x in S])
     Rp = (_I64 * n)(*[w.shape[0] for w in W])
     Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
     hp = None if hashes is None else _dev(hashes, torch.int64, "hashes")
@@ -321,7 +355,8 @@ class PreparedHashLookup:
             raise ValueError("W, S and out need one entry per engram layer")
         self._keep = (ids, start_pos, W, S, out, mask, hashes, cu_seqlens, cache_rows)  # the buffers stay alive
         self._W = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
-        self._S = (_P * n)(*[_dev(x, torch.float32, "S") for x in S])
+        sdt = engram_state_layout(state)["scale_dtype"]
+        self._S = (_P * n)(*[_dev_scales(x, sdt) for x in S])
         self._R = (_I64 * n)(*[w.shape[0] for w in W])
         self._O = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
         m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
@@ -352,14 +387,14 @@ class EngramHash:
     """A state plus the calls that use it (the hash module of the model, with its cache)."""
 
     def __init__(self, *, n_layers, max_ngram, n_heads, head_dim, block, max_batch, max_seq_len, token_map,
-                 multipliers, primes, offsets, dead=-1, pad_id=2):
+                 multipliers, primes, offsets, dead=-1, pad_id=2, scale_dtype=SCALE_F32):
         self.n_layers, self.max_ngram, self.n_heads = n_layers, max_ngram, n_heads
         self.n_cols = (max_ngram - 1) * n_heads
-        self.head_dim, self.block = head_dim, block
+        self.head_dim, self.block, self.scale_dtype = head_dim, block, int(scale_dtype)
         self.handle = engram_state_create(n_layers=n_layers, max_ngram=max_ngram, n_heads=n_heads, head_dim=head_dim,
                                           block=block, max_batch=max_batch, max_seq_len=max_seq_len,
                                           token_map=token_map, multipliers=multipliers, primes=primes,
-                                          offsets=offsets, dead=dead, pad_id=pad_id)
+                                          offsets=offsets, dead=dead, pad_id=pad_id, scale_dtype=scale_dtype)
 
     def close(self):
         if self.handle:
@@ -406,4 +441,4 @@ class EngramHash:
                                   cache_rows)
 
     def lookup(self, idx, W, S, out=None):
-        return engram_lookup(idx, W, S, self.block, out)
+        return engram_lookup(idx, W, S, self.block, out, scale_dtype=self.scale_dtype)

@@ -28,6 +28,13 @@ inline bool head_dim_ok(int32_t D, int32_t block) {
 
 int cols_total(const engram_layout& l) { return l.n_layers * (l.max_ngram - 1) * l.n_heads; }
 
+inline bool scale_dtype_ok(int32_t t) { return t >= ENGRAM_SCALE_F32 && t <= ENGRAM_SCALE_E4M3; }
+
+// bytes of one stored scale (also the alignment S needs)
+inline uintptr_t scale_bytes(int32_t t) {
+  return t == ENGRAM_SCALE_F32 ? 4 : (t == ENGRAM_SCALE_BF16 ? 2 : 1);
+}
+
 int check_layout(const engram_layout* l) {
   if (l == nullptr) return ENGRAM_ERR_INVALID;
   if (l->n_layers < 1 || l->max_ngram < 2 || l->n_heads < 1 || l->max_batch < 1 || l->max_seq_len < 1 ||
@@ -37,7 +44,7 @@ int check_layout(const engram_layout* l) {
   if ((int64_t)l->n_layers * (l->max_ngram - 1) * l->n_heads > ENGRAM_MAX_COLS_TOTAL) return ENGRAM_ERR_UNSUPPORTED;
   if (l->max_batch > 65535 || l->max_seq_len > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
   if (l->dead < INT32_MIN || l->dead > INT32_MAX) return ENGRAM_ERR_INVALID;
-  if (!head_dim_ok(l->head_dim, l->block)) return ENGRAM_ERR_UNSUPPORTED;
+  if (!head_dim_ok(l->head_dim, l->block) || !scale_dtype_ok(l->scale_dtype)) return ENGRAM_ERR_UNSUPPORTED;
   return ENGRAM_OK;
 }
 
@@ -105,16 +112,18 @@ engram::CallArgs call_args(const engram_state* st, const int64_t* ids, const uin
   a.B = B;
   a.head_dim = st->lay.head_dim;
   a.block = st->lay.block;
+  a.scale_dtype = st->lay.scale_dtype;
   return a;
 }
 
 // per-layer tables and outputs of a fused call (host arrays of n_layers device pointers)
-int fill_tables(const engram_state* st, const uint8_t* const* W, const float* const* S, const int64_t* rows,
+int fill_tables(const engram_state* st, const uint8_t* const* W, const void* const* S, const int64_t* rows,
                 uint16_t* const* out, engram::CallArgs* a) {
   if (W == nullptr || S == nullptr || rows == nullptr || out == nullptr) return ENGRAM_ERR_INVALID;
+  const uintptr_t sb = scale_bytes(st->lay.scale_dtype);
   for (int l = 0; l < st->lay.n_layers; ++l) {
     if (rows[l] < 0 || out[l] == nullptr || !aligned(out[l], 16)) return ENGRAM_ERR_INVALID;
-    if (rows[l] > 0 && (W[l] == nullptr || S[l] == nullptr || !aligned(W[l], 16) || !aligned(S[l], 4)))
+    if (rows[l] > 0 && (W[l] == nullptr || S[l] == nullptr || !aligned(W[l], 16) || !aligned(S[l], sb)))
       return ENGRAM_ERR_INVALID;
     a->W[l] = W[l];
     a->S[l] = S[l];
@@ -236,21 +245,23 @@ int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, co
   return engram::launch_hash(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
 }
 
-int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
-                  int32_t head_dim, int32_t block, uint16_t* out, engram_stream_t stream) {
+int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
+                  int32_t head_dim, int32_t block, int32_t scale_dtype, uint16_t* out, engram_stream_t stream) {
   if (n_idx < 0 || rows < 0) return ENGRAM_ERR_INVALID;
-  if (!head_dim_ok(head_dim, block)) return ENGRAM_ERR_UNSUPPORTED;
+  if (!head_dim_ok(head_dim, block) || !scale_dtype_ok(scale_dtype)) return ENGRAM_ERR_UNSUPPORTED;
   if (n_idx == 0) return ENGRAM_OK;
   if (idx == nullptr || out == nullptr || !aligned(idx, 8) || !aligned(out, 16)) return ENGRAM_ERR_INVALID;
-  if (rows > 0 && (W == nullptr || S == nullptr || !aligned(W, 16) || !aligned(S, 4))) return ENGRAM_ERR_INVALID;
+  if (rows > 0 && (W == nullptr || S == nullptr || !aligned(W, 16) || !aligned(S, scale_bytes(scale_dtype))))
+    return ENGRAM_ERR_INVALID;
   if (n_idx > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
-  cudaError_t e = engram::launch_lookup(idx, n_idx, W, S, rows, head_dim, block, out, (cudaStream_t)stream);
+  cudaError_t e =
+      engram::launch_lookup(idx, n_idx, W, S, rows, head_dim, block, scale_dtype, out, (cudaStream_t)stream);
   return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
 }
 
 int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
                        const int32_t* cache_rows, int32_t B, int64_t L, const uint8_t* const* W,
-                       const float* const* S, const int64_t* rows, uint16_t* const* out, int64_t* hashes,
+                       const void* const* S, const int64_t* rows, uint16_t* const* out, int64_t* hashes,
                        engram_stream_t stream) {
   int rc = check_call(state, ids, mask, start_pos, cache_rows, B, L);
   if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
@@ -298,7 +309,7 @@ int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* m
 
 int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
                               const int32_t* cu_seqlens, const int32_t* start_pos, const int32_t* cache_rows,
-                              int32_t B, int64_t T, int64_t max_len, const uint8_t* const* W, const float* const* S,
+                              int32_t B, int64_t T, int64_t max_len, const uint8_t* const* W, const void* const* S,
                               const int64_t* rows, uint16_t* const* out, int64_t* hashes, engram_stream_t stream) {
   engram::CallArgs a;
   int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, cache_rows, B, T, max_len, hashes, &a);
@@ -337,7 +348,8 @@ const char* engram_strerror(int code) {
     case ENGRAM_ERR_RANGE: return "out of range (B > max_batch or L > max_seq_len)";
     case ENGRAM_ERR_CUDA: return "CUDA runtime or launch error";
     case ENGRAM_ERR_NOMEM: return "device allocation failed";
-    case ENGRAM_ERR_UNSUPPORTED: return "size beyond the library limits (head_dim, block, layers, n-gram size)";
+    case ENGRAM_ERR_UNSUPPORTED:
+      return "beyond the library limits (head_dim, block, scale type, layers, n-gram size)";
     default: return "unknown error code";
   }
 }

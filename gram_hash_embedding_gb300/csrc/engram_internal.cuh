@@ -43,8 +43,9 @@ struct CallArgs {
   int64_t total;              // packed: tokens in ids (T); dense: B * L
   int32_t B;
   int32_t head_dim, block;
+  int32_t scale_dtype;        // ENGRAM_SCALE_*: storage type of S
   const uint8_t* W[ENGRAM_MAX_LAYERS];
-  const float* S[ENGRAM_MAX_LAYERS];
+  const void* S[ENGRAM_MAX_LAYERS];
   int64_t rows[ENGRAM_MAX_LAYERS];
   uint16_t* out[ENGRAM_MAX_LAYERS];
 };
@@ -55,7 +56,7 @@ cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s);
 cudaError_t launch_hash_lookup(const StateView& sv, const CallArgs& a, cudaStream_t s);
 cudaError_t launch_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* qw, const uint16_t* kw,
                         const uint8_t* mask, int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s);
-cudaError_t launch_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
-                          int32_t head_dim, int32_t block, uint16_t* out, cudaStream_t s);
+cudaError_t launch_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
+                          int32_t head_dim, int32_t block, int32_t scale_dtype, uint16_t* out, cudaStream_t s);
 
 }  // namespace engram

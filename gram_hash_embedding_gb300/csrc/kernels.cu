@@ -122,10 +122,36 @@ __device__ __forceinline__ uint2 ld_rows_v2(const uint8_t* p) {
   return v;
 }
 
-__device__ __forceinline__ float ld_scale(const float* p) {
-  float v;
-  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+// Raw bits of scale i of a scale tensor stored as SDT (ENGRAM_SCALE_*), zero-extended. The load
+// only parks the bits in a register; `widen_scale` runs later, once the whole batch of row loads is
+// in flight (widening right after the load would stall the thread on every scale).
+template <int SDT>
+__device__ __forceinline__ uint32_t ld_scale_bits(const void* S, int64_t i) {
+  uint32_t v;
+  if (SDT == ENGRAM_SCALE_F32) {
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(static_cast<const uint32_t*>(S) + i));
+  } else if (SDT == ENGRAM_SCALE_BF16) {
+    uint16_t h;
+    asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(h) : "l"(static_cast<const uint16_t*>(S) + i));
+    v = h;
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=r"(v) : "l"(static_cast<const uint8_t*>(S) + i));
+  }
   return v;
+}
+
+// The scale's value, widened to fp32 exactly.
+template <int SDT>
+__device__ __forceinline__ float widen_scale(uint32_t bits) {
+  if (SDT == ENGRAM_SCALE_F32) return __uint_as_float(bits);
+  if (SDT == ENGRAM_SCALE_BF16) return __uint_as_float(bits << 16);  // the upper half of a binary32
+  if (SDT == ENGRAM_SCALE_E8M0) {  // 2^(e-127): the exponent field of a binary32; 0 is the subnormal 2^-127
+    if (bits == 0xFFu) return __uint_as_float(0x7FC00000u);
+    return __uint_as_float(bits == 0u ? 0x00400000u : (bits << 23));
+  }
+  float lo, hi;  // E4M3, as the table codes
+  f16x2_to_f32(e4m3x2_to_f16x2(bits), lo, hi);
+  return lo;
 }
 
 __device__ __forceinline__ void st_out_v4(void* p, uint4 v) {
@@ -138,15 +164,15 @@ __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x
 // One lane's share of one output row: codes [8q, 8q+8) and [D/2+8q, D/2+8q+8) of table row `row`.
 struct RowPiece {
   uint2 v0, v1;
-  float s0, s1;
+  uint32_t s0, s1;  // raw scale bits (widened when the piece is stored)
   bool valid;
 };
 
 // D (head_dim) is a compile-time power of two, so row offsets are shifts; the scale block is a
-// power of two too (it divides D), passed as its log2. `one_block`: the row has a single scale
-// (block >= D), so both halves share one scale load.
-template <int D, bool ONE>
-__device__ __forceinline__ void piece_load(RowPiece& pc, const uint8_t* W, const float* S, int64_t rows, int64_t row,
+// power of two too (it divides D), passed as its log2. ONE: the row has a single scale (block >= D),
+// so both halves share one scale load. SDT: the scales' storage type (ENGRAM_SCALE_*).
+template <int D, bool ONE, int SDT>
+__device__ __forceinline__ void piece_load(RowPiece& pc, const uint8_t* W, const void* S, int64_t rows, int64_t row,
                                            int q, int blk_shift) {
   pc.valid = (row >= 0) && (row < rows);
   if (pc.valid) {
@@ -154,19 +180,19 @@ __device__ __forceinline__ void piece_load(RowPiece& pc, const uint8_t* W, const
     const int k0 = 8 * q, k1 = (D >> 1) + 8 * q;
     pc.v0 = ld_rows_v2(base + k0);
     pc.v1 = ld_rows_v2(base + k1);
-    const float* srow = S + (row << (ilog2(D) - blk_shift));
-    pc.s0 = ld_scale(srow + (k0 >> blk_shift));
-    pc.s1 = ONE ? pc.s0 : ld_scale(srow + (k1 >> blk_shift));
+    const int64_t srow = row << (ilog2(D) - blk_shift);
+    pc.s0 = ld_scale_bits<SDT>(S, srow + (k0 >> blk_shift));
+    pc.s1 = ONE ? pc.s0 : ld_scale_bits<SDT>(S, srow + (k1 >> blk_shift));
   }
 }
 
 // out_row: bf16 row of D values (2*D bytes)
-template <int D>
+template <int D, int SDT>
 __device__ __forceinline__ void piece_store(const RowPiece& pc, uint16_t* out_row, int q) {
   uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;  // masked rows are +0
   if (pc.valid) {
-    a = dequant8(pc.v0, pc.s0);
-    b = dequant8(pc.v1, pc.s1);
+    a = dequant8(pc.v0, widen_scale<SDT>(pc.s0));
+    b = dequant8(pc.v1, widen_scale<SDT>(pc.s1));
   }
   st_out_v4(out_row + 8 * q, a);
   st_out_v4(out_row + (D >> 1) + 8 * q, b);
@@ -316,7 +342,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
 // fused kernel: hash a tile, then (GATHER) stream its rows through registers.
 // grid = (ceil(L / tile), B); one CTA = `tile` consecutive tokens of sequence b.
 // D = head_dim (compile time); G = D / 16 lanes per output row. Unused when GATHER is false.
-template <bool GATHER, int D, bool ONE>
+template <bool GATHER, int D, bool ONE, int SDT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateView sv, const CallArgs a, const int tile) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ unsigned int flags_s;
@@ -373,13 +399,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
           }
           const int r = u / G;
           orow[k] = a.out[l] + (out_base_row + r) * D;
-          piece_load<D, ONE>(pc[k], a.W[l], a.S[l], a.rows[l], rowidx_s[l * rpl + r], u % G, blk_shift);
+          piece_load<D, ONE, SDT>(pc[k], a.W[l], a.S[l], a.rows[l], rowidx_s[l * rpl + r], u % G, blk_shift);
         }
       }
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
         const int u = base + k * kThreads;
-        if (orow[k] != nullptr) piece_store<D>(pc[k], orow[k], u % G);
+        if (orow[k] != nullptr) piece_store<D, SDT>(pc[k], orow[k], u % G);
       }
     }
   }
@@ -391,10 +417,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
 // ------------------------------------------------------------------------------------------------
 // standalone lookup: grid-stride over (index, lane) units
 
-template <int D, bool ONE>
+template <int D, bool ONE, int SDT>
 __global__ void __launch_bounds__(kThreads) lookup_kernel(const int64_t* __restrict__ idx, const int64_t n_idx,
                                                           const uint8_t* __restrict__ W,
-                                                          const float* __restrict__ S, const int64_t rows,
+                                                          const void* __restrict__ S, const int64_t rows,
                                                           const int blk_shift, uint16_t* __restrict__ out) {
   constexpr int G = D / 16;
   const int64_t units = n_idx * G;
@@ -404,12 +430,12 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const int64_t* __restr
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
       const int64_t u = base + k * stride;
-      if (u < units) piece_load<D, ONE>(pc[k], W, S, rows, __ldg(idx + u / G), (int)(u % G), blk_shift);
+      if (u < units) piece_load<D, ONE, SDT>(pc[k], W, S, rows, __ldg(idx + u / G), (int)(u % G), blk_shift);
     }
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
       const int64_t u = base + k * stride;
-      if (u < units) piece_store<D>(pc[k], out + (u / G) * D, (int)(u % G));
+      if (u < units) piece_store<D, SDT>(pc[k], out + (u / G) * D, (int)(u % G));
     }
   }
 }
@@ -430,10 +456,10 @@ int sm_count() {
   return n;
 }
 
-template <bool GATHER, int D, bool ONE>
+template <bool GATHER, int D, bool ONE, int SDT>
 cudaError_t launch_hash_k(const StateView& sv, const CallArgs& a, int tile, cudaStream_t s) {
   const SmemPlan plan = smem_plan(sv.n_layers, sv.max_ngram, sv.n_cols, tile, GATHER);
-  auto kern = hash_kernel<GATHER, D, ONE>;
+  auto kern = hash_kernel<GATHER, D, ONE, SDT>;
   if (plan.bytes > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.bytes);
     if (e != cudaSuccess) return e;
@@ -444,14 +470,25 @@ cudaError_t launch_hash_k(const StateView& sv, const CallArgs& a, int tile, cuda
 }
 
 // a row with a single scale block (block >= head_dim) loads its scale once
-template <bool GATHER, int D>
-cudaError_t launch_hash_g(const StateView& sv, const CallArgs& a, int tile, cudaStream_t s) {
-  if (GATHER && a.block >= D) return launch_hash_k<GATHER, D, true>(sv, a, tile, s);
-  return launch_hash_k<GATHER, D, false>(sv, a, tile, s);
+template <int D, int SDT>
+cudaError_t launch_fused_s(const StateView& sv, const CallArgs& a, int tile, cudaStream_t s) {
+  if (a.block >= D) return launch_hash_k<true, D, true, SDT>(sv, a, tile, s);
+  return launch_hash_k<true, D, false, SDT>(sv, a, tile, s);
 }
 
 template <int D>
-cudaError_t launch_lookup_g(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
+cudaError_t launch_fused_d(const StateView& sv, const CallArgs& a, int tile, cudaStream_t s) {
+  switch (a.scale_dtype) {
+    case ENGRAM_SCALE_F32: return launch_fused_s<D, ENGRAM_SCALE_F32>(sv, a, tile, s);
+    case ENGRAM_SCALE_BF16: return launch_fused_s<D, ENGRAM_SCALE_BF16>(sv, a, tile, s);
+    case ENGRAM_SCALE_E8M0: return launch_fused_s<D, ENGRAM_SCALE_E8M0>(sv, a, tile, s);
+    case ENGRAM_SCALE_E4M3: return launch_fused_s<D, ENGRAM_SCALE_E4M3>(sv, a, tile, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int D, int SDT>
+cudaError_t launch_lookup_s(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
                             int blk, uint16_t* out, cudaStream_t s) {
   constexpr int G = D / 16;
   const int64_t units = n_idx * G;
@@ -463,10 +500,22 @@ cudaError_t launch_lookup_g(const int64_t* idx, int64_t n_idx, const uint8_t* W,
   if (blocks < 1) blocks = 1;
   const int blk_shift = ilog2(blk);
   if (blk >= D)
-    lookup_kernel<D, true><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
+    lookup_kernel<D, true, SDT><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
   else
-    lookup_kernel<D, false><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
+    lookup_kernel<D, false, SDT><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_lookup_g(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
+                            int blk, int sdt, uint16_t* out, cudaStream_t s) {
+  switch (sdt) {
+    case ENGRAM_SCALE_F32: return launch_lookup_s<D, ENGRAM_SCALE_F32>(idx, n_idx, W, S, rows, blk, out, s);
+    case ENGRAM_SCALE_BF16: return launch_lookup_s<D, ENGRAM_SCALE_BF16>(idx, n_idx, W, S, rows, blk, out, s);
+    case ENGRAM_SCALE_E8M0: return launch_lookup_s<D, ENGRAM_SCALE_E8M0>(idx, n_idx, W, S, rows, blk, out, s);
+    case ENGRAM_SCALE_E4M3: return launch_lookup_s<D, ENGRAM_SCALE_E4M3>(idx, n_idx, W, S, rows, blk, out, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -480,7 +529,7 @@ cudaError_t launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s
 }
 
 cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s) {
-  return launch_hash_g<false, 16>(sv, a, kHashTile, s);
+  return launch_hash_k<false, 16, false, ENGRAM_SCALE_F32>(sv, a, kHashTile, s);
 }
 
 // Tokens per CTA of the fused kernel: the largest power of two in [kMinFusedTile, kFusedTile] that
@@ -502,25 +551,25 @@ int fused_tile(const CallArgs& a) {
 cudaError_t launch_hash_lookup(const StateView& sv, const CallArgs& a, cudaStream_t s) {
   const int tile = fused_tile(a);
   switch (a.head_dim) {
-    case 16: return launch_hash_g<true, 16>(sv, a, tile, s);
-    case 32: return launch_hash_g<true, 32>(sv, a, tile, s);
-    case 64: return launch_hash_g<true, 64>(sv, a, tile, s);
-    case 128: return launch_hash_g<true, 128>(sv, a, tile, s);
-    case 256: return launch_hash_g<true, 256>(sv, a, tile, s);
-    case 512: return launch_hash_g<true, 512>(sv, a, tile, s);
+    case 16: return launch_fused_d<16>(sv, a, tile, s);
+    case 32: return launch_fused_d<32>(sv, a, tile, s);
+    case 64: return launch_fused_d<64>(sv, a, tile, s);
+    case 128: return launch_fused_d<128>(sv, a, tile, s);
+    case 256: return launch_fused_d<256>(sv, a, tile, s);
+    case 512: return launch_fused_d<512>(sv, a, tile, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
-                          int32_t head_dim, int32_t block, uint16_t* out, cudaStream_t s) {
+cudaError_t launch_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
+                          int32_t head_dim, int32_t block, int32_t scale_dtype, uint16_t* out, cudaStream_t s) {
   switch (head_dim) {
-    case 16: return launch_lookup_g<16>(idx, n_idx, W, S, rows, block, out, s);
-    case 32: return launch_lookup_g<32>(idx, n_idx, W, S, rows, block, out, s);
-    case 64: return launch_lookup_g<64>(idx, n_idx, W, S, rows, block, out, s);
-    case 128: return launch_lookup_g<128>(idx, n_idx, W, S, rows, block, out, s);
-    case 256: return launch_lookup_g<256>(idx, n_idx, W, S, rows, block, out, s);
-    case 512: return launch_lookup_g<512>(idx, n_idx, W, S, rows, block, out, s);
+    case 16: return launch_lookup_g<16>(idx, n_idx, W, S, rows, block, scale_dtype, out, s);
+    case 32: return launch_lookup_g<32>(idx, n_idx, W, S, rows, block, scale_dtype, out, s);
+    case 64: return launch_lookup_g<64>(idx, n_idx, W, S, rows, block, scale_dtype, out, s);
+    case 128: return launch_lookup_g<128>(idx, n_idx, W, S, rows, block, scale_dtype, out, s);
+    case 256: return launch_lookup_g<256>(idx, n_idx, W, S, rows, block, scale_dtype, out, s);
+    case 512: return launch_lookup_g<512>(idx, n_idx, W, S, rows, block, scale_dtype, out, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -66,6 +66,14 @@ typedef struct engram_state engram_state;
 #define ENGRAM_STATUS_BAD_ROW 8u   /* a cache_rows entry outside [0, max_batch): that row (sequence) wrote nothing to
                                       the cache, its hash ids are -1 and its looked-up rows are +0 */
 
+/* Storage types of the scale tensors. The engram-first/lookup page leaves `scale_dtype` open and
+ * widens the scale with `.float()`; each type below widens to fp32 exactly before the one fp32
+ * multiply. Scales are stored like W: [rows][head_dim / block], each of the type's width. */
+#define ENGRAM_SCALE_F32 0  /* IEEE binary32 */
+#define ENGRAM_SCALE_BF16 1 /* bfloat16: the upper half of a binary32 */
+#define ENGRAM_SCALE_E8M0 2 /* OCP UE8M0: 2^(e - 127); e = 255 is NaN */
+#define ENGRAM_SCALE_E4M3 3 /* OCP E4M3 (fn), as the table codes */
+
 /* Library limits. */
 #define ENGRAM_MAX_LAYERS 8       /* n_layers */
 #define ENGRAM_MAX_NGRAM 8        /* max_ngram (>= 2) */
@@ -84,6 +92,7 @@ typedef struct engram_layout {
   int64_t raw_vocab;   /* entries of token_map (the tokenizer vocabulary) */
   int64_t dead;        /* DEAD sentinel stored for masked tokens; must fit int32 */
   int64_t pad_id;      /* token that fills blocked n-gram slots (engram_pad_id) */
+  int32_t scale_dtype; /* storage type of the tables' scales, ENGRAM_SCALE_* (0: fp32) */
 } engram_layout;
 
 /*
@@ -130,27 +139,29 @@ int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, co
 
 /*
  * The fp8 row lookup of one table (engram-first/lookup page, `ParallelEngramEmbedding.forward`, world size 1).
- *   idx   device int64 [n_idx] row indices; an index outside [0, rows) gives a row of +0
- *   W     device fp8 E4M3 codes [rows][head_dim], 16-byte aligned
- *   S     device fp32 [rows][head_dim / block], 4-byte aligned
- *   out   device bf16 bits [n_idx][head_dim], 16-byte aligned, written
- * out[i][k] = bf16_rne(fp32(W[idx[i]][k]) * S[idx[i]][k / block]) (one fp32 round-to-nearest multiply).
- * n_idx == 0 is a no-op. Errors: _INVALID, _UNSUPPORTED (head_dim / block).
+ *   idx          device int64 [n_idx] row indices; an index outside [0, rows) gives a row of +0
+ *   W            device fp8 E4M3 codes [rows][head_dim], 16-byte aligned
+ *   S            device scales [rows][head_dim / block] stored as scale_dtype, aligned to its width
+ *   scale_dtype  ENGRAM_SCALE_*
+ *   out          device bf16 bits [n_idx][head_dim], 16-byte aligned, written
+ * out[i][k] = bf16_rne(fp32(W[idx[i]][k]) * fp32(S[idx[i]][k / block])) (one fp32 round-to-nearest multiply).
+ * n_idx == 0 is a no-op. Errors: _INVALID, _UNSUPPORTED (head_dim / block / scale_dtype).
  */
-int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const float* S, int64_t rows,
-                  int32_t head_dim, int32_t block, uint16_t* out, engram_stream_t stream);
+int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
+                  int32_t head_dim, int32_t block, int32_t scale_dtype, uint16_t* out, engram_stream_t stream);
 
 /*
  * Hash and lookup in one launch: the hash of engram_hash (same cache update), then for every layer l the
  * lookup of its C columns in table l, as the model does for each engram layer.
- *   W, S, rows, out  host arrays of n_layers entries: per layer the device table, scales, row count
- *                    (as engram_lookup) and a device bf16 output [B][L][C][head_dim]
+ *   W, S, rows, out  host arrays of n_layers entries: per layer the device table, scales (stored as the
+ *                    layout's scale_dtype), row count (as engram_lookup) and a device bf16 output
+ *                    [B][L][C][head_dim]
  *   hashes           device int64 [B][L][n_layers][C] to also receive the hash ids, or NULL
  * Errors: as engram_hash and engram_lookup.
  */
 int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
                        const int32_t* cache_rows, int32_t B, int64_t L, const uint8_t* const* W,
-                       const float* const* S, const int64_t* rows, uint16_t* const* out, int64_t* hashes,
+                       const void* const* S, const int64_t* rows, uint16_t* const* out, int64_t* hashes,
                        engram_stream_t stream);
 
 /*
@@ -181,7 +192,7 @@ int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* m
  */
 int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
                               const int32_t* cu_seqlens, const int32_t* start_pos, const int32_t* cache_rows,
-                              int32_t B, int64_t T, int64_t max_len, const uint8_t* const* W, const float* const* S,
+                              int32_t B, int64_t T, int64_t max_len, const uint8_t* const* W, const void* const* S,
                               const int64_t* rows, uint16_t* const* out, int64_t* hashes, engram_stream_t stream);
 
 /*

@@ -287,11 +287,35 @@ def table_rows(seed: int, layer: int, rows, D: int) -> np.ndarray:
     return lut[pieces].reshape(rows.size, D)
 
 
-def table_scales(seed: int, layer: int, rows, n_scales: int) -> np.ndarray:
-    """fp32 scales of the given rows: float32 [len(rows), n_scales], uniform on [0.01, 1)."""
+# scale storage types (the same numbering as the library's and the oracle's, defined here on its own)
+SCALE_F32, SCALE_BF16, SCALE_E8M0, SCALE_E4M3 = 0, 1, 2, 3
+SCALE_BYTES = {SCALE_F32: 4, SCALE_BF16: 2, SCALE_E8M0: 1, SCALE_E4M3: 1}
+
+
+def scale_codes(w: np.ndarray, scale_dtype: int) -> np.ndarray:
+    """Scale bit patterns straight from generator words (integer operations only, so host and device
+    agree by construction): bf16 with exponent 2^-7..2^0 and 7 random mantissa bits; UE8M0
+    exponents 120..127 (2^-7..1); positive normal E4M3 codes with exponent 2^-3..2^0."""
+    w = np.asarray(w, dtype=np.uint64)
+    if scale_dtype == SCALE_BF16:
+        return (((np.uint64(120) + (w & np.uint64(7))) << np.uint64(7)) | ((w >> np.uint64(8)) & np.uint64(0x7F))
+                ).astype(np.uint16)
+    if scale_dtype == SCALE_E8M0:
+        return (np.uint64(120) + (w & np.uint64(7))).astype(np.uint8)
+    if scale_dtype == SCALE_E4M3:
+        return (((np.uint64(4) + (w & np.uint64(3))) << np.uint64(3)) | ((w >> np.uint64(8)) & np.uint64(7))
+                ).astype(np.uint8)
+    raise ValueError(scale_dtype)
+
+
+def table_scales(seed: int, layer: int, rows, n_scales: int, scale_dtype: int = SCALE_F32) -> np.ndarray:
+    """Scales of the given rows, [len(rows), n_scales]: fp32 values uniform on [0.01, 1), or the bit
+    patterns of the other storage types (`scale_codes`)."""
     rows = np.asarray(rows, dtype=np.uint64).reshape(-1)
     ctr = (rows[:, None] * np.uint64(n_scales) + np.arange(n_scales, dtype=np.uint64)[None, :]).reshape(-1)
     w = words(seed, TAG_SCALE + layer, ctr)
+    if scale_dtype != SCALE_F32:
+        return scale_codes(w, scale_dtype).reshape(rows.size, n_scales)
     t = (w >> np.uint64(40)).astype(np.float32) * np.float32(2.0 ** -24)
     s = np.float32(0.01) + np.float32(0.99) * t
     return s.astype(np.float32).reshape(rows.size, n_scales)
@@ -323,6 +347,9 @@ def _load():
         lib.synth_fill_fp8.restype = ctypes.c_int
         lib.synth_fill_scales.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p]
         lib.synth_fill_scales.restype = ctypes.c_int
+        lib.synth_fill_scale_codes.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int,
+                                               ctypes.c_void_p]
+        lib.synth_fill_scale_codes.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -330,9 +357,10 @@ def _load():
 _LUT_DEV: dict = {}
 
 
-def fill_table_device(W, S, seed: int, layer: int) -> None:
-    """Fill device tensors W (uint8 [rows, D]) and S (float32 [rows, n_scales]) with layer
-    ``layer``'s table from the counter-based generator, on torch's current stream."""
+def fill_table_device(W, S, seed: int, layer: int, scale_dtype: int = SCALE_F32) -> None:
+    """Fill device tensors W (uint8 [rows, D]) and S ([rows, n_scales]: float32, or any tensor of the
+    storage type's width for the other scale types) with layer ``layer``'s table from the
+    counter-based generator, on torch's current stream."""
     import torch
 
     lib = _load()
@@ -341,11 +369,16 @@ def fill_table_device(W, S, seed: int, layer: int) -> None:
         _LUT_DEV[dev] = torch.from_numpy(fp8_normal_lut()).to(dev)
     stream = torch.cuda.current_stream(dev).cuda_stream
     assert W.dtype == torch.uint8 and W.is_contiguous() and W.numel() % 16 == 0
-    assert S.dtype == torch.float32 and S.is_contiguous()
+    assert S.element_size() == SCALE_BYTES[scale_dtype] and S.is_contiguous()
+    assert scale_dtype != SCALE_F32 or S.dtype == torch.float32
     rc = lib.synth_fill_fp8(W.data_ptr(), W.numel(), stream_base(seed, TAG_TABLE + layer), _LUT_DEV[dev].data_ptr(), stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_fp8 failed: {rc}")
-    rc = lib.synth_fill_scales(S.data_ptr(), S.numel(), stream_base(seed, TAG_SCALE + layer), stream)
+    if scale_dtype == SCALE_F32:
+        rc = lib.synth_fill_scales(S.data_ptr(), S.numel(), stream_base(seed, TAG_SCALE + layer), stream)
+    else:
+        rc = lib.synth_fill_scale_codes(S.data_ptr(), S.numel(), stream_base(seed, TAG_SCALE + layer), scale_dtype,
+                                        stream)
     if rc != 0:
         raise RuntimeError(f"synth_fill_scales failed: {rc}")
 
@@ -367,6 +400,7 @@ class Layout:
     offsets: np.ndarray
     dead: int = DEAD
     pad_id: int = PAD_ID
+    scale_dtype: int = SCALE_F32  # storage type of the scale tensors (SCALE_*)
 
     @property
     def n_cols(self) -> int:
@@ -379,6 +413,10 @@ class Layout:
     @property
     def n_scales(self) -> int:
         return self.head_dim // self.block
+
+    @property
+    def scale_bytes(self) -> int:
+        return SCALE_BYTES[self.scale_dtype]
 
 
 @dataclass
@@ -414,10 +452,11 @@ def make_layout(kind: str, seed: int, full64: bool = False) -> Layout:
         primes = layered_primes(FULL_SCALE_PRIME_START, 2, 4, 8)
     elif kind == "profile":  # same shapes, ~0.5 GB per layer: small enough for a full ncu capture
         primes = layered_primes(160_000, 2, 4, 8)
-    elif kind == "full256":  # the released table sizes and head_dim (2 fp32 scales per row)
+    elif kind in ("full256", "full256e8"):  # the released table sizes and head_dim (2 scales per row)
         primes = layered_primes(FULL_SCALE_PRIME_START, 2, 4, 8)
         return Layout(2, 4, 8, 256, 128, RAW_VOCAB, COMPRESSED_VOCAB, token_map(seed), multipliers(seed, 2, 4, full64),
-                      primes, column_offsets(primes))
+                      primes, column_offsets(primes),
+                      scale_dtype=SCALE_E8M0 if kind == "full256e8" else SCALE_F32)
     else:
         raise ValueError(kind)
     return Layout(2, 4, 8, 128, 128, RAW_VOCAB, COMPRESSED_VOCAB, token_map(seed), multipliers(seed, 2, 4, full64),
@@ -467,6 +506,12 @@ def make_workload(cfg: int, seed: int = MASTER_SEED, full64: bool = False) -> Wo
         B, L = 8, 8192
         ids = uniform_ids(s, B * L).reshape(B, L)
         return Workload("full-scale head_dim 256 B8xL8192", lay, B, L, ids, None, np.zeros(B, np.int32), s, B, L)
+    if cfg == 8:  # released head_dim with power-of-two (UE8M0) scales: ~197 GB of codes + 1.5 GB of scales
+        lay = make_layout("full256e8", s, full64)
+        B, L = 8, 8192
+        ids = uniform_ids(s, B * L).reshape(B, L)
+        return Workload("full-scale head_dim 256 UE8M0 scales B8xL8192", lay, B, L, ids, None, np.zeros(B, np.int32),
+                        s, B, L)
     if cfg == 7:  # continuous batching on the full-scale tables: 192 decode steps + 64 prefill chunks
         lay = make_layout("full", s, full64)
         B, P = 256, 8192

@@ -52,6 +52,22 @@ __global__ void fill_scales_kernel(float* __restrict__ S, int64_t n, uint64_t ba
   }
 }
 
+// scale bit patterns of the other storage types, from one generator word each (integer operations
+// only; the host restatement is synth.scale_codes): kind 1 bf16, 2 UE8M0, 3 E4M3
+__global__ void fill_scale_codes_kernel(void* __restrict__ S, int64_t n, uint64_t base, int kind) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+    const uint64_t w = word_at(base, (uint64_t)i);
+    if (kind == 1) {
+      reinterpret_cast<uint16_t*>(S)[i] = (uint16_t)(((120u + (uint32_t)(w & 7u)) << 7) | (uint32_t)((w >> 8) & 0x7Fu));
+    } else if (kind == 2) {
+      reinterpret_cast<uint8_t*>(S)[i] = (uint8_t)(120u + (uint32_t)(w & 7u));
+    } else {
+      reinterpret_cast<uint8_t*>(S)[i] = (uint8_t)(((4u + (uint32_t)(w & 3u)) << 3) | (uint32_t)((w >> 8) & 7u));
+    }
+  }
+}
+
 int grid_for(int64_t n) {
   int64_t g = (n + 255) / 256;
   const int64_t cap = 152 * 16;
@@ -77,6 +93,14 @@ int synth_fill_scales(void* S, int64_t n, uint64_t base, void* stream) {
   if (n < 0 || (reinterpret_cast<uintptr_t>(S) % 4) != 0) return -1;
   if (n == 0) return 0;
   fill_scales_kernel<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>(reinterpret_cast<float*>(S), n, base);
+  return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+// S: device storage of n scales of kind 1 (bf16, 2-byte aligned), 2 (UE8M0) or 3 (E4M3).
+int synth_fill_scale_codes(void* S, int64_t n, uint64_t base, int kind, void* stream) {
+  if (n < 0 || kind < 1 || kind > 3 || (kind == 1 && (reinterpret_cast<uintptr_t>(S) % 2) != 0)) return -1;
+  if (n == 0) return 0;
+  fill_scale_codes_kernel<<<grid_for(n), 256, 0, (cudaStream_t)stream>>>(S, n, base, kind);
   return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -55,6 +55,7 @@ int main(int argc, char** argv) {
   lay.n_layers = (int32_t)p[0]; lay.max_ngram = (int32_t)p[1]; lay.n_heads = (int32_t)p[2];
   lay.head_dim = (int32_t)p[3]; lay.block = (int32_t)p[4]; lay.max_batch = (int32_t)p[5];
   lay.max_seq_len = p[6]; lay.dead = p[7]; lay.pad_id = p[8];
+  lay.scale_dtype = ENGRAM_SCALE_F32;
   const int32_t B = (int32_t)p[9];
   const int64_t L = p[10];
   size_t n_tm, n_mu, n_pr, n_of, n_ids, n_sp, n_w, n_s;
@@ -82,11 +83,11 @@ int main(int argc, char** argv) {
   void* d_hash = NULL;
   CK(cudaMalloc(&d_hash, hash_bytes));
   const uint8_t* Wl[ENGRAM_MAX_LAYERS];
-  const float* Sl[ENGRAM_MAX_LAYERS];
+  const void* Sl[ENGRAM_MAX_LAYERS];
   int64_t Rl[ENGRAM_MAX_LAYERS];
   uint16_t* Ol[ENGRAM_MAX_LAYERS];
   for (int l = 0; l < lay.n_layers; ++l) {
-    Wl[l] = (const uint8_t*)d_W; Sl[l] = (const float*)d_S; Rl[l] = rows;
+    Wl[l] = (const uint8_t*)d_W; Sl[l] = d_S; Rl[l] = rows;
     CK(cudaMalloc((void**)&Ol[l], out_bytes));
   }
   /* call row b uses cache row B-1-b: the reversed map must not change the hash ids */
@@ -106,8 +107,8 @@ int main(int argc, char** argv) {
   void* d_idx0 = to_dev(idx0, (size_t)n_idx * 8);
   uint16_t* d_rows0 = NULL;
   CK(cudaMalloc((void**)&d_rows0, out_bytes));
-  EK(engram_lookup((const int64_t*)d_idx0, n_idx, (const uint8_t*)d_W, (const float*)d_S, rows, lay.head_dim,
-                   lay.block, d_rows0, NULL));
+  EK(engram_lookup((const int64_t*)d_idx0, n_idx, (const uint8_t*)d_W, d_S, rows, lay.head_dim, lay.block,
+                   ENGRAM_SCALE_F32, d_rows0, NULL));
   uint32_t flags = 0;
   EK(engram_state_status(st, NULL, &flags, 1));
   CK(cudaDeviceSynchronize());

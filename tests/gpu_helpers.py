@@ -22,21 +22,26 @@ def make_state(wl: synth.Workload, max_batch=None, max_seq_len=None) -> geng.Eng
                            head_dim=lay.head_dim, block=lay.block, max_batch=max_batch or wl.max_batch,
                            max_seq_len=max_seq_len or wl.max_seq_len, token_map=lay.token_map,
                            multipliers=lay.multipliers, primes=lay.primes, offsets=lay.offsets, dead=lay.dead,
-                           pad_id=lay.pad_id)
+                           pad_id=lay.pad_id, scale_dtype=lay.scale_dtype)
 
 
 def make_oracle(wl: synth.Workload, max_batch=None, max_seq_len=None) -> oracle.OracleState:
     return oracle.OracleState.from_layout(wl.layout, max_batch or wl.max_batch, max_seq_len or wl.max_seq_len)
 
 
+SCALE_TORCH_DTYPE = {synth.SCALE_F32: torch.float32, synth.SCALE_BF16: torch.bfloat16,
+                     synth.SCALE_E8M0: getattr(torch, "float8_e8m0fnu", None), synth.SCALE_E4M3: torch.float8_e4m3fn}
+
+
 def device_tables(wl: synth.Workload, device="cuda"):
-    """Per-layer fp8 tables and scales, filled on the device by the counter-based generator."""
+    """Per-layer fp8 tables and scales (in the layout's scale storage type), filled on the device by
+    the counter-based generator."""
     lay = wl.layout
     Ws, Ss = [], []
     for l, rows in enumerate(lay.rows):
         W = torch.empty((rows, lay.head_dim), dtype=torch.uint8, device=device)
-        S = torch.empty((rows, lay.n_scales), dtype=torch.float32, device=device)
-        synth.fill_table_device(W, S, wl.table_seed, l)
+        S = torch.empty((rows, lay.n_scales), dtype=SCALE_TORCH_DTYPE[lay.scale_dtype], device=device)
+        synth.fill_table_device(W, S, wl.table_seed, l, lay.scale_dtype)
         Ws.append(W)
         Ss.append(S)
     torch.cuda.synchronize()
@@ -52,10 +57,10 @@ def oracle_lookup_rows(wl: synth.Workload, layer: int, idx: np.ndarray) -> np.nd
     valid = (flat >= 0) & (flat < lay.rows[layer])
     uniq, inv = np.unique(flat[valid], return_inverse=True)
     W = synth.table_rows(wl.table_seed, layer, uniq, lay.head_dim)
-    S = synth.table_scales(wl.table_seed, layer, uniq, lay.n_scales)
+    S = synth.table_scales(wl.table_seed, layer, uniq, lay.n_scales, lay.scale_dtype)
     local = np.full(flat.shape, -1, dtype=np.int64)
     local[valid] = inv
-    out = oracle.engram_lookup(local, W, S, len(uniq), lay.head_dim, lay.block)
+    out = oracle.engram_lookup(local, W, S, len(uniq), lay.head_dim, lay.block, scale_dtype=lay.scale_dtype)
     return out.reshape(np.asarray(idx).shape + (lay.head_dim,))
 
 

@@ -60,14 +60,17 @@ def test_host_side_checks_need_no_gpu(lib):
     assert lib.engram_state_create(ctypes.byref(lay), tm, arr, arr, arr, None, ctypes.byref(out)) == geng.ERR_UNSUPPORTED
     lay = geng._Layout(1, 4, 2, 32, 32, 1, 8, 10, 1 << 40, 2)  # DEAD beyond int32
     assert lib.engram_state_create(ctypes.byref(lay), tm, arr, arr, arr, None, ctypes.byref(out)) == geng.ERR_INVALID
+    lay = geng._Layout(1, 4, 2, 32, 32, 1, 8, 10, -1, 2, 4)  # no scale storage type 4
+    assert lib.engram_state_create(ctypes.byref(lay), tm, arr, arr, arr, None, ctypes.byref(out)) == geng.ERR_UNSUPPORTED
     # lookup: unsupported head_dim / block, and an empty call, need no device
     L = lib
     L.engram_lookup.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                                ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
-    assert L.engram_lookup(None, 5, None, None, 4, 48, 16, None, None) == geng.ERR_UNSUPPORTED
-    assert L.engram_lookup(None, 5, None, None, 4, 128, 12, None, None) == geng.ERR_UNSUPPORTED
-    assert L.engram_lookup(None, 0, None, None, 4, 128, 128, None, None) == geng.OK
-    assert L.engram_lookup(None, -1, None, None, 4, 128, 128, None, None) == geng.ERR_INVALID
+                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.engram_lookup(None, 5, None, None, 4, 48, 16, 0, None, None) == geng.ERR_UNSUPPORTED
+    assert L.engram_lookup(None, 5, None, None, 4, 128, 12, 0, None, None) == geng.ERR_UNSUPPORTED
+    assert L.engram_lookup(None, 5, None, None, 4, 128, 128, 4, None, None) == geng.ERR_UNSUPPORTED  # scale type
+    assert L.engram_lookup(None, 0, None, None, 4, 128, 128, geng.SCALE_E8M0, None, None) == geng.OK
+    assert L.engram_lookup(None, -1, None, None, 4, 128, 128, 0, None, None) == geng.ERR_INVALID
     assert lib.engram_state_destroy(None) == 0
 
 

@@ -51,3 +51,23 @@ def test_workloads_shapes():
     assert abs(frac - 0.15) < 0.01 and w4.mask[0, 8192:].all()
     # Zipf ids repeat
     assert len(np.unique(w4.ids)) < 0.5 * w4.ids.size
+
+
+def test_scale_codes_of_the_other_storage_types():
+    """bf16 / UE8M0 / E4M3 scale patterns: the documented ranges, finite and positive, and the
+    released head_dim workload with UE8M0 scales."""
+    rows = np.arange(4000)
+    bf = synth.table_scales(5, 0, rows, 2, synth.SCALE_BF16)
+    e8 = synth.table_scales(5, 0, rows, 2, synth.SCALE_E8M0)
+    e4 = synth.table_scales(5, 0, rows, 2, synth.SCALE_E4M3)
+    assert bf.dtype == np.uint16 and e8.dtype == np.uint8 and e4.dtype == np.uint8
+    bfv = (bf.astype(np.uint32) << 16).view(np.float32)
+    assert (bfv >= 2.0 ** -7).all() and (bfv < 2.0).all() and len(np.unique(bf)) > 500
+    assert set(np.unique(e8).tolist()) == set(range(120, 128))
+    e4_exp = (e4 >> 3) & 0xF
+    assert (e4 < 0x80).all() and set(np.unique(e4_exp).tolist()) == {4, 5, 6, 7}
+    # the same counters as the fp32 scales: row r, scale j is one word whatever the storage type
+    assert np.array_equal(synth.table_scales(5, 0, [7, 9], 2, synth.SCALE_E8M0), e8[[7, 9]])
+    w8 = synth.make_workload(8)
+    assert w8.layout.head_dim == 256 and w8.layout.scale_dtype == synth.SCALE_E8M0 and w8.layout.scale_bytes == 1
+    assert w8.layout.rows == synth.make_workload(6).layout.rows
