@@ -8,9 +8,12 @@
 //
 // Design: memory-bound (per token: read hc*dim residual values and (hc+1)*dim projections, write
 // hc*dim), so one CTA per token reads each input once with 16-byte loads, keeps the 3*hc partial
-// sums of every copy in registers, reduces them across the block, and then writes the outputs;
-// the second read of h and value hits L1/L2 (the token's inputs were just read). The page's
-// PyTorch code instead makes ~15 full passes over fp32 temporaries.
+// sums of every copy in registers, reduces them across the block, and then writes the outputs.
+// The second pass re-reads h, so the first pass loads h with an L2 evict-last policy and every
+// read-once stream (keys, the value, h on its last use) with evict-first: without the hints the
+// keys pushed a third of h out of L2 before its second read (1.73 GB of DRAM reads instead of
+// 1.51 GB at 16,384 tokens; 1.62 ms instead of 1.43 ms at 65,536). The page's PyTorch code instead
+// makes ~15 full passes over fp32 temporaries.
 #include <cstdint>
 
 #include "engram_internal.cuh"
@@ -46,7 +49,29 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   return r;
 }
 
+// L2 eviction policies for the loads below (createpolicy: the whole access gets the priority)
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ uint4 ld16(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// 16 bytes (8 bf16) with an L2 eviction policy
+__device__ __forceinline__ uint4 ld16(const uint16_t* p, uint64_t policy) {
+  uint4 v;
+  asm("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p), "l"(policy));
+  return v;
+}
 
 // grid = T CTAs; HC residual copies known at compile time (the partial sums live in registers)
 template <int HC>
@@ -64,6 +89,7 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS) gate_ker
   __shared__ float red[3 * kGateMaxCopies][kGateThreads / 32];
   __shared__ float gate_s[kGateMaxCopies];
 
+  const uint64_t keep = l2_evict_last(), stream = l2_evict_first();
   float sh[HC], sk[HC], sd[HC];
 #pragma unroll
   for (int i = 0; i < HC; ++i) sh[i] = sk[i] = sd[i] = 0.f;
@@ -71,9 +97,9 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS) gate_ker
 #pragma unroll
     for (int i = 0; i < HC; ++i) {
       float h[8], k[8], q[8], w[8];
-      bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v), h);
-      bf16x8_to_f32(ld16(kvt + (int64_t)i * dim + 8 * v), k);
-      bf16x8_to_f32(ld16(qw + (int64_t)i * dim + 8 * v), q);
+      bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v, keep), h);      // read again below
+      bf16x8_to_f32(ld16(kvt + (int64_t)i * dim + 8 * v, stream), k);   // read once
+      bf16x8_to_f32(ld16(qw + (int64_t)i * dim + 8 * v), q);  // shared by every token (L1)
       bf16x8_to_f32(ld16(kw + (int64_t)i * dim + 8 * v), w);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -121,11 +147,11 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS) gate_ker
   uint16_t* ot = out + t * (int64_t)HC * dim;
   for (int v = tid; v < nvec; v += nthr) {
     float val[8];
-    bf16x8_to_f32(ld16(vt + 8 * v), val);
+    bf16x8_to_f32(ld16(vt + 8 * v, stream), val);
 #pragma unroll
     for (int i = 0; i < HC; ++i) {
       float h[8];
-      bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v), h);
+      bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v, stream), h);  // last use
       const float g = gate_s[i];
       uint4 o;
       o.x = f32x2_to_bf16x2(h[0] + g * val[0], h[1] + g * val[1]);
