@@ -154,8 +154,13 @@ __device__ __forceinline__ float widen_scale(uint32_t bits) {
   return lo;
 }
 
+// bf16 output rows are written once and not read again by this kernel: an L2 evict-first policy
+// lets them leave L2 ahead of lines still in use (254.7 vs 257.0 us per full-scale launch)
 __device__ __forceinline__ void st_out_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+  uint64_t policy;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(policy)
                : "memory");
 }
 
