@@ -72,7 +72,8 @@ __global__ void probe_read(const unsigned char* __restrict__ region, const int64
 //        1: codes only (no scale read)
 //        2: records of STRIDE bytes: codes at STRIDE k, scale at STRIDE k + 128
 //        3: blocks of 32 rows: [32 x 128 B codes][32 x 4 B scales] (4,224 B)
-// MODE 0: read + write; 1: read only (a practically never taken store keeps the loads); 2: write only
+// MODE 0: read + write; 1: read only (a practically never taken store keeps the loads); 2: write only;
+//      3: read + write, the writes with an L2 evict-first policy (as the fused kernel writes its rows)
 template <int U, int LAYOUT, int STRIDE, int MODE>
 __global__ void __launch_bounds__(256) probe_gather(const unsigned char* __restrict__ base,
                                                     const float* __restrict__ sbase,
@@ -120,6 +121,13 @@ __global__ void __launch_bounds__(256) probe_gather(const unsigned char* __restr
       uint4* o = out + row * 16;
       if (MODE == 1) {
         if ((a.x ^ b.y ^ a.z) == 0x12345678u) o[lane8] = a;
+      } else if (MODE == 3) {
+        uint64_t pol;
+        asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+        asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(o + lane8), "r"(a.x), "r"(a.y),
+                     "r"(a.z), "r"(a.w), "l"(pol) : "memory");
+        asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(o + 8 + lane8), "r"(b.x),
+                     "r"(b.y), "r"(b.z), "r"(b.w), "l"(pol) : "memory");
       } else {
         o[lane8] = a;
         o[8 + lane8] = b;
@@ -149,7 +157,7 @@ int time_gather(const Gather& g, const char* what, int blocks, int64_t* const* i
   float ms = 0.f;
   CK(cudaEventElapsedTime(&ms, g.e0, g.e1));
   const double us = ms * 1e3 / reps;
-  const char* kind = MODE == 0 ? "read+write" : (MODE == 1 ? "read only" : "write only");
+  const char* kind = MODE == 0 ? "read+write" : (MODE == 1 ? "read only" : (MODE == 2 ? "write only" : "rw, evict-first writes"));
   std::printf("%-44s %-10s grid %6d x 256, %d rows/thread-group pass: %7.1f us per launch\n", what, kind, blocks, U, us);
   return 0;
 }
@@ -218,6 +226,7 @@ int run_gather(bool layout) {
               (long long)kN, (long long)kRowsFull);
   if (!layout) {
     rc |= time_gather<4, 0, 0, 0>(g, "separate scales, short CTAs", short_ctas, g.idx);
+    rc |= time_gather<4, 0, 0, 3>(g, "separate scales, short CTAs", short_ctas, g.idx);
     rc |= time_gather<1, 0, 0, 0>(g, "separate scales, one row per thread group", (int)(kN / 32), g.idx);
     rc |= time_gather<4, 0, 0, 0>(g, "separate scales, persistent 4 CTAs/SM", sms * 4, g.idx);
     rc |= time_gather<8, 0, 0, 0>(g, "separate scales, persistent 8 CTAs/SM", sms * 8, g.idx);
