@@ -50,6 +50,34 @@ struct CallArgs {
   uint16_t* out[ENGRAM_MAX_LAYERS];
 };
 
+// Programmatic dependent launch. Every kernel of this library starts with pdl_wait(): it returns
+// once the kernel before it on the stream has completed and its writes are visible (at once when
+// there is none or the launch was not programmatic), so stream order holds for every global read
+// and write. Then pdl_trigger() lets the next launch be scheduled while this grid drains: its CTAs
+// take SM slots as this grid's last wave leaves instead of after a full launch gap.
+#ifndef ENGRAM_PDL
+#define ENGRAM_PDL 1
+#endif
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KernelArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KernelArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = ENGRAM_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Launchers (kernels.cu). Return cudaGetLastError() of the launch.
 cudaError_t launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s);
 cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s);

@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS) gate_ker
                                                    const uint16_t* __restrict__ qw, const uint16_t* __restrict__ kw,
                                                    const uint8_t* __restrict__ mask, const int dim, const float eps,
                                                    const float inv_sqrt_dim, uint16_t* out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int nvec = dim >> 3;  // 8 bf16 per 16-byte vector
@@ -169,8 +171,8 @@ cudaError_t launch_gate_hc(const uint16_t* x, const uint16_t* kv, const uint16_t
   int threads = dim / 8;
   threads = threads < 32 ? 32 : (threads > kGateThreads ? kGateThreads : ((threads + 31) / 32) * 32);
   const float inv_sqrt_dim = (float)(1.0 / sqrt((double)dim));
-  gate_kernel<HC><<<(unsigned)T, threads, 0, s>>>(x, kv, qw, kw, mask, dim, eps, inv_sqrt_dim, out);
-  return cudaGetLastError();
+  return launch_pdl(gate_kernel<HC>, dim3((unsigned)T), dim3(threads), 0, s, x, kv, qw, kw, mask, dim, eps,
+                    inv_sqrt_dim, out);
 }
 
 }  // namespace

@@ -224,6 +224,15 @@ __host__ __device__ inline SmemPlan smem_plan(int n_layers, int max_ngram, int n
   return p;
 }
 
+// The per-column constants and the multipliers into shared memory (every thread of the CTA). They
+// are written once, when the state is created, so this may run before pdl_wait().
+__device__ __forceinline__ void stage_constants(const StateView& sv, unsigned char* smem, const SmemPlan& plan) {
+  ColParam* cols_s = reinterpret_cast<ColParam*>(smem + plan.cols_off);
+  uint64_t* mult_s = reinterpret_cast<uint64_t*>(smem + plan.mult_off);
+  for (int i = threadIdx.x; i < sv.n_layers * sv.n_cols; i += blockDim.x) cols_s[i] = sv.cols[i];
+  for (int i = threadIdx.x; i < sv.n_layers * sv.max_ngram; i += blockDim.x) mult_s[i] = sv.mult[i];
+}
+
 // ------------------------------------------------------------------------------------------------
 // hash phase of one tile: `ntok` consecutive tokens starting at t0 of sequence b, whose Lb tokens
 // start at element seq_off of ids / mask / hashes and use cache row b (or cache_rows[b]). Called by
@@ -233,7 +242,7 @@ __host__ __device__ inline SmemPlan smem_plan(int n_layers, int max_ngram, int n
 __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a, unsigned char* smem,
                                           const SmemPlan& plan, const int tile, const int b, const int64_t seq_off,
                                           const int64_t Lb, const int64_t t0, const int ntok, const bool want_rowidx,
-                                          unsigned int* flags_s) {
+                                          const bool staged, unsigned int* flags_s) {
   const int N = sv.max_ngram, NL = sv.n_layers, C = sv.n_cols, H = sv.n_heads;
   const int NC = NL * C;
   ColParam* cols_s = reinterpret_cast<ColParam*>(smem + plan.cols_off);
@@ -250,8 +259,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
   int32_t* cache_row = sv.cache + (slot_ok ? r_b : 0) * sv.max_seq_len;  // dereferenced only when row_ok
 
   if (tid == 0 && !row_ok) atomicOr(flags_s, slot_ok ? ENGRAM_STATUS_BAD_START : ENGRAM_STATUS_BAD_ROW);
-  for (int i = tid; i < NC; i += nthr) cols_s[i] = sv.cols[i];
-  for (int i = tid; i < NL * N; i += nthr) mult_s[i] = sv.mult[i];
+  if (!staged) stage_constants(sv, smem, plan);
 
   // 1. compressed tokens of the tile and its halo: tok_s[j] holds position t0 - (N-1) + j.
   //    In-chunk tokens come from ids (token_map, mask) and do not wait for the start position;
@@ -353,6 +361,12 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
   __shared__ unsigned int flags_s;
   const int NL = sv.n_layers, C = sv.n_cols;
   const SmemPlan plan = smem_plan(NL, sv.max_ngram, C, tile, GATHER);
+  // dense calls: every CTA has tokens, so it stages the state's constants while the previous kernel
+  // drains; packed calls learn their extents first (CTAs past a sequence's end exit at once)
+  const bool dense = a.cu_seqlens == nullptr;
+  if (dense) stage_constants(sv, smem, plan);
+  pdl_wait();
+  pdl_trigger();
   const int64_t* rowidx_s = reinterpret_cast<const int64_t*>(smem + plan.rowidx_off);
   const int tid = threadIdx.x;
   const int b = blockIdx.y;
@@ -375,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
   const int ntok = (int)min((int64_t)tile, Lb - t0);
   if (tid == 0) flags_s = 0u;
   __syncthreads();
-  hash_tile(sv, a, smem, plan, tile, b, seq_off, Lb, t0, ntok, GATHER, &flags_s);
+  hash_tile(sv, a, smem, plan, tile, b, seq_off, Lb, t0, ntok, GATHER, dense, &flags_s);
 
   if (GATHER) {
     __syncthreads();
@@ -427,6 +441,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const int64_t* __restr
                                                           const uint8_t* __restrict__ W,
                                                           const void* __restrict__ S, const int64_t rows,
                                                           const int blk_shift, uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int G = D / 16;
   const int64_t units = n_idx * G;
   const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -470,8 +486,7 @@ cudaError_t launch_hash_k(const StateView& sv, const CallArgs& a, int tile, cuda
     if (e != cudaSuccess) return e;
   }
   dim3 grid((unsigned)((a.L + tile - 1) / tile), (unsigned)a.B);
-  kern<<<grid, GATHER ? kThreads : kHashThreads, plan.bytes, s>>>(sv, a, tile);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(GATHER ? kThreads : kHashThreads), plan.bytes, s, sv, a, tile);
 }
 
 // a row with a single scale block (block >= head_dim) loads its scale once
@@ -504,11 +519,8 @@ cudaError_t launch_lookup_s(const int64_t* idx, int64_t n_idx, const uint8_t* W,
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const int blk_shift = ilog2(blk);
-  if (blk >= D)
-    lookup_kernel<D, true, SDT><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
-  else
-    lookup_kernel<D, false, SDT><<<(unsigned)blocks, kThreads, 0, s>>>(idx, n_idx, W, S, rows, blk_shift, out);
-  return cudaGetLastError();
+  auto kern = blk >= D ? lookup_kernel<D, true, SDT> : lookup_kernel<D, false, SDT>;
+  return launch_pdl(kern, dim3((unsigned)blocks), dim3(kThreads), 0, s, idx, n_idx, W, S, rows, blk_shift, out);
 }
 
 template <int D>
