@@ -1,0 +1,101 @@
+"""Stream order across back-to-back launches (every kernel of the library is launched as a
+programmatic dependent and waits for the kernel before it before touching global memory): a torch
+kernel that writes the ids right before the fused call, the hash call feeding the lookup, the gate
+consuming its own output, also inside a CUDA graph; each against an unpipelined run or the oracle
+(GPU only)."""
+import numpy as np
+import pytest
+import torch
+
+import gram_hash_embedding_gb300 as geng
+import synth
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    H.build_all()
+    wl = synth.make_workload(0, full64=True)
+    Ws, Ss = H.device_tables(wl)
+    yield wl, Ws, Ss
+
+
+def test_producer_kernel_then_fused_call(tiny):
+    wl, Ws, Ss = tiny
+    lay = wl.layout
+    rng = np.random.default_rng(91)
+    B, L, steps = 4, 48, 24
+    srcs = [H.to_dev(rng.integers(0, lay.raw_vocab, size=(B, L))) for _ in range(steps)]
+    ids = torch.empty((B, L), dtype=torch.int64, device="cuda")
+    out = [torch.empty((B, L, lay.n_cols, lay.head_dim), dtype=torch.bfloat16, device="cuda")]
+    hashes = torch.empty((B, L, 1, lay.n_cols), dtype=torch.int64, device="cuda")
+    st, orc = H.make_state(wl, B, L * steps), H.make_oracle(wl, B, L * steps)
+    kept_h, kept_r = [], []
+    for k in range(steps):  # no synchronisation anywhere in the loop
+        torch.add(srcs[k], 0, out=ids)  # a torch kernel writes the ids the next launch reads
+        st.hash_lookup(ids, Ws, Ss, start_pos=k * L, out=out, hashes=hashes)
+        kept_h.append(hashes.clone())
+        kept_r.append(out[0].clone())
+    torch.cuda.synchronize()
+    for k in range(steps):
+        exp_h, _ = orc.hash(srcs[k].cpu().numpy(), k * L)
+        H.assert_bits_equal(kept_h[k].cpu().numpy(), exp_h, f"step {k} hashes")
+        H.assert_bits_equal(H.bf16_bits(kept_r[k]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]), f"step {k} rows")
+
+
+def test_hash_then_lookup_and_graph_replay(tiny):
+    wl, Ws, Ss = tiny
+    lay = wl.layout
+    rng = np.random.default_rng(92)
+    B, L = 3, 40
+    ids = H.to_dev(rng.integers(0, lay.raw_vocab, size=(B, L)))
+    fused_state, split_state = H.make_state(wl, B, 4096), H.make_state(wl, B, 4096)
+    hashes = torch.empty((B, L, 1, lay.n_cols), dtype=torch.int64, device="cuda")
+    rows = torch.empty((B * L * lay.n_cols, lay.head_dim), dtype=torch.bfloat16, device="cuda")
+    fused = [torch.empty((B, L, lay.n_cols, lay.head_dim), dtype=torch.bfloat16, device="cuda")]
+    sp = torch.zeros(B, dtype=torch.int32, device="cuda")
+
+    def step():  # the lookup reads what the hash call just wrote; the start advances on the device
+        split_state.hash(ids, sp, hashes=hashes)
+        split_state.lookup(hashes.view(-1), Ws[0], Ss[0], out=rows)
+        fused_state.hash_lookup(ids, Ws, Ss, start_pos=sp, out=fused)
+        torch.add(sp, L, out=sp)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    assert torch.equal(rows.view(torch.int16), fused[0].reshape(-1, lay.head_dim).view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(rows.view(torch.int16), fused[0].reshape(-1, lay.head_dim).view(torch.int16))
+    assert int(sp[0]) == L * (3 + 20)  # capture records the step without running it
+    assert fused_state.status() == 0 and split_state.status() == 0
+
+
+def test_gate_consumes_its_own_output():
+    H.build_all()
+    torch.manual_seed(93)
+    T, hc, dim = 512, 4, 256
+    x = torch.randn((T, hc, dim)).to(torch.bfloat16).cuda()
+    kv = torch.randn((T, (hc + 1) * dim)).to(torch.bfloat16).cuda()
+    qw = torch.rand((hc, dim)).add_(0.5).to(torch.bfloat16).cuda()
+    kw = torch.rand((hc, dim)).add_(0.5).to(torch.bfloat16).cuda()
+    ref = x.clone()
+    for _ in range(6):  # one launch at a time, synchronised
+        ref = geng.engram_gate(ref, kv, qw, kw)
+        torch.cuda.synchronize()
+    y = x.clone()
+    for _ in range(6):  # back to back, in place: each launch reads what the previous one wrote
+        geng.engram_gate(y, kv, qw, kw, out=y)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
