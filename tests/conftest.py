@@ -14,7 +14,7 @@ def pytest_configure(config):
 
 def pytest_collection_modifyitems(config, items):
     # GPU tests skip (not fail) on a machine without a GPU, so `-m "not gpu"` and a
-    # plain run on a CPU machine both stay green; on a GPU machine they run.
+    # plain run on a CPU-only machine both stay green; on a machine with a GPU they run.
     try:
         import torch
 
