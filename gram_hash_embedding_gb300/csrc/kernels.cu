@@ -3,8 +3,9 @@
 // Method ("DeepSeek V4.1" pages):
 //   blocks/stack-hashes page, n-gram hash `forward`: compress, mask, cache, lookback with
 //     cumulative blocking, multiply, rolling XOR, floored mod by primes, + offsets.
-//   engram-first/lookup page, `ParallelEngramEmbedding.forward`: fp8 row + fp32 scale gather,
-//     one fp32 multiply, round-to-nearest-even to bf16, +0 for out-of-range rows.
+//   engram-first/lookup page, `ParallelEngramEmbedding.forward`: fp8 row + block-scale gather
+//     (the scale, stored as fp32, bf16, UE8M0 or E4M3, widened to fp32), one fp32 multiply,
+//     round-to-nearest-even to bf16, +0 for out-of-range rows.
 //
 // Design (GB300): the path is HBM-bound (random 128-B row reads, streaming bf16 writes, ~99.9%
 // of its bytes); there is no dense contraction, so no tensor cores. A CTA owns a tile of
