@@ -73,7 +73,10 @@ __global__ void probe_read(const unsigned char* __restrict__ region, const int64
 //        2: records of STRIDE bytes: codes at STRIDE k, scale at STRIDE k + 128
 //        3: blocks of 32 rows: [32 x 128 B codes][32 x 4 B scales] (4,224 B)
 // MODE 0: read + write; 1: read only (a practically never taken store keeps the loads); 2: write only;
-//      3: read + write, the writes with an L2 evict-first policy (as the fused kernel writes its rows)
+//      3: read + write, the writes with an L2 evict-first policy (as the fused kernel writes its rows);
+//      4: read + write in the fused kernel's layout: lane q loads codes [8q, 8q+8) and [64+8q, 64+8q+8)
+//         and writes 16 bytes into each half of the 256-byte output row, so every warp store covers
+//         whole 32-byte sectors
 template <int U, int LAYOUT, int STRIDE, int MODE>
 __global__ void __launch_bounds__(256) probe_gather(const unsigned char* __restrict__ base,
                                                     const float* __restrict__ sbase,
@@ -107,7 +110,13 @@ __global__ void __launch_bounds__(256) probe_gather(const unsigned char* __restr
           c = base + blk * 4224 + j * 128;
           sp = reinterpret_cast<const float*>(base + blk * 4224 + 4096 + j * 4);
         }
-        v[u] = __ldg(reinterpret_cast<const uint4*>(c) + lane8);
+        if (MODE == 4) {
+          const uint2 lo = __ldg(reinterpret_cast<const uint2*>(c) + lane8);
+          const uint2 hi = __ldg(reinterpret_cast<const uint2*>(c + 64) + lane8);
+          v[u] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        } else {
+          v[u] = __ldg(reinterpret_cast<const uint4*>(c) + lane8);
+        }
         if (LAYOUT != 1) s[u] = __ldg(sp);
       }
     }
@@ -121,6 +130,9 @@ __global__ void __launch_bounds__(256) probe_gather(const unsigned char* __restr
       uint4* o = out + row * 16;
       if (MODE == 1) {
         if ((a.x ^ b.y ^ a.z) == 0x12345678u) o[lane8] = a;
+      } else if (MODE == 4) {
+        o[lane8] = make_uint4(v[u].x ^ sb, v[u].y, v[u].x, v[u].y);
+        o[8 + lane8] = make_uint4(v[u].z ^ sb, v[u].w, v[u].z, v[u].w);
       } else if (MODE == 3) {
         uint64_t pol;
         asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -157,7 +169,9 @@ int time_gather(const Gather& g, const char* what, int blocks, int64_t* const* i
   float ms = 0.f;
   CK(cudaEventElapsedTime(&ms, g.e0, g.e1));
   const double us = ms * 1e3 / reps;
-  const char* kind = MODE == 0 ? "read+write" : (MODE == 1 ? "read only" : (MODE == 2 ? "write only" : "rw, evict-first writes"));
+  const char* kind = MODE == 0 ? "read+write"
+                     : (MODE == 1 ? "read only"
+                                  : (MODE == 2 ? "write only" : (MODE == 3 ? "rw, evict-first writes" : "rw, fused layout")));
   std::printf("%-44s %-10s grid %6d x 256, %d rows/thread-group pass: %7.1f us per launch\n", what, kind, blocks, U, us);
   return 0;
 }
@@ -227,6 +241,7 @@ int run_gather(bool layout) {
   if (!layout) {
     rc |= time_gather<4, 0, 0, 0>(g, "separate scales, short CTAs", short_ctas, g.idx);
     rc |= time_gather<4, 0, 0, 3>(g, "separate scales, short CTAs", short_ctas, g.idx);
+    rc |= time_gather<4, 0, 0, 4>(g, "separate scales, short CTAs", short_ctas, g.idx);
     rc |= time_gather<1, 0, 0, 0>(g, "separate scales, one row per thread group", (int)(kN / 32), g.idx);
     rc |= time_gather<4, 0, 0, 0>(g, "separate scales, persistent 4 CTAs/SM", sms * 4, g.idx);
     rc |= time_gather<8, 0, 0, 0>(g, "separate scales, persistent 8 CTAs/SM", sms * 8, g.idx);
