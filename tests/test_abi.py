@@ -71,6 +71,13 @@ def test_host_side_checks_need_no_gpu(lib):
     assert L.engram_lookup(None, 5, None, None, 4, 128, 128, 4, None, None) == geng.ERR_UNSUPPORTED  # scale type
     assert L.engram_lookup(None, 0, None, None, 4, 128, 128, geng.SCALE_E8M0, None, None) == geng.OK
     assert L.engram_lookup(None, -1, None, None, 4, 128, 128, 0, None, None) == geng.ERR_INVALID
+    # scale pointers must be aligned to their storage type's width (rejected before any launch:
+    # only rejected cases are tried, the addresses are never dereferenced)
+    base = 1 << 20
+    assert L.engram_lookup(base, 5, base, base + 2, 4, 128, 128, geng.SCALE_F32, base, None) == geng.ERR_INVALID
+    assert L.engram_lookup(base, 5, base, base + 1, 4, 128, 128, geng.SCALE_BF16, base, None) == geng.ERR_INVALID
+    assert L.engram_lookup(base + 4, 5, base, base, 4, 128, 128, geng.SCALE_E8M0, base, None) == geng.ERR_INVALID
+    assert L.engram_lookup(base, 5, base + 8, base, 4, 128, 128, geng.SCALE_E4M3, base, None) == geng.ERR_INVALID
     assert lib.engram_state_destroy(None) == 0
 
 
