@@ -360,3 +360,39 @@ def test_hash_moduli_at_the_extremes():
                                  max_seq_len=8, token_map=lay.token_map, multipliers=lay.multipliers,
                                  primes=lay.primes, offsets=bad)
     assert e.value.code == geng.ERR_INVALID
+
+
+def test_batch_at_the_grid_limit():
+    """max_batch 65,535 (the largest the library takes; one grid row per sequence, CUDA's
+    gridDim.y limit): a dense call over every row, some rows starting exactly at max_seq_len - L,
+    some with every token masked, and a packed call over all 65,535 sequences, against the oracle."""
+    wl = synth.make_workload(0, full64=True)
+    lay = wl.layout
+    B, L, max_seq = 65535, 3, 8
+    rng = np.random.default_rng(65535)
+    ids = rng.integers(0, lay.raw_vocab, size=(B, L))
+    start = rng.integers(0, max_seq - L + 1, size=B).astype(np.int32)
+    start[::7] = max_seq - L                       # the last position that fits
+    mask = rng.random((B, L)) > 0.1
+    mask[::11] = False                             # whole rows masked
+    Ws, Ss = H.device_tables(wl)
+    st, orc = H.make_state(wl, B, max_seq), H.make_oracle(wl, B, max_seq)
+    hashes = torch.empty((B, L, 1, lay.n_cols), dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup(H.to_dev(ids), Ws, Ss, start_pos=H.to_dev(start), mask=H.to_dev(mask), hashes=hashes)
+    exp_h, fl = orc.hash(ids, start.astype(np.int64), mask)
+    assert fl == 0 and st.status() == 0
+    H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "hashes at B=65535")
+    H.assert_bits_equal(H.bf16_bits(outs[0]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]), "rows at B=65535")
+    # packed: every sequence one token long, at the next position
+    cu = np.arange(B + 1, dtype=np.int32)
+    ids2 = rng.integers(0, lay.raw_vocab, size=B)
+    st2 = start + L
+    st2[st2 >= max_seq] = max_seq - 1
+    exp2, _ = orc.hash_varlen(ids2, cu, st2, None)
+    got2 = st.hash_varlen(H.to_dev(ids2), H.to_dev(cu), H.to_dev(st2), max_len=1)
+    H.assert_bits_equal(got2.cpu().numpy(), exp2, "packed hashes at B=65535")
+    with pytest.raises(geng.EngramError) as e:
+        geng.engram_state_create(n_layers=1, max_ngram=4, n_heads=2, head_dim=32, block=32, max_batch=65536,
+                                 max_seq_len=8, token_map=lay.token_map, multipliers=lay.multipliers,
+                                 primes=lay.primes, offsets=lay.offsets)
+    assert e.value.code == geng.ERR_UNSUPPORTED
