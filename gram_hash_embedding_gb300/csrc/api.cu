@@ -91,7 +91,8 @@ int check_call(const engram_state* st, const int64_t* ids, const uint8_t* mask, 
   if (ids == nullptr || start_pos == nullptr || !aligned(ids, 8) || !aligned(start_pos, 4)) return ENGRAM_ERR_INVALID;
   if (cache_rows != nullptr && !aligned(cache_rows, 4)) return ENGRAM_ERR_INVALID;
   if (B > st->lay.max_batch || L > st->lay.max_seq_len) return ENGRAM_ERR_RANGE;
-  if ((int64_t)B * L > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
+  // tiles of >= 4 tokens keep the grid's x extent, ceil(L / tile), inside CUDA's 2^31 - 1
+  if ((int64_t)B * L > ((int64_t)1 << 40) || L > ((int64_t)1 << 32)) return ENGRAM_ERR_UNSUPPORTED;
   if (!on_state_device(st)) return ENGRAM_ERR_INVALID;
   return ENGRAM_OK;
 }
@@ -288,6 +289,7 @@ int packed_call(const engram_state* st, const int64_t* ids, const uint8_t* mask,
   if (cache_rows != nullptr && !aligned(cache_rows, 4)) return ENGRAM_ERR_INVALID;
   if (B > st->lay.max_batch || max_len > st->lay.max_seq_len) return ENGRAM_ERR_RANGE;
   if (T > ((int64_t)1 << 31) - 1) return ENGRAM_ERR_UNSUPPORTED;  // int32 extents
+  if (max_len > ((int64_t)1 << 32)) return ENGRAM_ERR_UNSUPPORTED;  // grid x extent, as for dense calls
   if (!on_state_device(st)) return ENGRAM_ERR_INVALID;
   *a = call_args(st, ids, mask, start_pos, cache_rows, B, max_len, hashes);
   a->cu_seqlens = cu_seqlens;

@@ -132,7 +132,8 @@ int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* f
  *              that row and raises ENGRAM_STATUS_BAD_ROW.
  *   hashes     device int64 [B][L][n_layers][C], written
  * Writes cache[r][start_pos[b] + t] (r = row b's cache row) for every valid row. Rows never interact.
- * B == 0 or L == 0 is a no-op. Errors: _INVALID (null, misaligned), _RANGE (B > max_batch, L > max_seq_len).
+ * B == 0 or L == 0 is a no-op. Errors: _INVALID (null, misaligned), _RANGE (B > max_batch, L > max_seq_len),
+ * _UNSUPPORTED (B * L > 2^40 or L > 2^32).
  */
 int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
                 const int32_t* cache_rows, int32_t B, int64_t L, int64_t* hashes, engram_stream_t stream);
@@ -174,7 +175,7 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
  *   cu_seqlens  device int32 [B+1], non-decreasing, cu_seqlens[0] = 0 and cu_seqlens[B] = T expected
  *   start_pos   device int32 [B]
  *   cache_rows  device int32 [B] or NULL: the cache row of sequence b, as in engram_hash
- *   max_len     host: an upper bound on every sequence's length (sizes the grid; max_len <= max_seq_len)
+ *   max_len     host: an upper bound on every sequence's length (sizes the grid; max_len <= max_seq_len and <= 2^32)
  *   hashes      device int64 [T][n_layers][C]
  * A sequence whose extent is inconsistent is skipped and flagged (ENGRAM_STATUS_BAD_LENGTH); a start
  * position that does not fit is handled as in engram_hash. Extents must not overlap (tokens shared by
