@@ -27,7 +27,7 @@ __all__ = [
     "EngramError", "EngramHash", "build", "engram_state_create", "engram_state_destroy", "engram_cache_reset",
     "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
     "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START",
-    "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "SCALE_F32", "SCALE_BF16", "SCALE_E8M0", "SCALE_E4M3",
+    "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "STATUS_CHECK", "SCALE_F32", "SCALE_BF16", "SCALE_E8M0", "SCALE_E4M3",
     "library_path",
 ]
 
@@ -36,6 +36,7 @@ STATUS_BAD_START = 1
 STATUS_BAD_ID = 2
 STATUS_BAD_LENGTH = 4
 STATUS_BAD_ROW = 8
+STATUS_CHECK = 16  # checked builds only: a kernel skipped an access outside the call's buffers
 # storage types of the scale tensors (ENGRAM_SCALE_*)
 SCALE_F32, SCALE_BF16, SCALE_E8M0, SCALE_E4M3 = 0, 1, 2, 3
 _SCALE_BYTES = {SCALE_F32: 4, SCALE_BF16: 2, SCALE_E8M0: 1, SCALE_E4M3: 1}

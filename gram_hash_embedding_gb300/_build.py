@@ -31,18 +31,22 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=None, lib_path: str = LIB) -> str:
+    """Build `lib_path` (default: the package's libengram.so) when it is older than its sources.
+    A library built with extra flags (e.g. the checked build, -DENGRAM_CHECKED=1) goes to its own
+    path and object directory."""
     nvcc = os.environ.get("NVCC", "nvcc")
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(INCLUDE, "engram.h"))
     srcs = sources()
-    if not force and not _stale(LIB, srcs + headers + [__file__]):
-        return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    if not force and not _stale(lib_path, srcs + headers + [__file__]):
+        return lib_path
+    build_dir = BUILD_DIR if lib_path == LIB else BUILD_DIR + "_" + os.path.splitext(os.path.basename(lib_path))[0]
+    os.makedirs(build_dir, exist_ok=True)
     flags = NVCC_FLAGS + list(extra_flags or [])
     procs, objs = [], []
     for src in srcs:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         objs.append(obj)
         cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
@@ -57,10 +61,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
             failed.append(" ".join(cmd))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -63,6 +63,19 @@ constexpr int kTargetCtas = ENGRAM_TARGET_CTAS;    // fused grid size the tile c
 constexpr int kHashTile = ENGRAM_HASH_TILE;        // tokens per CTA, hash-only kernel
 constexpr int kHashThreads = ENGRAM_HASH_THREADS;  // threads per CTA, hash-only kernel (<= kThreads)
 
+// Checked builds (-DENGRAM_CHECKED=1, a debugging aid in place of a memory checker): the hash and
+// fused kernels test every global access against the call's sizes before making it; an access
+// outside them is skipped and raises ENGRAM_STATUS_CHECK. Release builds compile the tests away.
+#ifndef ENGRAM_CHECKED
+#define ENGRAM_CHECKED 0
+#endif
+
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned int* flags_s) {
+  if (!ENGRAM_CHECKED || ok) return true;
+  atomicOr(flags_s, ENGRAM_STATUS_CHECK);
+  return false;
+}
+
 // ------------------------------------------------------------------------------------------------
 // integer helpers
 
@@ -270,16 +283,18 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
     const int64_t t = t0 - (N - 1) + j;
     int32_t c = dead;
     if (t >= 0) {
-      const int64_t id = a.ids[seq_off + t];
-      if (id < 0 || id >= sv.raw_vocab) {
-        if (row_ok) atomicOr(flags_s, ENGRAM_STATUS_BAD_ID);
-      } else {
-        c = sv.token_map[id];
+      if (in_bounds(seq_off + t >= 0 && seq_off + t < a.total, flags_s)) {
+        const int64_t id = a.ids[seq_off + t];
+        if (id < 0 || id >= sv.raw_vocab) {
+          if (row_ok) atomicOr(flags_s, ENGRAM_STATUS_BAD_ID);
+        } else {
+          c = sv.token_map[id];
+        }
+        if (a.mask != nullptr && a.mask[seq_off + t] == 0) c = dead;
       }
-      if (a.mask != nullptr && a.mask[seq_off + t] == 0) c = dead;
     } else if (row_ok) {
       const int64_t p = s_b + t;
-      c = (p >= 0) ? cache_row[p] : dead;
+      if (p >= 0 && in_bounds(p < sv.max_seq_len && r_b >= 0 && r_b < sv.max_batch, flags_s)) c = cache_row[p];
     }
     tok_s[j] = c;
   }
@@ -290,7 +305,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
     for (int t = tid; t < ntok; t += nthr) {
       const int32_t cur = tok_s[t + N - 1];
       const int64_t pos = s_b + t0 + t;
-      cache_row[pos] = cur;
+      if (in_bounds(pos >= 0 && pos < sv.max_seq_len, flags_s)) cache_row[pos] = cur;
       int64_t tok[ENGRAM_MAX_NGRAM];
       bool blocked = false;
 #pragma unroll
@@ -330,7 +345,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
       for (int t = tid / NC; t < ntok; t += tstep) {
         int64_t h = -1;
         if (row_ok) h = floored_mod(roll_s[(t * NL + l) * (N - 1) + i], cp) + cp.offset;
-        if (a.hashes != nullptr) a.hashes[(seq_off + t0 + t) * NC + j] = h;
+        if (a.hashes != nullptr && in_bounds(seq_off + t0 + t < a.total, flags_s)) a.hashes[(seq_off + t0 + t) * NC + j] = h;
         if (want_rowidx) rowidx_s[(l * ntok + t) * C + col] = h;
       }
     }
@@ -345,7 +360,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
         const ColParam cp = cols_s[j];
         h = floored_mod(roll_s[(t * NL + l) * (N - 1) + col / H], cp) + cp.offset;
       }
-      if (a.hashes != nullptr) a.hashes[(seq_off + t0 + t) * NC + j] = h;
+      if (a.hashes != nullptr && in_bounds(seq_off + t0 + t < a.total, flags_s)) a.hashes[(seq_off + t0 + t) * NC + j] = h;
       if (want_rowidx) rowidx_s[(l * ntok + t) * C + col] = h;
     }
   }
@@ -418,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
             ++l;
           }
           const int r = u / G;
+          if (!in_bounds(out_base_row + r < a.total * C, &flags_s)) continue;
           orow[k] = a.out[l] + (out_base_row + r) * D;
           piece_load<D, ONE, SDT>(pc[k], a.W[l], a.S[l], a.rows[l], rowidx_s[l * rpl + r], u % G, blk_shift);
         }

@@ -65,6 +65,9 @@ typedef struct engram_state engram_state;
                                        write, its hash ids and rows left unwritten) */
 #define ENGRAM_STATUS_BAD_ROW 8u   /* a cache_rows entry outside [0, max_batch): that row (sequence) wrote nothing to
                                       the cache, its hash ids are -1 and its looked-up rows are +0 */
+#define ENGRAM_STATUS_CHECK 16u    /* checked builds only (compiled with -DENGRAM_CHECKED=1): a hash or fused kernel
+                                      skipped a memory access outside the call's buffers. A library bug, never a
+                                      data error; release builds do not test for it */
 
 /* Storage types of the scale tensors. The engram-first/lookup page leaves `scale_dtype` open and
  * widens the scale with `.float()`; each type below widens to fp32 exactly before the one fp32
