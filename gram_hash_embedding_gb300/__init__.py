@@ -196,6 +196,28 @@ def _start_tensor(start_pos, B: int, device) -> torch.Tensor:
     return torch.full((B,), int(start_pos), dtype=torch.int32, device=device)
 
 
+def _size(t, n: int, name: str) -> None:
+    """Sizes are checked here, before any pointer reaches the library: the C calls take raw pointers
+    and would read or write past a buffer that is too small."""
+    if t is not None and isinstance(t, torch.Tensor) and t.numel() != n:
+        raise ValueError(f"{name} has {t.numel()} elements, expected {n}")
+
+
+def _tables(lay: dict, W: list, S: list, out: list | None, n_rows_out: int) -> None:
+    """Per-layer tables of a fused call: one W, S (and out) per engram layer of the state, W [rows, D],
+    S holding rows * D / block scales, out holding n_rows_out * C rows of D values."""
+    n = lay["n_layers"]
+    if len(W) != n or len(S) != n or (out is not None and len(out) != n):
+        raise ValueError(f"W, S and out need one entry per engram layer ({n})")
+    D, C = lay["head_dim"], (lay["max_ngram"] - 1) * lay["n_heads"]
+    for l in range(n):
+        if W[l].dim() != 2 or W[l].shape[1] != D:
+            raise ValueError(f"W[{l}] must be [rows, {D}], got {tuple(W[l].shape)}")
+        _size(S[l], W[l].shape[0] * (D // lay["block"]), f"S[{l}]")
+        if out is not None:
+            _size(out[l], n_rows_out * C * D, f"out[{l}]")
+
+
 def _rows_ptr(cache_rows):
     return None if cache_rows is None else _dev(cache_rows, torch.int32, "cache_rows")
 
@@ -207,10 +229,15 @@ def engram_hash(state: int, ids: torch.Tensor, start_pos, mask: torch.Tensor | N
     cache_rows int32 [B] or None (row b uses cache row cache_rows[b], else b).
     Returns (or fills) int64 hash ids [B, L, n_layers, C]."""
     B, L = ids.shape
+    lay = engram_state_layout(state)
+    NC = lay["n_layers"] * (lay["max_ngram"] - 1) * lay["n_heads"]
     if hashes is None:
-        lay = engram_state_layout(state)
         hashes = torch.empty((B, L, lay["n_layers"], (lay["max_ngram"] - 1) * lay["n_heads"]), dtype=torch.int64,
                              device=ids.device)
+    _size(hashes, B * L * NC, "hashes")
+    _size(mask, B * L, "mask")
+    _size(cache_rows, B, "cache_rows")
+    _size(start_pos, B, "start_pos")
     sp = _start_tensor(start_pos, B, ids.device)
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     _check(_lib().engram_hash(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"),
@@ -231,6 +258,9 @@ def engram_lookup(idx: torch.Tensor, W: torch.Tensor, S: torch.Tensor, block: in
     rows, D = W.shape
     if out is None:
         out = torch.empty(tuple(idx.shape) + (D,), dtype=torch.bfloat16, device=idx.device)
+    _size(out, idx.numel() * D, "out")
+    if int(block) > 0 and D % int(block) == 0:
+        _size(S, rows * (D // int(block)), "S")
     Wu = W.view(torch.uint8)
     _check(_lib().engram_lookup(_dev(idx, torch.int64, "idx"), idx.numel(), _dev(Wu, torch.uint8, "W"),
                                 _dev_scales(S, sdt), rows, D, int(block), sdt, _dev(out, torch.bfloat16, "out"),
@@ -244,18 +274,20 @@ def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: lis
     """Hash + per-layer lookup in one launch. W/S: per-layer tables. Returns (or fills) the
     per-layer bf16 outputs [B, L, C, D]."""
     B, L = ids.shape
+    lay = engram_state_layout(state)
     n = len(W)
-    if n != len(S) or n > MAX_LAYERS:
-        raise ValueError("W and S need one entry per engram layer")
-    D = W[0].shape[1]
-    if out is None:
-        lay = engram_state_layout(state)
-        C = (lay["max_ngram"] - 1) * lay["n_heads"]
+    D, C = lay["head_dim"], (lay["max_ngram"] - 1) * lay["n_heads"]
+    if out is None and len(W) == lay["n_layers"]:
         out = [torch.empty((B, L, C, D), dtype=torch.bfloat16, device=ids.device) for _ in range(n)]
+    _tables(lay, W, S, out, B * L)
+    _size(hashes, B * L * lay["n_layers"] * C, "hashes")
+    _size(mask, B * L, "mask")
+    _size(cache_rows, B, "cache_rows")
+    _size(start_pos, B, "start_pos")
     sp = _start_tensor(start_pos, B, ids.device)
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     Wp = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
-    sdt = engram_state_layout(state)["scale_dtype"]
+    sdt = lay["scale_dtype"]
     Sp = (_P * n)(*[_dev_scales(s, sdt) for s in S])
     Rp = (_I64 * n)(*[w.shape[0] for w in W])
     Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
@@ -280,10 +312,14 @@ def engram_hash_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, 
     Returns (or fills) int64 hash ids [T, n_layers, C]."""
     T = ids.numel()
     B = cu_seqlens.numel() - 1
+    lay = engram_state_layout(state)
     if hashes is None:
-        lay = engram_state_layout(state)
         hashes = torch.empty((T, lay["n_layers"], (lay["max_ngram"] - 1) * lay["n_heads"]), dtype=torch.int64,
                              device=ids.device)
+    _size(hashes, T * lay["n_layers"] * (lay["max_ngram"] - 1) * lay["n_heads"], "hashes")
+    _size(mask, T, "mask")
+    _size(start_pos, B, "start_pos")
+    _size(cache_rows, B, "cache_rows")
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     _check(_lib().engram_hash_varlen(state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"),
                                      _dev(start_pos, torch.int32, "start_pos"), _rows_ptr(cache_rows), B, T,
@@ -300,17 +336,19 @@ def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.T
     outputs [T, C, D]."""
     T = ids.numel()
     B = cu_seqlens.numel() - 1
+    lay = engram_state_layout(state)
     n = len(W)
-    if n != len(S) or n > MAX_LAYERS:
-        raise ValueError("W and S need one entry per engram layer")
-    D = W[0].shape[1]
-    if out is None:
-        lay = engram_state_layout(state)
-        C = (lay["max_ngram"] - 1) * lay["n_heads"]
+    D, C = lay["head_dim"], (lay["max_ngram"] - 1) * lay["n_heads"]
+    if out is None and len(W) == lay["n_layers"]:
         out = [torch.empty((T, C, D), dtype=torch.bfloat16, device=ids.device) for _ in range(n)]
+    _tables(lay, W, S, out, T)
+    _size(hashes, T * lay["n_layers"] * C, "hashes")
+    _size(mask, T, "mask")
+    _size(start_pos, B, "start_pos")
+    _size(cache_rows, B, "cache_rows")
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     Wp = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
-    sdt = engram_state_layout(state)["scale_dtype"]
+    sdt = lay["scale_dtype"]
     Sp = (_P * n)(*[_dev_scales(x, sdt) for x in S])
     Rp = (_I64 * n)(*[w.shape[0] for w in W])
     Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
@@ -332,6 +370,11 @@ def engram_gate(x: torch.Tensor, kv: torch.Tensor, q_weight: torch.Tensor, k_wei
     T = x.numel() // (hc * dim)
     if out is None:
         out = torch.empty_like(x)
+    _size(kv, T * (hc + 1) * dim, "kv")
+    _size(q_weight, hc * dim, "q_weight")
+    _size(k_weight, hc * dim, "k_weight")
+    _size(mask, T, "mask")
+    _size(out, T * hc * dim, "out")
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     _check(_lib().engram_gate(_dev(x, torch.bfloat16, "x"), _dev(kv, torch.bfloat16, "kv"),
                               _dev(q_weight, torch.bfloat16, "q_weight"), _dev(k_weight, torch.bfloat16, "k_weight"),
@@ -352,11 +395,22 @@ class PreparedHashLookup:
                  cu_seqlens: torch.Tensor | None = None, max_len: int | None = None, stream=None,
                  cache_rows: torch.Tensor | None = None):
         n = len(W)
-        if n != len(S) or n != len(out) or n > MAX_LAYERS:
-            raise ValueError("W, S and out need one entry per engram layer")
+        lay = engram_state_layout(state)
+        NC = lay["n_layers"] * (lay["max_ngram"] - 1) * lay["n_heads"]
+        if cu_seqlens is None:
+            B, T = ids.shape
+            rows_out = B * T
+        else:
+            B, T = cu_seqlens.numel() - 1, ids.numel()
+            rows_out = T
+        _tables(lay, W, S, out, rows_out)
+        _size(hashes, rows_out * NC, "hashes")
+        _size(mask, rows_out, "mask")
+        _size(start_pos, B, "start_pos")
+        _size(cache_rows, B, "cache_rows")
         self._keep = (ids, start_pos, W, S, out, mask, hashes, cu_seqlens, cache_rows)  # the buffers stay alive
         self._W = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
-        sdt = engram_state_layout(state)["scale_dtype"]
+        sdt = lay["scale_dtype"]
         self._S = (_P * n)(*[_dev_scales(x, sdt) for x in S])
         self._R = (_I64 * n)(*[w.shape[0] for w in W])
         self._O = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
@@ -367,11 +421,9 @@ class PreparedHashLookup:
         self._stream = None if stream is None else _stream(stream)
         L = _lib()
         if cu_seqlens is None:
-            B, T = ids.shape
             self._fn = L.engram_hash_lookup
             self._args = (state, _dev(ids, torch.int64, "ids"), m, sp, cr, B, T, self._W, self._S, self._R, self._O, h)
         else:
-            B = cu_seqlens.numel() - 1
             self._fn = L.engram_hash_lookup_varlen
             self._args = (state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"), sp, cr,
                           B, ids.numel(), _max_len(cu_seqlens, max_len), self._W, self._S, self._R, self._O, h)

@@ -95,3 +95,23 @@ def test_oracle_is_not_referenced_by_the_product():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read().lower()
                 assert "oracle" not in text, f"{f} mentions the oracle"
+
+
+def test_binding_checks_sizes_before_any_pointer():
+    """Buffers of the wrong size are refused by the binding before it takes a pointer (the C calls
+    take raw pointers and cannot tell); CPU tensors reach the size checks first, so no GPU is needed."""
+    import torch
+
+    idx = torch.zeros(10, dtype=torch.int64)
+    W = torch.zeros((4, 128), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="S has"):
+        geng.engram_lookup(idx, W, torch.zeros((4, 2), dtype=torch.float32), 128)      # 1 scale per row expected
+    with pytest.raises(ValueError, match="out has"):
+        geng.engram_lookup(idx, W, torch.zeros((4, 1), dtype=torch.float32), 128,
+                           out=torch.empty((9, 128), dtype=torch.bfloat16))
+    x = torch.zeros((3, 4, 64), dtype=torch.bfloat16)
+    w = torch.zeros((4, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="kv has"):
+        geng.engram_gate(x, torch.zeros((3, 4 * 64), dtype=torch.bfloat16), w, w)      # the value row is missing
+    with pytest.raises(ValueError, match="mask has"):
+        geng.engram_gate(x, torch.zeros((3, 5 * 64), dtype=torch.bfloat16), w, w, mask=torch.ones(4, dtype=torch.bool))

@@ -5,6 +5,8 @@ multiply then round-to-nearest-even to bf16 on both sides: bit-exact (0 ulp).
 The seeded tables never hold the NaN codes, so no NaN payload is compared;
 the all-codes test compares NaN positions only.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -396,3 +398,33 @@ def test_batch_at_the_grid_limit():
                                  max_seq_len=8, token_map=lay.token_map, multipliers=lay.multipliers,
                                  primes=lay.primes, offsets=lay.offsets)
     assert e.value.code == geng.ERR_UNSUPPORTED
+
+
+def test_binding_refuses_wrong_sizes():
+    """One table per engram layer and buffers of the call's sizes, or a ValueError before anything
+    is launched (the C calls take raw pointers)."""
+    base = synth.make_workload(0, full64=True)
+    lay = dataclasses.replace(base.layout, n_layers=2, multipliers=np.concatenate([base.layout.multipliers] * 2),
+                              primes=np.concatenate([base.layout.primes] * 2),
+                              offsets=np.concatenate([base.layout.offsets] * 2))
+    wl = dataclasses.replace(base, layout=lay)
+    Ws, Ss = H.device_tables(wl)
+    st = H.make_state(wl, 2, 64)
+    ids = H.to_dev(np.zeros((2, 8), dtype=np.int64))
+    C, D = lay.n_cols, lay.head_dim
+    with pytest.raises(ValueError, match="one entry per engram layer"):
+        st.hash_lookup(ids, Ws[:1], Ss[:1])
+    with pytest.raises(ValueError, match="out"):
+        st.hash_lookup(ids, Ws, Ss, out=[torch.empty((2, 8, C, D), dtype=torch.bfloat16, device="cuda"),
+                                         torch.empty((2, 7, C, D), dtype=torch.bfloat16, device="cuda")])
+    with pytest.raises(ValueError, match="hashes"):
+        st.hash_lookup(ids, Ws, Ss, hashes=torch.empty((2, 8, 1, C), dtype=torch.int64, device="cuda"))
+    with pytest.raises(ValueError, match="mask"):
+        st.hash(ids, 0, mask=torch.ones((2, 7), dtype=torch.bool, device="cuda"))
+    with pytest.raises(ValueError, match="S\\[1\\]"):
+        st.hash_lookup(ids, Ws, [Ss[0], Ss[1][:-1]])
+    out = [torch.empty((2, 8, C, D), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    with pytest.raises(ValueError, match="start_pos"):
+        st.prepare_hash_lookup(ids, torch.zeros(3, dtype=torch.int32, device="cuda"), Ws, Ss, out)
+    torch.cuda.synchronize()
+    assert st.status() == 0
