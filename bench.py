@@ -65,11 +65,21 @@ def parse_args(argv=None):
                    help="L2 between timed steps: flush = write 256 MB before every step and time the kernels "
                         "alone; auto (default) = flush when the steps' rows fit in L2 (decode) and launches are "
                         "eager; none = back to back")
+    p.add_argument("--l2-fetch", type=int, default=32, choices=[0, 32, 64, 128],
+                   help="the context's L2 fetch granularity limit for the run (bytes; 0 leaves the context "
+                        "default, 64 on GB300). At 32 a row's random 4-byte scale read costs a 32-byte DRAM "
+                        "sector instead of a 128-byte line (engram_set_l2_fetch_granularity)")
     p.add_argument("--probe", choices=["access", "gather", "layout"],
                    help="run a DRAM measurement probe (bench_probe.cu) instead of the benchmark: access = DRAM "
                         "bytes per random read size (under ncu), gather = the fused kernel's byte pattern without "
                         "the hash, layout = scale placement next to the codes")
     return p.parse_args(argv)
+
+
+def apply_l2_fetch(geng, nbytes: int):
+    """Set the L2 fetch granularity limit of this process's context (0: leave it as it is); returns
+    the previous value, or None when it was left."""
+    return geng.set_l2_fetch_granularity(nbytes) if nbytes else None
 
 
 L2_BYTES = 129 * 1000 * 1000  # GB300 L2
@@ -241,9 +251,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(cfg: int):
+def recorded_traffic(cfg: int, l2_fetch: int = 0):
     """DRAM bytes per launch of the fused kernel from the committed ncu summary ("key: value" lines),
-    or None when the kernel sources changed since the counters were taken or the workload differs."""
+    or None when the kernel sources changed since the counters were taken, or the workload or the L2
+    fetch granularity setting (0: the context default) differs."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     d = {}
@@ -254,6 +265,8 @@ def recorded_traffic(cfg: int):
             k, v = line.split(":", 1)
             d[k.strip()] = v.strip()
     if d.get("source_sha256") != kernel_source_hash() or int(d.get("cfg", -1)) != cfg:
+        return None
+    if int(d.get("l2_fetch_granularity", 0)) != l2_fetch:
         return None
     return float(d["dram_bytes_per_launch"])
 
@@ -742,6 +755,7 @@ def run_ours(args):
     import gram_hash_embedding_gb300 as geng
 
     geng._lib()
+    l2_default = apply_l2_fetch(geng, args.l2_fetch)
     runner = Runner(args.cfg, rank, device)
     runner.setup_mode(args.mode)
     stream = torch.cuda.current_stream(device)
@@ -807,7 +821,7 @@ def run_ours(args):
     launch_s = mean_launch / runner.launches_per_step
     peak, peak_kind = measured_peaks()
     achieved = algo_bytes / launch_s / 1e9
-    traffic = recorded_traffic(args.cfg) if args.mode == "fused" else None
+    traffic = recorded_traffic(args.cfg, args.l2_fetch) if args.mode == "fused" else None
 
     cpu = cpu_all = cpu_torch = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not runner.varlen and args.mode == "fused":
@@ -843,6 +857,8 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (no exchange step)",
             "l2": l2_note(runner, flush_l2, fits_l2),
             "status_flags_after_warmup": flags,
+            "l2_fetch_granularity": (f"{args.l2_fetch} B (context default {l2_default} B)" if args.l2_fetch
+                                     else "context default"),
             "launch": "CUDA graph replay" if args.graph else "eager launches from Python",
         },
         "gathered_gbs": achieved,
@@ -886,6 +902,7 @@ def run_block(args):
         import __graft_entry__
 
         __graft_entry__.build()
+    l2_default = apply_l2_fetch(geng, args.l2_fetch)
     runner = Runner(args.cfg, rank, device)
     lay = runner.lay
     T = runner.tokens_per_step
@@ -952,7 +969,9 @@ def run_block(args):
         "metric": "Engram block (hash + fp8 lookup + wkv projection + gate) tokens/s",
         "value": T * K_steps / total, "unit": "tokens/s", "n_gpus": 1, "steps": K_steps,
         "ms_per_step": total / K_steps * 1e3, "higher_is_better": True, "dtype": "bf16/f32", "data": "synthetic",
-        "config": {"workload": runner.wl.name, "dim": dim, "hc_mult": hc, "wkv": [dim * (hc + 1), K]},
+        "config": {"workload": runner.wl.name, "dim": dim, "hc_mult": hc, "wkv": [dim * (hc + 1), K],
+                   "l2_fetch_granularity": (f"{args.l2_fetch} B (context default {l2_default} B)" if args.l2_fetch
+                                            else "context default")},
         "component_us": comp, "roofline": roof,
     }
     print(json.dumps(line), flush=True)

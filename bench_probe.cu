@@ -5,12 +5,14 @@
 // path. Built and run by `python bench.py --probe access|gather|layout`.
 //
 //   access  3,145,728 random reads of 4, 16, 32, 64 and 128 bytes (one kernel per size, named
-//           probe_read_<size>) into a 48 GB region; run it under ncu with dram__bytes_read.sum to
-//           see the DRAM bytes each access costs.
+//           probe_read_<size>) into a 48 GB region; then 4-byte reads with other load flavours
+//           (probe_read_flavour<.cg / .cs / relaxed>) and with the context's L2 fetch granularity
+//           limit set to 32 bytes (a per-context setting: it ends with the process). Run it under ncu
+//           with dram__bytes_read.sum to see the DRAM bytes each access costs.
 //   gather  the fused kernel's bytes without the hash: per row a random 128-B code row and a random
 //           4-B scale read, 256 B written in order; 3,145,728 rows (one full-scale launch) out of
 //           768,022,850 (both full-scale tables), several launch shapes; read-only and write-only
-//           splits.
+//           splits; then the main patterns again with the L2 fetch granularity limit at 32 bytes.
 //   layout  the same gather with the scale stored separately, not read, right after the codes
 //           (144-B and 256-B records) or in a block after every 32 rows.
 #include <cuda_runtime.h>
@@ -63,6 +65,25 @@ __global__ void probe_read(const unsigned char* __restrict__ region, const int64
   } else {
     const uint4 w = __ldg(reinterpret_cast<const uint4*>(p) + lane);
     v = w.x ^ w.y ^ w.z ^ w.w;
+  }
+  if (v == 0x9E3779B9u) sink[0] = v;  // keeps the load; practically never taken
+}
+
+// 4-byte reads at the start of a random 128-B slot with another load flavour:
+// 0 ld.global.cg (L2 only), 1 ld.global.cs (streaming), 2 ld.relaxed.gpu.global
+template <int FLAVOUR>
+__global__ void probe_read_flavour(const unsigned char* __restrict__ region, const int64_t* __restrict__ idx,
+                                   int64_t n, uint32_t* __restrict__ sink) {
+  const int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (g >= n) return;
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(region + idx[g] * 128);
+  uint32_t v;
+  if (FLAVOUR == 0) {
+    asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  } else if (FLAVOUR == 1) {
+    asm volatile("ld.global.cs.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  } else {
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
   }
   if (v == 0x9E3779B9u) sink[0] = v;  // keeps the load; practically never taken
 }
@@ -191,7 +212,7 @@ int run_access(int64_t region_bytes) {
   CK(cudaEventCreate(&e1));
   std::printf("access probe: %lld random reads per launch into %.1f GB (one 128-B slot each)\n", (long long)kN,
               slots * 128 / 1e9);
-  auto timed = [&](auto kernel, int bytes, int lanes) -> int {
+  auto timed = [&](auto kernel, const char* name, int bytes, int lanes) -> int {
     const int64_t threads = kN * lanes;
     const unsigned blocks = (unsigned)((threads + 255) / 256);
     for (int r = 0; r < 3; ++r) kernel<<<blocks, 256>>>(region, idx, kN, sink);
@@ -202,15 +223,27 @@ int run_access(int64_t region_bytes) {
     CK(cudaEventSynchronize(e1));
     float ms = 0.f;
     CK(cudaEventElapsedTime(&ms, e0, e1));
-    std::printf("probe_read_%d: %d-byte accesses, %7.1f us\n", bytes, bytes, ms * 1e3);
+    std::printf("%-28s %3d-byte accesses, %7.1f us\n", name, bytes, ms * 1e3);
     return 0;
   };
   int rc = 0;
-  rc |= timed(probe_read<4>, 4, 1);
-  rc |= timed(probe_read<16>, 16, 1);
-  rc |= timed(probe_read<32>, 32, 2);
-  rc |= timed(probe_read<64>, 64, 4);
-  rc |= timed(probe_read<128>, 128, 8);
+  rc |= timed(probe_read<4>, "probe_read<4>", 4, 1);
+  rc |= timed(probe_read<16>, "probe_read<16>", 16, 1);
+  rc |= timed(probe_read<32>, "probe_read<32>", 32, 2);
+  rc |= timed(probe_read<64>, "probe_read<64>", 64, 4);
+  rc |= timed(probe_read<128>, "probe_read<128>", 128, 8);
+  std::printf("4-byte reads with other load flavours:\n");
+  rc |= timed(probe_read_flavour<0>, "probe_read_flavour<.cg>", 4, 1);
+  rc |= timed(probe_read_flavour<1>, "probe_read_flavour<.cs>", 4, 1);
+  rc |= timed(probe_read_flavour<2>, "probe_read_flavour<relaxed>", 4, 1);
+  size_t gran = 0;
+  CK(cudaDeviceGetLimit(&gran, cudaLimitMaxL2FetchGranularity));
+  CK(cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, 32));
+  size_t now = 0;
+  CK(cudaDeviceGetLimit(&now, cudaLimitMaxL2FetchGranularity));
+  std::printf("L2 fetch granularity limit %zu -> %zu bytes for this context:\n", gran, now);
+  rc |= timed(probe_read<4>, "probe_read<4> (32-B limit)", 4, 1);
+  CK(cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, gran));
   return rc;
 }
 
@@ -249,6 +282,14 @@ int run_gather(bool layout) {
     rc |= time_gather<4, 0, 0, 1>(g, "separate scales, short CTAs", short_ctas, g.idx);
     rc |= time_gather<1, 0, 0, 1>(g, "separate scales, one row per thread group", (int)(kN / 32), g.idx);
     rc |= time_gather<4, 0, 0, 2>(g, "separate scales, 8 CTAs/SM", sms * 8, g.idx);
+    size_t gran = 0;  // the same patterns with the context's L2 fetch granularity limit at 32 bytes
+    CK(cudaDeviceGetLimit(&gran, cudaLimitMaxL2FetchGranularity));
+    CK(cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, 32));
+    std::printf("L2 fetch granularity limit %zu -> 32 bytes:\n", gran);
+    rc |= time_gather<4, 0, 0, 0>(g, "separate scales, short CTAs", short_ctas, g.idx);
+    rc |= time_gather<4, 0, 0, 4>(g, "separate scales, short CTAs", short_ctas, g.idx);
+    rc |= time_gather<4, 0, 0, 1>(g, "separate scales, short CTAs", short_ctas, g.idx);
+    CK(cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, gran));
   } else {
     for (int m = 0; m < 2; ++m) {
       if (m == 0) {

@@ -28,7 +28,7 @@ __all__ = [
     "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
     "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START",
     "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "STATUS_CHECK", "SCALE_F32", "SCALE_BF16", "SCALE_E8M0", "SCALE_E4M3",
-    "library_path",
+    "library_path", "set_l2_fetch_granularity",
 ]
 
 OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
@@ -87,6 +87,7 @@ def _lib():
         L.engram_state_layout.argtypes = [_P, ctypes.POINTER(_Layout)]
         L.engram_gate.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _I32, ctypes.c_float, _P, _P]
         L.engram_strerror.argtypes = [ctypes.c_int]
+        L.engram_set_l2_fetch_granularity.argtypes = [_I32, ctypes.POINTER(_I32)]
         L.engram_strerror.restype = ctypes.c_char_p
         for name in ("engram_state_create", "engram_state_destroy", "engram_cache_reset", "engram_state_status",
                      "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout",
@@ -194,6 +195,15 @@ def _start_tensor(start_pos, B: int, device) -> torch.Tensor:
     if isinstance(start_pos, torch.Tensor):
         return start_pos
     return torch.full((B,), int(start_pos), dtype=torch.int32, device=device)
+
+
+def set_l2_fetch_granularity(nbytes: int) -> int:
+    """Set the current device context's L2 fetch granularity limit (0, 32, 64 or 128 bytes; a hint)
+    and return the previous value. Process-wide and not stream-ordered: call it at set-up. At 32 a
+    random 4-byte scale read costs one 32-byte DRAM sector instead of a 128-byte line."""
+    prev = _I32(0)
+    _check(_lib().engram_set_l2_fetch_granularity(int(nbytes), ctypes.byref(prev)), "engram_set_l2_fetch_granularity")
+    return prev.value
 
 
 def _size(t, n: int, name: str) -> None:

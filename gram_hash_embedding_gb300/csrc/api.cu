@@ -337,6 +337,18 @@ int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight,
   return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
 }
 
+int engram_set_l2_fetch_granularity(int32_t bytes, int32_t* previous) {
+  if (bytes != 0 && bytes != 32 && bytes != 64 && bytes != 128) return ENGRAM_ERR_INVALID;
+  size_t old = 0;
+  if (cudaDeviceGetLimit(&old, cudaLimitMaxL2FetchGranularity) != cudaSuccess ||
+      cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, (size_t)bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return ENGRAM_ERR_CUDA;
+  }
+  if (previous != nullptr) *previous = (int32_t)old;
+  return ENGRAM_OK;
+}
+
 int engram_state_layout(const engram_state* state, engram_layout* layout) {
   if (state == nullptr || layout == nullptr) return ENGRAM_ERR_INVALID;
   *layout = state->lay;

@@ -217,6 +217,18 @@ int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight,
                 const uint8_t* mask, int64_t T, int32_t hc, int32_t dim, float eps, uint16_t* out,
                 engram_stream_t stream);
 
+/*
+ * Set the L2 fetch granularity limit of the current device's context (cudaLimitMaxL2FetchGranularity:
+ * the most bytes L2 fetches from DRAM for one missed sector, a hint; 0, 32, 64 or 128) and return the
+ * previous value in *previous (may be NULL). Process-wide for that context and not stream-ordered:
+ * call it while none of the process's kernels run, e.g. at set-up; it lasts until the context ends.
+ * The library never calls it on its own. At the default (64 on GB300) every random read of up to 128
+ * bytes fetches a whole 128-byte line, so a row's 4-byte fp32 scale costs as much DRAM traffic as its
+ * 128 bytes of codes; at 32 it costs one 32-byte sector (the full-scale gather then moves ~19% fewer
+ * DRAM bytes). Errors: _INVALID (another value), _CUDA.
+ */
+int engram_set_l2_fetch_granularity(int32_t bytes, int32_t* previous);
+
 /* Layout the state was created with (host copy). */
 int engram_state_layout(const engram_state* state, engram_layout* layout);
 

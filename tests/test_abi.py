@@ -79,6 +79,9 @@ def test_host_side_checks_need_no_gpu(lib):
     assert L.engram_lookup(base + 4, 5, base, base, 4, 128, 128, geng.SCALE_E8M0, base, None) == geng.ERR_INVALID
     assert L.engram_lookup(base, 5, base + 8, base, 4, 128, 128, geng.SCALE_E4M3, base, None) == geng.ERR_INVALID
     assert lib.engram_state_destroy(None) == 0
+    lib.engram_set_l2_fetch_granularity.argtypes = [ctypes.c_int32, ctypes.c_void_p]
+    for bad in (7, -32, 256):  # refused before the CUDA runtime is called
+        assert lib.engram_set_l2_fetch_granularity(bad, None) == geng.ERR_INVALID
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

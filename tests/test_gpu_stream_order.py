@@ -99,3 +99,25 @@ def test_gate_consumes_its_own_output():
         geng.engram_gate(y, kv, qw, kw, out=y)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+
+
+def test_l2_fetch_granularity_changes_no_result(tiny):
+    """The context's L2 fetch granularity limit is a cache policy: hash ids and rows are the same
+    at 32 bytes as at the context default, and the previous value comes back for the restore."""
+    wl, Ws, Ss = tiny
+    lay = wl.layout
+    ids = H.to_dev(np.random.default_rng(94).integers(0, lay.raw_vocab, size=(2, 64)))
+    st_a, st_b = H.make_state(wl, 2, 64), H.make_state(wl, 2, 64)
+    ref = st_a.hash_lookup(ids, Ws, Ss)
+    default = geng.set_l2_fetch_granularity(32)
+    try:
+        assert default in (0, 32, 64, 128)
+        got = st_b.hash_lookup(ids, Ws, Ss)
+        torch.cuda.synchronize()
+        for r, g in zip(ref, got):
+            assert torch.equal(r.view(torch.int16), g.view(torch.int16))
+        assert geng.set_l2_fetch_granularity(default) == 32
+    finally:
+        geng.set_l2_fetch_granularity(default)
+    with pytest.raises(geng.EngramError):
+        geng.set_l2_fetch_granularity(48)
