@@ -39,7 +39,7 @@ struct CallArgs {
   const int32_t* cache_rows;  // [B] cache row of each call row; null: row b uses cache row b
   int64_t* hashes;            // may be null (fused)
   const int32_t* cu_seqlens;  // packed calls: [B+1] sequence extents in ids; null for dense [B, L] calls
-  int64_t L;                  // dense: tokens per row; packed: the longest sequence (grid bound)
+  int64_t L;                  // dense: tokens per row; packed: max_len (a longer sequence is skipped)
   int64_t total;              // packed: tokens in ids (T); dense: B * L
   int32_t B;
   int32_t head_dim, block;

@@ -368,8 +368,68 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
 }
 
 // ------------------------------------------------------------------------------------------------
+// packed calls: which tile of which sequence a CTA takes
+
+__device__ __forceinline__ int64_t floor_div(int64_t x, int64_t d) {
+  const int64_t q = x / d;
+  return (x % d != 0 && x < 0) ? q - 1 : q;
+}
+
+// An extent the kernels can run: inside [0, T] and at most max_len (a.L) tokens long.
+__device__ __forceinline__ bool extent_ok(const CallArgs& a, int64_t start, int64_t end) {
+  return start >= 0 && end <= a.total && end >= start && end - start <= a.L;
+}
+
+// CTA k of a packed launch (a 1-D grid of floor(T / tile) + B CTAs) takes tile j = k - Q(b) of the
+// last sequence b with Q(b) <= k, where Q(b) = floor(cu_seqlens[b] / tile) + b. For non-decreasing
+// cu_seqlens, Q increases strictly and Q(b+1) - Q(b) >= floor(L_b / tile) + 1 >= ceil(L_b / tile), so
+// every tile of every sequence gets its own CTA and at most one CTA per sequence finds no tokens (a
+// grid sized by the longest sequence left most CTAs of a decode-heavy batch empty). The search samples
+// Q at up to blockDim.x points per round: one round up to blockDim.x sequences, two up to its square.
+// CTA k < B also checks the extent of sequence k and raises ENGRAM_STATUS_BAD_LENGTH if it is
+// inconsistent, so every such sequence is flagged whether or not a CTA lands on it. Called by all
+// threads of the CTA; the result is the same in every thread. False: nothing to do.
+__device__ bool packed_tile(const StateView& sv, const CallArgs& a, const int tile, int& b, int64_t& seq_off,
+                            int64_t& Lb, int64_t& t0) {
+  __shared__ int32_t cu_s[kThreads];  // the last round's samples: the extents of the candidates
+  const int64_t k = blockIdx.x;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int32_t* cu = a.cu_seqlens;
+  if (tid == 0 && k < a.B && !extent_ok(a, cu[k], cu[k + 1])) atomicOr(sv.status, ENGRAM_STATUS_BAD_LENGTH);
+  int64_t lo = 0, n = a.B, end;  // candidates lo .. lo + n - 1 (lo + n <= B throughout)
+  for (;;) {
+    const int64_t step = (n + nthr - 1) / nthr;
+    bool le = false;
+    if (tid * step < n) {
+      const int64_t i = lo + tid * step;
+      const int32_t v = cu[i];
+      le = floor_div(v, tile) + i <= k;
+      if (step == 1) cu_s[tid] = v;
+    } else if (step == 1 && tid == n) {
+      cu_s[tid] = cu[lo + n];  // the end of the last candidate
+    }
+    const int c = __syncthreads_count(le);  // the samples with Q <= k are a prefix when Q increases
+    if (c == 0) return false;
+    if (step == 1) {  // every candidate was sampled: b is the last one with Q <= k
+      b = (int)(lo + c - 1);
+      seq_off = cu_s[c - 1];
+      end = c < nthr ? cu_s[c] : cu[b + 1];
+      break;
+    }
+    lo += (int64_t)(c - 1) * step;
+    n = min(step, n - (int64_t)(c - 1) * step);
+  }
+  if (!extent_ok(a, seq_off, end)) return false;  // flagged by CTA b
+  Lb = end - seq_off;
+  const int64_t j = k - (floor_div(seq_off, tile) + b);
+  t0 = j * tile;
+  return j >= 0 && t0 < Lb;
+}
+
+// ------------------------------------------------------------------------------------------------
 // fused kernel: hash a tile, then (GATHER) stream its rows through registers.
-// grid = (ceil(L / tile), B); one CTA = `tile` consecutive tokens of sequence b.
+// Dense calls: grid = (ceil(L / tile), B), one CTA = `tile` consecutive tokens of sequence b. Packed
+// calls: a 1-D grid of floor(T / tile) + B CTAs mapped to (sequence, tile) pairs by packed_tile.
 // D = head_dim (compile time); G = D / 16 lanes per output row. Unused when GATHER is false.
 template <bool GATHER, int D, bool ONE, int SDT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateView sv, const CallArgs a, const int tile) {
@@ -378,30 +438,24 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
   const int NL = sv.n_layers, C = sv.n_cols;
   const SmemPlan plan = smem_plan(NL, sv.max_ngram, C, tile, GATHER);
   // dense calls: every CTA has tokens, so it stages the state's constants while the previous kernel
-  // drains; packed calls learn their extents first (CTAs past a sequence's end exit at once)
+  // drains; packed calls learn their extents first (CTAs without tokens exit at once)
   const bool dense = a.cu_seqlens == nullptr;
   if (dense) stage_constants(sv, smem, plan);
   pdl_wait();
   pdl_trigger();
   const int64_t* rowidx_s = reinterpret_cast<const int64_t*>(smem + plan.rowidx_off);
   const int tid = threadIdx.x;
-  const int b = blockIdx.y;
-  // sequence b: dense calls hold L tokens per row; packed calls read its extent from cu_seqlens
-  int64_t seq_off, Lb;
+  int b;
+  int64_t seq_off, Lb, t0;
   if (a.cu_seqlens != nullptr) {
-    seq_off = a.cu_seqlens[b];
-    const int64_t end = a.cu_seqlens[b + 1];
-    Lb = end - seq_off;
-    if (seq_off < 0 || end > a.total || Lb < 0 || Lb > a.L) {  // inconsistent extent: nothing is done
-      if (blockIdx.x == 0 && tid == 0) atomicOr(sv.status, ENGRAM_STATUS_BAD_LENGTH);
-      return;
-    }
+    if (!packed_tile(sv, a, tile, b, seq_off, Lb, t0)) return;
   } else {
+    b = blockIdx.y;
     seq_off = (int64_t)b * a.L;
     Lb = a.L;
+    t0 = (int64_t)blockIdx.x * tile;
   }
-  const int64_t t0 = (int64_t)blockIdx.x * tile;
-  if (t0 >= Lb) return;  // past this sequence's end (packed calls size the grid for the longest)
+  if (t0 >= Lb) return;
   const int ntok = (int)min((int64_t)tile, Lb - t0);
   if (tid == 0) flags_s = 0u;
   __syncthreads();
@@ -508,7 +562,8 @@ cudaError_t launch_hash_k(const StateView& sv, const CallArgs& a, int tile, cuda
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plan.bytes);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid((unsigned)((a.L + tile - 1) / tile), (unsigned)a.B);
+  const dim3 grid = a.cu_seqlens != nullptr ? dim3((unsigned)(a.total / tile + a.B))
+                                             : dim3((unsigned)((a.L + tile - 1) / tile), (unsigned)a.B);
   return launch_pdl(kern, grid, dim3(GATHER ? kThreads : kHashThreads), plan.bytes, s, sv, a, tile);
 }
 

@@ -178,12 +178,17 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
  *   cu_seqlens  device int32 [B+1], non-decreasing, cu_seqlens[0] = 0 and cu_seqlens[B] = T expected
  *   start_pos   device int32 [B]
  *   cache_rows  device int32 [B] or NULL: the cache row of sequence b, as in engram_hash
- *   max_len     host: an upper bound on every sequence's length (sizes the grid; max_len <= max_seq_len and <= 2^32)
+ *   max_len     host: an upper bound on every sequence's length (a longer one is skipped and flagged;
+ *               max_len <= max_seq_len)
  *   hashes      device int64 [T][n_layers][C]
  * A sequence whose extent is inconsistent is skipped and flagged (ENGRAM_STATUS_BAD_LENGTH); a start
- * position that does not fit is handled as in engram_hash. Extents must not overlap (tokens shared by
- * two sequences would be written twice). B == 0, T == 0 or max_len == 0 is a no-op.
- * Errors: _INVALID (null, misaligned, negative sizes), _RANGE (B > max_batch, max_len > max_seq_len).
+ * position that does not fit is handled as in engram_hash. Where cu_seqlens decreases, the sequence at
+ * the decrease is flagged and skipped and which other sequences are processed is unspecified. Extents
+ * must not overlap (tokens shared by two sequences would be written twice). B == 0, T == 0 or
+ * max_len == 0 is a no-op. The launch has floor(T / tile) + B CTAs (tile: 4 to 64 tokens), each
+ * taking one tile of one sequence, so its cost follows T, not B x max_len.
+ * Errors: _INVALID (null, misaligned, negative sizes), _RANGE (B > max_batch, max_len > max_seq_len),
+ * _UNSUPPORTED (T > 2^31 - 1, or T / 4 + B > 2^31 - 1).
  */
 int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
                        const int32_t* start_pos, const int32_t* cache_rows, int32_t B, int64_t T, int64_t max_len,

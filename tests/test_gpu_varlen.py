@@ -118,3 +118,47 @@ def test_prepared_call_matches_the_plain_call():
         torch.cuda.synchronize()
         assert (ha >= 0).all() and a.status() == 0 and b.status() == 0
         assert torch.equal(ha, hb) and torch.equal(out_a[0].view(torch.int16), out_b[0].view(torch.int16))
+
+
+def test_many_short_sequences_after_unused_tokens():
+    """700 packed sequences, more than a CTA has threads, so the search that maps a CTA to its sequence
+    and tile takes two rounds in both kernels; most are 0-2 tokens long, their cache rows permuted, and
+    the packed tokens start after 3 unused ones and end 2 before T. Every sequence's hash ids and rows
+    equal the oracle's; the unused tokens' outputs are not written."""
+    wl = synth.make_workload(0, full64=True)
+    lay = wl.layout
+    B, lead, trail = 700, 3, 2
+    rng = np.random.default_rng(700)
+    lens = rng.choice([0, 1, 1, 1, 2, 5, 9, 33], size=B)
+    starts = rng.integers(0, 60, size=B).astype(np.int32)
+    rows_map = rng.permutation(B).astype(np.int32)
+    cu = (lead + np.concatenate([[0], np.cumsum(lens)])).astype(np.int32)
+    T = int(cu[-1]) + trail
+    ids = rng.integers(0, lay.raw_vocab, size=T)
+    mask = rng.random(T) > 0.1
+    hist = rng.integers(0, lay.raw_vocab, size=(B, 60))
+    states = []
+    for _ in range(2):  # one for the fused call, one for the hash-only call, with the same history
+        st = H.make_state(wl, B, 128)
+        st.hash(H.to_dev(hist), 0)
+        states.append(st)
+    orc = H.make_oracle(wl, B, 128)
+    orc.hash(hist, 0)
+    Ws, Ss = H.device_tables(wl)
+    d_ids, d_cu, d_st, d_mask, d_map = (H.to_dev(x) for x in (ids, cu, starts, mask, rows_map))
+    hashes = torch.full((T, 1, 6), -9, dtype=torch.int64, device="cuda")
+    out = [torch.full((T, 6, lay.head_dim), -7.0, dtype=torch.bfloat16, device="cuda")]
+    states[0].hash_lookup_varlen(d_ids, d_cu, d_st, Ws, Ss, mask=d_mask, out=out, hashes=hashes, max_len=33,
+                                 cache_rows=d_map)
+    h2 = torch.full((T, 1, 6), -9, dtype=torch.int64, device="cuda")
+    states[1].hash_varlen(d_ids, d_cu, d_st, mask=d_mask, hashes=h2, max_len=33, cache_rows=d_map)
+    exp_h, fl = orc.hash_varlen(ids, cu, starts, mask, cache_rows=rows_map)
+    assert fl == 0 and states[0].status() == 0 and states[1].status() == 0
+    seq = slice(lead, T - trail)
+    H.assert_bits_equal(hashes.cpu().numpy()[seq], exp_h[seq], "packed hashes")
+    H.assert_bits_equal(h2.cpu().numpy()[seq], exp_h[seq], "packed hash-only")
+    H.assert_bits_equal(H.bf16_bits(out[0])[seq], H.oracle_lookup_rows(wl, 0, exp_h[seq, 0, :]), "packed rows")
+    for h in (hashes, h2):
+        assert (h[:lead] == -9).all() and (h[T - trail:] == -9).all()
+    unused = torch.cat([out[0][:lead], out[0][T - trail:]])
+    assert (unused == -7.0).all()
