@@ -288,9 +288,9 @@ int packed_call(const engram_state* st, const int64_t* ids, const uint8_t* mask,
   if (hashes != nullptr && !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
   if (cache_rows != nullptr && !aligned(cache_rows, 4)) return ENGRAM_ERR_INVALID;
   if (B > st->lay.max_batch || max_len > st->lay.max_seq_len) return ENGRAM_ERR_RANGE;
-  if (T > ((int64_t)1 << 31) - 1) return ENGRAM_ERR_UNSUPPORTED;  // int32 extents
-  // the packed grid has floor(T / tile) + B CTAs with tiles of >= 4 tokens: inside CUDA's 2^31 - 1
-  if (T / 4 + B > ((int64_t)1 << 31) - 1) return ENGRAM_ERR_UNSUPPORTED;
+  // int32 extents; the packed grid then has floor(T / tile) + B < 2^29 + 2^16 CTAs (tiles of >= 4
+  // tokens, B <= max_batch <= 65,535), inside CUDA's 2^31 - 1
+  if (T > ((int64_t)1 << 31) - 1) return ENGRAM_ERR_UNSUPPORTED;
   if (!on_state_device(st)) return ENGRAM_ERR_INVALID;
   *a = call_args(st, ids, mask, start_pos, cache_rows, B, max_len, hashes);
   a->cu_seqlens = cu_seqlens;

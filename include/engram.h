@@ -188,7 +188,7 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
  * max_len == 0 is a no-op. The launch has floor(T / tile) + B CTAs (tile: 4 to 64 tokens), each
  * taking one tile of one sequence, so its cost follows T, not B x max_len.
  * Errors: _INVALID (null, misaligned, negative sizes), _RANGE (B > max_batch, max_len > max_seq_len),
- * _UNSUPPORTED (T > 2^31 - 1, or T / 4 + B > 2^31 - 1).
+ * _UNSUPPORTED (T > 2^31 - 1).
  */
 int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* cu_seqlens,
                        const int32_t* start_pos, const int32_t* cache_rows, int32_t B, int64_t T, int64_t max_len,
