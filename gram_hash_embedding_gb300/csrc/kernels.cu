@@ -16,11 +16,11 @@
 // sectors: lane q of a row's D/16-lane group converts codes [8q, 8q+8) and [D/2+8q, D/2+8q+8) and
 // writes 16 bytes into each half of the output row.
 //
-// On this GPU every random read of 4 to 128 bytes costs one 128-byte DRAM access, so a row
-// (128 B of codes) and its 4-byte scale cost two; with the 256-byte bf16 write that is 512 DRAM
-// bytes per row for 388 algorithmic bytes. A variant that landed rows and scales in shared memory
-// with bulk copies (TMA engine) and per-warp mbarrier pipelines was built and measured slower at
-// every shape tried (its shared-memory slots cap the SM at ~1000 rows in flight and leave 8-16
+// DRAM per row: 128 B of codes, the sector holding its scale (32 B with the context's L2 fetch
+// limit at 32 B, engram_set_l2_fetch_granularity; a 128-B line at the 64-B default) and the 256-B
+// bf16 write: 416 (512) DRAM bytes for 388 algorithmic bytes. A variant that landed rows and scales
+// in shared memory with bulk copies (TMA engine) and per-warp mbarrier pipelines was measured slower
+// at every shape tried (its shared-memory slots cap the SM at ~1000 rows in flight and leave 8-16
 // warps to convert), so the register path is the one kept.
 #include <cstdint>
 
