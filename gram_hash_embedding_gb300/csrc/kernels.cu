@@ -46,10 +46,10 @@ namespace {
 #define ENGRAM_TARGET_CTAS 1216
 #endif
 #ifndef ENGRAM_HASH_TILE
-#define ENGRAM_HASH_TILE 64
+#define ENGRAM_HASH_TILE 32
 #endif
 #ifndef ENGRAM_HASH_THREADS
-#define ENGRAM_HASH_THREADS 128
+#define ENGRAM_HASH_THREADS 96
 #endif
 
 constexpr int kThreads = ENGRAM_THREADS;           // threads per CTA, fused and lookup kernels
@@ -61,7 +61,8 @@ constexpr int kFusedTile = ENGRAM_FUSED_TILE;      // largest tile (tokens per C
 constexpr int kMinFusedTile = 4;                   // below 4 tokens the halo and hash phase dominate
 constexpr int kTargetCtas = ENGRAM_TARGET_CTAS;    // fused grid size the tile choice aims for (2 waves)
 constexpr int kHashTile = ENGRAM_HASH_TILE;        // tokens per CTA, hash-only kernel
-constexpr int kHashThreads = ENGRAM_HASH_THREADS;  // threads per CTA, hash-only kernel (<= kThreads)
+constexpr int kHashThreads = ENGRAM_HASH_THREADS;  // threads per CTA, hash-only kernel (<= kThreads); 96 keeps
+                                                   // every thread busy in step 3 at 48 columns (2 tokens a pass)
 
 // Checked builds (-DENGRAM_CHECKED=1, a debugging aid in place of a memory checker): the hash and
 // fused kernels test every global access against the call's sizes before making it; an access
