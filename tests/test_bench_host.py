@@ -25,7 +25,9 @@ def test_traffic_record_matches_the_kernel_sources():
     # the committed ncu record is only used for the kernel it was taken on
     t = bench.recorded_traffic(3)
     assert t is None or 1.2e9 < t < 2.0e9
-    assert bench.recorded_traffic(1) is None
+    t32 = bench.recorded_traffic(3, 32)  # the record is taken at bench.py's default 32-B fetch limit
+    assert t32 is None or 1.2e9 < t32 < 1.4e9
+    assert bench.recorded_traffic(1) is None and bench.recorded_traffic(1, 32) is None
 
 
 def test_clock_summary_parses_nvidia_smi_lines():
