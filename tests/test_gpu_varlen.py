@@ -162,3 +162,21 @@ def test_many_short_sequences_after_unused_tokens():
         assert (h[:lead] == -9).all() and (h[T - trail:] == -9).all()
     unused = torch.cat([out[0][:lead], out[0][T - trail:]])
     assert (unused == -7.0).all()
+
+
+def test_decreasing_extents_are_flagged():
+    """Where cu_seqlens decreases, the sequence at the decrease is flagged; which other sequences run
+    is unspecified, but every read stays inside cu_seqlens (checked on the host before this test was
+    first run) and both packed kernels return normally."""
+    wl = synth.make_workload(0)
+    Ws, Ss = H.device_tables(wl)
+    ids = torch.arange(10, dtype=torch.int64, device="cuda")
+    starts = torch.zeros(3, dtype=torch.int32, device="cuda")
+    for cu_list in ([0, 8, 3, 10], [5, 2, 9, 10]):
+        st = H.make_state(wl, 3, 64)
+        cu = torch.tensor(cu_list, dtype=torch.int32, device="cuda")
+        hashes = torch.full((10, 1, 6), -9, dtype=torch.int64, device="cuda")
+        st.hash_lookup_varlen(ids, cu, starts, Ws, Ss, hashes=hashes, max_len=10)
+        st.hash_varlen(ids, cu, starts, hashes=hashes, max_len=10)
+        torch.cuda.synchronize()
+        assert st.status() & geng.STATUS_BAD_LENGTH
