@@ -166,8 +166,8 @@ def test_many_short_sequences_after_unused_tokens():
 
 def test_decreasing_extents_are_flagged():
     """Where cu_seqlens decreases, the sequence at the decrease is flagged; which other sequences run
-    is unspecified, but every read stays inside cu_seqlens (checked on the host before this test was
-    first run) and both packed kernels return normally."""
+    is unspecified, but the kernels read cu_seqlens only at indices 0..B (the search picks indices,
+    never follows values) and both packed kernels return normally."""
     wl = synth.make_workload(0)
     Ws, Ss = H.device_tables(wl)
     ids = torch.arange(10, dtype=torch.int64, device="cuda")
