@@ -65,7 +65,7 @@ def _rows_equal(got, exp, what):
     H.assert_bits_equal(np.where(nan_e, 0, got), np.where(nan_e, 0, exp), what)
 
 
-@pytest.mark.parametrize("seed", range(48))
+@pytest.mark.parametrize("seed", range(200))
 def test_random_case(seed):
     rng, lay = _random_case(seed)
     Ws, Ss = _tables(rng, lay)

@@ -180,3 +180,37 @@ def test_decreasing_extents_are_flagged():
         st.hash_varlen(ids, cu, starts, hashes=hashes, max_len=10)
         torch.cuda.synchronize()
         assert st.status() & geng.STATUS_BAD_LENGTH
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_packed_batches_of_many_sequences(seed):
+    """90 to 1,200 packed sequences of 0 to 64 tokens (one or two search rounds in the fused kernel's
+    256-thread CTAs, two in the hash-only kernel's 96-thread CTAs), unused tokens around them, cache
+    rows permuted: hash ids and rows equal the oracle's."""
+    wl = synth.make_workload(0, full64=True)
+    lay = wl.layout
+    rng = np.random.default_rng(9000 + seed)
+    B = int(rng.integers(90, 1200))
+    lens = rng.choice([0, 1, 1, 2, 3, 7, 16, 31, 64], size=B)
+    starts = rng.integers(0, 40, size=B).astype(np.int32)
+    rows_map = rng.permutation(B).astype(np.int32)
+    cu = (int(rng.integers(0, 5)) + np.concatenate([[0], np.cumsum(lens)])).astype(np.int32)
+    T = int(cu[-1]) + int(rng.integers(0, 5))
+    ids = rng.integers(0, lay.raw_vocab, size=T)
+    mask = rng.random(T) > 0.1
+    hist = rng.integers(0, lay.raw_vocab, size=(B, 40))
+    st, st2, orc = H.make_state(wl, B, 128), H.make_state(wl, B, 128), H.make_oracle(wl, B, 128)
+    st.hash(H.to_dev(hist), 0)
+    st2.hash(H.to_dev(hist), 0)
+    orc.hash(hist, 0)
+    Ws, Ss = H.device_tables(wl)
+    d_ids, d_cu, d_st, d_mask, d_map = (H.to_dev(x) for x in (ids, cu, starts, mask, rows_map))
+    hashes = torch.full((T, 1, 6), -9, dtype=torch.int64, device="cuda")
+    outs = st.hash_lookup_varlen(d_ids, d_cu, d_st, Ws, Ss, mask=d_mask, hashes=hashes, max_len=64, cache_rows=d_map)
+    h2 = st2.hash_varlen(d_ids, d_cu, d_st, mask=d_mask, max_len=64, cache_rows=d_map)
+    exp_h, fl = orc.hash_varlen(ids, cu, starts, mask, cache_rows=rows_map)
+    assert fl == 0 and st.status() == 0 and st2.status() == 0
+    seq = slice(int(cu[0]), int(cu[-1]))
+    H.assert_bits_equal(hashes.cpu().numpy()[seq], exp_h[seq], "packed hashes")
+    H.assert_bits_equal(h2.cpu().numpy()[seq], exp_h[seq], "packed hash-only")
+    H.assert_bits_equal(H.bf16_bits(outs[0])[seq], H.oracle_lookup_rows(wl, 0, exp_h[seq, 0, :]), "packed rows")
