@@ -69,10 +69,11 @@ def parse_args(argv=None):
                    help="the context's L2 fetch granularity limit for the run (bytes; 0 leaves the context "
                         "default, 64 on GB300). At 32 a row's random 4-byte scale read costs a 32-byte DRAM "
                         "sector instead of a 128-byte line (engram_set_l2_fetch_granularity)")
-    p.add_argument("--probe", choices=["access", "gather", "layout"],
+    p.add_argument("--probe", choices=["access", "gather", "layout", "depth"],
                    help="run a DRAM measurement probe (bench_probe.cu) instead of the benchmark: access = DRAM "
                         "bytes per random read size (under ncu), gather = the fused kernel's byte pattern without "
-                        "the hash, layout = scale placement next to the codes")
+                        "the hash, layout = scale placement next to the codes, depth = rows in flight in "
+                        "registers vs landed in shared memory by cp.async")
     return p.parse_args(argv)
 
 

@@ -2,7 +2,7 @@
 // this GPU, how fast the fused kernel's byte pattern can move at all, and whether placing a row's
 // fp32 scale next to its fp8 codes would change that. Timing and counting only: the regions are
 // uninitialised device memory, the outputs are meaningless, and nothing here is on the product
-// path. Built and run by `python bench.py --probe access|gather|layout`.
+// path. Built and run by `python bench.py --probe access|gather|layout|depth`.
 //
 //   access  3,145,728 random reads of 4, 16, 32, 64 and 128 bytes (one kernel per size, named
 //           probe_read_<size>) into a 48 GB region; then 4-byte reads with other load flavours
@@ -15,6 +15,8 @@
 //           splits; then the main patterns again with the L2 fetch granularity limit at 32 bytes.
 //   layout  the same gather with the scale stored separately, not read, right after the codes
 //           (144-B and 256-B records) or in a block after every 32 rows.
+//   depth   the gather (read + write, separate scales) with 2 to 8 rows in flight per 8-lane group in
+//           registers, and 4 to 16 rows landed in shared memory by cp.async, at the 32-B fetch limit.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -197,6 +199,73 @@ int time_gather(const Gather& g, const char* what, int blocks, int64_t* const* i
   return 0;
 }
 
+// The separate-scales gather (read + write) with its row loads landed in shared memory by
+// cp.async instead of registers, so a thread keeps U rows in flight without holding them: lane q of a
+// row's 8-lane group copies codes [16q, 16q+16) and lane 0 the row's 4-byte scale, then every lane
+// waits for its own copies, the warp synchronises (the scale is another lane's copy), and the lane
+// writes its two 16-byte pieces of the 256-B output row. Shared memory per CTA: U x 4,224 bytes.
+template <int U>
+__global__ void __launch_bounds__(256) probe_gather_async(const unsigned char* __restrict__ base,
+                                                          const float* __restrict__ sbase,
+                                                          const int64_t* __restrict__ idx, uint4* __restrict__ out,
+                                                          int64_t n_rows) {
+  extern __shared__ __align__(16) unsigned char sm[];
+  uint4* codes_s = reinterpret_cast<uint4*>(sm);                   // [U][256]
+  float* scales_s = reinterpret_cast<float*>(sm + U * 256 * 16);   // [U][32]
+  const int lane8 = threadIdx.x & 7, grp = threadIdx.x >> 3;
+  const int64_t groups = (int64_t)gridDim.x * 32;
+  const int64_t g0 = blockIdx.x * 32LL + grp;
+  for (int64_t b0 = g0; b0 < n_rows; b0 += groups * U) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = b0 + (int64_t)u * groups;
+      if (row < n_rows) {
+        const int64_t k = __ldg(idx + row);
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(codes_s + u * 256 + threadIdx.x);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(base + k * 128 + lane8 * 16)
+                     : "memory");
+        if (lane8 == 0) {
+          const uint32_t sdst = (uint32_t)__cvta_generic_to_shared(scales_s + u * 32 + grp);
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sdst), "l"(sbase + k) : "memory");
+        }
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = b0 + (int64_t)u * groups;
+      if (row >= n_rows) continue;
+      const uint4 v = codes_s[u * 256 + threadIdx.x];
+      const uint32_t sb = __float_as_uint(scales_s[u * 32 + grp]);
+      uint4* o = out + row * 16;
+      o[lane8] = make_uint4(v.x ^ sb, v.y, v.z, v.w);
+      o[8 + lane8] = make_uint4(v.x, v.y ^ sb, v.z, v.w);
+    }
+    __syncwarp();  // the next pass overwrites this warp's slots
+  }
+}
+
+template <int U>
+int time_gather_async(const Gather& g, const char* what, int blocks, int64_t* const* idx) {
+  const int reps = 200;
+  const int smem = U * 4224;
+  CK(cudaFuncSetAttribute(probe_gather_async<U>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  for (int w = 0; w < 3; ++w) probe_gather_async<U><<<blocks, 256, smem>>>(g.base, g.sbase, idx[w & 3], g.out, kN);
+  CK(cudaGetLastError());
+  CK(cudaDeviceSynchronize());
+  CK(cudaEventRecord(g.e0));
+  for (int i = 0; i < reps; ++i) probe_gather_async<U><<<blocks, 256, smem>>>(g.base, g.sbase, idx[i & 3], g.out, kN);
+  CK(cudaEventRecord(g.e1));
+  CK(cudaEventSynchronize(g.e1));
+  float ms = 0.f;
+  CK(cudaEventElapsedTime(&ms, g.e0, g.e1));
+  std::printf("%-44s %-10s grid %6d x 256, %d rows/thread-group pass: %7.1f us per launch\n", what, "read+write",
+              blocks, U, ms * 1e3 / reps);
+  return 0;
+}
+
 int run_access(int64_t region_bytes) {
   const int64_t slots = region_bytes / 128;
   unsigned char* region;
@@ -247,7 +316,7 @@ int run_access(int64_t region_bytes) {
   return rc;
 }
 
-int run_gather(bool layout) {
+int run_gather(int mode) {  // 0 gather, 1 layout, 2 depth
   const int64_t region = kRowsFull * 144;  // 110.6 GB: room for every layout
   Gather g;
   unsigned char* base;
@@ -271,7 +340,20 @@ int run_gather(bool layout) {
   int rc = 0;
   std::printf("gather probe: %lld random rows per launch out of %lld (128-B codes + 4-B scale read, 256 B written)\n",
               (long long)kN, (long long)kRowsFull);
-  if (!layout) {
+  if (mode == 2) {  // rows in flight: registers vs shared memory, at the 32-B fetch limit
+    size_t gran = 0;
+    CK(cudaDeviceGetLimit(&gran, cudaLimitMaxL2FetchGranularity));
+    CK(cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, 32));
+    std::printf("L2 fetch granularity limit %zu -> 32 bytes:\n", gran);
+    rc |= time_gather<2, 0, 0, 0>(g, "registers, short CTAs", (int)(kN / 64), g.idx);
+    rc |= time_gather<4, 0, 0, 0>(g, "registers, short CTAs", short_ctas, g.idx);
+    rc |= time_gather<8, 0, 0, 0>(g, "registers, short CTAs", (int)(kN / 256), g.idx);
+    rc |= time_gather_async<4>(g, "cp.async to shared memory, short CTAs", short_ctas, g.idx);
+    rc |= time_gather_async<8>(g, "cp.async to shared memory, short CTAs", (int)(kN / 256), g.idx);
+    rc |= time_gather_async<16>(g, "cp.async to shared memory, short CTAs", (int)(kN / 512), g.idx);
+    rc |= time_gather_async<8>(g, "cp.async to shared memory, 6 CTAs/SM", sms * 6, g.idx);
+    CK(cudaDeviceSetLimit(cudaLimitMaxL2FetchGranularity, gran));
+  } else if (mode == 0) {
     rc |= time_gather<4, 0, 0, 0>(g, "separate scales, short CTAs", short_ctas, g.idx);
     rc |= time_gather<4, 0, 0, 3>(g, "separate scales, short CTAs", short_ctas, g.idx);
     rc |= time_gather<4, 0, 0, 4>(g, "separate scales, short CTAs", short_ctas, g.idx);
@@ -313,8 +395,9 @@ int run_gather(bool layout) {
 }  // namespace
 
 int main(int argc, char** argv) {
-  if (argc != 2 || (std::strcmp(argv[1], "access") && std::strcmp(argv[1], "gather") && std::strcmp(argv[1], "layout"))) {
-    std::printf("usage: %s access|gather|layout\n", argv[0]);
+  if (argc != 2 || (std::strcmp(argv[1], "access") && std::strcmp(argv[1], "gather") && std::strcmp(argv[1], "layout") &&
+                    std::strcmp(argv[1], "depth"))) {
+    std::printf("usage: %s access|gather|layout|depth\n", argv[0]);
     return 2;
   }
   size_t free_b = 0, total_b = 0;
@@ -325,5 +408,6 @@ int main(int argc, char** argv) {
     std::printf("probe needs %.1f GB of free device memory, %.1f GB free\n", need / 1e9, free_b / 1e9);
     return 3;
   }
-  return access ? run_access((int64_t)48e9) : run_gather(!std::strcmp(argv[1], "layout"));
+  if (access) return run_access((int64_t)48e9);
+  return run_gather(!std::strcmp(argv[1], "layout") ? 1 : (!std::strcmp(argv[1], "depth") ? 2 : 0));
 }
