@@ -151,3 +151,32 @@ def test_prepared_call_with_a_map(tiny):
     exp_h, _ = orc.hash(ids.cpu().numpy(), L, cache_rows=[2, 0, 1])
     H.assert_bits_equal(hashes.cpu().numpy(), exp_h, "prepared with map, second chunk")
     H.assert_bits_equal(H.bf16_bits(out[0]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]), "prepared rows")
+
+
+def test_a_reused_row_needs_no_reset(tiny):
+    """Continuous batching reuses a finished sequence's cache row for a new sequence starting at
+    position 0: the new sequence reads only positions it writes itself, so its hash ids equal those
+    of the same sequence on a fresh state, while another sequence decodes in the next row."""
+    wl, Ws, Ss = tiny
+    lay = wl.layout
+    rng = np.random.default_rng(73)
+    old = rng.integers(0, lay.raw_vocab, size=(1, 300))
+    other = rng.integers(0, lay.raw_vocab, size=(1, 301))
+    new = rng.integers(0, lay.raw_vocab, size=40)
+    st = H.make_state(wl, 2, 512)
+    for c0 in range(0, 300, 100):  # the finished sequence: three chunks in row 0
+        st.hash(H.to_dev(old[:, c0:c0 + 100]), _i32([c0]), cache_rows=_i32([0]))
+    st.hash(H.to_dev(other[:, :300]), _i32([0]), cache_rows=_i32([1]))
+    # one packed call: the new sequence (40 tokens at position 0 of row 0), the other decoding at 300
+    pid = np.concatenate([new, other[0, 300:301]])
+    cu, sp, rows = _i32([0, 40, 41]), _i32([0, 300]), _i32([0, 1])
+    h = st.hash_varlen(H.to_dev(pid), cu, sp, max_len=40, cache_rows=rows)
+    fresh = H.make_state(wl, 1, 512)
+    h_new = fresh.hash(H.to_dev(new.reshape(1, -1)), 0)
+    assert torch.equal(h[:40].cpu(), h_new.reshape(40, 1, 6).cpu())
+    orc = H.make_oracle(wl, 2, 512)
+    orc.hash(other[:, :300], 0, cache_rows=np.array([1]))
+    exp_h, fl = orc.hash(other[:, 300:301], np.array([300]), cache_rows=np.array([1]))
+    assert fl == 0
+    H.assert_bits_equal(h[40:].cpu().numpy().reshape(exp_h.shape), exp_h, "decoding sequence")
+    assert st.status() == 0
