@@ -12,9 +12,9 @@
 // consecutive tokens of one sequence: it stages the tile's compressed tokens plus the
 // (max_ngram-1)-token halo in shared memory, computes every hash id of the tile there, and then
 // all its threads stream the tile's rows through registers, several rows in flight per thread.
-// For one layer the tile's output rows are contiguous, so each warp store covers whole 32-byte
-// sectors: lane q of a row's D/16-lane group converts codes [8q, 8q+8) and [D/2+8q, D/2+8q+8) and
-// writes 16 bytes into each half of the output row.
+// For one layer the tile's output rows are contiguous: lane q of a row's D/16-lane group loads codes
+// [16q, 16q+16) with one 16-byte load and writes their 32 bf16 bytes, one whole sector, with one
+// 256-bit store, so a warp moves 4 rows per load and per store instruction.
 //
 // DRAM per row: 128 B of codes, the sector holding its scale (32 B with the context's L2 fetch
 // limit at 32 B, engram_set_l2_fetch_granularity; a 128-B line at the 64-B default) and the 256-B
@@ -131,9 +131,11 @@ __device__ __forceinline__ uint4 dequant8(uint2 w, float s) {
   return o;
 }
 
-__device__ __forceinline__ uint2 ld_rows_v2(const uint8_t* p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+__device__ __forceinline__ uint4 ld_rows_v4(const uint8_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
   return v;
 }
 
@@ -170,18 +172,30 @@ __device__ __forceinline__ float widen_scale(uint32_t bits) {
 }
 
 // bf16 output rows are written once and not read again by this kernel: an L2 evict-first policy
-// lets them leave L2 ahead of lines still in use (254.7 vs 257.0 us per full-scale launch)
-__device__ __forceinline__ void st_out_v4(void* p, uint4 v) {
+// lets them leave L2 ahead of lines still in use (254.7 vs 257.0 us per full-scale launch). A lane
+// writes its 32 bytes with one 256-bit store (a whole sector) when the output is 32-byte aligned,
+// else with two 16-byte stores.
+__device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t policy;
   asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+__device__ __forceinline__ void st_out_v4(void* p, uint4 v, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w), "l"(policy)
                : "memory");
 }
 
+__device__ __forceinline__ void st_out_v8(void* p, uint4 a, uint4 b, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(a.x),
+               "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w), "l"(policy)
+               : "memory");
+}
+
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
 
-// One lane's share of one output row: codes [8q, 8q+8) and [D/2+8q, D/2+8q+8) of table row `row`.
+// One lane's share of one output row: codes [16q, 16q+8) and [16q+8, 16q+16) of table row `row`.
 struct RowPiece {
   uint2 v0, v1;
   uint32_t s0, s1;  // raw scale bits (widened when the piece is stored)
@@ -197,9 +211,10 @@ __device__ __forceinline__ void piece_load(RowPiece& pc, const uint8_t* W, const
   pc.valid = (row >= 0) && (row < rows);
   if (pc.valid) {
     const uint8_t* base = W + (row << ilog2(D));
-    const int k0 = 8 * q, k1 = (D >> 1) + 8 * q;
-    pc.v0 = ld_rows_v2(base + k0);
-    pc.v1 = ld_rows_v2(base + k1);
+    const int k0 = 16 * q, k1 = 16 * q + 8;
+    const uint4 w = ld_rows_v4(base + k0);  // one 16-byte load: the row is one request of its 8 lanes
+    pc.v0 = make_uint2(w.x, w.y);
+    pc.v1 = make_uint2(w.z, w.w);
     const int64_t srow = row << (ilog2(D) - blk_shift);
     pc.s0 = ld_scale_bits<SDT>(S, srow + (k0 >> blk_shift));
     pc.s1 = ONE ? pc.s0 : ld_scale_bits<SDT>(S, srow + (k1 >> blk_shift));
@@ -214,8 +229,14 @@ __device__ __forceinline__ void piece_store(const RowPiece& pc, uint16_t* out_ro
     a = dequant8(pc.v0, widen_scale<SDT>(pc.s0));
     b = dequant8(pc.v1, widen_scale<SDT>(pc.s1));
   }
-  st_out_v4(out_row + 8 * q, a);
-  st_out_v4(out_row + (D >> 1) + 8 * q, b);
+  const uint64_t policy = evict_first_policy();
+  uint16_t* p = out_row + 16 * q;  // 32 bytes: a whole sector when the output is 32-byte aligned
+  if ((reinterpret_cast<uintptr_t>(p) & 31) == 0) {
+    st_out_v8(p, a, b, policy);
+  } else {
+    st_out_v4(p, a, policy);
+    st_out_v4(p + 8, b, policy);
+  }
 }
 
 // ------------------------------------------------------------------------------------------------

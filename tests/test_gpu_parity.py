@@ -428,3 +428,30 @@ def test_binding_refuses_wrong_sizes():
         st.prepare_hash_lookup(ids, torch.zeros(3, dtype=torch.int32, device="cuda"), Ws, Ss, out)
     torch.cuda.synchronize()
     assert st.status() == 0
+
+
+def test_outputs_only_16_byte_aligned():
+    """A lane writes its 32 bytes of a row with one 256-bit store when the output is 32-byte aligned,
+    else with two 16-byte stores: outputs that start 16 bytes into their buffer get the same bits,
+    from the fused call and from the lookup."""
+    wl = synth.make_workload(0)
+    lay = wl.layout
+    Ws, Ss = H.device_tables(wl)
+    ids = H.to_dev(np.random.default_rng(5).integers(0, lay.raw_vocab, size=(1, 64)))
+    st, st2 = H.make_state(wl, 1, 64), H.make_state(wl, 1, 64)
+    hashes = torch.empty((1, 64, 1, 6), dtype=torch.int64, device="cuda")
+    ref = st.hash_lookup(ids, Ws, Ss, hashes=hashes)
+    buf = torch.full((ref[0].numel() + 8,), -3.0, dtype=torch.bfloat16, device="cuda")
+    out = [buf[8:].view(ref[0].shape)]
+    assert out[0].data_ptr() % 32 == 16
+    st2.hash_lookup(ids, Ws, Ss, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0].view(torch.int16), ref[0].view(torch.int16))
+    assert (buf[:8] == -3.0).all()
+    idx = hashes[..., 0, :].reshape(-1).contiguous()
+    r1 = st.lookup(idx, Ws[0], Ss[0])
+    buf2 = torch.empty((r1.numel() + 8,), dtype=torch.bfloat16, device="cuda")
+    o2 = buf2[8:].view(r1.shape)
+    st.lookup(idx, Ws[0], Ss[0], out=o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o2.view(torch.int16), r1.view(torch.int16))
