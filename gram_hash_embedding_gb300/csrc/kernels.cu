@@ -212,7 +212,7 @@ __device__ __forceinline__ void piece_load(RowPiece& pc, const uint8_t* W, const
   if (pc.valid) {
     const uint8_t* base = W + (row << ilog2(D));
     const int k0 = 16 * q, k1 = 16 * q + 8;
-    const uint4 w = ld_rows_v4(base + k0);  // one 16-byte load: the row is one request of its 8 lanes
+    const uint4 w = ld_rows_v4(base + k0);  // one 16-byte load: a row's D/16 lanes fetch it in one request
     pc.v0 = make_uint2(w.x, w.y);
     pc.v1 = make_uint2(w.z, w.w);
     const int64_t srow = row << (ilog2(D) - blk_shift);
