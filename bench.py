@@ -34,7 +34,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_fullscale_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_profile_case_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "gram_hash_embedding_gb300", "csrc", f) for f in
                   ("kernels.cu", "engram_internal.cuh")]
 
@@ -69,11 +69,6 @@ def parse_args(argv=None):
                    help="the context's L2 fetch granularity limit for the run (bytes; 0 leaves the context "
                         "default, 64 on GB300). At 32 a row's random 4-byte scale read costs a 32-byte DRAM "
                         "sector instead of a 128-byte line (engram_set_l2_fetch_granularity)")
-    p.add_argument("--probe", choices=["access", "gather", "layout", "depth"],
-                   help="run a DRAM measurement probe (bench_probe.cu) instead of the benchmark: access = DRAM "
-                        "bytes per random read size (under ncu), gather = the fused kernel's byte pattern without "
-                        "the hash, layout = scale placement next to the codes, depth = rows in flight in "
-                        "registers vs landed in shared memory by cp.async")
     return p.parse_args(argv)
 
 
@@ -110,19 +105,6 @@ def l2_note(runner, flushed: bool, fits: bool) -> str:
                 f"129 MB L2 (back-to-back steps, no flush)")
     return (f"inputs larger than L2: {tables / 1e9:.1f} GB of tables read at random, {ws / 1e6:.0f} MB touched "
             f"over the {len(runner.ids)} cycled id batches")
-
-
-PROBE_SRC = os.path.join(ROOT, "bench_probe.cu")
-PROBE_BIN = os.path.join(ROOT, "_build", "bench_probe")
-
-
-def run_probe(mode: str) -> int:
-    """Compile bench_probe.cu for sm_103a (when stale) and run one of its modes."""
-    if not os.path.exists(PROBE_BIN) or os.path.getmtime(PROBE_BIN) < os.path.getmtime(PROBE_SRC):
-        os.makedirs(os.path.dirname(PROBE_BIN), exist_ok=True)
-        subprocess.check_call([os.environ.get("NVCC", "nvcc"), "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
-                               "-std=c++17", "-o", PROBE_BIN, PROBE_SRC])
-    return subprocess.call([PROBE_BIN, mode])
 
 
 # ----------------------------------------------------------------------------- distributed plumbing
@@ -252,12 +234,15 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
-def recorded_traffic(cfg: int, l2_fetch: int = 0):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary ("key: value" lines),
-    or None when the kernel sources changed since the counters were taken, or the workload or the L2
-    fetch granularity setting (0: the context default) differs."""
+def recorded_traffic(lay, rows_per_launch: int, l2_fetch: int = 0):
+    """DRAM bytes per launch of the fused kernel, from the committed one-pass ncu capture of the
+    profiling case (about 1 GB of tables: small enough for any capture), scaled to this launch by
+    its count of gathered rows (the kernel's DRAM bytes grow with the rows it gathers: a code row,
+    a scale sector and a bf16 row each). Returns (bytes, note), or (None, reason) when the kernel
+    sources changed since the counters were taken, the row format (head_dim, scale storage) or the
+    L2 fetch granularity setting (0: the context default) differs from the capture's."""
     if not os.path.exists(TRAFFIC_FILE):
-        return None
+        return None, "no capture recorded"
     d = {}
     with open(TRAFFIC_FILE) as f:
         for line in f:
@@ -265,11 +250,19 @@ def recorded_traffic(cfg: int, l2_fetch: int = 0):
                 continue
             k, v = line.split(":", 1)
             d[k.strip()] = v.strip()
-    if d.get("source_sha256") != kernel_source_hash() or int(d.get("cfg", -1)) != cfg:
-        return None
+    if d.get("source_sha256") != kernel_source_hash():
+        return None, "kernel sources changed since the capture"
+    if int(d.get("head_dim", -1)) != lay.head_dim or int(d.get("scale_bytes", -1)) != lay.scale_bytes * (
+            lay.head_dim // lay.block):
+        return None, "another row format than the capture's"
     if int(d.get("l2_fetch_granularity", 0)) != l2_fetch:
-        return None
-    return float(d["dram_bytes_per_launch"])
+        return None, "another L2 fetch granularity than the capture's"
+    cap_rows = int(d["rows_per_launch"])
+    factor = rows_per_launch / cap_rows
+    note = (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of the profiling case (cfg {d['cfg']}, "
+            f"{cap_rows:,} gathered rows per launch, {float(d['dram_bytes_per_launch']):,.0f} B), scaled by "
+            f"{factor:g} to this launch's {rows_per_launch:,} rows ({TRAFFIC_FILE[len(ROOT) + 1:]})")
+    return float(d["dram_bytes_per_launch"]) * factor, note
 
 
 def algo_bytes_per_token(lay) -> int:
@@ -845,7 +838,8 @@ def run_ours(args):
     launch_s = mean_launch / runner.launches_per_step
     peak, peak_kind = measured_peaks()
     achieved = algo_bytes / launch_s / 1e9
-    traffic = recorded_traffic(args.cfg, args.l2_fetch) if args.mode == "fused" else None
+    traffic, traffic_note = (recorded_traffic(lay, per_launch_tokens * lay.n_layers * lay.n_cols, args.l2_fetch)
+                             if args.mode == "fused" else (None, "recorded for the fused kernel only"))
 
     cpu = cpu_all = cpu_torch = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not runner.varlen and args.mode == "fused":
@@ -887,7 +881,7 @@ def run_ours(args):
         },
         "gathered_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": peak_kind,
+                     "traffic": traffic, "traffic_source": traffic_note, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": algo_bytes, "launch_us": launch_s * 1e6,
                      "launch_us_median": median_launch / runner.launches_per_step * 1e6,
                      "kernel": runner.kernel_name},
@@ -1075,8 +1069,6 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.probe:
-        sys.exit(run_probe(args.probe))
     if args.impl == "reference":
         run_reference(args)
     elif args.block:

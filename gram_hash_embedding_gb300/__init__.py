@@ -112,6 +112,27 @@ def _stream(stream) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _launch_stream(stream, temps=()) -> int:
+    """The stream handle a call launches on. The wrapper's own temporaries (a start_pos array built
+    from an int, outputs it allocates) are made on the current stream; when the caller names another
+    stream, that stream first waits for the current one, and each temporary is marked as in use on it
+    so the caching allocator does not hand its memory out again before the library's kernel is done."""
+    cur = torch.cuda.current_stream()
+    if stream is None:
+        return cur.cuda_stream
+    if not isinstance(stream, torch.cuda.Stream):
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        if handle == cur.cuda_stream:
+            return handle
+        stream = torch.cuda.ExternalStream(handle)
+    if stream.cuda_stream != cur.cuda_stream:
+        stream.wait_stream(cur)
+        for t in temps:
+            if isinstance(t, torch.Tensor):
+                t.record_stream(stream)
+    return stream.cuda_stream
+
+
 def _dev(t: torch.Tensor, dtype, name: str) -> int:
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
@@ -241,18 +262,22 @@ def engram_hash(state: int, ids: torch.Tensor, start_pos, mask: torch.Tensor | N
     B, L = ids.shape
     lay = engram_state_layout(state)
     NC = lay["n_layers"] * (lay["max_ngram"] - 1) * lay["n_heads"]
+    temps = []
     if hashes is None:
         hashes = torch.empty((B, L, lay["n_layers"], (lay["max_ngram"] - 1) * lay["n_heads"]), dtype=torch.int64,
                              device=ids.device)
+        temps.append(hashes)
     _size(hashes, B * L * NC, "hashes")
     _size(mask, B * L, "mask")
     _size(cache_rows, B, "cache_rows")
     _size(start_pos, B, "start_pos")
     sp = _start_tensor(start_pos, B, ids.device)
+    if sp is not start_pos:
+        temps.append(sp)
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     _check(_lib().engram_hash(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"),
-                              _rows_ptr(cache_rows), B, L, _dev(hashes, torch.int64, "hashes"), _stream(stream)),
-           "engram_hash")
+                              _rows_ptr(cache_rows), B, L, _dev(hashes, torch.int64, "hashes"),
+                              _launch_stream(stream, temps)), "engram_hash")
     return hashes
 
 
@@ -266,15 +291,17 @@ def engram_lookup(idx: torch.Tensor, W: torch.Tensor, S: torch.Tensor, block: in
     bfloat16, float8_e8m0fnu or float8_e4m3fn; or raw bits with scale_dtype). Returns (or fills) bf16 [..., D]."""
     sdt = _scale_dtype_of(S, scale_dtype)
     rows, D = W.shape
+    temps = []
     if out is None:
         out = torch.empty(tuple(idx.shape) + (D,), dtype=torch.bfloat16, device=idx.device)
+        temps.append(out)
     _size(out, idx.numel() * D, "out")
     if int(block) > 0 and D % int(block) == 0:
         _size(S, rows * (D // int(block)), "S")
     Wu = W.view(torch.uint8)
     _check(_lib().engram_lookup(_dev(idx, torch.int64, "idx"), idx.numel(), _dev(Wu, torch.uint8, "W"),
                                 _dev_scales(S, sdt), rows, D, int(block), sdt, _dev(out, torch.bfloat16, "out"),
-                                _stream(stream)), "engram_lookup")
+                                _launch_stream(stream, temps)), "engram_lookup")
     return out
 
 
@@ -287,14 +314,18 @@ def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: lis
     lay = engram_state_layout(state)
     n = len(W)
     D, C = lay["head_dim"], (lay["max_ngram"] - 1) * lay["n_heads"]
+    temps = []
     if out is None and len(W) == lay["n_layers"]:
         out = [torch.empty((B, L, C, D), dtype=torch.bfloat16, device=ids.device) for _ in range(n)]
+        temps.extend(out)
     _tables(lay, W, S, out, B * L)
     _size(hashes, B * L * lay["n_layers"] * C, "hashes")
     _size(mask, B * L, "mask")
     _size(cache_rows, B, "cache_rows")
     _size(start_pos, B, "start_pos")
     sp = _start_tensor(start_pos, B, ids.device)
+    if sp is not start_pos:
+        temps.append(sp)
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     Wp = (_P * n)(*[_dev(w.view(torch.uint8), torch.uint8, "W") for w in W])
     sdt = lay["scale_dtype"]
@@ -303,7 +334,7 @@ def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: lis
     Op = (_P * n)(*[_dev(o, torch.bfloat16, "out") for o in out])
     hp = None if hashes is None else _dev(hashes, torch.int64, "hashes")
     _check(_lib().engram_hash_lookup(state, _dev(ids, torch.int64, "ids"), m, _dev(sp, torch.int32, "start_pos"),
-                                     _rows_ptr(cache_rows), B, L, Wp, Sp, Rp, Op, hp, _stream(stream)),
+                                     _rows_ptr(cache_rows), B, L, Wp, Sp, Rp, Op, hp, _launch_stream(stream, temps)),
            "engram_hash_lookup")
     return out
 
@@ -323,9 +354,11 @@ def engram_hash_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, 
     T = ids.numel()
     B = cu_seqlens.numel() - 1
     lay = engram_state_layout(state)
+    temps = []
     if hashes is None:
         hashes = torch.empty((T, lay["n_layers"], (lay["max_ngram"] - 1) * lay["n_heads"]), dtype=torch.int64,
                              device=ids.device)
+        temps.append(hashes)
     _size(hashes, T * lay["n_layers"] * (lay["max_ngram"] - 1) * lay["n_heads"], "hashes")
     _size(mask, T, "mask")
     _size(start_pos, B, "start_pos")
@@ -334,7 +367,7 @@ def engram_hash_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.Tensor, 
     _check(_lib().engram_hash_varlen(state, _dev(ids, torch.int64, "ids"), m, _dev(cu_seqlens, torch.int32, "cu_seqlens"),
                                      _dev(start_pos, torch.int32, "start_pos"), _rows_ptr(cache_rows), B, T,
                                      _max_len(cu_seqlens, max_len), _dev(hashes, torch.int64, "hashes"),
-                                     _stream(stream)), "engram_hash_varlen")
+                                     _launch_stream(stream, temps)), "engram_hash_varlen")
     return hashes
 
 
@@ -349,8 +382,10 @@ def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.T
     lay = engram_state_layout(state)
     n = len(W)
     D, C = lay["head_dim"], (lay["max_ngram"] - 1) * lay["n_heads"]
+    temps = []
     if out is None and len(W) == lay["n_layers"]:
         out = [torch.empty((T, C, D), dtype=torch.bfloat16, device=ids.device) for _ in range(n)]
+        temps.extend(out)
     _tables(lay, W, S, out, T)
     _size(hashes, T * lay["n_layers"] * C, "hashes")
     _size(mask, T, "mask")
@@ -366,7 +401,8 @@ def engram_hash_lookup_varlen(state: int, ids: torch.Tensor, cu_seqlens: torch.T
     _check(_lib().engram_hash_lookup_varlen(state, _dev(ids, torch.int64, "ids"), m,
                                             _dev(cu_seqlens, torch.int32, "cu_seqlens"),
                                             _dev(start_pos, torch.int32, "start_pos"), _rows_ptr(cache_rows), B, T,
-                                            _max_len(cu_seqlens, max_len), Wp, Sp, Rp, Op, hp, _stream(stream)),
+                                            _max_len(cu_seqlens, max_len), Wp, Sp, Rp, Op, hp,
+                                            _launch_stream(stream, temps)),
            "engram_hash_lookup_varlen")
     return out
 
@@ -378,8 +414,10 @@ def engram_gate(x: torch.Tensor, kv: torch.Tensor, q_weight: torch.Tensor, k_wei
     q_weight / k_weight [hc, dim], mask [...] bool or None. Returns (or fills; may be x) bf16 [..., hc, dim]."""
     hc, dim = x.shape[-2], x.shape[-1]
     T = x.numel() // (hc * dim)
+    temps = []
     if out is None:
         out = torch.empty_like(x)
+        temps.append(out)
     _size(kv, T * (hc + 1) * dim, "kv")
     _size(q_weight, hc * dim, "q_weight")
     _size(k_weight, hc * dim, "k_weight")
@@ -388,8 +426,8 @@ def engram_gate(x: torch.Tensor, kv: torch.Tensor, q_weight: torch.Tensor, k_wei
     m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
     _check(_lib().engram_gate(_dev(x, torch.bfloat16, "x"), _dev(kv, torch.bfloat16, "kv"),
                               _dev(q_weight, torch.bfloat16, "q_weight"), _dev(k_weight, torch.bfloat16, "k_weight"),
-                              m, T, hc, dim, float(eps), _dev(out, torch.bfloat16, "out"), _stream(stream)),
-           "engram_gate")
+                              m, T, hc, dim, float(eps), _dev(out, torch.bfloat16, "out"),
+                              _launch_stream(stream, temps)), "engram_gate")
     return out
 
 

@@ -15,11 +15,26 @@ struct engram_state {
   engram::ColParam* d_cols;
   int32_t* d_cache;
   unsigned int* d_status;
+  unsigned int* d_status_taken;  // engram_state_status: the word as read by the atomic exchange
 };
 
 namespace {
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Return code of a launch path. A failed launch leaves its error in the runtime's last-error slot,
+// where the caller's next unrelated launch check would find it; take it out here.
+inline int launch_rc(cudaError_t e) {
+  if (e == cudaSuccess) return ENGRAM_OK;
+  cudaGetLastError();
+  return ENGRAM_ERR_CUDA;
+}
+
+// Reads the status word and, when asked, clears it in the same atomic step, so that a flag raised
+// by a kernel on another stream between the read and the clear is not lost.
+__global__ void status_take_kernel(unsigned int* status, unsigned int* taken, int clear) {
+  *taken = clear ? atomicExch(status, 0u) : atomicOr(status, 0u);
+}
 
 inline bool head_dim_ok(int32_t D, int32_t block) {
   const bool pow2 = D == 16 || D == 32 || D == 64 || D == 128 || D == 256 || D == 512;
@@ -79,6 +94,7 @@ void free_state(engram_state* st) {
   cudaFree(st->d_cols);
   cudaFree(st->d_cache);
   cudaFree(st->d_status);
+  cudaFree(st->d_status_taken);
   delete st;
 }
 
@@ -186,7 +202,8 @@ int engram_state_create(const engram_layout* layout, const int64_t* token_map, c
       cudaMalloc(&st->d_mult, mult.size() * sizeof(uint64_t)) != cudaSuccess ||
       cudaMalloc(&st->d_cols, cols.size() * sizeof(engram::ColParam)) != cudaSuccess ||
       cudaMalloc(&st->d_cache, cache_n * sizeof(int32_t)) != cudaSuccess ||
-      cudaMalloc(&st->d_status, sizeof(unsigned int)) != cudaSuccess) {
+      cudaMalloc(&st->d_status, sizeof(unsigned int)) != cudaSuccess ||
+      cudaMalloc(&st->d_status_taken, sizeof(unsigned int)) != cudaSuccess) {
     cudaGetLastError();
     free_state(st);
     return ENGRAM_ERR_NOMEM;
@@ -200,6 +217,7 @@ int engram_state_create(const engram_layout* layout, const int64_t* token_map, c
   if (e == cudaSuccess) e = engram::launch_fill_i32(st->d_cache, cache_n, (int32_t)l.dead, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);  // host staging vectors go out of scope
   if (e != cudaSuccess) {
+    cudaGetLastError();
     free_state(st);
     return ENGRAM_ERR_CUDA;
   }
@@ -220,19 +238,20 @@ int engram_state_destroy(engram_state* state) {
 
 int engram_cache_reset(engram_state* state, engram_stream_t stream) {
   if (state == nullptr || !on_state_device(state)) return ENGRAM_ERR_INVALID;
-  cudaError_t e = engram::launch_fill_i32(state->d_cache, (int64_t)state->lay.max_batch * state->lay.max_seq_len,
-                                          (int32_t)state->lay.dead, (cudaStream_t)stream);
-  return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+  return launch_rc(engram::launch_fill_i32(state->d_cache,
+                                           (int64_t)state->lay.max_batch * state->lay.max_seq_len,
+                                           (int32_t)state->lay.dead, (cudaStream_t)stream));
 }
 
 int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* flags, int clear) {
   if (state == nullptr || flags == nullptr || !on_state_device(state)) return ENGRAM_ERR_INVALID;
   cudaStream_t s = (cudaStream_t)stream;
   unsigned int v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, state->d_status, sizeof v, cudaMemcpyDeviceToHost, s);
+  status_take_kernel<<<1, 1, 0, s>>>(state->d_status, state->d_status_taken, clear ? 1 : 0);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&v, state->d_status_taken, sizeof v, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess && clear) e = cudaMemsetAsync(state->d_status, 0, sizeof(unsigned int), s);
-  if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+  if (e != cudaSuccess) return launch_rc(e);
   *flags = v;
   return ENGRAM_OK;
 }
@@ -243,7 +262,7 @@ int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, co
   if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
   if (hashes == nullptr || !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
   engram::CallArgs a = call_args(state, ids, mask, start_pos, cache_rows, B, L, hashes);
-  return engram::launch_hash(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+  return launch_rc(engram::launch_hash(view(state), a, (cudaStream_t)stream));
 }
 
 int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
@@ -255,9 +274,8 @@ int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const voi
   if (rows > 0 && (W == nullptr || S == nullptr || !aligned(W, 16) || !aligned(S, scale_bytes(scale_dtype))))
     return ENGRAM_ERR_INVALID;
   if (n_idx > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
-  cudaError_t e =
-      engram::launch_lookup(idx, n_idx, W, S, rows, head_dim, block, scale_dtype, out, (cudaStream_t)stream);
-  return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+  return launch_rc(
+      engram::launch_lookup(idx, n_idx, W, S, rows, head_dim, block, scale_dtype, out, (cudaStream_t)stream));
 }
 
 int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
@@ -270,8 +288,7 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
   engram::CallArgs a = call_args(state, ids, mask, start_pos, cache_rows, B, L, hashes);
   rc = fill_tables(state, W, S, rows, out, &a);
   if (rc != ENGRAM_OK) return rc;
-  return engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK
-                                                                                          : ENGRAM_ERR_CUDA;
+  return launch_rc(engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream));
 }
 
 namespace {
@@ -307,7 +324,7 @@ int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* m
   engram::CallArgs a;
   int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, cache_rows, B, T, max_len, hashes, &a);
   if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
-  return engram::launch_hash(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+  return launch_rc(engram::launch_hash(view(state), a, (cudaStream_t)stream));
 }
 
 int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
@@ -319,8 +336,7 @@ int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uin
   if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
   rc = fill_tables(state, W, S, rows, out, &a);
   if (rc != ENGRAM_OK) return rc;
-  return engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream) == cudaSuccess ? ENGRAM_OK
-                                                                                          : ENGRAM_ERR_CUDA;
+  return launch_rc(engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream));
 }
 
 int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight, const uint16_t* k_weight,
@@ -334,8 +350,7 @@ int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight,
     return ENGRAM_ERR_INVALID;
   if (!aligned(x, 16) || !aligned(kv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) || !aligned(out, 16))
     return ENGRAM_ERR_INVALID;
-  cudaError_t e = engram::launch_gate(x, kv, q_weight, k_weight, mask, T, hc, dim, eps, out, (cudaStream_t)stream);
-  return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+  return launch_rc(engram::launch_gate(x, kv, q_weight, k_weight, mask, T, hc, dim, eps, out, (cudaStream_t)stream));
 }
 
 int engram_set_l2_fetch_granularity(int32_t bytes, int32_t* previous) {

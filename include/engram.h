@@ -99,16 +99,22 @@ typedef struct engram_layout {
 } engram_layout;
 
 /*
- * Create a state. All table-independent parameters of the hash module are
- * copied to the device; the cache [max_batch, max_seq_len] is allocated and
- * filled with DEAD (so history that was never written reads as blocked).
+ * Create a state: the hash module of the blocks/stack-hashes page. Its constructor holds the
+ * table-independent parameters that the hash `forward` uses -- the token_map compression table,
+ * the DEAD sentinel for masked tokens, pad_id for blocked n-gram slots, the per-layer multipliers,
+ * the bucket primes and the per-column offsets -- and the compressed-token cache that `forward`
+ * writes at [start_pos, start_pos + L) and reads back for the lookback. All of them are copied to
+ * the device once; the cache [max_batch, max_seq_len] is allocated and filled with DEAD (the pages
+ * do not show its initial contents; DEAD makes history that was never written read as blocked).
  *   token_map   host int64 [raw_vocab]; every value and `dead` must fit in int32
  *   multipliers host int64 [n_layers][max_ngram]
  *   primes      host int64 [n_layers][max_ngram-1][n_heads]; each in [1, 2^62)
  *   offsets     host int64 [n_layers][C], column = (n-2)*n_heads + head for n-gram size n;
  *               offset + prime - 1 must not overflow int64
- * On success *out receives the state; the call synchronises `stream` once.
- * Errors: ENGRAM_ERR_INVALID / _UNSUPPORTED for bad layout values, _NOMEM, _CUDA.
+ * Ownership: the host arrays are read during the call only; the state owns its device copies and
+ * the cache until engram_state_destroy. On success *out receives the state; the call synchronises
+ * `stream` once. Errors: ENGRAM_ERR_INVALID / _UNSUPPORTED for bad layout values, _NOMEM, _CUDA;
+ * on error *out is NULL and nothing stays allocated.
  */
 int engram_state_create(const engram_layout* layout, const int64_t* token_map, const int64_t* multipliers,
                         const int64_t* primes, const int64_t* offsets, engram_stream_t stream, engram_state** out);
@@ -116,11 +122,18 @@ int engram_state_create(const engram_layout* layout, const int64_t* token_map, c
 /* Free the state's device memory (synchronises the device first). NULL is accepted. */
 int engram_state_destroy(engram_state* state);
 
-/* Refill the whole cache with DEAD (asynchronous on stream). */
+/* Refill the whole cache with DEAD, the state's starting contents (asynchronous on stream): the
+ * cache of the hash `forward` (blocks/stack-hashes page) forgets every sequence, so positions below
+ * a later call's start_pos read as blocked. Errors: _INVALID (NULL state, another current device),
+ * _CUDA. */
 int engram_cache_reset(engram_state* state, engram_stream_t stream);
 
-/* Read the accumulated ENGRAM_STATUS_* flags into *flags (synchronises stream);
- * clears them when `clear` is non-zero. */
+/* Read the accumulated ENGRAM_STATUS_* flags into *flags (synchronises stream); clears them when
+ * `clear` is non-zero. The pages have no counterpart: their hash `forward` assumes valid ids and
+ * start positions (blocks/stack-hashes page); this library instead records the data errors it
+ * handled without faulting. Reading and clearing is one atomic exchange on the device, ordered
+ * after the work already enqueued on `stream`; a flag that a kernel on another stream raises
+ * concurrently is kept for the next read. Errors: _INVALID, _CUDA. */
 int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* flags, int clear);
 
 /*
@@ -155,8 +168,12 @@ int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const voi
                   int32_t head_dim, int32_t block, int32_t scale_dtype, uint16_t* out, engram_stream_t stream);
 
 /*
- * Hash and lookup in one launch: the hash of engram_hash (same cache update), then for every layer l the
- * lookup of its C columns in table l, as the model does for each engram layer.
+ * Hash and lookup in one launch, as one forward of the model does: `Transformer.forward`
+ * (blocks/stack-hashes page) calls the hash module once for all engram layers and hands each
+ * engram layer its slice [:, :, l, :] of the hash ids, and that layer's embedding
+ * (`ParallelEngramEmbedding.forward`, engram-first/lookup page, world size 1) turns the slice into
+ * rows of its own table. So: the hash of engram_hash (same cache update), then for every layer l
+ * the lookup of its C columns in table l, with the row ids kept on chip.
  *   W, S, rows, out  host arrays of n_layers entries: per layer the device table, scales (stored as the
  *                    layout's scale_dtype), row count (as engram_lookup) and a device bf16 output
  *                    [B][L][C][head_dim]
@@ -170,7 +187,8 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
 
 /*
  * Packed (variable-length) sequences, for continuous batching: B sequences of different lengths are
- * concatenated into one token array. Sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1,
+ * concatenated into one token array (an extension: the pages' hash `forward`, blocks/stack-hashes
+ * page, takes one [B, L] batch at one start position). Sequence b holds tokens cu_seqlens[b] .. cu_seqlens[b+1]-1,
  * sits at positions start_pos[b] .. of its cache row (b, or cache_rows[b]), and is hashed exactly as
  * engram_hash would hash it alone (blocks/stack-hashes page, hash `forward`, applied per sequence).
  *   ids         device int64 [T] raw token ids
@@ -183,7 +201,9 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
  *   hashes      device int64 [T][n_layers][C]
  * A sequence whose extent is inconsistent is skipped and flagged (ENGRAM_STATUS_BAD_LENGTH); a start
  * position that does not fit is handled as in engram_hash. Where cu_seqlens decreases, the sequence at
- * the decrease is flagged and skipped and which other sequences are processed is unspecified. Extents
+ * the decrease is flagged and skipped and which other sequences are processed is unspecified: once a
+ * call raises ENGRAM_STATUS_BAD_LENGTH, treat every output of that call (hash ids, rows, and the
+ * cache positions it was to write) as undefined, valid sequences included. Extents
  * must not overlap (tokens shared by two sequences would be written twice). B == 0, T == 0 or
  * max_len == 0 is a no-op. The launch has floor(T / tile) + B CTAs (tile: 4 to 64 tokens), each
  * taking one tile of one sequence, so its cost follows T, not B x max_len.
@@ -195,7 +215,8 @@ int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* m
                        int64_t* hashes, engram_stream_t stream);
 
 /*
- * Packed sequences, hash and lookup in one launch (as engram_hash_lookup): out[l] is device bf16
+ * Packed sequences, hash and lookup in one launch (as engram_hash_lookup: `Transformer.forward`'s
+ * one hash call and each layer's `ParallelEngramEmbedding.forward`, applied per sequence): out[l] is device bf16
  * [T][C][head_dim] for layer l, hashes ([T][n_layers][C]) may be NULL. Other arguments and errors as
  * engram_hash_varlen and engram_hash_lookup.
  */

@@ -22,12 +22,17 @@ def test_algorithmic_bytes_per_token():
 
 
 def test_traffic_record_matches_the_kernel_sources():
-    # the committed ncu record is only used for the kernel it was taken on
-    t = bench.recorded_traffic(3)
-    assert t is None or 1.2e9 < t < 2.0e9
-    t32 = bench.recorded_traffic(3, 32)  # the record is taken at bench.py's default 32-B fetch limit
-    assert t32 is None or 1.2e9 < t32 < 1.4e9
-    assert bench.recorded_traffic(1) is None and bench.recorded_traffic(1, 32) is None
+    # the committed ncu record (profiling case) is only used for the kernel and row format it was
+    # taken on, at the fetch limit it was taken at, and scales with the gathered rows
+    full = synth.make_layout("full", 1)
+    rows = 65_536 * 48
+    t, note = bench.recorded_traffic(full, rows, 32)
+    assert t is None or (1.15e9 < t < 1.45e9 and "scaled" in note), (t, note)
+    if t is not None:
+        t2, _ = bench.recorded_traffic(full, rows // 4, 32)
+        assert abs(t2 * 4 - t) < 1.0
+    assert bench.recorded_traffic(full, rows, 64)[0] is None
+    assert bench.recorded_traffic(synth.make_layout("tiny", 1), rows, 32)[0] is None  # head_dim 32
 
 
 def test_clock_summary_parses_nvidia_smi_lines():

@@ -251,16 +251,19 @@ def _run_fused_vs_oracle(lay, B, L, rows_override=None, seed=0, with_mask=True):
                                      (512, 128), (512, 64), (128, 8), (256, 16)])
 @pytest.mark.parametrize("L", [1, 33, 100])
 def test_fused_paths_all_shapes(D, block, L):
-    """1, 2 or 4 scales per row take the bulk-copy path; 8 or 16 take the register path."""
+    """Every head_dim / block pair the library accepts: a row with one scale block (block == D) takes
+    the kernel instantiation that loads one scale per lane; rows with 2 to 64 scale blocks take the one
+    that loads the scale of each 8-code half of the lane's 16 codes. Tokens per row 1, 33 and 100 give one
+    partial tile, several tiles with a ragged tail, and many tiles."""
     lay = _custom_layout(D + block, 2, 4, 3, D, block)
     _run_fused_vs_oracle(lay, 3, L, seed=D * 1000 + block + L)
 
 
 @pytest.mark.parametrize("D,block", [(128, 128), (256, 128), (64, 16), (512, 64)])
 def test_fused_small_tables_edge_rows(D, block):
-    """Bucket ranges of 5 and 7 rows: every row is hit, including the last ones, whose 16-byte scale
-    chunk would run past the scale array; passing tables with fewer rows than the hash range makes
-    the top hash ids out of range (+0 rows)."""
+    """Bucket ranges of 5 and 7 rows: every row is hit, including the table's last rows and their
+    last scales (a read one past them would leave the arrays); passing tables with fewer rows than
+    the hash range makes the top hash ids out of range (+0 rows), down to a one-row table."""
     lay = _custom_layout(3, 1, 2, 2, D, block, primes=[[[5, 7]]])
     assert lay.rows == [12]
     _run_fused_vs_oracle(lay, 2, 200, seed=D)

@@ -121,3 +121,40 @@ def test_l2_fetch_granularity_changes_no_result(tiny):
         geng.set_l2_fetch_granularity(default)
     with pytest.raises(geng.EngramError):
         geng.set_l2_fetch_granularity(48)
+
+
+def test_explicit_side_stream_with_wrapper_temporaries(tiny):
+    """A call on a stream other than the current one, with an int start_pos and outputs left to the
+    wrapper: the start_pos array and the outputs are made on the current stream, so the named stream
+    must wait for it and keep them alive until its kernel is done. Each step first makes garbage on
+    the current stream (allocations that would reuse freed blocks), then calls on the side stream;
+    every step's results must equal the oracle's."""
+    wl, Ws, Ss = tiny
+    lay = wl.layout
+    rng = np.random.default_rng(17)
+    B, L, steps = 2, 40, 12
+    st, orc = H.make_state(wl, B, L * steps), H.make_oracle(wl, B, L * steps)
+    side = torch.cuda.Stream()
+    got_h, got_r, host_ids = [], [], []
+    for k in range(steps):
+        ids_h = rng.integers(0, lay.raw_vocab, size=(B, L))
+        host_ids.append(ids_h)
+        ids = H.to_dev(ids_h)
+        torch.cuda.current_stream().wait_stream(side)  # ids reuse memory the side stream may still read
+        junk = torch.full((1 << 16,), 7, dtype=torch.int32, device="cuda")  # current-stream traffic
+        del junk
+        hashes = geng.engram_hash(st.handle, ids, k * L, stream=side)
+        with torch.cuda.stream(side):
+            idx = hashes[:, :, 0, :].contiguous()
+        rows = geng.engram_lookup(idx, Ws[0], Ss[0], lay.block, stream=side)
+        with torch.cuda.stream(side):
+            got_h.append(hashes.clone())
+            got_r.append(rows.clone())
+            ids.record_stream(side)
+    torch.cuda.synchronize()
+    for k in range(steps):
+        exp_h, _ = orc.hash(host_ids[k], k * L)
+        H.assert_bits_equal(got_h[k].cpu().numpy(), exp_h, f"side-stream hashes, step {k}")
+        H.assert_bits_equal(H.bf16_bits(got_r[k]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]),
+                            f"side-stream rows, step {k}")
+    assert st.status() == 0
