@@ -28,7 +28,8 @@ __all__ = [
     "engram_state_status", "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_hash_varlen",
     "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START",
     "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "STATUS_CHECK", "SCALE_F32", "SCALE_BF16", "SCALE_E8M0", "SCALE_E4M3",
-    "library_path", "set_l2_fetch_granularity",
+    "library_path", "set_l2_fetch_granularity", "engram_project", "engram_project_gate",
+    "engram_project_gate_workspace", "engram_device_status", "STATUS_TIMEOUT",
 ]
 
 OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
@@ -37,6 +38,7 @@ STATUS_BAD_ID = 2
 STATUS_BAD_LENGTH = 4
 STATUS_BAD_ROW = 8
 STATUS_CHECK = 16  # checked builds only: a kernel skipped an access outside the call's buffers
+STATUS_TIMEOUT = 32  # a tensor-core kernel gave up a wait (engram_device_status)
 # storage types of the scale tensors (ENGRAM_SCALE_*)
 SCALE_F32, SCALE_BF16, SCALE_E8M0, SCALE_E4M3 = 0, 1, 2, 3
 _SCALE_BYTES = {SCALE_F32: 4, SCALE_BF16: 2, SCALE_E8M0: 1, SCALE_E4M3: 1}
@@ -86,12 +88,19 @@ def _lib():
         L.engram_hash_lookup_varlen.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _P]
         L.engram_state_layout.argtypes = [_P, ctypes.POINTER(_Layout)]
         L.engram_gate.argtypes = [_P, _P, _P, _P, _P, _I64, _I32, _I32, ctypes.c_float, _P, _P]
+        L.engram_project.argtypes = [_P, _P, _I64, _I32, _I32, _P, _P]
+        L.engram_project_gate_workspace.argtypes = [_I64, _I32, _I32]
+        L.engram_project_gate_workspace.restype = ctypes.c_uint64
+        L.engram_project_gate.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, ctypes.c_float, _P,
+                                          ctypes.c_uint64, _P, _P]
+        L.engram_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
         L.engram_strerror.argtypes = [ctypes.c_int]
         L.engram_set_l2_fetch_granularity.argtypes = [_I32, ctypes.POINTER(_I32)]
         L.engram_strerror.restype = ctypes.c_char_p
         for name in ("engram_state_create", "engram_state_destroy", "engram_cache_reset", "engram_state_status",
                      "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout",
-                     "engram_hash_varlen", "engram_hash_lookup_varlen", "engram_gate"):
+                     "engram_hash_varlen", "engram_hash_lookup_varlen", "engram_gate", "engram_project",
+                     "engram_project_gate", "engram_device_status"):
             getattr(L, name).restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -429,6 +438,77 @@ def engram_gate(x: torch.Tensor, kv: torch.Tensor, q_weight: torch.Tensor, k_wei
                               m, T, hc, dim, float(eps), _dev(out, torch.bfloat16, "out"),
                               _launch_stream(stream, temps)), "engram_gate")
     return out
+
+
+def engram_project(emb: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The `wkv` projection on the tensor cores: emb bf16 [..., K] (T rows), w bf16 [N, K].
+    Returns (or fills) bf16 [..., N] = bf16(emb @ w^T), fp32 accumulation."""
+    K = emb.shape[-1]
+    T = emb.numel() // K if K else 0
+    N = w.shape[0]
+    if w.dim() != 2 or w.shape[1] != K:
+        raise ValueError(f"w must be [N, {K}], got {tuple(w.shape)}")
+    temps = []
+    if out is None:
+        out = torch.empty(tuple(emb.shape[:-1]) + (N,), dtype=torch.bfloat16, device=emb.device)
+        temps.append(out)
+    _size(out, T * N, "out")
+    _check(_lib().engram_project(_dev(emb, torch.bfloat16, "emb"), _dev(w, torch.bfloat16, "w"), T, K, N,
+                                 _dev(out, torch.bfloat16, "out"), _launch_stream(stream, temps)), "engram_project")
+    return out
+
+
+def engram_project_gate_workspace(T: int, hc: int, dim: int) -> int:
+    """Bytes of workspace engram_project_gate needs (0 for T == 0 or an unsupported hc / dim)."""
+    return int(_lib().engram_project_gate_workspace(int(T), int(hc), int(dim)))
+
+
+def engram_project_gate(x: torch.Tensor, emb: torch.Tensor, wkv: torch.Tensor, q_weight: torch.Tensor,
+                        k_weight: torch.Tensor, mask: torch.Tensor | None = None, eps: float = 1e-20,
+                        workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """The Engram block after the lookup, fused: the `wkv` projection with the gate's sums in its
+    epilogue (keys never written), then the gate. x bf16 [T, hc, dim]; emb bf16 [T, K];
+    wkv bf16 [(hc+1)*dim, K]; q_weight / k_weight bf16 [hc, dim]; mask [T] bool or None;
+    workspace: a uint8 CUDA tensor of at least engram_project_gate_workspace(T, hc, dim) bytes
+    (allocated here when None). Returns (or fills; may be x) bf16 [T, hc, dim]."""
+    hc, dim = x.shape[-2], x.shape[-1]
+    T = x.numel() // (hc * dim)
+    K = emb.shape[-1]
+    temps = []
+    if out is None:
+        out = torch.empty_like(x)
+        temps.append(out)
+    _size(emb, T * K, "emb")
+    _size(wkv, (hc + 1) * dim * K, "wkv")
+    _size(q_weight, hc * dim, "q_weight")
+    _size(k_weight, hc * dim, "k_weight")
+    _size(mask, T, "mask")
+    _size(out, T * hc * dim, "out")
+    need = engram_project_gate_workspace(T, hc, dim)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+        temps.append(workspace)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace holds {workspace.numel() * workspace.element_size()} bytes, need {need}")
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+    _check(_lib().engram_project_gate(_dev(x, torch.bfloat16, "x"), _dev(emb, torch.bfloat16, "emb"),
+                                      _dev(wkv, torch.bfloat16, "wkv"), _dev(q_weight, torch.bfloat16, "q_weight"),
+                                      _dev(k_weight, torch.bfloat16, "k_weight"), m, T, K, hc, dim, float(eps),
+                                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                      _dev(out, torch.bfloat16, "out"), _launch_stream(stream, temps)),
+           "engram_project_gate")
+    return out
+
+
+def engram_device_status(clear: bool = True, stream=None) -> int:
+    """Status flags of the kernels that have no state object (STATUS_TIMEOUT) on the current device;
+    synchronises the stream."""
+    v = ctypes.c_uint32(0)
+    _check(_lib().engram_device_status(_stream(stream), ctypes.byref(v), int(bool(clear))), "engram_device_status")
+    return v.value
 
 
 class PreparedHashLookup:

@@ -6,6 +6,7 @@
 #include <vector>
 
 #include "engram_internal.cuh"
+#include "proj.cuh"
 
 struct engram_state {
   engram_layout lay;
@@ -351,6 +352,62 @@ int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight,
   if (!aligned(x, 16) || !aligned(kv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) || !aligned(out, 16))
     return ENGRAM_ERR_INVALID;
   return launch_rc(engram::launch_gate(x, kv, q_weight, k_weight, mask, T, hc, dim, eps, out, (cudaStream_t)stream));
+}
+
+int engram_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
+                   engram_stream_t stream) {
+  if (T < 0) return ENGRAM_ERR_INVALID;
+  if (K < 8 || K % 8 != 0 || N < 8 || N % 8 != 0 || N > INT32_MAX - 256 || T > INT32_MAX)
+    return ENGRAM_ERR_UNSUPPORTED;
+  if (T == 0) return ENGRAM_OK;
+  if (emb == nullptr || w == nullptr || out == nullptr || !aligned(emb, 16) || !aligned(w, 16) || !aligned(out, 16))
+    return ENGRAM_ERR_INVALID;
+  return launch_rc(engram::launch_project(emb, w, T, K, N, out, (cudaStream_t)stream));
+}
+
+namespace {
+inline bool gate_shape_ok(int32_t hc, int32_t dim) {
+  return (hc == 1 || hc == 2 || hc == 4 || hc == 8) && dim >= 256 && dim % 256 == 0 &&
+         (int64_t)(hc + 1) * dim <= INT32_MAX - 256;
+}
+
+uint64_t round256(uint64_t b) { return (b + 255u) & ~(uint64_t)255u; }
+}  // namespace
+
+uint64_t engram_project_gate_workspace(int64_t T, int32_t hc, int32_t dim) {
+  if (T <= 0 || !gate_shape_ok(hc, dim)) return 0;
+  return round256((uint64_t)T * (uint64_t)dim * 2u) +
+         round256((uint64_t)engram::project_gate_partials(T, hc, dim) * sizeof(float));
+}
+
+int engram_project_gate(const uint16_t* x, const uint16_t* emb, const uint16_t* wkv, const uint16_t* q_weight,
+                        const uint16_t* k_weight, const uint8_t* mask, int64_t T, int32_t K, int32_t hc, int32_t dim,
+                        float eps, void* workspace, uint64_t workspace_bytes, uint16_t* out, engram_stream_t stream) {
+  if (T < 0) return ENGRAM_ERR_INVALID;
+  if (!gate_shape_ok(hc, dim) || K < 8 || K % 8 != 0 || T > INT32_MAX) return ENGRAM_ERR_UNSUPPORTED;
+  if (T == 0) return ENGRAM_OK;
+  if (x == nullptr || emb == nullptr || wkv == nullptr || q_weight == nullptr || k_weight == nullptr ||
+      out == nullptr || workspace == nullptr)
+    return ENGRAM_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(emb, 16) || !aligned(wkv, 16) || !aligned(q_weight, 16) ||
+      !aligned(k_weight, 16) || !aligned(out, 16) || !aligned(workspace, 256))
+    return ENGRAM_ERR_INVALID;
+  if (workspace_bytes < engram_project_gate_workspace(T, hc, dim)) return ENGRAM_ERR_INVALID;
+  uint16_t* value = static_cast<uint16_t*>(workspace);
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256((uint64_t)T * dim * 2u));
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = launch_rc(engram::launch_project_gate_sums(x, emb, wkv, q_weight, k_weight, T, K, hc, dim, value, part, s));
+  if (rc != ENGRAM_OK) return rc;
+  return launch_rc(engram::launch_gate_finish(x, value, part, mask, T, hc, dim, eps, out, s));
+}
+
+int engram_device_status(engram_stream_t stream, uint32_t* flags, int clear) {
+  if (flags == nullptr) return ENGRAM_ERR_INVALID;
+  unsigned int v = 0;
+  int rc = launch_rc(engram::device_status_take(&v, clear ? 1 : 0, (cudaStream_t)stream));
+  if (rc != ENGRAM_OK) return rc;
+  *flags = v;
+  return ENGRAM_OK;
 }
 
 int engram_set_l2_fetch_granularity(int32_t bytes, int32_t* previous) {

@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "engram_internal.cuh"
+#include "proj.cuh"
 
 namespace engram {
 namespace {
@@ -175,7 +176,86 @@ cudaError_t launch_gate_hc(const uint16_t* x, const uint16_t* kv, const uint16_t
                     inv_sqrt_dim, out);
 }
 
+// The gate's second half after engram_project_gate's projection: the projection epilogue left, for
+// every row block of 128 tokens and every key tile u (256 columns of copy u / tpc), the per-token sums
+// of h^2, key^2 and h*q_weight*k_weight*key over the tile at part[block][u][0..2][token % 128]. One CTA
+// per token adds them up per copy (tpc tiles each), forms the hc gates exactly as gate_kernel does,
+// and writes out = bf16(h + gate * value) from the value rows the projection stored.
+template <int HC>
+__global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS)
+    gate_finish_kernel(const uint16_t* x, const uint16_t* __restrict__ value, const float* __restrict__ part,
+                       const uint8_t* __restrict__ mask, const int dim, const int tpc, const float eps,
+                       const float inv_sqrt_dim, uint16_t* out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t t = blockIdx.x;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int nvec = dim >> 3;
+  __shared__ float red[3 * kGateMaxCopies];
+  __shared__ float gate_s[kGateMaxCopies];
+  if (tid < 3 * HC) {  // thread (copy i, quantity q) sums its copy's tpc tiles
+    const int i = tid / 3, q = tid - 3 * (tid / 3);
+    const float* pt = part + ((t >> 7) * (int64_t)(HC * tpc) * 3 + q) * 128 + (t & 127);
+    float a = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < tpc; ++j) a += pt[(int64_t)(i * tpc + j) * 3 * 128];
+    red[tid] = a;
+  }
+  __syncthreads();
+  if (tid < HC) {
+    const float rd = 1.0f / (float)dim;
+    const float rstd = (1.0f / sqrtf(red[3 * tid] * rd + eps)) * (1.0f / sqrtf(red[3 * tid + 1] * rd + eps));
+    const float dot = red[3 * tid + 2] * rstd * inv_sqrt_dim;
+    const float z = copysignf(sqrtf(fmaxf(fabsf(dot), 1e-6f)), dot);
+    float g = 1.0f / (1.0f + expf(-z));
+    if (mask != nullptr && mask[t] == 0) g = 0.f;
+    gate_s[tid] = g;
+  }
+  __syncthreads();
+  const uint64_t stream = l2_evict_first();
+  const uint16_t* xt = x + t * (int64_t)HC * dim;
+  const uint16_t* vt = value + t * (int64_t)dim;
+  uint16_t* ot = out + t * (int64_t)HC * dim;
+  for (int v = tid; v < nvec; v += nthr) {
+    float val[8];
+    bf16x8_to_f32(ld16(vt + 8 * v, stream), val);
+#pragma unroll
+    for (int i = 0; i < HC; ++i) {
+      float h[8];
+      bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v, stream), h);
+      const float g = gate_s[i];
+      uint4 o;
+      o.x = f32x2_to_bf16x2(h[0] + g * val[0], h[1] + g * val[1]);
+      o.y = f32x2_to_bf16x2(h[2] + g * val[2], h[3] + g * val[3]);
+      o.z = f32x2_to_bf16x2(h[4] + g * val[4], h[5] + g * val[5]);
+      o.w = f32x2_to_bf16x2(h[6] + g * val[6], h[7] + g * val[7]);
+      *reinterpret_cast<uint4*>(ot + (int64_t)i * dim + 8 * v) = o;
+    }
+  }
+}
+
+template <int HC>
+cudaError_t launch_gate_finish_hc(const uint16_t* x, const uint16_t* value, const float* part, const uint8_t* mask,
+                                  int64_t T, int dim, float eps, uint16_t* out, cudaStream_t s) {
+  int threads = dim / 8;
+  threads = threads < 32 ? 32 : (threads > kGateThreads ? kGateThreads : ((threads + 31) / 32) * 32);
+  const float inv_sqrt_dim = (float)(1.0 / sqrt((double)dim));
+  return launch_pdl(gate_finish_kernel<HC>, dim3((unsigned)T), dim3(threads), 0, s, x, value, part, mask, dim,
+                    dim / 256, eps, inv_sqrt_dim, out);
+}
+
 }  // namespace
+
+cudaError_t launch_gate_finish(const uint16_t* x, const uint16_t* value, const float* part, const uint8_t* mask,
+                               int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s) {
+  switch (hc) {
+    case 1: return launch_gate_finish_hc<1>(x, value, part, mask, T, dim, eps, out, s);
+    case 2: return launch_gate_finish_hc<2>(x, value, part, mask, T, dim, eps, out, s);
+    case 4: return launch_gate_finish_hc<4>(x, value, part, mask, T, dim, eps, out, s);
+    case 8: return launch_gate_finish_hc<8>(x, value, part, mask, T, dim, eps, out, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* qw, const uint16_t* kw,
                         const uint8_t* mask, int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s) {

@@ -1,0 +1,467 @@
+// The Engram `wkv` projection on the sm_103a tensor cores: "DeepSeek V4.1" pages, blocks/stack-hashes
+// page, `Engram.forward`, kv = wkv(embedding rows flattened over the hash columns):
+//   kv[t][n] = bf16_rne( sum_k emb[t][k] * wkv[n][k] )     (bf16 inputs, fp32 accumulation)
+// and, fused into the same kernel's epilogue, the sums that the gate after it needs, so that the
+// keys are never written to memory (engram_project_gate).
+//
+// Design (GB300): a dense contraction (T x K x N = 65,536 x 3,072 x 25,600 per layer at the released
+// width), so it runs on the 5th-generation tensor cores. One persistent CTA per SM walks a list of
+// 128 x 256 output tiles. Its warps specialise:
+//   warp 0      one thread issues TMA loads of 128 x 64 (A = emb) and 256 x 64 (B = wkv) bf16 boxes,
+//               128-byte swizzled, into a 4-stage shared-memory ring (48 KB a stage);
+//   warp 1      allocates 512 columns of tensor memory (two 128 x 256 fp32 accumulators) and one of
+//               its threads issues tcgen05.mma (M 128, N 256, K 16; 4 per stage), committing each
+//               stage back to the loader and each finished tile to the epilogue;
+//   warps 2-5   the epilogue: each thread owns one row of the tile (one tensor-memory lane), reads
+//               its 256 fp32 accumulators 32 columns at a time, and either rounds them to bf16 and
+//               stores them, or (gate epilogue) turns a key tile into three partial sums per row.
+// The two accumulators let the epilogue of tile i run while the tensor cores compute tile i+1.
+// Tiles are visited in groups of 16 row blocks, column block outer: the 152 tiles in flight at any
+// time share ~16 A blocks and ~10 B blocks, which stay in L2.
+//
+// Every wait is bounded (tc_ptx.cuh): a wait that runs out raises ENGRAM_STATUS_TIMEOUT in the
+// library's device status word, the CTA stops issuing work, waits for its copies and MMAs in
+// flight, frees its tensor memory and exits.
+#include <cuda.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "engram_internal.cuh"
+#include "proj.cuh"
+#include "tc_ptx.cuh"
+
+namespace engram {
+
+// Flags raised by kernels that have no state object (read with engram_device_status).
+__device__ unsigned int g_device_status;
+
+namespace {
+
+constexpr int kBM = 128;           // tile rows (tokens)
+constexpr int kBN = 256;           // tile columns (output features)
+constexpr int kBK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kUmmaK = 16;         // K of one tcgen05.mma (kind::f16)
+constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
+constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kGroupM = 16;        // row blocks per tile group
+constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
+constexpr uint32_t kABytes = kBM * kBK * 2;
+constexpr uint32_t kBBytes = kBN * kBK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, kBN);
+
+// shared memory: the stage ring (1024-byte aligned), then barriers and two words
+constexpr uint32_t kRingBytes = kStages * kStageBytes;
+constexpr uint32_t kBarOff = kRingBytes;                     // full[S], empty[S], acc_full[2], acc_empty[2], drain
+constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+constexpr uint32_t kTmemSlotOff = kBarOff + 8 * kNumBars;    // tensor-memory base address written by the alloc
+constexpr uint32_t kAbortOff = kTmemSlotOff + 4;             // set by a role whose wait ran out
+constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;        // + slack to align the ring to 1024 bytes
+
+enum Epilogue { EPI_STORE = 0, EPI_GATE = 1 };
+
+struct ProjParams {
+  int64_t T;        // rows of emb (tokens)
+  int32_t K;        // columns of emb and wkv
+  int32_t N;        // rows of wkv = output columns
+  int32_t num_kb;   // ceil(K / kBK)
+  int32_t n_mblk;   // ceil(T / kBM)
+  int32_t n_nblk;   // ceil(N / kBN)
+  int64_t n_tiles;
+  // EPI_STORE: out [T][N] bf16
+  uint16_t* out;
+  // EPI_GATE: N = (hc + 1) * dim, dim a multiple of kBN. Key tiles (columns < hc * dim) produce the
+  // partial sums sum(h^2), sum(k^2), sum(h * q_weight * k_weight * k) of every row over their 256
+  // columns into part[m_blk][n_blk][3][kBM]; value tiles store bf16 rows into value [T][dim].
+  const uint16_t* x;   // [T][hc][dim] residual copies (h)
+  const uint16_t* qw;  // [hc][dim]
+  const uint16_t* kw;  // [hc][dim]
+  uint16_t* value;     // [T][dim]
+  float* part;         // [n_mblk][hc * dim / kBN][3][kBM]
+  int32_t hc, dim;
+};
+
+// tile index -> (row block, column block): groups of kGroupM row blocks, column block outer
+__device__ __forceinline__ void tile_coords(const ProjParams& p, int64_t tile, int32_t& mb, int32_t& nb) {
+  const int64_t per_group = (int64_t)kGroupM * p.n_nblk;
+  const int64_t g = tile / per_group;
+  const int64_t r = tile - g * per_group;
+  const int32_t m0 = (int32_t)(g * kGroupM);
+  const int32_t gm = min(kGroupM, p.n_mblk - m0);
+  mb = m0 + (int32_t)(r % gm);
+  nb = (int32_t)(r / gm);
+}
+
+__device__ __forceinline__ void raise_timeout(volatile int* abort) {
+  *abort = 1;
+  atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
+}
+
+// lane 0 waits, the warp follows its verdict (keeps the warp converged for .sync.aligned tcgen05 ops)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    ok = tc::mbar_wait(bar, parity, abort) ? 1 : 0;
+    if (!ok) raise_timeout(abort);
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_v4(uint16_t* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  return make_uint4(tc::f32x2_to_bf16x2(v[0], v[1]), tc::f32x2_to_bf16x2(v[2], v[3]),
+                    tc::f32x2_to_bf16x2(v[4], v[5]), tc::f32x2_to_bf16x2(v[6], v[7]));
+}
+
+// bf16 rows of one accumulator tile: dst points at column 0 of this thread's row (null: row past T);
+// ncols_left = columns of the tile inside the matrix (a multiple of 8)
+__device__ __forceinline__ void store_tile_row(uint32_t taddr, uint16_t* dst, int ncols_left) {
+#pragma unroll 1
+  for (int c = 0; c < kAccCols / 32; ++c) {
+    float v[32];
+    tc::tmem_load_32cols(taddr + 32 * c, v);  // every lane loads: the load is warp-wide
+    if (dst != nullptr) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        if (32 * c + 8 * g < ncols_left) st_v4(dst + 32 * c + 8 * g, pack8(v + 8 * g));
+    }
+  }
+}
+
+// Gate sums of one key tile over its 256 columns for this thread's row: the key values are the
+// accumulators rounded to bf16 (the projection's output type); h, q_weight and k_weight are bf16.
+// sums[0] = sum h^2, sums[1] = sum k^2, sums[2] = sum h * (q_weight * k_weight) * k, in fp32.
+__device__ __forceinline__ void gate_tile_row(uint32_t taddr, const uint16_t* hrow, const uint16_t* qrow,
+                                              const uint16_t* wrow, float (&sums)[3]) {
+  float sh = 0.f, sk = 0.f, sd = 0.f;
+  uint4 hb[4], hn[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) hb[g] = hrow != nullptr ? ld_nc_v4(hrow + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+  for (int c = 0; c < kAccCols / 32; ++c) {
+    if (c + 1 < kAccCols / 32) {  // the next chunk's h is in flight while this chunk is reduced
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        hn[g] = hrow != nullptr ? ld_nc_v4(hrow + 32 * (c + 1) + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float v[32];
+    tc::tmem_load_32cols(taddr + 32 * c, v);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float h[8], q[8], w[8], k[8];
+      bf16x8_to_f32(hb[g], h);
+      bf16x8_to_f32(ld_nc_v4(qrow + 32 * c + 8 * g), q);  // the same for every row: L1 hits
+      bf16x8_to_f32(ld_nc_v4(wrow + 32 * c + 8 * g), w);
+      bf16x8_to_f32(pack8(v + 8 * g), k);                    // round the keys to bf16
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sh = fmaf(h[e], h[e], sh);
+        sk = fmaf(k[e], k[e], sk);
+        sd = fmaf(h[e] * (q[e] * w[e]), k[e], sd);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) hb[g] = hn[g];
+  }
+  sums[0] = sh;
+  sums[1] = sk;
+  sums[2] = sd;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const ProjParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + kAbortOff);
+  const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + kTmemSlotOff);
+  auto bar = [&](int i) { return base + kBarOff + 8u * (uint32_t)i; };
+  auto full = [&](uint32_t s) { return bar((int)s); };
+  auto empty = [&](uint32_t s) { return bar(kStages + (int)s); };
+  auto acc_full = [&](uint32_t a) { return bar(2 * kStages + (int)a); };
+  auto acc_empty = [&](uint32_t a) { return bar(2 * kStages + 2 + (int)a); };
+  const uint32_t drain = bar(2 * kStages + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(full(s), 1);
+      tc::mbar_init(empty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(acc_full(a), 1);
+      tc::mbar_init(acc_empty(a), 4);  // one arrival per epilogue warp
+    }
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_barrier_init();
+    tc::tma_prefetch_descriptor(&tmA);
+    tc::tma_prefetch_descriptor(&tmB);
+  }
+  // inputs may come from the previous kernel on the stream, and its tensor memory must be free
+  pdl_wait();
+  if (warp == 1) {
+    tc::tmem_alloc(base + kTmemSlotOff, kTmemCols);
+    tc::tmem_relinquish_alloc_permit();
+  }
+  tc::fence_before_thread_sync();
+  __syncthreads();
+  tc::fence_after_thread_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA loader
+    int64_t issued = 0;
+    uint32_t stage = 0, phase = 0;
+    for (int64_t tile = blockIdx.x; tile < p.n_tiles && !*abort; tile += gridDim.x) {
+      int32_t mb, nb;
+      tile_coords(p, tile, mb, nb);
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!tc::mbar_wait(empty(stage), phase ^ 1u, abort)) {
+          raise_timeout(abort);
+          break;
+        }
+        tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
+        const uint32_t a_dst = base + stage * kStageBytes;
+        tc::tma_load_2d(a_dst, &tmA, full(stage), kb * kBK, mb * kBM);
+        tc::tma_load_2d(a_dst + kABytes, &tmB, full(stage), kb * kBK, nb * kBN);
+        ++issued;
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // no copy may still be landing in shared memory when the CTA exits: wait for the last ones
+    for (int64_t i = issued - (issued < kStages ? issued : kStages); i < issued; ++i)
+      if (!tc::mbar_wait(full((uint32_t)(i % kStages)), (uint32_t)((i / kStages) & 1), nullptr))
+        atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+    bool ok = true;
+    for (int64_t tile = blockIdx.x; ok && tile < p.n_tiles && !*abort; tile += gridDim.x) {
+      if (!tc::mbar_wait(acc_empty(acc), acc_phase ^ 1u, abort)) {
+        raise_timeout(abort);
+        break;
+      }
+      tc::fence_after_thread_sync();
+      const uint32_t d = tmem_base + acc * kAccCols;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!tc::mbar_wait(full(stage), phase, abort)) {
+          raise_timeout(abort);
+          ok = false;
+          break;
+        }
+        tc::fence_after_thread_sync();
+        const uint32_t a0 = base + stage * kStageBytes, b0 = a0 + kABytes;
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k)
+          tc::mma_bf16(d, tc::sw128_kmajor_desc(a0 + 2 * kUmmaK * k), tc::sw128_kmajor_desc(b0 + 2 * kUmmaK * k),
+                       kIdesc, (kb | k) != 0 ? 1u : 0u);
+        tc::commit(empty(stage));  // the stage returns to the loader once these MMAs have read it
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc::commit(acc_full(acc));  // the tile's accumulator is complete once every MMA above is
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // every MMA this thread issued has completed before tensor memory is freed
+    tc::commit(drain);
+    if (!tc::mbar_wait(drain, 0, nullptr)) atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
+  } else if (warp >= 2) {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
+    uint32_t acc = 0, acc_phase = 0;
+    for (int64_t tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x) {
+      int32_t mb, nb;
+      tile_coords(p, tile, mb, nb);
+      if (!warp_wait(acc_full(acc), acc_phase, abort)) break;
+      tc::fence_after_thread_sync();
+      const int r = quarter * 32 + lane;
+      const int64_t row = (int64_t)mb * kBM + r;
+      const bool row_ok = row < p.T;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols;
+      const int col0 = nb * kBN;
+      if (EPI == EPI_STORE) {
+        store_tile_row(taddr, row_ok ? p.out + row * p.N + col0 : nullptr, p.N - col0);
+      } else {
+        const int key_cols = p.hc * p.dim;
+        if (col0 < key_cols) {
+          const int i = col0 / p.dim, j0 = col0 - i * p.dim;
+          float sums[3];
+          gate_tile_row(taddr, row_ok ? p.x + (row * p.hc + i) * p.dim + j0 : nullptr, p.qw + i * p.dim + j0,
+                        p.kw + i * p.dim + j0, sums);
+          float* dst = p.part + ((int64_t)mb * (key_cols / kBN) + nb) * 3 * kBM + r;
+          dst[0] = sums[0];
+          dst[kBM] = sums[1];
+          dst[2 * kBM] = sums[2];
+        } else {
+          store_tile_row(taddr, row_ok ? p.value + row * p.dim + (col0 - key_cols) : nullptr, kBN);
+        }
+      }
+      tc::fence_before_thread_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(acc_empty(acc));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  pdl_trigger();
+  tc::fence_before_thread_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_thread_sync();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------------------
+// host side
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime (no link to libcuda)
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// [rows][K] bf16 row-major, read in boxes of box_rows x kBK with 128-byte swizzling; reads past
+// the matrix (ragged rows or K) are filled with zeros
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, emb, (uint64_t)p.T, (uint64_t)p.K, kBM) || !make_map(&tb, w, (uint64_t)p.N, (uint64_t)p.K, kBN))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(proj_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = p.n_tiles < sms ? p.n_tiles : sms;
+  return launch_pdl(proj_kernel<EPI>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, ta, tb, p);
+}
+
+ProjParams base_params(int64_t T, int32_t K, int32_t N) {
+  ProjParams p = {};
+  p.T = T;
+  p.K = K;
+  p.N = N;
+  p.num_kb = (K + kBK - 1) / kBK;
+  p.n_mblk = (int32_t)((T + kBM - 1) / kBM);
+  p.n_nblk = (N + kBN - 1) / kBN;
+  p.n_tiles = (int64_t)p.n_mblk * p.n_nblk;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
+                           cudaStream_t s) {
+  ProjParams p = base_params(T, K, N);
+  p.out = out;
+  return launch_proj<EPI_STORE>(emb, w, p, s);
+}
+
+int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim) {
+  return ((T + kBM - 1) / kBM) * (int64_t)(hc * dim / kBN) * 3 * kBM;
+}
+
+cudaError_t launch_project_gate_sums(const uint16_t* x, const uint16_t* emb, const uint16_t* wkv, const uint16_t* qw,
+                                     const uint16_t* kw, int64_t T, int32_t K, int32_t hc, int32_t dim,
+                                     uint16_t* value, float* part, cudaStream_t s) {
+  ProjParams p = base_params(T, K, (hc + 1) * dim);
+  p.x = x;
+  p.qw = qw;
+  p.kw = kw;
+  p.value = value;
+  p.part = part;
+  p.hc = hc;
+  p.dim = dim;
+  return launch_proj<EPI_GATE>(emb, wkv, p, s);
+}
+
+namespace {
+__device__ unsigned int g_device_status_taken;
+
+__global__ void device_status_take_kernel(int clear) {
+  g_device_status_taken = clear ? atomicExch(&g_device_status, 0u) : atomicOr(&g_device_status, 0u);
+}
+}  // namespace
+
+// Read (and optionally clear, in one atomic step) the device status word, ordered after the work
+// already on stream s; synchronises s.
+cudaError_t device_status_take(unsigned int* flags, int clear, cudaStream_t s) {
+  device_status_take_kernel<<<1, 1, 0, s>>>(clear);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = cudaMemcpyFromSymbolAsync(flags, g_device_status_taken, sizeof(unsigned int), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e;
+}
+
+}  // namespace engram

@@ -1,0 +1,28 @@
+// Internal declarations of the tensor-core projection (proj.cu) and the gate's finishing pass
+// (gate.cu), used by the C-ABI layer.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace engram {
+
+// out[T][N] = bf16(emb[T][K] @ w[N][K]^T)
+cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
+                           cudaStream_t s);
+
+// fp32 values of the partial-sum array of the fused gate projection for T tokens
+int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim);
+
+// projection with the gate epilogue: value [T][dim] bf16 and the key tiles' partial sums
+cudaError_t launch_project_gate_sums(const uint16_t* x, const uint16_t* emb, const uint16_t* wkv, const uint16_t* qw,
+                                     const uint16_t* kw, int64_t T, int32_t K, int32_t hc, int32_t dim,
+                                     uint16_t* value, float* part, cudaStream_t s);
+
+// the gate from the partial sums, out = bf16(h + gate * value)
+cudaError_t launch_gate_finish(const uint16_t* x, const uint16_t* value, const float* part, const uint8_t* mask,
+                               int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s);
+
+cudaError_t device_status_take(unsigned int* flags, int clear, cudaStream_t s);
+
+}  // namespace engram

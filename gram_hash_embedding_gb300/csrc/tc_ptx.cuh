@@ -55,15 +55,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase of parity `parity` has completed. Gives up (returns false) when *abort is
-// set by another role of the CTA or after kWaitLimitNs.
+// Wait until the phase of parity `parity` has completed. Gives up (returns false) after
+// kWaitLimitNs, or as soon as *abort is set by another role of the CTA (abort may be null: then
+// only the time limit ends the wait, as when draining copies still in flight).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
-      if (*abort) return false;
+      if (abort != nullptr && *abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
   }
@@ -130,6 +131,7 @@ __device__ __forceinline__ void commit(uint32_t bar) {
 // the registers can be scheduled before they hold the data.
 __device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
+  __syncwarp();  // the load is warp-wide (.sync.aligned): reconverge after any per-lane branch
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "

@@ -68,6 +68,9 @@ typedef struct engram_state engram_state;
 #define ENGRAM_STATUS_CHECK 16u    /* checked builds only (compiled with -DENGRAM_CHECKED=1): a hash or fused kernel
                                       skipped a memory access outside the call's buffers. A library bug, never a
                                       data error; release builds do not test for it */
+#define ENGRAM_STATUS_TIMEOUT 32u  /* a tensor-core kernel (engram_project, engram_project_gate) gave up a wait that
+                                      did not complete within a second: its outputs are undefined. A library or
+                                      device fault, never a data error; read with engram_device_status */
 
 /* Storage types of the scale tensors. The engram-first/lookup page leaves `scale_dtype` open and
  * widens the scale with `.float()`; each type below widens to fp32 exactly before the one fp32
@@ -242,6 +245,57 @@ int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uin
 int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight, const uint16_t* k_weight,
                 const uint8_t* mask, int64_t T, int32_t hc, int32_t dim, float eps, uint16_t* out,
                 engram_stream_t stream);
+
+/*
+ * The Engram `wkv` projection on the tensor cores (blocks/stack-hashes page, `Engram.forward`:
+ * kv = wkv(embedding rows flattened over the hash columns)):
+ *   out[t][n] = bf16_rne( sum_k emb[t][k] * w[n][k] )      for t < T, n < N
+ * with bf16 inputs and fp32 accumulation (the sum is formed in an unspecified order).
+ *   emb  device bf16 [T][K] (for the Engram block: a lookup output [T][C][head_dim], K = C * head_dim)
+ *   w    device bf16 [N][K] (the weight as `Linear` stores it: out_features x in_features)
+ *   out  device bf16 [T][N], written
+ * All three 16-byte aligned; K and N multiples of 8 (rows stay 16-byte aligned), K >= 8, N >= 8.
+ * T == 0 is a no-op. A kernel fault that stops progress raises ENGRAM_STATUS_TIMEOUT instead of
+ * hanging (engram_device_status). Errors: _INVALID (null, misaligned, negative T), _UNSUPPORTED
+ * (K or N not a multiple of 8 or below 8, T >= 2^31, N > 2^31 - 256), _CUDA.
+ */
+int engram_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
+                   engram_stream_t stream);
+
+/* Bytes of device workspace that engram_project_gate needs for T tokens (a multiple of 256). */
+uint64_t engram_project_gate_workspace(int64_t T, int32_t hc, int32_t dim);
+
+/*
+ * The Engram block after the lookup, fused (blocks/stack-hashes page, `Engram.forward`): the `wkv`
+ * projection kv = emb @ wkv^T (as engram_project, bf16 keys and value), then the gate of engram_gate
+ * on it, in two launches that never write the keys to memory:
+ *   1. the projection; the epilogue of each key tile turns its accumulators (rounded to bf16, the
+ *      projection's output type) into per-row partial sums of h^2, key^2 and h*q_weight*k_weight*key
+ *      over the tile's 256 columns, and each value tile stores its bf16 value rows;
+ *   2. per token: the partial sums give the hc gates (as engram_gate), then
+ *      out[t][i] = bf16_rne(h + gate * value).
+ *   x         device bf16 [T][hc][dim] (the residual copies h)
+ *   emb       device bf16 [T][K] (the lookup rows, flattened)
+ *   wkv       device bf16 [(hc+1)*dim][K]: hc key blocks of dim rows, then the value block
+ *   q_weight, k_weight  device bf16 [hc][dim]
+ *   mask      device uint8 [T] (non-zero = the token's gate is open) or NULL
+ *   workspace device memory of at least engram_project_gate_workspace(T, hc, dim) bytes, 256-byte
+ *             aligned, owned by the caller; holds the value rows and the partial sums between the
+ *             two launches, so calls that use one workspace must not overlap on the GPU
+ *   out       device bf16 [T][hc][dim]; may be the same buffer as x
+ * The result equals engram_gate(x, engram_project(emb, wkv), ...) up to the fp32 summation order.
+ * hc in {1, 2, 4, 8}; dim a multiple of 256; K a multiple of 8, K >= 8. T == 0 is a no-op.
+ * Errors: _INVALID (null, misaligned, workspace too small), _UNSUPPORTED (hc, dim, K, T >= 2^31), _CUDA.
+ */
+int engram_project_gate(const uint16_t* x, const uint16_t* emb, const uint16_t* wkv, const uint16_t* q_weight,
+                        const uint16_t* k_weight, const uint8_t* mask, int64_t T, int32_t K, int32_t hc, int32_t dim,
+                        float eps, void* workspace, uint64_t workspace_bytes, uint16_t* out, engram_stream_t stream);
+
+/* Read the status flags of the kernels that have no state object (ENGRAM_STATUS_TIMEOUT) for the
+ * current device into *flags, ordered after the work already on `stream` (synchronises it); clears
+ * them in the same atomic step when `clear` is non-zero. The pages have no counterpart: it reports
+ * a failure that the library turns into a flag instead of a hang. Errors: _INVALID, _CUDA. */
+int engram_device_status(engram_stream_t stream, uint32_t* flags, int clear);
 
 /*
  * Set the L2 fetch granularity limit of the current device's context (cudaLimitMaxL2FetchGranularity:

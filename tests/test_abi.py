@@ -118,3 +118,32 @@ def test_binding_checks_sizes_before_any_pointer():
         geng.engram_gate(x, torch.zeros((3, 4 * 64), dtype=torch.bfloat16), w, w)      # the value row is missing
     with pytest.raises(ValueError, match="mask has"):
         geng.engram_gate(x, torch.zeros((3, 5 * 64), dtype=torch.bfloat16), w, w, mask=torch.ones(4, dtype=torch.bool))
+
+
+def test_projection_checks_need_no_gpu(lib):
+    P = ctypes.c_void_p
+    lib.engram_project.argtypes = [P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P]
+    lib.engram_project_gate_workspace.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]
+    lib.engram_project_gate_workspace.restype = ctypes.c_uint64
+    lib.engram_project_gate.argtypes = [P, P, P, P, P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_float, P, ctypes.c_uint64, P, P]
+    a = P(4096)  # never dereferenced: every call below is rejected (or is a no-op) before a launch
+    assert lib.engram_project(a, a, 0, 64, 64, a, None) == geng.OK  # T == 0: nothing to do
+    assert lib.engram_project(a, a, -1, 64, 64, a, None) == geng.ERR_INVALID
+    assert lib.engram_project(a, a, 5, 60, 64, a, None) == geng.ERR_UNSUPPORTED  # K not a multiple of 8
+    assert lib.engram_project(a, a, 5, 64, 4, a, None) == geng.ERR_UNSUPPORTED   # N below 8
+    assert lib.engram_project(a, a, 1 << 31, 64, 64, a, None) == geng.ERR_UNSUPPORTED
+    assert lib.engram_project(None, a, 5, 64, 64, a, None) == geng.ERR_INVALID
+    assert lib.engram_project(P(4098), a, 5, 64, 64, a, None) == geng.ERR_INVALID  # misaligned
+    # workspace: value rows (T x dim bf16) + 3 partial sums per (128-token block, key tile, token)
+    assert lib.engram_project_gate_workspace(128, 4, 256) == 128 * 256 * 2 + 4 * 3 * 128 * 4
+    assert lib.engram_project_gate_workspace(129, 4, 5120) == (129 * 5120 * 2 + 255) // 256 * 256 + 2 * 80 * 3 * 128 * 4
+    assert lib.engram_project_gate_workspace(0, 4, 256) == 0
+    assert lib.engram_project_gate_workspace(8, 3, 256) == 0 and lib.engram_project_gate_workspace(8, 4, 200) == 0
+    need = lib.engram_project_gate_workspace(8, 4, 256)
+    assert lib.engram_project_gate(a, a, a, a, a, None, 8, 64, 3, 256, 1e-20, a, need, a, None) == geng.ERR_UNSUPPORTED
+    assert lib.engram_project_gate(a, a, a, a, a, None, 8, 64, 4, 320, 1e-20, a, need, a, None) == geng.ERR_UNSUPPORTED
+    assert lib.engram_project_gate(a, a, a, a, a, None, 8, 64, 4, 256, 1e-20, a, need - 1, a, None) == geng.ERR_INVALID
+    assert lib.engram_project_gate(a, a, a, a, a, None, 8, 64, 4, 256, 1e-20, P(4096 + 16), need, a, None) == \
+        geng.ERR_INVALID  # workspace must be 256-byte aligned
+    assert lib.engram_project_gate(a, a, a, a, a, None, 0, 64, 4, 256, 1e-20, None, 0, a, None) == geng.OK
