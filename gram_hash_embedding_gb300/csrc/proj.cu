@@ -38,27 +38,37 @@ __device__ unsigned int g_device_status;
 
 namespace {
 
-constexpr int kBM = 128;           // tile rows (tokens)
+constexpr int kBM = 128;           // tile rows of one CTA (tokens)
 constexpr int kBN = 256;           // tile columns (output features)
 constexpr int kBK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma (kind::f16)
 constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
 constexpr int kTmemCols = 2 * kAccCols;
-constexpr int kGroupM = 16;        // row blocks per tile group
 constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
 constexpr uint32_t kABytes = kBM * kBK * 2;
-constexpr uint32_t kBBytes = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kBM, kBN);
 
-// shared memory: the stage ring (1024-byte aligned), then barriers and two words
-constexpr uint32_t kRingBytes = kStages * kStageBytes;
-constexpr uint32_t kBarOff = kRingBytes;                     // full[S], empty[S], acc_full[2], acc_empty[2], drain
-constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
-constexpr uint32_t kTmemSlotOff = kBarOff + 8 * kNumBars;    // tensor-memory base address written by the alloc
-constexpr uint32_t kAbortOff = kTmemSlotOff + 4;             // set by a role whose wait ran out
-constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;        // + slack to align the ring to 1024 bytes
+// PAIR = false: one CTA computes a 128 x 256 tile with M = 128 MMAs (4 stages of A + all of B, 48 KB).
+// PAIR = true: a cluster of two CTAs computes a 256 x 256 tile with M = 256 pair MMAs issued by the
+// leader; each CTA loads its own 128 rows of A and its half (128 rows) of B, so a stage is 32 KB and
+// the ring holds 6 of them, and each SM reads 2/3 of the bytes per MMA from L2 that a single CTA does.
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBRows = PAIR ? kBN / 2 : kBN;          // rows of the B tile this CTA loads
+  static constexpr uint32_t kBBytes = kBRows * kBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTxBytes = PAIR ? 2 * kStageBytes : kStageBytes;  // per stage, both CTAs
+  static constexpr int kTileM = PAIR ? 2 * kBM : kBM;          // rows of one (cluster) tile
+  static constexpr int kGroup = PAIR ? 8 : 16;                 // tile rows per group: 16 row blocks of 128
+  static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kBN);
+  // shared memory: the stage ring (1024-byte aligned), then barriers and two words
+  static constexpr uint32_t kRingBytes = kStages * kStageBytes;
+  static constexpr uint32_t kBarOff = kRingBytes;  // full[S], empty[S], acc_full[2], acc_empty[2], drain
+  static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
+  static constexpr uint32_t kTmemSlotOff = kBarOff + 8 * kNumBars;  // tensor-memory base written by the alloc
+  static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;          // set by a role whose wait ran out
+  static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;     // + slack to align the ring to 1024 bytes
+};
 
 enum Epilogue { EPI_STORE = 0, EPI_GATE = 1 };
 
@@ -67,7 +77,7 @@ struct ProjParams {
   int32_t K;        // columns of emb and wkv
   int32_t N;        // rows of wkv = output columns
   int32_t num_kb;   // ceil(K / kBK)
-  int32_t n_mblk;   // ceil(T / kBM)
+  int32_t n_mtile;  // ceil(T / tile rows)
   int32_t n_nblk;   // ceil(N / kBN)
   int64_t n_tiles;
   // EPI_STORE: out [T][N] bf16
@@ -79,18 +89,19 @@ struct ProjParams {
   const uint16_t* qw;  // [hc][dim]
   const uint16_t* kw;  // [hc][dim]
   uint16_t* value;     // [T][dim]
-  float* part;         // [n_mblk][hc * dim / kBN][3][kBM]
+  float* part;         // [ceil(T / kBM)][hc * dim / kBN][3][kBM]
   int32_t hc, dim;
 };
 
-// tile index -> (row block, column block): groups of kGroupM row blocks, column block outer
-__device__ __forceinline__ void tile_coords(const ProjParams& p, int64_t tile, int32_t& mb, int32_t& nb) {
-  const int64_t per_group = (int64_t)kGroupM * p.n_nblk;
+// tile index -> (tile row, column block): groups of `group` tile rows, column block outer, so the
+// tiles in flight at one time share a few A and B blocks, which stay in L2
+__device__ __forceinline__ void tile_coords(const ProjParams& p, int group, int64_t tile, int32_t& mt, int32_t& nb) {
+  const int64_t per_group = (int64_t)group * p.n_nblk;
   const int64_t g = tile / per_group;
   const int64_t r = tile - g * per_group;
-  const int32_t m0 = (int32_t)(g * kGroupM);
-  const int32_t gm = min(kGroupM, p.n_mblk - m0);
-  mb = m0 + (int32_t)(r % gm);
+  const int32_t m0 = (int32_t)(g * group);
+  const int32_t gm = min(group, p.n_mtile - m0);
+  mt = m0 + (int32_t)(r % gm);
   nb = (int32_t)(r / gm);
 }
 
@@ -191,31 +202,37 @@ __device__ __forceinline__ void gate_tile_row(uint32_t taddr, const uint16_t* hr
   sums[2] = sd;
 }
 
-template <int EPI>
+template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const ProjParams p) {
+  using C = Cfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t base = (raw + 1023u) & ~1023u;  // the same offset in both CTAs of a pair
   uint8_t* gbase = smem_raw + (base - raw);
-  volatile int* abort = reinterpret_cast<volatile int*>(gbase + kAbortOff);
-  const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + kTmemSlotOff);
-  auto bar = [&](int i) { return base + kBarOff + 8u * (uint32_t)i; };
+  volatile int* abort = reinterpret_cast<volatile int*>(gbase + C::kAbortOff);
+  const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + C::kTmemSlotOff);
+  auto bar = [&](int i) { return base + C::kBarOff + 8u * (uint32_t)i; };
   auto full = [&](uint32_t s) { return bar((int)s); };
-  auto empty = [&](uint32_t s) { return bar(kStages + (int)s); };
-  auto acc_full = [&](uint32_t a) { return bar(2 * kStages + (int)a); };
-  auto acc_empty = [&](uint32_t a) { return bar(2 * kStages + 2 + (int)a); };
-  const uint32_t drain = bar(2 * kStages + 4);
+  auto empty = [&](uint32_t s) { return bar(C::kStages + (int)s); };
+  auto acc_full = [&](uint32_t a) { return bar(2 * C::kStages + (int)a); };
+  auto acc_empty = [&](uint32_t a) { return bar(2 * C::kStages + 2 + (int)a); };
+  const uint32_t drain = bar(2 * C::kStages + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a pair: rank 0 leads (issues the MMAs; its full and acc_empty barriers count for both CTAs)
+  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int64_t unit = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;  // cluster (or CTA) index
+  const int64_t n_units = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(full(s), 1);
-      tc::mbar_init(empty(s), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      tc::mbar_init(full(s), 1);   // the leader's arrive + the bytes of both CTAs' loads
+      tc::mbar_init(empty(s), 1);  // the leader's MMA commit, multicast to both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(acc_full(a), 1);
-      tc::mbar_init(acc_empty(a), 4);  // one arrival per epilogue warp
+      tc::mbar_init(acc_empty(a), PAIR ? 8 : 4);  // one arrival per epilogue warp of every CTA of the tile
     }
     tc::mbar_init(drain, 1);
     *abort = 0;
@@ -225,9 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // inputs may come from the previous kernel on the stream, and its tensor memory must be free
   pdl_wait();
+  if (PAIR) tc::cluster_sync();  // the peer's barriers exist before anyone signals them
   if (warp == 1) {
-    tc::tmem_alloc(base + kTmemSlotOff, kTmemCols);
-    tc::tmem_relinquish_alloc_permit();
+    if (PAIR) {
+      tc::tmem_alloc_pair(base + C::kTmemSlotOff, kTmemCols);
+      tc::tmem_relinquish_alloc_permit_pair();
+    } else {
+      tc::tmem_alloc(base + C::kTmemSlotOff, kTmemCols);
+      tc::tmem_relinquish_alloc_permit();
+    }
   }
   tc::fence_before_thread_sync();
   __syncthreads();
@@ -235,37 +258,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------------------------------------------------------- TMA loader
+    // ---------------------------------------------------------------- TMA loader (every CTA)
     int64_t issued = 0;
     uint32_t stage = 0, phase = 0;
-    for (int64_t tile = blockIdx.x; tile < p.n_tiles && !*abort; tile += gridDim.x) {
-      int32_t mb, nb;
-      tile_coords(p, tile, mb, nb);
+    for (int64_t tile = unit; tile < p.n_tiles && !*abort; tile += n_units) {
+      int32_t mt, nb;
+      tile_coords(p, C::kGroup, tile, mt, nb);
+      const int32_t row0 = mt * C::kTileM + (int32_t)rank * kBM;
+      const int32_t brow0 = nb * kBN + (int32_t)rank * C::kBRows;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (!tc::mbar_wait(empty(stage), phase ^ 1u, abort)) {
           raise_timeout(abort);
           break;
         }
-        tc::mbar_arrive_expect_tx(full(stage), kStageBytes);
-        const uint32_t a_dst = base + stage * kStageBytes;
-        tc::tma_load_2d(a_dst, &tmA, full(stage), kb * kBK, mb * kBM);
-        tc::tma_load_2d(a_dst + kABytes, &tmB, full(stage), kb * kBK, nb * kBN);
+        const uint32_t a_dst = base + stage * C::kStageBytes;
+        if (PAIR) {
+          const uint32_t fb = tc::map_to_rank(full(stage), 0);
+          if (leader) tc::mbar_arrive_expect_tx(full(stage), C::kTxBytes);
+          tc::tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, row0);
+          tc::tma_load_2d_pair(a_dst + kABytes, &tmB, fb, kb * kBK, brow0);
+        } else {
+          tc::mbar_arrive_expect_tx(full(stage), C::kTxBytes);
+          tc::tma_load_2d(a_dst, &tmA, full(stage), kb * kBK, row0);
+          tc::tma_load_2d(a_dst + kABytes, &tmB, full(stage), kb * kBK, brow0);
+        }
         ++issued;
-        if (++stage == kStages) {
+        if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    // no copy may still be landing in shared memory when the CTA exits: wait for the last ones
-    for (int64_t i = issued - (issued < kStages ? issued : kStages); i < issued; ++i)
-      if (!tc::mbar_wait(full((uint32_t)(i % kStages)), (uint32_t)((i / kStages) & 1), nullptr))
+    // No copy may still be landing in shared memory when the CTA exits. A CTA of a pair counts its
+    // loads on the leader's barriers, so it waits for the MMAs that read its last loads instead
+    // (which implies they landed); a lone CTA waits for the loads themselves.
+    for (int64_t i = issued - (issued < C::kStages ? issued : C::kStages); i < issued; ++i) {
+      const uint32_t s = (uint32_t)(i % C::kStages), ph = (uint32_t)((i / C::kStages) & 1);
+      if (!tc::mbar_wait(PAIR ? empty(s) : full(s), ph, nullptr))
         atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------------------------------------------------------- MMA issuer (the leader)
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
-    for (int64_t tile = blockIdx.x; ok && tile < p.n_tiles && !*abort; tile += gridDim.x) {
+    for (int64_t tile = unit; ok && tile < p.n_tiles && !*abort; tile += n_units) {
       if (!tc::mbar_wait(acc_empty(acc), acc_phase ^ 1u, abort)) {
         raise_timeout(abort);
         break;
@@ -279,38 +315,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc::fence_after_thread_sync();
-        const uint32_t a0 = base + stage * kStageBytes, b0 = a0 + kABytes;
+        const uint32_t a0 = base + stage * C::kStageBytes, b0 = a0 + kABytes;
 #pragma unroll
-        for (int k = 0; k < kBK / kUmmaK; ++k)
-          tc::mma_bf16(d, tc::sw128_kmajor_desc(a0 + 2 * kUmmaK * k), tc::sw128_kmajor_desc(b0 + 2 * kUmmaK * k),
-                       kIdesc, (kb | k) != 0 ? 1u : 0u);
-        tc::commit(empty(stage));  // the stage returns to the loader once these MMAs have read it
-        if (++stage == kStages) {
+        for (int k = 0; k < kBK / kUmmaK; ++k) {
+          const uint64_t ad = tc::sw128_kmajor_desc(a0 + 2 * kUmmaK * k);
+          const uint64_t bd = tc::sw128_kmajor_desc(b0 + 2 * kUmmaK * k);
+          if (PAIR)
+            tc::mma_bf16_pair(d, ad, bd, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+          else
+            tc::mma_bf16(d, ad, bd, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        // the stage returns to the loaders once these MMAs have read it
+        if (PAIR)
+          tc::commit_pair_multicast(empty(stage), 3);
+        else
+          tc::commit(empty(stage));
+        if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (!ok) break;
-      tc::commit(acc_full(acc));  // the tile's accumulator is complete once every MMA above is
+      // the tile's accumulators are complete once every MMA above is
+      if (PAIR)
+        tc::commit_pair_multicast(acc_full(acc), 3);
+      else
+        tc::commit(acc_full(acc));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
     }
     // every MMA this thread issued has completed before tensor memory is freed
-    tc::commit(drain);
+    if (PAIR)
+      tc::commit_pair_multicast(drain, 1);
+    else
+      tc::commit(drain);
     if (!tc::mbar_wait(drain, 0, nullptr)) atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
   } else if (warp >= 2) {
-    // ---------------------------------------------------------------- epilogue
+    // ---------------------------------------------------------------- epilogue (every CTA)
     const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
     uint32_t acc = 0, acc_phase = 0;
-    for (int64_t tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x) {
-      int32_t mb, nb;
-      tile_coords(p, tile, mb, nb);
+    for (int64_t tile = unit; tile < p.n_tiles; tile += n_units) {
+      int32_t mt, nb;
+      tile_coords(p, C::kGroup, tile, mt, nb);
       if (!warp_wait(acc_full(acc), acc_phase, abort)) break;
       tc::fence_after_thread_sync();
       const int r = quarter * 32 + lane;
-      const int64_t row = (int64_t)mb * kBM + r;
+      const int64_t mb = (int64_t)mt * (C::kTileM / kBM) + rank;  // this CTA's block of 128 rows
+      const int64_t row = mb * kBM + r;
       const bool row_ok = row < p.T;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols;
       const int col0 = nb * kBN;
@@ -323,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float sums[3];
           gate_tile_row(taddr, row_ok ? p.x + (row * p.hc + i) * p.dim + j0 : nullptr, p.qw + i * p.dim + j0,
                         p.kw + i * p.dim + j0, sums);
-          float* dst = p.part + ((int64_t)mb * (key_cols / kBN) + nb) * 3 * kBM + r;
+          float* dst = p.part + (mb * (key_cols / kBN) + nb) * 3 * kBM + r;
           dst[0] = sums[0];
           dst[kBM] = sums[1];
           dst[2 * kBM] = sums[2];
@@ -333,7 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_before_thread_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(acc_empty(acc));
+      if (lane == 0) {
+        if (PAIR)
+          tc::mbar_arrive_cluster(tc::map_to_rank(acc_empty(acc), 0));
+        else
+          tc::mbar_arrive(acc_empty(acc));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -343,10 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   tc::fence_before_thread_sync();
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still signal its barriers or read its memory
+  if (PAIR) tc::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc::fence_after_thread_sync();
-    tc::tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR)
+      tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tc::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -392,19 +455,10 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EPI>
-cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, emb, (uint64_t)p.T, (uint64_t)p.K, kBM) || !make_map(&tb, w, (uint64_t)p.N, (uint64_t)p.K, kBN))
-    return cudaErrorInvalidValue;
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(proj_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int64_t grid = p.n_tiles < sms ? p.n_tiles : sms;
-  return launch_pdl(proj_kernel<EPI>, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, s, ta, tb, p);
-}
+#ifndef ENGRAM_PROJ_PAIR
+#define ENGRAM_PROJ_PAIR 1
+#endif
+constexpr bool kPair = ENGRAM_PROJ_PAIR != 0;  // CTA pairs (M = 256 MMAs) unless built otherwise
 
 ProjParams base_params(int64_t T, int32_t K, int32_t N) {
   ProjParams p = {};
@@ -412,10 +466,51 @@ ProjParams base_params(int64_t T, int32_t K, int32_t N) {
   p.K = K;
   p.N = N;
   p.num_kb = (K + kBK - 1) / kBK;
-  p.n_mblk = (int32_t)((T + kBM - 1) / kBM);
+  p.n_mtile = (int32_t)((T + Cfg<kPair>::kTileM - 1) / Cfg<kPair>::kTileM);
   p.n_nblk = (N + kBN - 1) / kBN;
-  p.n_tiles = (int64_t)p.n_mblk * p.n_nblk;
+  p.n_tiles = (int64_t)p.n_mtile * p.n_nblk;
   return p;
+}
+
+// one persistent CTA (or CTA pair) per SM (pair of SMs) that can be resident at once, launched as a
+// programmatic dependent like every kernel of the library
+template <int EPI>
+cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
+  using C = Cfg<kPair>;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, emb, (uint64_t)p.T, (uint64_t)p.K, kBM) ||
+      !make_map(&tb, w, (uint64_t)p.N, (uint64_t)p.K, (uint32_t)C::kBRows))
+    return cudaErrorInvalidValue;
+  auto kern = proj_kernel<EPI, kPair>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = ENGRAM_PDL;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kPair ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  int units = 0;
+  if (kPair) {
+    cfg.gridDim = dim3(2);
+    e = cudaOccupancyMaxActiveClusters(&units, kern, &cfg);
+  } else {
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&units, cudaDevAttrMultiProcessorCount, dev);
+  }
+  if (e != cudaSuccess) return e;
+  if (units < 1) return cudaErrorInvalidConfiguration;
+  const int64_t n = p.n_tiles < units ? p.n_tiles : units;
+  cfg.gridDim = dim3((unsigned)(n * (kPair ? 2 : 1)));
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
 }
 
 }  // namespace
@@ -428,7 +523,9 @@ cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, in
 }
 
 int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim) {
-  return ((T + kBM - 1) / kBM) * (int64_t)(hc * dim / kBN) * 3 * kBM;
+  // whole (cluster) tiles: the second CTA of a pair's last tile writes its block even past T
+  const int64_t tiles = (T + Cfg<kPair>::kTileM - 1) / Cfg<kPair>::kTileM;
+  return tiles * (Cfg<kPair>::kTileM / kBM) * (int64_t)(hc * dim / kBN) * 3 * kBM;
 }
 
 cudaError_t launch_project_gate_sums(const uint16_t* x, const uint16_t* emb, const uint16_t* wkv, const uint16_t* qw,

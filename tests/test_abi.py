@@ -136,7 +136,8 @@ def test_projection_checks_need_no_gpu(lib):
     assert lib.engram_project(None, a, 5, 64, 64, a, None) == geng.ERR_INVALID
     assert lib.engram_project(P(4098), a, 5, 64, 64, a, None) == geng.ERR_INVALID  # misaligned
     # workspace: value rows (T x dim bf16) + 3 partial sums per (128-token block, key tile, token)
-    assert lib.engram_project_gate_workspace(128, 4, 256) == 128 * 256 * 2 + 4 * 3 * 128 * 4
+    # partial sums are kept for whole 256-row tiles (a pair of 128-row blocks)
+    assert lib.engram_project_gate_workspace(128, 4, 256) == 128 * 256 * 2 + 2 * 4 * 3 * 128 * 4
     assert lib.engram_project_gate_workspace(129, 4, 5120) == (129 * 5120 * 2 + 255) // 256 * 256 + 2 * 80 * 3 * 128 * 4
     assert lib.engram_project_gate_workspace(0, 4, 256) == 0
     assert lib.engram_project_gate_workspace(8, 3, 256) == 0 and lib.engram_project_gate_workspace(8, 4, 200) == 0
