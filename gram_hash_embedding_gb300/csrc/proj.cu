@@ -165,25 +165,29 @@ __device__ __forceinline__ void store_tile_row(uint32_t taddr, uint16_t* dst, in
 // Gate sums of one key tile over its 256 columns for this thread's row: the key values are the
 // accumulators rounded to bf16 (the projection's output type); h, q_weight and k_weight are bf16.
 // sums[0] = sum h^2, sums[1] = sum k^2, sums[2] = sum h * (q_weight * k_weight) * k, in fp32.
+// h streams from memory (it was prefetched into L2 a tile earlier); two 32-column chunks of it are
+// in flight in registers while a third is reduced.
+__device__ __forceinline__ void load_h_chunk(uint4 (&d)[4], const uint16_t* hrow, int c) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) d[g] = hrow != nullptr ? ld_nc_v4(hrow + 32 * c + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
+}
+
 __device__ __forceinline__ void gate_tile_row(uint32_t taddr, const uint16_t* hrow, const uint16_t* qrow,
                                               const uint16_t* wrow, float (&sums)[3]) {
+  constexpr int kChunks = kAccCols / 32;
   float sh = 0.f, sk = 0.f, sd = 0.f;
-  uint4 hb[4], hn[4];
-#pragma unroll
-  for (int g = 0; g < 4; ++g) hb[g] = hrow != nullptr ? ld_nc_v4(hrow + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
+  uint4 h0[4], h1[4], h2[4];
+  load_h_chunk(h0, hrow, 0);
+  load_h_chunk(h1, hrow, 1);
 #pragma unroll 1
-  for (int c = 0; c < kAccCols / 32; ++c) {
-    if (c + 1 < kAccCols / 32) {  // the next chunk's h is in flight while this chunk is reduced
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-        hn[g] = hrow != nullptr ? ld_nc_v4(hrow + 32 * (c + 1) + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
-    }
+  for (int c = 0; c < kChunks; ++c) {
+    if (c + 2 < kChunks) load_h_chunk(h2, hrow, c + 2);
     float v[32];
     tc::tmem_load_32cols(taddr + 32 * c, v);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       float h[8], q[8], w[8], k[8];
-      bf16x8_to_f32(hb[g], h);
+      bf16x8_to_f32(h0[g], h);
       bf16x8_to_f32(ld_nc_v4(qrow + 32 * c + 8 * g), q);  // the same for every row: L1 hits
       bf16x8_to_f32(ld_nc_v4(wrow + 32 * c + 8 * g), w);
       bf16x8_to_f32(pack8(v + 8 * g), k);                    // round the keys to bf16
@@ -195,11 +199,22 @@ __device__ __forceinline__ void gate_tile_row(uint32_t taddr, const uint16_t* hr
       }
     }
 #pragma unroll
-    for (int g = 0; g < 4; ++g) hb[g] = hn[g];
+    for (int g = 0; g < 4; ++g) {
+      h0[g] = h1[g];
+      h1[g] = h2[g];
+    }
   }
   sums[0] = sh;
   sums[1] = sk;
   sums[2] = sd;
+}
+
+// the row of h that this thread's row of a key tile reads (null: a value tile or a row past T)
+__device__ __forceinline__ const uint16_t* h_row(const ProjParams& p, int64_t row, int col0) {
+  const int key_cols = p.hc * p.dim;
+  if (col0 >= key_cols || row >= p.T) return nullptr;
+  const int i = col0 / p.dim;
+  return p.x + (row * p.hc + i) * p.dim + (col0 - i * p.dim);
 }
 
 template <int EPI, bool PAIR>
@@ -355,13 +370,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue (every CTA)
     const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
+    const int r = quarter * 32 + lane;
     uint32_t acc = 0, acc_phase = 0;
+    // the gate epilogue reads h: each thread prefetches its row of the next key tile into L2 one tile ahead
+    auto prefetch_h = [&](int64_t t) {
+      if (EPI != EPI_GATE || t >= p.n_tiles) return;
+      int32_t pm, pn;
+      tile_coords(p, C::kGroup, t, pm, pn);
+      const uint16_t* hr = h_row(p, ((int64_t)pm * (C::kTileM / kBM) + rank) * kBM + r, pn * kBN);
+      if (hr != nullptr) tc::prefetch_l2_bulk(hr, kBN * 2);
+    };
+    prefetch_h(unit);
     for (int64_t tile = unit; tile < p.n_tiles; tile += n_units) {
       int32_t mt, nb;
       tile_coords(p, C::kGroup, tile, mt, nb);
       if (!warp_wait(acc_full(acc), acc_phase, abort)) break;
       tc::fence_after_thread_sync();
-      const int r = quarter * 32 + lane;
+      prefetch_h(tile + n_units);
       const int64_t mb = (int64_t)mt * (C::kTileM / kBM) + rank;  // this CTA's block of 128 rows
       const int64_t row = mb * kBM + r;
       const bool row_ok = row < p.T;
@@ -374,8 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (col0 < key_cols) {
           const int i = col0 / p.dim, j0 = col0 - i * p.dim;
           float sums[3];
-          gate_tile_row(taddr, row_ok ? p.x + (row * p.hc + i) * p.dim + j0 : nullptr, p.qw + i * p.dim + j0,
-                        p.kw + i * p.dim + j0, sums);
+          gate_tile_row(taddr, h_row(p, row, col0), p.qw + i * p.dim + j0, p.kw + i * p.dim + j0, sums);
           float* dst = p.part + (mb * (key_cols / kBN) + nb) * 3 * kBM + r;
           dst[0] = sums[0];
           dst[kBM] = sums[1];
