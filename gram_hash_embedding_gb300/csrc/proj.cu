@@ -46,6 +46,9 @@ constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
 constexpr uint32_t kABytes = kBM * kBK * 2;
+#ifndef ENGRAM_PROJ_GROUP
+#define ENGRAM_PROJ_GROUP 8  // 256-row blocks per tile group
+#endif
 
 // PAIR = false: one CTA computes a 128 x 256 tile with M = 128 MMAs (4 stages of A + all of B, 48 KB).
 // PAIR = true: a cluster of two CTAs computes a 256 x 256 tile with M = 256 pair MMAs issued by the
@@ -59,7 +62,7 @@ struct Cfg {
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTxBytes = PAIR ? 2 * kStageBytes : kStageBytes;  // per stage, both CTAs
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;          // rows of one (cluster) tile
-  static constexpr int kGroup = PAIR ? 8 : 16;                 // tile rows per group: 16 row blocks of 128
+  static constexpr int kGroup = (PAIR ? 1 : 2) * ENGRAM_PROJ_GROUP;  // tile rows per group (in 256-row units)
   static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kBN);
   // shared memory: the stage ring (1024-byte aligned), then barriers and two words
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
