@@ -57,7 +57,11 @@ def parse_args(argv=None):
                         "lookup: engram_lookup alone on the workload's row ids, one launch per layer")
     p.add_argument("--block", action="store_true",
                    help="time the whole Engram block per step: hash + lookup, then per layer the wkv projection "
-                        "(cuBLAS bf16 GEMM) and the gate kernel, at the released width (dim 5120, 4 copies)")
+                        "and the gate, at the released width (dim 5120, 4 copies)")
+    p.add_argument("--proj", choices=["fused", "tcgen05", "cublas"], default="fused",
+                   help="--block: fused = engram_project_gate (tensor-core projection with the gate's sums in its "
+                        "epilogue, keys never written, then the gate's finishing pass); tcgen05 = engram_project "
+                        "then engram_gate; cublas = torch.matmul (cuBLAS) then engram_gate")
     p.add_argument("--graph", action="store_true",
                    help="capture the steps in a CUDA graph and replay it (removes host launch overhead; for the "
                         "small decode / chunk launches)")
@@ -907,7 +911,7 @@ def run_ours(args):
 # ----------------------------------------------------------------------------- the whole Engram block
 def run_block(args):
     """Engram block per step on workload args.cfg: the fused hash + lookup, then for each engram layer
-    kv = rows @ wkv^T (a plain cuBLAS bf16 GEMM) and the gate kernel (in place on the residual copies).
+    the wkv projection and the gate (in place on the residual copies), by the path --proj names.
     Weights are seeded synthetic values; dims are the released model's (dim 5120, hc_mult 4)."""
     import numpy as np
     import torch
@@ -933,10 +937,15 @@ def run_block(args):
     qw = [torch.rand((hc, dim), generator=g).add_(0.5).to(torch.bfloat16).to(device) for _ in range(lay.n_layers)]
     kw = [torch.rand((hc, dim), generator=g).add_(0.5).to(torch.bfloat16).to(device) for _ in range(lay.n_layers)]
     x = torch.randn((T, hc, dim), generator=g).to(torch.bfloat16).to(device)
-    kv = torch.empty((T, dim * (hc + 1)), dtype=torch.bfloat16, device=device)
+    kv = None if args.proj == "fused" else torch.empty((T, dim * (hc + 1)), dtype=torch.bfloat16, device=device)
+    ws = (torch.empty(geng.engram_project_gate_workspace(T, hc, dim), dtype=torch.uint8, device=device)
+          if args.proj == "fused" else None)
     mask = None if runner.masks[0] is None else runner.masks[0].reshape(-1)
     stream = torch.cuda.current_stream(device)
-    names = ["hash+lookup"] + [f"{n}{l}" for l in range(lay.n_layers) for n in ("wkv", "gate")]
+    if args.proj == "fused":
+        names = ["hash+lookup"] + [f"wkv+gate{l}" for l in range(lay.n_layers)]
+    else:
+        names = ["hash+lookup"] + [f"{n}{l}" for l in range(lay.n_layers) for n in ("wkv", "gate")]
 
     def step(k, ev=None):
         if ev is not None:
@@ -946,7 +955,15 @@ def run_block(args):
         for l in range(lay.n_layers):
             if ev is not None:
                 ev[i].record(stream)
-            torch.matmul(runner.out[l].view(T, K), wkv[l].t(), out=kv)
+            emb = runner.out[l].view(T, K)
+            if args.proj == "fused":
+                geng.engram_project_gate(x, emb, wkv[l], qw[l], kw[l], mask, workspace=ws, out=x)
+                i += 1
+                continue
+            if args.proj == "tcgen05":
+                geng.engram_project(emb, wkv[l], out=kv)
+            else:
+                torch.matmul(emb, wkv[l].t(), out=kv)
             if ev is not None:
                 ev[i + 1].record(stream)
             geng.engram_gate(x, kv, qw[l], kw[l], mask, out=x)
@@ -961,11 +978,14 @@ def run_block(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K_steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
     t0.record(stream)
     for k in range(K_steps):
         step(k, evs[k])
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks.stop()
     total = t0.elapsed_time(t1) / 1e3
     comp = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) * 1e3 for i, n in enumerate(names)}
     peak_hbm, _ = measured_peaks()
@@ -976,10 +996,18 @@ def run_block(args):
     lookup_bytes = T * algo_bytes_per_token(lay)
     roof = {"hash+lookup": {"bound": "hbm", "achieved": lookup_bytes / comp["hash+lookup"] / 1e3, "peak": peak_hbm,
                             "unit": "GB/s"}}
+    proj_kernel = {"fused": "engram_project_gate: tcgen05 projection (CTA pairs) with the gate's sums in its "
+                            "epilogue + the gate's finishing pass",
+                   "tcgen05": "engram_project: tcgen05 projection (CTA pairs)",
+                   "cublas": "cuBLAS bf16 GEMM (library)"}[args.proj]
     for l in range(lay.n_layers):
+        if args.proj == "fused":
+            roof[f"wkv+gate{l}"] = {"bound": "tensor", "achieved": gemm_flops / comp[f"wkv+gate{l}"] / 1e6,
+                                    "peak": float(peaks["bf16_tflops_sustained"]), "unit": "TFLOP/s",
+                                    "kernel": proj_kernel}
+            continue
         roof[f"wkv{l}"] = {"bound": "tensor", "achieved": gemm_flops / comp[f"wkv{l}"] / 1e6,
-                           "peak": float(peaks["bf16_tflops_sustained"]), "unit": "TFLOP/s",
-                           "kernel": "cuBLAS bf16 GEMM (library)"}
+                           "peak": float(peaks["bf16_tflops_sustained"]), "unit": "TFLOP/s", "kernel": proj_kernel}
         roof[f"gate{l}"] = {"bound": "hbm", "achieved": gate_bytes / comp[f"gate{l}"] / 1e3, "peak": peak_hbm,
                             "unit": "GB/s"}
     for r in roof.values():
@@ -989,9 +1017,13 @@ def run_block(args):
         "value": T * K_steps / total, "unit": "tokens/s", "n_gpus": 1, "steps": K_steps,
         "ms_per_step": total / K_steps * 1e3, "higher_is_better": True, "dtype": "bf16/f32", "data": "synthetic",
         "config": {"workload": runner.wl.name, "dim": dim, "hc_mult": hc, "wkv": [dim * (hc + 1), K],
+                   "projection": args.proj,
                    "l2_fetch_granularity": (f"{args.l2_fetch} B (context default {l2_default} B)" if args.l2_fetch
                                             else "context default")},
-        "component_us": comp, "roofline": roof,
+        "component_us": comp, "roofline": roof, "clocks": clocks.summary(),
+        # ours per step: the fused hash + lookup, and per layer projection + finishing pass (fused), projection +
+        # gate (tcgen05), or the gate alone (cublas: the projection is cuBLAS's)
+        "gpu_launches": K_steps * (runner.launches_per_step + lay.n_layers * (2 if args.proj != "cublas" else 1)),
     }
     print(json.dumps(line), flush=True)
 

@@ -8,7 +8,8 @@ covers the rounding. The gate itself comes from fp32 sums over dim terms (relati
 case (|dot| at the 1e-6 clamp, where d gate / d dot peaks at ~125), hence + 1e-3 |value|. Masked
 tokens must come out bit-exact (h + 0 * value = h). For the whole block the projection is a
 cuBLAS bf16 GEMM (fp32 accumulation, bf16 output) against an exact float64 sum rounded once: one
-bf16 ulp (2^-8 relative) on a key or the value, so the bound widens to 2^-7 (|out64| + |value|).
+bf16 ulp (2^-8 relative) on a key or the value, so the bound widens to 2^-7 (|out64| + |value|); the
+same holds for the library's tensor-core projection, alone or with the gate fused into it.
 """
 import numpy as np
 import pytest
@@ -85,9 +86,12 @@ def test_gate_in_place_and_errors():
                             _dev_bf16(_bf16(np.ones((4, 16)))), _dev_bf16(_bf16(np.ones((4, 16))))).shape == (0, 4, 16)
 
 
-def test_engram_block_end_to_end():
-    """ids -> fused hash + lookup (this library) -> wkv projection (cuBLAS bf16 GEMM) -> gate (this
-    library), for both engram layers of the prefill layout, against the oracle chain."""
+@pytest.mark.parametrize("proj", ["fused", "tcgen05", "cublas"])
+def test_engram_block_end_to_end(proj):
+    """ids -> fused hash + lookup (this library) -> wkv projection -> gate, for both engram layers of
+    the prefill layout, against the oracle chain. The projection and gate run as one fused call
+    (engram_project_gate: the tensor-core projection with the gate's sums in its epilogue), as the
+    library's projection followed by its gate, or as a cuBLAS GEMM followed by the gate."""
     wl = synth.make_workload(1)
     lay = wl.layout
     B, L = 2, 64
@@ -100,7 +104,6 @@ def test_engram_block_end_to_end():
     exp_h, _ = orc.hash(ids, 0, mask)
     # only the rows this test touches are materialised (compact tables, indices remapped)
     rng = np.random.default_rng(5)
-    outs_expected = []
     for l in range(2):
         flat = exp_h[:, :, l, :].reshape(-1)
         uniq, inv = np.unique(flat, return_inverse=True)
@@ -115,13 +118,16 @@ def test_engram_block_end_to_end():
         emb.append(geng.engram_lookup(idx.reshape(-1), Ws[l], Ss[l], lay.block).view(B * L, lay.n_cols * lay.head_dim))
     K = lay.n_cols * lay.head_dim
     x = _bf16(rng.standard_normal((B * L, hc, dim)))
+    md = torch.from_numpy(mask.reshape(-1)).cuda()
     for l in range(2):
         wkv = _bf16(rng.standard_normal((dim * (hc + 1), K)) * K ** -0.5)
         qw = _bf16(rng.uniform(0.5, 1.5, (hc, dim)))
         kw = _bf16(rng.uniform(0.5, 1.5, (hc, dim)))
-        kv = emb[l] @ _dev_bf16(wkv).t()  # the projection: a plain library GEMM
-        out = geng.engram_gate(_dev_bf16(x), kv.contiguous(), _dev_bf16(qw), _dev_bf16(kw),
-                               torch.from_numpy(mask.reshape(-1)).cuda())
+        if proj == "fused":
+            out = geng.engram_project_gate(_dev_bf16(x), emb[l], _dev_bf16(wkv), _dev_bf16(qw), _dev_bf16(kw), md)
+        else:
+            kv = geng.engram_project(emb[l], _dev_bf16(wkv)) if proj == "tcgen05" else emb[l] @ _dev_bf16(wkv).t()
+            out = geng.engram_gate(_dev_bf16(x), kv.contiguous(), _dev_bf16(qw), _dev_bf16(kw), md)
         got = out.view(torch.int16).cpu().numpy().view(np.uint16)
         # oracle chain: lookup rows (bit-exact against the kernel), exact projection, float64 gate
         rows = oracle.engram_lookup(rows_needed[l].reshape(-1), synth.table_rows(wl.table_seed, l, np.unique(exp_h[:, :, l, :]), lay.head_dim),
@@ -131,4 +137,4 @@ def test_engram_block_end_to_end():
         kv64 = oracle.engram_linear(rows, wkv)
         exp = oracle.engram_gate(x, kv64, qw, kw, mask.reshape(-1))
         value = oracle.bf16_bits_to_f64(kv64).reshape(B * L, hc + 1, dim)[:, hc:hc + 1, :].repeat(hc, 1)
-        _check(got, exp, value, 2.0 ** -7, 2.0 ** -7, f"engram block layer {l}")
+        _check(got, exp, value, 2.0 ** -7, 2.0 ** -7, f"engram block layer {l} ({proj})")
