@@ -29,7 +29,8 @@ __all__ = [
     "engram_hash_lookup_varlen", "engram_gate", "PreparedHashLookup", "engram_strerror", "STATUS_BAD_START",
     "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "STATUS_CHECK", "SCALE_F32", "SCALE_BF16", "SCALE_E8M0", "SCALE_E4M3",
     "library_path", "set_l2_fetch_granularity", "engram_project", "engram_project_gate",
-    "engram_project_gate_workspace", "engram_device_status", "STATUS_TIMEOUT",
+    "engram_project_gate_workspace", "engram_device_status", "STATUS_TIMEOUT", "engram_shard_pack",
+    "engram_shard_unpack", "shard_part", "sharded_lookup", "dist_exchange",
 ]
 
 OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
@@ -94,13 +95,17 @@ def _lib():
         L.engram_project_gate.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, ctypes.c_float, _P,
                                           ctypes.c_uint64, _P, _P]
         L.engram_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+        L.engram_shard_pack_workspace.argtypes = [_I64, _I32]
+        L.engram_shard_pack_workspace.restype = ctypes.c_uint64
+        L.engram_shard_pack.argtypes = [_P, _I64, _I64, _I32, _P, _P, _P, _P, ctypes.c_uint64, _P]
+        L.engram_shard_unpack.argtypes = [_P, _P, _I64, _I64, _I32, _P, _P]
         L.engram_strerror.argtypes = [ctypes.c_int]
         L.engram_set_l2_fetch_granularity.argtypes = [_I32, ctypes.POINTER(_I32)]
         L.engram_strerror.restype = ctypes.c_char_p
         for name in ("engram_state_create", "engram_state_destroy", "engram_cache_reset", "engram_state_status",
                      "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout",
                      "engram_hash_varlen", "engram_hash_lookup_varlen", "engram_gate", "engram_project",
-                     "engram_project_gate", "engram_device_status"):
+                     "engram_project_gate", "engram_device_status", "engram_shard_pack", "engram_shard_unpack"):
             getattr(L, name).restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -509,6 +514,96 @@ def engram_device_status(clear: bool = True, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(_lib().engram_device_status(_stream(stream), ctypes.byref(v), int(bool(clear))), "engram_device_status")
     return v.value
+
+
+def shard_part(rows: int, world: int) -> int:
+    """Rows per rank of a table split over `world` ranks, as `ParallelEngramEmbedding` splits it:
+    rank r holds rows [r * part, (r + 1) * part)."""
+    return -(-int(rows) // int(world))
+
+
+def engram_shard_pack(idx: torch.Tensor, rows: int, world: int, stream=None):
+    """Group the indices of one lookup by the rank that owns their row. Returns (counts int64
+    [world + 1], local_rows int64 [n], positions int64 [n]): bucket r = rank r's rows as rows of its
+    shard, then the indices no rank owns; each bucket in index order; positions index into idx."""
+    n = idx.numel()
+    dev = idx.device
+    counts = torch.zeros(world + 1, dtype=torch.int64, device=dev)
+    local_rows = torch.empty(n, dtype=torch.int64, device=dev)
+    positions = torch.empty(n, dtype=torch.int64, device=dev)
+    ws = torch.empty(max(int(_lib().engram_shard_pack_workspace(n, int(world))), 16), dtype=torch.uint8, device=dev)
+    _check(_lib().engram_shard_pack(_dev(idx, torch.int64, "idx"), n, int(rows), int(world), counts.data_ptr(),
+                                    local_rows.data_ptr(), positions.data_ptr(), ws.data_ptr(), ws.numel(),
+                                    _launch_stream(stream, (counts, local_rows, positions, ws))), "engram_shard_pack")
+    return counts, local_rows, positions
+
+
+def engram_shard_unpack(rows: torch.Tensor, positions: torch.Tensor, m: int, head_dim: int,
+                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[positions[i]] = rows[i] for i < m, +0 rows at positions[m:] (the unowned indices).
+    rows bf16 [m, head_dim]; returns (or fills) bf16 [n, head_dim]."""
+    n = positions.numel()
+    temps = []
+    if out is None:
+        out = torch.empty((n, head_dim), dtype=torch.bfloat16, device=positions.device)
+        temps.append(out)
+    _size(out, n * head_dim, "out")
+    _size(rows, int(m) * head_dim, "rows")
+    rp = _dev(rows, torch.bfloat16, "rows") if int(m) > 0 else None
+    _check(_lib().engram_shard_unpack(rp, _dev(positions, torch.int64, "positions"), int(m), n, int(head_dim),
+                                      _dev(out, torch.bfloat16, "out"), _launch_stream(stream, temps)),
+           "engram_shard_unpack")
+    return out
+
+
+def dist_exchange(group=None):
+    """The all-to-all of sharded_lookup over a torch.distributed process group (NCCL on GPUs):
+    exchange(t, send_splits, recv_splits) sends t's first send_splits[0] rows to rank 0, the next
+    send_splits[1] to rank 1, ..., and returns the rows received, rank 0's first."""
+    import torch.distributed as dist
+
+    def exchange(t: torch.Tensor, send_splits, recv_splits) -> torch.Tensor:
+        # moved as raw bytes (row = dim 0): any element type travels, on every backend
+        rest = tuple(t.shape[1:])
+        row_bytes = t.element_size() * int(torch.tensor(rest).prod()) if rest else t.element_size()
+        if t.numel() == 0:
+            b = torch.empty((t.shape[0], row_bytes), dtype=torch.uint8, device=t.device)
+        else:
+            b = t.contiguous().view(torch.uint8).reshape(t.shape[0], row_bytes)
+        out = torch.empty((int(sum(recv_splits)), row_bytes), dtype=torch.uint8, device=t.device)
+        dist.all_to_all_single(out, b, [int(c) for c in recv_splits], [int(c) for c in send_splits], group=group)
+        return out.view(t.dtype).reshape((out.shape[0],) + rest)
+
+    return exchange
+
+
+def sharded_lookup(idx: torch.Tensor, W_shard: torch.Tensor, S_shard: torch.Tensor, rows: int, block: int,
+                   world: int, exchange, scale_dtype: int | None = None, ops=None) -> torch.Tensor:
+    """One rank's part of a row-sharded lookup (engram-first/lookup page, `ParallelEngramEmbedding`,
+    world > 1): this rank holds rows [rank * part, ...) of a table of `rows` rows (W_shard, S_shard:
+    its shard_part(rows, world) rows, fewer for the last rank) and looks up its own indices idx [n].
+    Instead of looking every index up locally, zeroing foreign rows and all-reducing, each request
+    goes to the rank that owns its row and only that row comes back:
+      pack by owner -> exchange the counts -> exchange the row ids -> look them up in the shard ->
+      exchange the rows back -> unpack (+0 rows where no rank owns the index).
+    `exchange(t, send_splits, recv_splits)` is the all-to-all (dist_exchange(group) over NCCL).
+    `ops` replaces the device steps (pack, lookup, unpack) with others of the same contract; the
+    library's kernels when None. Returns bf16 [n, head_dim], equal to engram_lookup on the whole table."""
+    if ops is None:
+        ops = (engram_shard_pack,
+               lambda r, W, S: engram_lookup(r, W, S, block, scale_dtype=scale_dtype),
+               engram_shard_unpack)
+    pack, lookup, unpack = ops
+    D = W_shard.shape[1]
+    n = idx.numel()
+    counts, local_rows, positions = pack(idx.reshape(-1), rows, world)
+    send = [int(c) for c in counts[:world].cpu()]  # split sizes are host values for the exchange
+    m = sum(send)
+    recv = [int(c) for c in exchange(counts[:world].reshape(world, 1), [1] * world, [1] * world).reshape(-1).cpu()]
+    wanted = exchange(local_rows[:m], send, recv)          # row ids other ranks want from this shard
+    found = lookup(wanted, W_shard, S_shard).reshape(-1, D)  # this shard's rows for them
+    back = exchange(found, recv, send)                      # this rank's rows, in packed order
+    return unpack(back, positions, m, D).reshape(tuple(idx.shape) + (D,))
 
 
 class PreparedHashLookup:

@@ -410,6 +410,39 @@ int engram_device_status(engram_stream_t stream, uint32_t* flags, int clear) {
   return ENGRAM_OK;
 }
 
+uint64_t engram_shard_pack_workspace(int64_t n, int32_t world) {
+  if (n <= 0 || world < 1 || world > ENGRAM_MAX_SHARDS) return 0;
+  return round256((uint64_t)engram::shard_pack_segments(n) * (uint64_t)(world + 1) * sizeof(int32_t));
+}
+
+int engram_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
+                      int64_t* local_rows, int64_t* positions, void* workspace, uint64_t workspace_bytes,
+                      engram_stream_t stream) {
+  if (n < 0 || rows < 0) return ENGRAM_ERR_INVALID;
+  if (world < 1 || world > ENGRAM_MAX_SHARDS) return ENGRAM_ERR_UNSUPPORTED;
+  if (n == 0) return ENGRAM_OK;
+  if (n > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
+  if (idx == nullptr || counts == nullptr || local_rows == nullptr || positions == nullptr || workspace == nullptr)
+    return ENGRAM_ERR_INVALID;
+  if (!aligned(idx, 8) || !aligned(counts, 8) || !aligned(local_rows, 8) || !aligned(positions, 8) ||
+      !aligned(workspace, 16))
+    return ENGRAM_ERR_INVALID;
+  if (workspace_bytes < engram_shard_pack_workspace(n, world)) return ENGRAM_ERR_INVALID;
+  return launch_rc(engram::launch_shard_pack(idx, n, rows, world, counts, local_rows, positions,
+                                             static_cast<int32_t*>(workspace), (cudaStream_t)stream));
+}
+
+int engram_shard_unpack(const uint16_t* rows, const int64_t* positions, int64_t m, int64_t n, int32_t head_dim,
+                        uint16_t* out, engram_stream_t stream) {
+  if (n < 0 || m < 0 || m > n) return ENGRAM_ERR_INVALID;
+  if (head_dim < 8 || head_dim % 8 != 0 || head_dim > 65536) return ENGRAM_ERR_UNSUPPORTED;
+  if (n == 0) return ENGRAM_OK;
+  if (positions == nullptr || out == nullptr || (m > 0 && rows == nullptr)) return ENGRAM_ERR_INVALID;
+  if (!aligned(positions, 8) || !aligned(out, 16) || (m > 0 && !aligned(rows, 16))) return ENGRAM_ERR_INVALID;
+  if (n > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
+  return launch_rc(engram::launch_shard_unpack(rows, positions, m, n, head_dim, out, (cudaStream_t)stream));
+}
+
 int engram_set_l2_fetch_granularity(int32_t bytes, int32_t* previous) {
   if (bytes != 0 && bytes != 32 && bytes != 64 && bytes != 128) return ENGRAM_ERR_INVALID;
   size_t old = 0;

@@ -1,5 +1,5 @@
-// Internal declarations of the tensor-core projection (proj.cu) and the gate's finishing pass
-// (gate.cu), used by the C-ABI layer.
+// Internal declarations of the tensor-core projection (proj.cu), the gate's finishing pass (gate.cu)
+// and the two ends of the sharded lookup's exchange (shard.cu), used by the C-ABI layer.
 #pragma once
 
 #include <cstdint>
@@ -24,5 +24,12 @@ cudaError_t launch_gate_finish(const uint16_t* x, const uint16_t* value, const f
                                int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s);
 
 cudaError_t device_status_take(unsigned int* flags, int clear, cudaStream_t s);
+
+// sharded lookup: segments of the pack's count pass (one int32 count per segment and bucket)
+int64_t shard_pack_segments(int64_t n);
+cudaError_t launch_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
+                              int64_t* local_rows, int64_t* positions, int32_t* seg_counts, cudaStream_t s);
+cudaError_t launch_shard_unpack(const uint16_t* recv, const int64_t* positions, int64_t m, int64_t n,
+                                int32_t head_dim, uint16_t* out, cudaStream_t s);
 
 }  // namespace engram

@@ -1,0 +1,159 @@
+// Row-sharded lookup over several ranks ("DeepSeek V4.1" pages, engram-first/lookup page,
+// `ParallelEngramEmbedding`): rank r holds rows [r * part, (r + 1) * part) of each table, with
+// part = ceil(rows / world). The pages look up every index on every rank, zero the rows a rank does
+// not own and sum the mostly-zero [.., D] results over all ranks with an all-reduce. Here a rank
+// instead sends each of its requests only to the rank that owns the row and receives that one row
+// back: these kernels are the two ends of that exchange.
+//
+//   shard_pack   groups the indices of one lookup by owning rank (bucket `world` = indices outside
+//                [0, rows), which no rank owns), stable within a bucket, and emits for each the
+//                owner-local row id and its position in the request list; the bucket sizes are the
+//                split sizes of the all-to-all exchanges.
+//   shard_unpack scatters the rows received back (in the packed order) to their positions and writes
+//                +0 rows at the positions of the unowned indices, as the pages' masked rows.
+//
+// Design: pack is two passes over the indices (HBM-bound, 8 B read per index per pass, 16 B written):
+// a per-segment count, then a scatter that derives each segment's offsets from all the counts and
+// ranks elements inside a segment with warp ballots, so the order is deterministic. Unpack moves
+// 2 * head_dim bytes per row with 16-byte accesses.
+#include <cstdint>
+
+#include "engram_internal.cuh"
+#include "proj.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kPackThreads = 256;
+constexpr int kPackPerThread = 16;
+constexpr int kSeg = kPackThreads * kPackPerThread;  // indices per segment (one CTA)
+constexpr int kMaxBuckets = ENGRAM_MAX_SHARDS + 1;
+
+__device__ __forceinline__ int bucket_of(int64_t v, int64_t rows, int64_t part, int world) {
+  if (v < 0 || v >= rows) return world;
+  return (int)(v / part);
+}
+
+// seg_counts[s][b]: indices of segment s in bucket b
+__global__ void __launch_bounds__(kPackThreads) shard_count_kernel(const int64_t* __restrict__ idx, int64_t n,
+                                                                   int64_t rows, int64_t part, int world,
+                                                                   int32_t* __restrict__ seg_counts) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int cnt[kMaxBuckets];
+  const int nb = world + 1;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) cnt[b] = 0;
+  __syncthreads();
+  const int64_t s0 = (int64_t)blockIdx.x * kSeg;
+  for (int j = 0; j < kPackPerThread; ++j) {
+    const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
+    if (i < n) atomicAdd(&cnt[bucket_of(idx[i], rows, part, world)], 1);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) seg_counts[(int64_t)blockIdx.x * nb + b] = cnt[b];
+}
+
+// Writes every index of segment s to its bucket, in index order within the bucket.
+__global__ void __launch_bounds__(kPackThreads) shard_scatter_kernel(const int64_t* __restrict__ idx, int64_t n,
+                                                                     int64_t rows, int64_t part, int world,
+                                                                     const int32_t* __restrict__ seg_counts,
+                                                                     int64_t n_seg, int64_t* __restrict__ counts,
+                                                                     int64_t* __restrict__ local_rows,
+                                                                     int64_t* __restrict__ positions) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int64_t base[kMaxBuckets];                      // where this segment's part of bucket b starts
+  __shared__ int warp_cnt[kPackThreads / 32][kMaxBuckets];   // this round's elements per (warp, bucket)
+  const int nb = world + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < nb) {
+    const int b = threadIdx.x;
+    int64_t before = 0, total = 0;  // this bucket's elements in earlier segments; in all segments
+    for (int64_t s = 0; s < n_seg; ++s) {
+      const int64_t c = seg_counts[s * nb + b];
+      if (s < (int64_t)blockIdx.x) before += c;
+      total += c;
+    }
+    base[b] = before;
+    if (blockIdx.x == 0) counts[b] = total;
+    // buckets are laid out one after the other: add the totals of the buckets before b
+    int64_t earlier = 0;
+    for (int bb = 0; bb < b; ++bb)
+      for (int64_t s = 0; s < n_seg; ++s) earlier += seg_counts[s * nb + bb];
+    base[b] += earlier;
+  }
+  __syncthreads();
+  const int64_t s0 = (int64_t)blockIdx.x * kSeg;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int j = 0; j < kPackPerThread; ++j) {
+    const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
+    const bool in = i < n;
+    const int64_t v = in ? idx[i] : 0;
+    const int b = in ? bucket_of(v, rows, part, world) : -1;
+    // rank of this element among the warp's elements of the same bucket
+    int my_rank = 0;
+    for (int bb = 0; bb < nb; ++bb) {
+      const unsigned m = __ballot_sync(0xffffffffu, b == bb);
+      if (b == bb) my_rank = __popc(m & lt);
+      if (lane == 0) warp_cnt[warp][bb] = __popc(m);
+    }
+    __syncthreads();
+    if (in) {
+      int64_t off = base[b] + my_rank;
+      for (int w = 0; w < warp; ++w) off += warp_cnt[w][b];
+      local_rows[off] = b < world ? v - (int64_t)b * part : v;
+      positions[off] = i;
+    }
+    __syncthreads();
+    if (threadIdx.x < nb) {
+      int add = 0;
+      for (int w = 0; w < kPackThreads / 32; ++w) add += warp_cnt[w][threadIdx.x];
+      base[threadIdx.x] += add;
+    }
+    __syncthreads();
+  }
+}
+
+// unit u = (entry u / G, 16-byte piece u % G) with G = 2 * D / 16 pieces per row
+__global__ void __launch_bounds__(256) shard_unpack_kernel(const uint4* __restrict__ recv,
+                                                           const int64_t* __restrict__ positions, int64_t m,
+                                                           int64_t n, int G, uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t units = n * G;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = u / G;
+    const int q = (int)(u - e * G);
+    const int64_t pos = positions[e];
+    if (pos < 0 || pos >= n) continue;  // not a position of this lookup: nothing to write
+    out[pos * G + q] = e < m ? recv[e * G + q] : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+}  // namespace
+
+int64_t shard_pack_segments(int64_t n) { return (n + kSeg - 1) / kSeg; }
+
+cudaError_t launch_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
+                              int64_t* local_rows, int64_t* positions, int32_t* seg_counts, cudaStream_t s) {
+  const int64_t part = (rows + world - 1) / world;
+  const int64_t n_seg = shard_pack_segments(n);
+  cudaError_t e = launch_pdl(shard_count_kernel, dim3((unsigned)n_seg), dim3(kPackThreads), 0, s, idx, n, rows,
+                             part < 1 ? (int64_t)1 : part, (int)world, seg_counts);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(shard_scatter_kernel, dim3((unsigned)n_seg), dim3(kPackThreads), 0, s, idx, n, rows,
+                    part < 1 ? (int64_t)1 : part, (int)world, (const int32_t*)seg_counts, n_seg, counts, local_rows,
+                    positions);
+}
+
+cudaError_t launch_shard_unpack(const uint16_t* recv, const int64_t* positions, int64_t m, int64_t n,
+                                int32_t head_dim, uint16_t* out, cudaStream_t s) {
+  const int G = head_dim * 2 / 16;
+  const int64_t units = n * G;
+  int64_t blocks = (units + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  return launch_pdl(shard_unpack_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
+                    reinterpret_cast<const uint4*>(recv), positions, m, n, G, reinterpret_cast<uint4*>(out));
+}
+
+}  // namespace engram

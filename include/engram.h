@@ -86,6 +86,7 @@ typedef struct engram_state engram_state;
 #define ENGRAM_MAX_COLS_TOTAL 512 /* n_layers * (max_ngram - 1) * n_heads */
 /* head_dim must be one of 16, 32, 64, 128, 256, 512; block must divide head_dim and be a multiple of 8. */
 #define ENGRAM_GATE_MAX_COPIES 8  /* engram_gate: residual copies hc in {1, 2, 4, 8}; dim a multiple of 8 */
+#define ENGRAM_MAX_SHARDS 64      /* engram_shard_pack: ranks a table is split over */
 
 typedef struct engram_layout {
   int32_t n_layers;    /* engram layers hashed per call (the config's engram_layer_ids count) */
@@ -296,6 +297,48 @@ int engram_project_gate(const uint16_t* x, const uint16_t* emb, const uint16_t* 
  * them in the same atomic step when `clear` is non-zero. The pages have no counterpart: it reports
  * a failure that the library turns into a flag instead of a hang. Errors: _INVALID, _CUDA. */
 int engram_device_status(engram_stream_t stream, uint32_t* flags, int clear);
+
+/*
+ * Row-sharded lookup over `world` ranks (engram-first/lookup page, `ParallelEngramEmbedding`: rank r
+ * holds rows [r * part, (r + 1) * part) of the table, part = ceil(rows / world)). The pages look up
+ * every index on every rank, zero the rows a rank does not own and all-reduce the mostly-zero result;
+ * here each request travels only to the rank that owns its row, and only that row travels back:
+ *   1. engram_shard_pack groups a rank's indices by owner;
+ *   2. an all-to-all exchange (the caller's, e.g. NCCL) sends local_rows bucket r to rank r;
+ *   3. each rank looks the rows it received up in its shard (engram_lookup, rows = its shard size);
+ *   4. a second all-to-all returns them in the same order;
+ *   5. engram_shard_unpack puts them at their positions, +0 rows where no rank owns the index.
+ * The result equals engram_lookup on the whole table bit for bit.
+ *
+ * engram_shard_pack
+ *   idx         device int64 [n]: global row ids (any values; those outside [0, rows) are owned by no rank)
+ *   rows        the whole table's row count; world in [1, ENGRAM_MAX_SHARDS]
+ *   counts      device int64 [world + 1], written: counts[r] = indices owned by rank r, counts[world] =
+ *               indices owned by none
+ *   local_rows  device int64 [n], written: bucket 0 (rank 0's rows), then bucket 1, ..., then the unowned
+ *               indices; inside a bucket in index order; a rank's entries are rows of its shard
+ *               (global id - r * part), the unowned entries keep their global id
+ *   positions   device int64 [n], written: the index (into idx) of each entry of local_rows
+ *   workspace   device memory of engram_shard_pack_workspace(n, world) bytes, 16-byte aligned; calls
+ *               that use one workspace must not overlap on the GPU
+ * n == 0 is a no-op (counts is not written).
+ * Errors: _INVALID (null, misaligned, negative n or rows, workspace too small), _UNSUPPORTED (world), _CUDA.
+ */
+uint64_t engram_shard_pack_workspace(int64_t n, int32_t world);
+int engram_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
+                      int64_t* local_rows, int64_t* positions, void* workspace, uint64_t workspace_bytes,
+                      engram_stream_t stream);
+
+/*
+ * engram_shard_unpack: out[positions[i]] = rows[i] for i < m (the rows received back, in the packed
+ * order of the owned buckets), and out[positions[i]] = +0 for m <= i < n (the unowned indices).
+ *   rows       device bf16 [m][head_dim];  positions  device int64 [n] (from engram_shard_pack)
+ *   m          sum of counts[0 .. world-1];  out  device bf16 [n][head_dim], written
+ * head_dim a multiple of 8; rows and out 16-byte aligned. n == 0 is a no-op.
+ * Errors: _INVALID (null, misaligned, m outside [0, n]), _UNSUPPORTED (head_dim), _CUDA.
+ */
+int engram_shard_unpack(const uint16_t* rows, const int64_t* positions, int64_t m, int64_t n, int32_t head_dim,
+                        uint16_t* out, engram_stream_t stream);
 
 /*
  * Set the L2 fetch granularity limit of the current device's context (cudaLimitMaxL2FetchGranularity:

@@ -148,3 +148,26 @@ def test_projection_checks_need_no_gpu(lib):
     assert lib.engram_project_gate(a, a, a, a, a, None, 8, 64, 4, 256, 1e-20, P(4096 + 16), need, a, None) == \
         geng.ERR_INVALID  # workspace must be 256-byte aligned
     assert lib.engram_project_gate(a, a, a, a, a, None, 0, 64, 4, 256, 1e-20, None, 0, a, None) == geng.OK
+
+
+def test_shard_checks_need_no_gpu(lib):
+    P = ctypes.c_void_p
+    lib.engram_shard_pack_workspace.argtypes = [ctypes.c_int64, ctypes.c_int32]
+    lib.engram_shard_pack_workspace.restype = ctypes.c_uint64
+    lib.engram_shard_pack.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, P, P, P, P, ctypes.c_uint64, P]
+    lib.engram_shard_unpack.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, P, P]
+    a = P(4096)  # never dereferenced: every call below is rejected (or is a no-op) before a launch
+    # one int32 count per (segment of 4096 indices, bucket), rounded up to 256 bytes
+    assert lib.engram_shard_pack_workspace(4096, 8) == 256
+    assert lib.engram_shard_pack_workspace(1_572_864, 8) == (384 * 9 * 4 + 255) // 256 * 256
+    assert lib.engram_shard_pack_workspace(10, 0) == 0 and lib.engram_shard_pack_workspace(10, 65) == 0
+    ws = lib.engram_shard_pack_workspace(100, 4)
+    assert lib.engram_shard_pack(a, 0, 10, 4, a, a, a, a, ws, None) == geng.OK
+    assert lib.engram_shard_pack(a, 100, 10, 0, a, a, a, a, ws, None) == geng.ERR_UNSUPPORTED
+    assert lib.engram_shard_pack(a, 100, 10, 65, a, a, a, a, ws, None) == geng.ERR_UNSUPPORTED
+    assert lib.engram_shard_pack(a, 100, -1, 4, a, a, a, a, ws, None) == geng.ERR_INVALID
+    assert lib.engram_shard_pack(a, 100, 10, 4, a, a, a, a, ws - 1, None) == geng.ERR_INVALID
+    assert lib.engram_shard_pack(None, 100, 10, 4, a, a, a, a, ws, None) == geng.ERR_INVALID
+    assert lib.engram_shard_unpack(a, a, 5, 4, 128, a, None) == geng.ERR_INVALID  # m > n
+    assert lib.engram_shard_unpack(a, a, 1, 4, 12, a, None) == geng.ERR_UNSUPPORTED  # head_dim not a multiple of 8
+    assert lib.engram_shard_unpack(None, a, 0, 0, 128, a, None) == geng.OK
