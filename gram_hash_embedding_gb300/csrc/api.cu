@@ -432,6 +432,22 @@ int engram_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world
                                              static_cast<int32_t*>(workspace), (cudaStream_t)stream));
 }
 
+int engram_shard_pack_static(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
+                             int64_t* local_rows, int64_t* positions, engram_stream_t stream) {
+  if (n < 0 || rows < 0) return ENGRAM_ERR_INVALID;
+  if (world < 1 || world > ENGRAM_MAX_SHARDS) return ENGRAM_ERR_UNSUPPORTED;
+  if (n == 0) return ENGRAM_OK;
+  if (n > engram::static_pack_max_n(world)) return ENGRAM_ERR_UNSUPPORTED;  // beyond the fixed scratch
+  if (idx == nullptr || counts == nullptr || local_rows == nullptr || positions == nullptr) return ENGRAM_ERR_INVALID;
+  if (!aligned(idx, 8) || !aligned(counts, 8) || !aligned(local_rows, 8) || !aligned(positions, 8))
+    return ENGRAM_ERR_INVALID;
+  int32_t* scratch = nullptr;
+  int rc = launch_rc(engram::static_pack_scratch(&scratch));
+  if (rc != ENGRAM_OK) return rc;
+  return launch_rc(
+      engram::launch_shard_pack(idx, n, rows, world, counts, local_rows, positions, scratch, (cudaStream_t)stream));
+}
+
 int engram_shard_unpack(const uint16_t* rows, const int64_t* positions, int64_t m, int64_t n, int32_t head_dim,
                         uint16_t* out, engram_stream_t stream) {
   if (n < 0 || m < 0 || m > n) return ENGRAM_ERR_INVALID;

@@ -29,6 +29,9 @@ cudaError_t device_status_take(unsigned int* flags, int clear, cudaStream_t s);
 int64_t shard_pack_segments(int64_t n);
 cudaError_t launch_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
                               int64_t* local_rows, int64_t* positions, int32_t* seg_counts, cudaStream_t s);
+// engram_shard_pack_static: largest n for `world` ranks, and the fixed scratch array's device address
+int64_t static_pack_max_n(int32_t world);
+cudaError_t static_pack_scratch(int32_t** out);
 cudaError_t launch_shard_unpack(const uint16_t* recv, const int64_t* positions, int64_t m, int64_t n,
                                 int32_t head_dim, uint16_t* out, cudaStream_t s);
 

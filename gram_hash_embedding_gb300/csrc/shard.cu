@@ -17,6 +17,7 @@
 // ranks elements inside a segment with warp ballots, so the order is deterministic. Unpack moves
 // 2 * head_dim bytes per row with 16-byte accesses.
 #include <cstdint>
+#include <mutex>
 
 #include "engram_internal.cuh"
 #include "proj.cuh"
@@ -154,6 +155,49 @@ cudaError_t launch_shard_unpack(const uint16_t* recv, const int64_t* positions, 
   if (blocks > 152 * 16) blocks = 152 * 16;
   return launch_pdl(shard_unpack_kernel, dim3((unsigned)blocks), dim3(256), 0, s,
                     reinterpret_cast<const uint4*>(recv), positions, m, n, G, reinterpret_cast<uint4*>(out));
+}
+
+}  // namespace engram
+
+// ------------------------------------------------------------------------------------------------
+// engram_shard_pack_static: the same pack for callers that cannot allocate device memory.
+//
+// Some callers may not call cudaMalloc (or any routine that allocates) at the point where they pack:
+// a serving loop whose device memory is all handed out up front by its own pool, code that runs
+// while a stream is being captured into a CUDA graph (where a plain cudaMalloc is not allowed), or a
+// runtime that forbids the latency and synchronisation of an allocation on its hot path. They still
+// own the inputs and outputs; only the pack's scratch (one int32 count per segment of 4096 indices
+// and bucket) comes from this fixed array instead of a caller's workspace. Every device that loads
+// the library holds the array until the process exits.
+namespace engram {
+
+constexpr int64_t kStaticPackCounts = 16384;  // 64 KB: n <= 16384 / (world + 1) segments of 4096 indices
+__device__ __align__(256) static int32_t g_pack_scratch[kStaticPackCounts];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_pack_scratch_mutex;
+int32_t* g_pack_scratch_ptr[kMaxDevices] = {};  // device address of g_pack_scratch, per device
+}  // namespace
+
+int64_t static_pack_max_n(int32_t world) { return (kStaticPackCounts / (world + 1)) * (int64_t)kSeg; }
+
+// The array's device address on the current device, looked up once per device. In host code the
+// name g_pack_scratch is only a host-side stand-in, never a device address.
+cudaError_t static_pack_scratch(int32_t** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_pack_scratch_mutex);
+  if (g_pack_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_pack_scratch);
+    if (e != cudaSuccess) return e;
+    g_pack_scratch_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_pack_scratch_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace engram

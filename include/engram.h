@@ -330,6 +330,26 @@ int engram_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world
                       engram_stream_t stream);
 
 /*
+ * engram_shard_pack without a workspace, for callers that may not allocate device memory where they
+ * pack: a serving loop whose device memory is all handed out up front by its own pool, code running
+ * while a stream is captured into a CUDA graph (where a plain cudaMalloc is not allowed), or a hot
+ * path that must not take an allocation's latency. The pages have no counterpart: it is a
+ * convenience of this library. Same arguments and results as engram_shard_pack, without workspace:
+ * the scratch (one int32 per segment of 4096 indices and bucket) is a fixed 64 KB array inside the
+ * library, which every device that loads the library holds until the process exits.
+ *   limit   n <= floor(16384 / (world + 1)) * 4096 (7,454,720 indices at world 8; 1,028,096 at world
+ *           64); a larger n returns ENGRAM_ERR_UNSUPPORTED and launches nothing
+ *   set-up  the first call on each device looks up the array's device address there (with that
+ *           device current); make that first call before any stream capture
+ *   sharing every call on a device uses the same array, and the count pass overwrites every entry a
+ *           call reads, so no entry has to start at zero; calls that overlap on the GPU (on different
+ *           streams, or unordered) race on it and their results are undefined
+ * The call allocates nothing and calls no allocating routine. Errors: as engram_shard_pack.
+ */
+int engram_shard_pack_static(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
+                             int64_t* local_rows, int64_t* positions, engram_stream_t stream);
+
+/*
  * engram_shard_unpack: out[positions[i]] = rows[i] for i < m (the rows received back, in the packed
  * order of the owned buckets), and out[positions[i]] = +0 for m <= i < n (the unowned indices).
  *   rows       device bf16 [m][head_dim];  positions  device int64 [n] (from engram_shard_pack)
