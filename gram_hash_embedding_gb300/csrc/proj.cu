@@ -46,6 +46,9 @@ constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
 constexpr uint32_t kABytes = kBM * kBK * 2;
+#ifndef ENGRAM_PROJ_PAIR_STAGES
+#define ENGRAM_PROJ_PAIR_STAGES 6  // stages of 32 KB in the ring of a CTA of a pair (7 still fit in 227 KB)
+#endif
 #ifndef ENGRAM_PROJ_GROUP
 #define ENGRAM_PROJ_GROUP 16  // 256-row blocks per tile group (16 measured ahead of 4, 8 and 32)
 #endif
@@ -56,7 +59,7 @@ constexpr uint32_t kABytes = kBM * kBK * 2;
 // the ring holds 6 of them, and each SM reads 2/3 of the bytes per MMA from L2 that a single CTA does.
 template <bool PAIR>
 struct Cfg {
-  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kStages = PAIR ? ENGRAM_PROJ_PAIR_STAGES : 4;
   static constexpr int kBRows = PAIR ? kBN / 2 : kBN;          // rows of the B tile this CTA loads
   static constexpr uint32_t kBBytes = kBRows * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
