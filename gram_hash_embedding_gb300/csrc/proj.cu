@@ -46,30 +46,39 @@ constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
 constexpr uint32_t kABytes = kBM * kBK * 2;
+constexpr uint32_t kEpiChunkBytes = 32 * 32 * 2;  // one epilogue warp's 32 rows x 32 columns of bf16
 #ifndef ENGRAM_PROJ_PAIR_STAGES
-#define ENGRAM_PROJ_PAIR_STAGES 6  // stages of 32 KB in the ring of a CTA of a pair (7 still fit in 227 KB)
+#define ENGRAM_PROJ_PAIR_STAGES 6  // stages of 32 KB in the ring of a CTA of a pair
 #endif
 #ifndef ENGRAM_PROJ_GROUP
 #define ENGRAM_PROJ_GROUP 16  // 256-row blocks per tile group (16 measured ahead of 4, 8 and 32)
 #endif
 
-// PAIR = false: one CTA computes a 128 x 256 tile with M = 128 MMAs (4 stages of A + all of B, 48 KB).
-// PAIR = true: a cluster of two CTAs computes a 256 x 256 tile with M = 256 pair MMAs issued by the
-// leader; each CTA loads its own 128 rows of A and its half (128 rows) of B, so a stage is 32 KB and
-// the ring holds 6 of them, and each SM reads 2/3 of the bytes per MMA from L2 that a single CTA does.
-template <bool PAIR>
+// CS = 1: one CTA computes a 128 x 256 tile with M = 128 MMAs (4 stages of A + all of B, 48 KB).
+// CS = 2: a cluster of two CTAs (a pair) computes a 256 x 256 tile with M = 256 pair MMAs issued by
+// the leader; each CTA loads its own 128 rows of A and its half (128 rows) of B, so a stage is 32 KB
+// and the ring holds 6 of them: each SM reads 2/3 of the bytes per MMA from L2 that a lone CTA does.
+// CS = 4: two pairs side by side along N compute a 256 x 512 tile and share A: each CTA loads 64 of
+// its 128 A rows and multicasts them to the CTA at the same place in the other pair, so L2 serves
+// 3/4 of the bytes per MMA of a pair. Four-CTA clusters fill 144 of the 152 SMs.
+template <int CS>
 struct Cfg {
-  static constexpr int kStages = PAIR ? ENGRAM_PROJ_PAIR_STAGES : 4;
-  static constexpr int kBRows = PAIR ? kBN / 2 : kBN;          // rows of the B tile this CTA loads
+  static constexpr bool kPairs = CS >= 2;
+  static constexpr int kStages = kPairs ? ENGRAM_PROJ_PAIR_STAGES : 4;
+  static constexpr int kBRows = kPairs ? kBN / 2 : kBN;        // rows of the B tile this CTA loads
+  static constexpr int kARows = CS == 4 ? kBM / 2 : kBM;        // rows of A this CTA loads per stage
   static constexpr uint32_t kBBytes = kBRows * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kTxBytes = PAIR ? 2 * kStageBytes : kStageBytes;  // per stage, both CTAs
-  static constexpr int kTileM = PAIR ? 2 * kBM : kBM;          // rows of one (cluster) tile
-  static constexpr int kGroup = (PAIR ? 1 : 2) * ENGRAM_PROJ_GROUP;  // tile rows per group (in 256-row units)
+  static constexpr uint32_t kTxBytes = kPairs ? 2 * kStageBytes : kStageBytes;  // per stage, both CTAs of a pair
+  static constexpr int kTileM = kPairs ? 2 * kBM : kBM;        // rows of one cluster tile
+  static constexpr int kNBlocks = CS == 4 ? 2 : 1;             // 256-column blocks of one cluster tile
+  static constexpr int kGroup = (kPairs ? 1 : 2) * ENGRAM_PROJ_GROUP;  // tile rows per group (256-row units)
   static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kBN);
   // shared memory: the stage ring (1024-byte aligned), then barriers and two words
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
-  static constexpr uint32_t kBarOff = kRingBytes;  // full[S], empty[S], acc_full[2], acc_empty[2], drain
+  static constexpr uint32_t kEpiOff = kRingBytes;  // output staging: 2 chunks of 32 x 32 bf16 per epilogue warp
+  static constexpr uint32_t kEpiBytes = 4 * 2 * kEpiChunkBytes;
+  static constexpr uint32_t kBarOff = kEpiOff + kEpiBytes;  // full[S], empty[S], acc_full[2], acc_empty[2], drain
   static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
   static constexpr uint32_t kTmemSlotOff = kBarOff + 8 * kNumBars;  // tensor-memory base written by the alloc
   static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;          // set by a role whose wait ran out
@@ -83,8 +92,9 @@ struct ProjParams {
   int32_t K;        // columns of emb and wkv
   int32_t N;        // rows of wkv = output columns
   int32_t num_kb;   // ceil(K / kBK)
-  int32_t n_mtile;  // ceil(T / tile rows)
+  int32_t n_mtile;  // ceil(T / cluster tile rows)
   int32_t n_nblk;   // ceil(N / kBN)
+  int32_t n_ntile;  // ceil(n_nblk / 256-column blocks per cluster tile)
   int64_t n_tiles;
   // EPI_STORE: out [T][N] bf16
   uint16_t* out;
@@ -102,7 +112,7 @@ struct ProjParams {
 // tile index -> (tile row, column block): groups of `group` tile rows, column block outer, so the
 // tiles in flight at one time share a few A and B blocks, which stay in L2
 __device__ __forceinline__ void tile_coords(const ProjParams& p, int group, int64_t tile, int32_t& mt, int32_t& nb) {
-  const int64_t per_group = (int64_t)group * p.n_nblk;
+  const int64_t per_group = (int64_t)group * p.n_ntile;
   const int64_t g = tile / per_group;
   const int64_t r = tile - g * per_group;
   const int32_t m0 = (int32_t)(g * group);
@@ -134,11 +144,6 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint16_t* p) {
   return v;
 }
 
-__device__ __forceinline__ void st_v4(uint16_t* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -153,17 +158,31 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
                     tc::f32x2_to_bf16x2(v[4], v[5]), tc::f32x2_to_bf16x2(v[6], v[7]));
 }
 
-// bf16 rows of one accumulator tile: dst points at column 0 of this thread's row (null: row past T);
-// ncols_left = columns of the tile inside the matrix (a multiple of 8)
-__device__ __forceinline__ void store_tile_row(uint32_t taddr, uint16_t* dst, int ncols_left) {
+// bf16 output of one accumulator tile, for this warp's 32 rows (rows y0 .. y0 + 31 of the tensor of
+// `tmap`, columns x0 .. x0 + 255): 32 columns at a time, each thread converts its row to bf16 and
+// writes it into a 2 KB staging chunk (64-byte rows, 16-byte pieces swizzled as the tensor map's
+// 64-byte swizzle expects, so the warp's writes hit distinct banks), and lane 0 stores the chunk with
+// one TMA copy. Two chunks per warp alternate; a chunk is rewritten only after the copy issued from it
+// two chunks earlier has read it. Whole 128-byte lines reach L2 instead of a 16-byte piece of each of
+// 32 rows per store instruction, which costs less power (the projection runs at the power limit).
+__device__ __forceinline__ void store_tile_rows_tma(uint32_t taddr, const void* tmap, uint32_t stage_base, int x0,
+                                                    int32_t y0) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll 1
   for (int c = 0; c < kAccCols / 32; ++c) {
     float v[32];
-    tc::tmem_load_32cols(taddr + 32 * c, v);  // every lane loads: the load is warp-wide
-    if (dst != nullptr) {
+    tc::tmem_load_32cols(taddr + 32 * c, v);
+    const uint32_t chunk = stage_base + (uint32_t)(c & 1) * kEpiChunkBytes;
+    if (lane == 0) tc::bulk_wait_group_read_1();
+    __syncwarp();
+    const uint32_t row = chunk + (uint32_t)lane * 64u;
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
-        if (32 * c + 8 * g < ncols_left) st_v4(dst + 32 * c + 8 * g, pack8(v + 8 * g));
+    for (int g = 0; g < 4; ++g) tc::st_shared_v4(row + (uint32_t)((g ^ ((lane >> 1) & 3)) * 16), pack8(v + 8 * g));
+    tc::fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+      tc::tma_store_2d(tmap, chunk, x0 + 32 * c, y0);
+      tc::bulk_commit_group();
     }
   }
 }
@@ -223,13 +242,15 @@ __device__ __forceinline__ const uint16_t* h_row(const ProjParams& p, int64_t ro
   return p.x + (row * p.hc + i) * p.dim + (col0 - i * p.dim);
 }
 
-template <int EPI, bool PAIR>
+template <int EPI, int CS>
 __global__ void __launch_bounds__(kThreads, 1)
-    proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const ProjParams p) {
-  using C = Cfg<PAIR>;
+    proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmO, const ProjParams p) {
+  using C = Cfg<CS>;
+  constexpr bool PAIR = C::kPairs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // the same offset in both CTAs of a pair
+  const uint32_t base = (raw + 1023u) & ~1023u;  // the same offset in every CTA of a cluster
   uint8_t* gbase = smem_raw + (base - raw);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + C::kAbortOff);
   const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + C::kTmemSlotOff);
@@ -240,30 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto acc_empty = [&](uint32_t a) { return bar(2 * C::kStages + 2 + (int)a); };
   const uint32_t drain = bar(2 * C::kStages + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // a pair: rank 0 leads (issues the MMAs; its full and acc_empty barriers count for both CTAs)
-  const uint32_t rank = PAIR ? tc::cluster_ctarank() : 0u;
-  const bool leader = rank == 0;
-  const int64_t unit = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;  // cluster (or CTA) index
-  const int64_t n_units = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+  // place in the cluster: pair pr (of CS / 2), position q in the pair; q = 0 leads (issues the pair's
+  // MMAs; its full and acc_empty barriers count for both CTAs of the pair)
+  const uint32_t rank = CS > 1 ? tc::cluster_ctarank() : 0u;
+  const uint32_t q = PAIR ? (rank & 1u) : 0u;
+  const uint32_t pr = CS == 4 ? (rank >> 1) : 0u;
+  const uint32_t lead = rank & ~1u;
+  const bool leader = q == 0;
+  const int64_t unit = (int64_t)(blockIdx.x / CS);  // cluster index
+  const int64_t n_units = (int64_t)(gridDim.x / CS);
+  // the loads and MMAs of a stage must have been read by every pair that writes into this CTA's copy
+  // of it: with CS = 4 the other pair multicasts half of A into it
+  constexpr uint32_t kEmptyArrivals = CS == 4 ? 2 : 1;
+  constexpr uint16_t kAllCtas = (uint16_t)((1u << CS) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      tc::mbar_init(full(s), 1);   // the leader's arrive + the bytes of both CTAs' loads
-      tc::mbar_init(empty(s), 1);  // the leader's MMA commit, multicast to both CTAs
+      tc::mbar_init(full(s), 1);                // the leader's arrive + the bytes of its pair's loads
+      tc::mbar_init(empty(s), kEmptyArrivals);  // a commit of every pair's leader
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(acc_full(a), 1);
-      tc::mbar_init(acc_empty(a), PAIR ? 8 : 4);  // one arrival per epilogue warp of every CTA of the tile
+      tc::mbar_init(acc_empty(a), PAIR ? 8 : 4);  // one arrival per epilogue warp of the pair (or CTA)
     }
     tc::mbar_init(drain, 1);
     *abort = 0;
     tc::fence_barrier_init();
     tc::tma_prefetch_descriptor(&tmA);
     tc::tma_prefetch_descriptor(&tmB);
+    tc::tma_prefetch_descriptor(&tmO);
   }
   // inputs may come from the previous kernel on the stream, and its tensor memory must be free
   pdl_wait();
-  if (PAIR) tc::cluster_sync();  // the peer's barriers exist before anyone signals them
+  if (CS > 1) tc::cluster_sync();  // every CTA's barriers exist before anyone signals them
   if (warp == 1) {
     if (PAIR) {
       tc::tmem_alloc_pair(base + C::kTmemSlotOff, kTmemCols);
@@ -283,10 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t issued = 0;
     uint32_t stage = 0, phase = 0;
     for (int64_t tile = unit; tile < p.n_tiles && !*abort; tile += n_units) {
-      int32_t mt, nb;
-      tile_coords(p, C::kGroup, tile, mt, nb);
-      const int32_t row0 = mt * C::kTileM + (int32_t)rank * kBM;
-      const int32_t brow0 = nb * kBN + (int32_t)rank * C::kBRows;
+      int32_t mt, nt;
+      tile_coords(p, C::kGroup, tile, mt, nt);
+      const int32_t nb = nt * C::kNBlocks + (int32_t)pr;
+      const int32_t arow0 = mt * C::kTileM + (int32_t)q * kBM + (int32_t)pr * C::kARows;
+      const int32_t brow0 = nb * kBN + (int32_t)q * C::kBRows;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (!tc::mbar_wait(empty(stage), phase ^ 1u, abort)) {
           raise_timeout(abort);
@@ -294,13 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t a_dst = base + stage * C::kStageBytes;
         if (PAIR) {
-          const uint32_t fb = tc::map_to_rank(full(stage), 0);
+          const uint32_t fb = tc::map_to_rank(full(stage), lead);
           if (leader) tc::mbar_arrive_expect_tx(full(stage), C::kTxBytes);
-          tc::tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, row0);
+          if (CS == 4)  // this CTA's half of its A block, to itself and its counterpart in the other pair
+            tc::tma_load_2d_pair_multicast(a_dst + pr * (C::kARows * kBK * 2), &tmA, fb, kb * kBK, arow0,
+                                           (uint16_t)((1u << q) | (1u << (q + 2))));
+          else
+            tc::tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, arow0);
           tc::tma_load_2d_pair(a_dst + kABytes, &tmB, fb, kb * kBK, brow0);
         } else {
           tc::mbar_arrive_expect_tx(full(stage), C::kTxBytes);
-          tc::tma_load_2d(a_dst, &tmA, full(stage), kb * kBK, row0);
+          tc::tma_load_2d(a_dst, &tmA, full(stage), kb * kBK, arow0);
           tc::tma_load_2d(a_dst + kABytes, &tmB, full(stage), kb * kBK, brow0);
         }
         ++issued;
@@ -311,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // No copy may still be landing in shared memory when the CTA exits. A CTA of a pair counts its
-    // loads on the leader's barriers, so it waits for the MMAs that read its last loads instead
+    // loads on its leader's barriers, so it waits for the MMAs that read its last loads instead
     // (which implies they landed); a lone CTA waits for the loads themselves.
     for (int64_t i = issued - (issued < C::kStages ? issued : C::kStages); i < issued; ++i) {
       const uint32_t s = (uint32_t)(i % C::kStages), ph = (uint32_t)((i / C::kStages) & 1);
@@ -319,9 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
     }
   } else if (warp == 1 && lane == 0 && leader) {
-    // ---------------------------------------------------------------- MMA issuer (the leader)
+    // ---------------------------------------------------------------- MMA issuer (a pair's leader)
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
+    const uint16_t pair_ctas = (uint16_t)(3u << lead);
     for (int64_t tile = unit; ok && tile < p.n_tiles && !*abort; tile += n_units) {
       if (!tc::mbar_wait(acc_empty(acc), acc_phase ^ 1u, abort)) {
         raise_timeout(abort);
@@ -346,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             tc::mma_bf16(d, ad, bd, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
         }
-        // the stage returns to the loaders once these MMAs have read it
+        // the stage returns to every loader that writes into it once these MMAs have read it
         if (PAIR)
-          tc::commit_pair_multicast(empty(stage), 3);
+          tc::commit_pair_multicast(empty(stage), kAllCtas);
         else
           tc::commit(empty(stage));
         if (++stage == C::kStages) {
@@ -359,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // the tile's accumulators are complete once every MMA above is
       if (PAIR)
-        tc::commit_pair_multicast(acc_full(acc), 3);
+        tc::commit_pair_multicast(acc_full(acc), pair_ctas);
       else
         tc::commit(acc_full(acc));
       if (++acc == 2) {
@@ -369,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // every MMA this thread issued has completed before tensor memory is freed
     if (PAIR)
-      tc::commit_pair_multicast(drain, 1);
+      tc::commit_pair_multicast(drain, (uint16_t)(1u << rank));
     else
       tc::commit(drain);
     if (!tc::mbar_wait(drain, 0, nullptr)) atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
@@ -383,42 +419,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EPI != EPI_GATE || t >= p.n_tiles) return;
       int32_t pm, pn;
       tile_coords(p, C::kGroup, t, pm, pn);
-      const uint16_t* hr = h_row(p, ((int64_t)pm * (C::kTileM / kBM) + rank) * kBM + r, pn * kBN);
+      const int col = (pn * C::kNBlocks + (int)pr) * kBN;
+      if (col >= p.N) return;
+      const uint16_t* hr = h_row(p, ((int64_t)pm * (C::kTileM / kBM) + q) * kBM + r, col);
       if (hr != nullptr) tc::prefetch_l2_bulk(hr, kBN * 2);
     };
     prefetch_h(unit);
     for (int64_t tile = unit; tile < p.n_tiles; tile += n_units) {
-      int32_t mt, nb;
-      tile_coords(p, C::kGroup, tile, mt, nb);
+      int32_t mt, nt;
+      tile_coords(p, C::kGroup, tile, mt, nt);
       if (!warp_wait(acc_full(acc), acc_phase, abort)) break;
       tc::fence_after_thread_sync();
       prefetch_h(tile + n_units);
-      const int64_t mb = (int64_t)mt * (C::kTileM / kBM) + rank;  // this CTA's block of 128 rows
+      const int64_t mb = (int64_t)mt * (C::kTileM / kBM) + q;  // this CTA's block of 128 rows
       const int64_t row = mb * kBM + r;
-      const bool row_ok = row < p.T;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols;
-      const int col0 = nb * kBN;
+      const int col0 = (nt * C::kNBlocks + (int)pr) * kBN;  // a pair past the last column block stores nothing
+      const uint32_t stage_base = base + C::kEpiOff + (uint32_t)quarter * 2u * kEpiChunkBytes;
+      const int32_t y0 = (int32_t)(mb * kBM) + quarter * 32;  // TMA stores skip rows past T
       if (EPI == EPI_STORE) {
-        store_tile_row(taddr, row_ok ? p.out + row * p.N + col0 : nullptr, p.N - col0);
-      } else {
+        if (col0 < p.N) store_tile_rows_tma(taddr, &tmO, stage_base, col0, y0);
+      } else if (col0 < p.N) {
         const int key_cols = p.hc * p.dim;
         if (col0 < key_cols) {
           const int i = col0 / p.dim, j0 = col0 - i * p.dim;
           float sums[3];
           gate_tile_row(taddr, h_row(p, row, col0), p.qw + i * p.dim + j0, p.kw + i * p.dim + j0, sums);
-          float* dst = p.part + (mb * (key_cols / kBN) + nb) * 3 * kBM + r;
+          float* dst = p.part + (mb * (key_cols / kBN) + col0 / kBN) * 3 * kBM + r;
           dst[0] = sums[0];
           dst[kBM] = sums[1];
           dst[2 * kBM] = sums[2];
         } else {
-          store_tile_row(taddr, row_ok ? p.value + row * p.dim + (col0 - key_cols) : nullptr, kBN);
+          store_tile_rows_tma(taddr, &tmO, stage_base, col0 - key_cols, y0);
         }
       }
       tc::fence_before_thread_sync();
       __syncwarp();
       if (lane == 0) {
         if (PAIR)
-          tc::mbar_arrive_cluster(tc::map_to_rank(acc_empty(acc), 0));
+          tc::mbar_arrive_cluster(tc::map_to_rank(acc_empty(acc), lead));
         else
           tc::mbar_arrive(acc_empty(acc));
       }
@@ -427,12 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) tc::bulk_wait_group_0();  // this warp's output copies are done before the CTA exits
+    __syncwarp();
   }
   pdl_trigger();
   tc::fence_before_thread_sync();
   __syncthreads();
-  // neither CTA of a pair leaves while the other may still signal its barriers or read its memory
-  if (PAIR) tc::cluster_sync();
+  // no CTA of a cluster leaves while another may still signal its barriers or read its memory
+  if (CS > 1) tc::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc::fence_after_thread_sync();
@@ -471,24 +512,27 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [rows][K] bf16 row-major, read in boxes of box_rows x kBK with 128-byte swizzling; reads past
-// the matrix (ragged rows or K) are filled with zeros
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+// [rows][cols] bf16 row-major, moved in boxes of box_rows x box_cols: operands are read with 128-byte
+// swizzling (reads past the matrix, ragged rows or K, are filled with zeros), outputs written from
+// 64-byte swizzled staging chunks (writes past the matrix are dropped)
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              uint32_t box_cols = kBK, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {K, rows};
-  const cuuint64_t strides[1] = {K * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-#ifndef ENGRAM_PROJ_PAIR
-#define ENGRAM_PROJ_PAIR 1
+#ifndef ENGRAM_PROJ_CLUSTER
+#define ENGRAM_PROJ_CLUSTER 4
 #endif
-constexpr bool kPair = ENGRAM_PROJ_PAIR != 0;  // CTA pairs (M = 256 MMAs) unless built otherwise
+constexpr int kCS = ENGRAM_PROJ_CLUSTER;  // CTAs per cluster: 1, 2 (a pair) or 4 (two pairs sharing A)
+static_assert(kCS == 1 || kCS == 2 || kCS == 4, "cluster of 1, 2 or 4 CTAs");
 
 ProjParams base_params(int64_t T, int32_t K, int32_t N) {
   ProjParams p = {};
@@ -496,22 +540,27 @@ ProjParams base_params(int64_t T, int32_t K, int32_t N) {
   p.K = K;
   p.N = N;
   p.num_kb = (K + kBK - 1) / kBK;
-  p.n_mtile = (int32_t)((T + Cfg<kPair>::kTileM - 1) / Cfg<kPair>::kTileM);
+  p.n_mtile = (int32_t)((T + Cfg<kCS>::kTileM - 1) / Cfg<kCS>::kTileM);
   p.n_nblk = (N + kBN - 1) / kBN;
-  p.n_tiles = (int64_t)p.n_mtile * p.n_nblk;
+  p.n_ntile = (p.n_nblk + Cfg<kCS>::kNBlocks - 1) / Cfg<kCS>::kNBlocks;
+  p.n_tiles = (int64_t)p.n_mtile * p.n_ntile;
   return p;
 }
 
-// one persistent CTA (or CTA pair) per SM (pair of SMs) that can be resident at once, launched as a
-// programmatic dependent like every kernel of the library
+// as many persistent clusters as can be resident at once, launched as a programmatic dependent like
+// every kernel of the library
 template <int EPI>
 cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
-  using C = Cfg<kPair>;
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, emb, (uint64_t)p.T, (uint64_t)p.K, kBM) ||
-      !make_map(&tb, w, (uint64_t)p.N, (uint64_t)p.K, (uint32_t)C::kBRows))
+  using C = Cfg<kCS>;
+  CUtensorMap ta, tb, to;
+  // the output tensor: out [T][N], or the value rows [T][dim] of the gate epilogue
+  const uint16_t* optr = EPI == EPI_STORE ? p.out : p.value;
+  const uint64_t ocols = EPI == EPI_STORE ? (uint64_t)p.N : (uint64_t)p.dim;
+  if (!make_map(&ta, emb, (uint64_t)p.T, (uint64_t)p.K, (uint32_t)C::kARows) ||
+      !make_map(&tb, w, (uint64_t)p.N, (uint64_t)p.K, (uint32_t)C::kBRows) ||
+      !make_map(&to, optr, (uint64_t)p.T, ocols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto kern = proj_kernel<EPI, kPair>;
+  auto kern = proj_kernel<EPI, kCS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -519,7 +568,7 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = ENGRAM_PDL;
   attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = kPair ? 2 : 1;
+  attr[1].val.clusterDim.x = kCS;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads);
@@ -528,8 +577,8 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   int units = 0;
-  if (kPair) {
-    cfg.gridDim = dim3(2);
+  if (kCS > 1) {
+    cfg.gridDim = dim3(kCS);
     e = cudaOccupancyMaxActiveClusters(&units, kern, &cfg);
   } else {
     int dev = 0;
@@ -539,8 +588,8 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
   if (e != cudaSuccess) return e;
   if (units < 1) return cudaErrorInvalidConfiguration;
   const int64_t n = p.n_tiles < units ? p.n_tiles : units;
-  cfg.gridDim = dim3((unsigned)(n * (kPair ? 2 : 1)));
-  return cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  cfg.gridDim = dim3((unsigned)(n * kCS));
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, to, p);
 }
 
 }  // namespace
@@ -554,8 +603,8 @@ cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, in
 
 int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim) {
   // whole (cluster) tiles: the second CTA of a pair's last tile writes its block even past T
-  const int64_t tiles = (T + Cfg<kPair>::kTileM - 1) / Cfg<kPair>::kTileM;
-  return tiles * (Cfg<kPair>::kTileM / kBM) * (int64_t)(hc * dim / kBN) * 3 * kBM;
+  const int64_t tiles = (T + Cfg<kCS>::kTileM - 1) / Cfg<kCS>::kTileM;
+  return tiles * (Cfg<kCS>::kTileM / kBM) * (int64_t)(hc * dim / kBN) * 3 * kBM;
 }
 
 cudaError_t launch_project_gate_sums(const uint16_t* x, const uint16_t* emb, const uint16_t* wkv, const uint16_t* qw,

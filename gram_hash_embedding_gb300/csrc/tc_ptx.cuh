@@ -256,3 +256,55 @@ __device__ __forceinline__ void commit_pair_multicast(uint32_t bar, uint16_t cta
 
 }  // namespace tc
 }  // namespace engram
+
+namespace engram {
+namespace tc {
+
+// 2-D tiled load multicast to the CTAs of `cta_mask` (the same shared-memory offset in each); the
+// completion of each copy is counted on the mbarrier at offset `bar` of the leader of the
+// destination CTA's pair (`bar` a shared::cluster address of a pair leader)
+__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const void* tmap, uint32_t bar, int32_t x,
+                                                           int32_t y, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
+}  // namespace tc
+}  // namespace engram
+
+namespace engram {
+namespace tc {
+
+// ------------------------------------------------------------------------------------------ TMA stores
+// make this thread's generic-proxy shared-memory writes visible to the bulk copy engine
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2-D tiled store of one box from shared memory; rows or columns past the tensor are not written
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// wait until at most one of this thread's committed bulk stores still reads its shared memory
+__device__ __forceinline__ void bulk_wait_group_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// wait until all of this thread's committed bulk stores have completed
+__device__ __forceinline__ void bulk_wait_group_0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+}  // namespace tc
+}  // namespace engram
