@@ -1,6 +1,8 @@
 """Full-scale tables (384,006,168 and 384,016,682 rows x 128 fp8, ~98 GB on the device):
-the launch configuration the benchmark times, checked against the oracle on every hash id
-and on sampled output rows (GPU only)."""
+the launch configuration the benchmark times, checked against the oracle on every hash id and every
+output row of both layers (3,145,728 rows: the oracle regenerates the ~3.1M distinct table rows the
+launch touches on the host); the long chunked prefill on every hash id and sampled rows (its chunked
+output equals its one-shot output bit for bit) (GPU only)."""
 import numpy as np
 import pytest
 import torch
@@ -56,11 +58,12 @@ def test_full_scale_hash_lookup(full_tables):
     P = wl.layout.primes.reshape(2, -1)
     O = wl.layout.offsets
     assert ((exp_h >= O) & (exp_h < O + P)).all()
-    _check_sampled_rows(wl, outs, exp_h, np.random.default_rng(3), tag="full-scale")
-    # the rows of a whole sequence end (last 8 tokens of the last row), every column
+    # every output row of both layers: [8, 8192, 24, 128] bf16 per layer
     for layer in range(2):
-        got = H.bf16_bits(outs[layer][-1, -8:])
-        H.assert_bits_equal(got, H.oracle_lookup_rows(wl, layer, exp_h[-1, -8:, layer, :]), "sequence tail")
+        got = H.bf16_bits(outs[layer])
+        exp = H.oracle_lookup_rows(wl, layer, exp_h[:, :, layer, :])
+        H.assert_bits_equal(got, exp, f"full-scale rows layer {layer}")
+        del got, exp
     assert st.status() == 0
 
 
