@@ -529,9 +529,12 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 }
 
 #ifndef ENGRAM_PROJ_CLUSTER
-#define ENGRAM_PROJ_CLUSTER 4
+#define ENGRAM_PROJ_CLUSTER 2
 #endif
-constexpr int kCS = ENGRAM_PROJ_CLUSTER;  // CTAs per cluster: 1, 2 (a pair) or 4 (two pairs sharing A)
+// CTAs per cluster: 1, 2 (a pair) or 4 (two pairs sharing A). Sustained at the block shape on one box
+// (power-limited, alternating rounds) pairs took 5.91 ms and four-CTA clusters 5.94 ms: the multicast
+// saves L2 traffic but leaves 8 SMs idle, so pairs are the default.
+constexpr int kCS = ENGRAM_PROJ_CLUSTER;
 static_assert(kCS == 1 || kCS == 2 || kCS == 4, "cluster of 1, 2 or 4 CTAs");
 
 ProjParams base_params(int64_t T, int32_t K, int32_t N) {
