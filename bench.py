@@ -62,6 +62,10 @@ def parse_args(argv=None):
                    help="--block: fused = engram_project_gate (tensor-core projection with the gate's sums in its "
                         "epilogue, keys never written, then the gate's finishing pass); tcgen05 = engram_project "
                         "then engram_gate; cublas = torch.matmul (cuBLAS) then engram_gate")
+    p.add_argument("--shard", type=int, default=0, metavar="W",
+                   help="time the device steps of the row-sharded lookup for W ranks on this GPU: engram_shard_pack "
+                        "of the workload's layer-0 row ids and engram_shard_unpack of as many head_dim rows (the "
+                        "exchange between ranks is the caller's all-to-all and is not timed here)")
     p.add_argument("--graph", action="store_true",
                    help="capture the steps in a CUDA graph and replay it (removes host launch overhead; for the "
                         "small decode / chunk launches)")
@@ -1028,6 +1032,71 @@ def run_block(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- sharded lookup's device steps
+def run_shard(args):
+    """engram_shard_pack and engram_shard_unpack on the row ids of one engram layer of workload
+    args.cfg (the hash is computed once, untimed), for args.shard ranks, CUDA events over the launches."""
+    import numpy as np
+    import torch
+
+    import gram_hash_embedding_gb300 as geng
+    import synth
+
+    torch.cuda.set_device(0)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    wl = synth.make_workload(args.cfg)
+    lay = wl.layout
+    st = geng.EngramHash(n_layers=lay.n_layers, max_ngram=lay.max_ngram, n_heads=lay.n_heads, head_dim=lay.head_dim,
+                         block=lay.block, max_batch=wl.max_batch, max_seq_len=wl.max_seq_len, token_map=lay.token_map,
+                         multipliers=lay.multipliers, primes=lay.primes, offsets=lay.offsets, dead=lay.dead,
+                         pad_id=lay.pad_id)
+    ids = torch.from_numpy(np.ascontiguousarray(wl.ids.reshape(wl.B, -1)[:, :wl.L])).cuda()
+    idx = st.hash(ids, 0)[:, :, 0, :].contiguous().reshape(-1)
+    n, world, rows, D = idx.numel(), int(args.shard), int(lay.rows[0]), lay.head_dim
+    L = geng._lib()
+    s = torch.cuda.current_stream().cuda_stream
+    counts = torch.empty(world + 1, dtype=torch.int64, device="cuda")
+    local = torch.empty(n, dtype=torch.int64, device="cuda")
+    pos = torch.empty(n, dtype=torch.int64, device="cuda")
+    ws = torch.empty(max(int(L.engram_shard_pack_workspace(n, world)), 16), dtype=torch.uint8, device="cuda")
+    recv = torch.zeros((n, D), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((n, D), dtype=torch.bfloat16, device="cuda")
+
+    def pack():
+        L.engram_shard_pack(idx.data_ptr(), n, rows, world, counts.data_ptr(), local.data_ptr(), pos.data_ptr(),
+                            ws.data_ptr(), ws.numel(), s)
+
+    def unpack():
+        L.engram_shard_unpack(recv.data_ptr(), pos.data_ptr(), n, n, D, out.data_ptr(), s)
+
+    def timed(fn, k):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(k):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / k * 1e3
+
+    K = max(3, min(args.steps, 200))
+    t_pack, t_unpack = timed(pack, K), timed(unpack, K)
+    pack_bytes = n * (8 + 8 + 16)  # two passes over the ids, local row + position written
+    unpack_bytes = n * (8 + 4 * D)  # position read, row read and written
+    peak, peak_kind = measured_peaks()
+    line = {"metric": "sharded lookup device steps (us per launch pair)", "workload": wl.name, "indices": n,
+            "world": world, "head_dim": D, "steps": K,
+            "pack_us": t_pack, "pack_gbs": pack_bytes / t_pack / 1e3,
+            "unpack_us": t_unpack, "unpack_gbs": unpack_bytes / t_unpack / 1e3,
+            "unpack_frac_of_hbm": unpack_bytes / t_unpack / 1e3 / peak, "peak_kind": peak_kind,
+            "counts": [int(c) for c in counts.cpu()]}
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args):
     """The CPU oracle as it stands, timed on the host cores: each step hashes a bounded sample of
@@ -1105,6 +1174,8 @@ def main(argv=None):
         run_reference(args)
     elif args.block:
         run_block(args)
+    elif args.shard:
+        run_shard(args)
     else:
         run_ours(args)
 

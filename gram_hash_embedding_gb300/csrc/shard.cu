@@ -64,24 +64,31 @@ __global__ void __launch_bounds__(kPackThreads) shard_scatter_kernel(const int64
   pdl_wait();
   pdl_trigger();
   __shared__ int64_t base[kMaxBuckets];                      // where this segment's part of bucket b starts
+  __shared__ unsigned long long before_s[kMaxBuckets];       // bucket b's elements in earlier segments
+  __shared__ unsigned long long total_s[kMaxBuckets];        // bucket b's elements in all segments
   __shared__ int warp_cnt[kPackThreads / 32][kMaxBuckets];   // this round's elements per (warp, bucket)
   const int nb = world + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < nb) {
-    const int b = threadIdx.x;
-    int64_t before = 0, total = 0;  // this bucket's elements in earlier segments; in all segments
-    for (int64_t s = 0; s < n_seg; ++s) {
-      const int64_t c = seg_counts[s * nb + b];
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) before_s[b] = total_s[b] = 0ull;
+  __syncthreads();
+  // every thread sums a strided share of the segment counts, then adds its sums into shared memory
+  for (int b = 0; b < nb; ++b) {
+    unsigned long long before = 0, total = 0;
+    for (int64_t s = threadIdx.x; s < n_seg; s += blockDim.x) {
+      const unsigned long long c = (unsigned long long)seg_counts[s * nb + b];
       if (s < (int64_t)blockIdx.x) before += c;
       total += c;
     }
-    base[b] = before;
-    if (blockIdx.x == 0) counts[b] = total;
-    // buckets are laid out one after the other: add the totals of the buckets before b
-    int64_t earlier = 0;
-    for (int bb = 0; bb < b; ++bb)
-      for (int64_t s = 0; s < n_seg; ++s) earlier += seg_counts[s * nb + bb];
-    base[b] += earlier;
+    if (total != 0ull) atomicAdd(&total_s[b], total);
+    if (before != 0ull) atomicAdd(&before_s[b], before);
+  }
+  __syncthreads();
+  if (threadIdx.x < nb) {
+    const int b = threadIdx.x;
+    int64_t earlier = 0;  // buckets are laid out one after the other: the totals of the buckets before b
+    for (int bb = 0; bb < b; ++bb) earlier += (int64_t)total_s[bb];
+    base[b] = earlier + (int64_t)before_s[b];
+    if (blockIdx.x == 0) counts[b] = (int64_t)total_s[b];
   }
   __syncthreads();
   const int64_t s0 = (int64_t)blockIdx.x * kSeg;
