@@ -46,9 +46,16 @@ __global__ void __launch_bounds__(kPackThreads) shard_count_kernel(const int64_t
   for (int b = threadIdx.x; b < nb; b += blockDim.x) cnt[b] = 0;
   __syncthreads();
   const int64_t s0 = (int64_t)blockIdx.x * kSeg;
+  int64_t v[kPackPerThread];  // all of this thread's indices in flight at once
+#pragma unroll
   for (int j = 0; j < kPackPerThread; ++j) {
     const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
-    if (i < n) atomicAdd(&cnt[bucket_of(idx[i], rows, part, world)], 1);
+    v[j] = i < n ? idx[i] : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < kPackPerThread; ++j) {
+    const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
+    if (i < n) atomicAdd(&cnt[bucket_of(v[j], rows, part, world)], 1);
   }
   __syncthreads();
   for (int b = threadIdx.x; b < nb; b += blockDim.x) seg_counts[(int64_t)blockIdx.x * nb + b] = cnt[b];
@@ -93,10 +100,20 @@ __global__ void __launch_bounds__(kPackThreads) shard_scatter_kernel(const int64
   __syncthreads();
   const int64_t s0 = (int64_t)blockIdx.x * kSeg;
   const unsigned lt = (1u << lane) - 1u;
+  int64_t vals[kPackPerThread];  // all of this thread's indices in flight at once
+#pragma unroll
+  for (int j = 0; j < kPackPerThread; ++j) {
+    const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
+    vals[j] = i < n ? idx[i] : 0;
+  }
+#pragma unroll 1
   for (int j = 0; j < kPackPerThread; ++j) {
     const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
     const bool in = i < n;
-    const int64_t v = in ? idx[i] : 0;
+    int64_t v = 0;
+#pragma unroll
+    for (int jj = 0; jj < kPackPerThread; ++jj)
+      if (jj == j) v = vals[jj];  // a register, not a local-memory array: j is a loop variable
     const int b = in ? bucket_of(v, rows, part, world) : -1;
     // rank of this element among the warp's elements of the same bucket
     int my_rank = 0;
