@@ -3,6 +3,8 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "engram_internal.cuh"
@@ -29,6 +31,49 @@ inline int launch_rc(cudaError_t e) {
   if (e == cudaSuccess) return ENGRAM_OK;
   cudaGetLastError();
   return ENGRAM_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------------------------------------
+// What this library's last launch on each stream writes. Every kernel of the library is a
+// programmatic dependent launch: it may be scheduled while the kernel before it on the stream drains,
+// and only that kernel can still be running when it starts (a kernel launched otherwise, a copy or an
+// event wait in between is waited for in full, and each of our kernels triggers its successor only
+// after its own wait). So a fused hash + lookup may read its inputs before waiting when none of them
+// overlaps what our last launch on the same stream writes; a stale record (a stream handle reused)
+// can only be more cautious than needed, never less, because the kernel before it is then not ours.
+struct Span {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+std::mutex g_writes_mutex;
+std::unordered_map<uintptr_t, std::vector<Span>> g_last_writes;
+
+inline Span span(const void* p, uint64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Span{lo, lo + (uintptr_t)bytes};
+}
+
+void record_writes(cudaStream_t s, std::vector<Span> writes) {
+  std::lock_guard<std::mutex> lock(g_writes_mutex);
+  g_last_writes[reinterpret_cast<uintptr_t>(s)] = std::move(writes);
+}
+
+bool untouched_by_last_launch(cudaStream_t s, const std::vector<Span>& inputs) {
+  std::lock_guard<std::mutex> lock(g_writes_mutex);
+  auto it = g_last_writes.find(reinterpret_cast<uintptr_t>(s));
+  if (it == g_last_writes.end()) return true;
+  for (const Span& w : it->second)
+    for (const Span& r : inputs)
+      if (r.lo < w.hi && w.lo < r.hi) return false;
+  return true;
+}
+
+// After a launch path: record what it wrote on success; after a failure what ran is unknown, so the
+// next fused call on the stream reads nothing early.
+int launched(int rc, cudaStream_t s, std::vector<Span> writes) {
+  if (rc != ENGRAM_OK) writes = {Span{0, ~(uintptr_t)0}};
+  record_writes(s, std::move(writes));
+  return rc;
 }
 
 // Reads the status word and, when asked, clears it in the same atomic step, so that a flag raised
@@ -239,9 +284,10 @@ int engram_state_destroy(engram_state* state) {
 
 int engram_cache_reset(engram_state* state, engram_stream_t stream) {
   if (state == nullptr || !on_state_device(state)) return ENGRAM_ERR_INVALID;
-  return launch_rc(engram::launch_fill_i32(state->d_cache,
-                                           (int64_t)state->lay.max_batch * state->lay.max_seq_len,
-                                           (int32_t)state->lay.dead, (cudaStream_t)stream));
+  return launched(launch_rc(engram::launch_fill_i32(state->d_cache,
+                                                    (int64_t)state->lay.max_batch * state->lay.max_seq_len,
+                                                    (int32_t)state->lay.dead, (cudaStream_t)stream)),
+                  (cudaStream_t)stream, {});
 }
 
 int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* flags, int clear) {
@@ -252,9 +298,9 @@ int engram_state_status(engram_state* state, engram_stream_t stream, uint32_t* f
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaMemcpyAsync(&v, state->d_status_taken, sizeof v, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return launch_rc(e);
+  if (e != cudaSuccess) return launched(launch_rc(e), s, {});
   *flags = v;
-  return ENGRAM_OK;
+  return launched(ENGRAM_OK, s, {});
 }
 
 int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
@@ -263,7 +309,9 @@ int engram_hash(engram_state* state, const int64_t* ids, const uint8_t* mask, co
   if (rc != ENGRAM_OK || B == 0 || L == 0) return rc;
   if (hashes == nullptr || !aligned(hashes, 8)) return ENGRAM_ERR_INVALID;
   engram::CallArgs a = call_args(state, ids, mask, start_pos, cache_rows, B, L, hashes);
-  return launch_rc(engram::launch_hash(view(state), a, (cudaStream_t)stream));
+  const int NC = cols_total(state->lay);
+  return launched(launch_rc(engram::launch_hash(view(state), a, (cudaStream_t)stream)), (cudaStream_t)stream,
+                  {span(hashes, (uint64_t)B * L * NC * 8)});
 }
 
 int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const void* S, int64_t rows,
@@ -275,8 +323,9 @@ int engram_lookup(const int64_t* idx, int64_t n_idx, const uint8_t* W, const voi
   if (rows > 0 && (W == nullptr || S == nullptr || !aligned(W, 16) || !aligned(S, scale_bytes(scale_dtype))))
     return ENGRAM_ERR_INVALID;
   if (n_idx > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
-  return launch_rc(
-      engram::launch_lookup(idx, n_idx, W, S, rows, head_dim, block, scale_dtype, out, (cudaStream_t)stream));
+  return launched(
+      launch_rc(engram::launch_lookup(idx, n_idx, W, S, rows, head_dim, block, scale_dtype, out, (cudaStream_t)stream)),
+      (cudaStream_t)stream, {span(out, (uint64_t)n_idx * head_dim * 2)});
 }
 
 int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* mask, const int32_t* start_pos,
@@ -289,7 +338,22 @@ int engram_hash_lookup(engram_state* state, const int64_t* ids, const uint8_t* m
   engram::CallArgs a = call_args(state, ids, mask, start_pos, cache_rows, B, L, hashes);
   rc = fill_tables(state, W, S, rows, out, &a);
   if (rc != ENGRAM_OK) return rc;
-  return launch_rc(engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream));
+  cudaStream_t s = (cudaStream_t)stream;
+  const engram_layout& lay = state->lay;
+  const int C = (lay.max_ngram - 1) * lay.n_heads;
+  const uint64_t n_tok = (uint64_t)B * L;
+  std::vector<Span> reads = {span(ids, n_tok * 8), span(start_pos, (uint64_t)B * 4)};
+  if (mask != nullptr) reads.push_back(span(mask, n_tok));
+  if (cache_rows != nullptr) reads.push_back(span(cache_rows, (uint64_t)B * 4));
+  std::vector<Span> writes;
+  if (hashes != nullptr) writes.push_back(span(hashes, n_tok * cols_total(lay) * 8));
+  for (int l = 0; l < lay.n_layers; ++l) {
+    reads.push_back(span(W[l], (uint64_t)rows[l] * lay.head_dim));
+    reads.push_back(span(S[l], (uint64_t)rows[l] * (lay.head_dim / lay.block) * scale_bytes(lay.scale_dtype)));
+    writes.push_back(span(out[l], n_tok * C * lay.head_dim * 2));
+  }
+  a.early = untouched_by_last_launch(s, reads) ? 1 : 0;
+  return launched(launch_rc(engram::launch_hash_lookup(view(state), a, s)), s, std::move(writes));
 }
 
 namespace {
@@ -325,7 +389,8 @@ int engram_hash_varlen(engram_state* state, const int64_t* ids, const uint8_t* m
   engram::CallArgs a;
   int rc = packed_call(state, ids, mask, cu_seqlens, start_pos, cache_rows, B, T, max_len, hashes, &a);
   if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
-  return launch_rc(engram::launch_hash(view(state), a, (cudaStream_t)stream));
+  return launched(launch_rc(engram::launch_hash(view(state), a, (cudaStream_t)stream)), (cudaStream_t)stream,
+                  {span(hashes, (uint64_t)T * cols_total(state->lay) * 8)});
 }
 
 int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uint8_t* mask,
@@ -337,7 +402,13 @@ int engram_hash_lookup_varlen(engram_state* state, const int64_t* ids, const uin
   if (rc != ENGRAM_OK || B == 0 || T == 0 || max_len == 0) return rc;
   rc = fill_tables(state, W, S, rows, out, &a);
   if (rc != ENGRAM_OK) return rc;
-  return launch_rc(engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream));
+  std::vector<Span> writes;
+  const engram_layout& lay = state->lay;
+  const int C = (lay.max_ngram - 1) * lay.n_heads;
+  if (hashes != nullptr) writes.push_back(span(hashes, (uint64_t)T * cols_total(lay) * 8));
+  for (int l = 0; l < lay.n_layers; ++l) writes.push_back(span(out[l], (uint64_t)T * C * lay.head_dim * 2));
+  return launched(launch_rc(engram::launch_hash_lookup(view(state), a, (cudaStream_t)stream)), (cudaStream_t)stream,
+                  std::move(writes));
 }
 
 int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight, const uint16_t* k_weight,
@@ -351,7 +422,9 @@ int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight,
     return ENGRAM_ERR_INVALID;
   if (!aligned(x, 16) || !aligned(kv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) || !aligned(out, 16))
     return ENGRAM_ERR_INVALID;
-  return launch_rc(engram::launch_gate(x, kv, q_weight, k_weight, mask, T, hc, dim, eps, out, (cudaStream_t)stream));
+  return launched(
+      launch_rc(engram::launch_gate(x, kv, q_weight, k_weight, mask, T, hc, dim, eps, out, (cudaStream_t)stream)),
+      (cudaStream_t)stream, {span(out, (uint64_t)T * hc * dim * 2)});
 }
 
 int engram_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
@@ -362,7 +435,8 @@ int engram_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K,
   if (T == 0) return ENGRAM_OK;
   if (emb == nullptr || w == nullptr || out == nullptr || !aligned(emb, 16) || !aligned(w, 16) || !aligned(out, 16))
     return ENGRAM_ERR_INVALID;
-  return launch_rc(engram::launch_project(emb, w, T, K, N, out, (cudaStream_t)stream));
+  return launched(launch_rc(engram::launch_project(emb, w, T, K, N, out, (cudaStream_t)stream)), (cudaStream_t)stream,
+                  {span(out, (uint64_t)T * N * 2)});
 }
 
 namespace {
@@ -397,14 +471,16 @@ int engram_project_gate(const uint16_t* x, const uint16_t* emb, const uint16_t* 
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256((uint64_t)T * dim * 2u));
   cudaStream_t s = (cudaStream_t)stream;
   int rc = launch_rc(engram::launch_project_gate_sums(x, emb, wkv, q_weight, k_weight, T, K, hc, dim, value, part, s));
-  if (rc != ENGRAM_OK) return rc;
-  return launch_rc(engram::launch_gate_finish(x, value, part, mask, T, hc, dim, eps, out, s));
+  if (rc != ENGRAM_OK) return launched(rc, s, {});
+  return launched(launch_rc(engram::launch_gate_finish(x, value, part, mask, T, hc, dim, eps, out, s)), s,
+                  {span(out, (uint64_t)T * hc * dim * 2), span(workspace, workspace_bytes)});
 }
 
 int engram_device_status(engram_stream_t stream, uint32_t* flags, int clear) {
   if (flags == nullptr) return ENGRAM_ERR_INVALID;
   unsigned int v = 0;
-  int rc = launch_rc(engram::device_status_take(&v, clear ? 1 : 0, (cudaStream_t)stream));
+  int rc = launched(launch_rc(engram::device_status_take(&v, clear ? 1 : 0, (cudaStream_t)stream)),
+                    (cudaStream_t)stream, {});
   if (rc != ENGRAM_OK) return rc;
   *flags = v;
   return ENGRAM_OK;
@@ -428,8 +504,11 @@ int engram_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world
       !aligned(workspace, 16))
     return ENGRAM_ERR_INVALID;
   if (workspace_bytes < engram_shard_pack_workspace(n, world)) return ENGRAM_ERR_INVALID;
-  return launch_rc(engram::launch_shard_pack(idx, n, rows, world, counts, local_rows, positions,
-                                             static_cast<int32_t*>(workspace), (cudaStream_t)stream));
+  return launched(launch_rc(engram::launch_shard_pack(idx, n, rows, world, counts, local_rows, positions,
+                                                      static_cast<int32_t*>(workspace), (cudaStream_t)stream)),
+                  (cudaStream_t)stream,
+                  {span(counts, (uint64_t)(world + 1) * 8), span(local_rows, (uint64_t)n * 8),
+                   span(positions, (uint64_t)n * 8), span(workspace, workspace_bytes)});
 }
 
 int engram_shard_pack_static(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
@@ -444,8 +523,11 @@ int engram_shard_pack_static(const int64_t* idx, int64_t n, int64_t rows, int32_
   int32_t* scratch = nullptr;
   int rc = launch_rc(engram::static_pack_scratch(&scratch));
   if (rc != ENGRAM_OK) return rc;
-  return launch_rc(
-      engram::launch_shard_pack(idx, n, rows, world, counts, local_rows, positions, scratch, (cudaStream_t)stream));
+  return launched(
+      launch_rc(engram::launch_shard_pack(idx, n, rows, world, counts, local_rows, positions, scratch,
+                                          (cudaStream_t)stream)),
+      (cudaStream_t)stream,
+      {span(counts, (uint64_t)(world + 1) * 8), span(local_rows, (uint64_t)n * 8), span(positions, (uint64_t)n * 8)});
 }
 
 int engram_shard_unpack(const uint16_t* rows, const int64_t* positions, int64_t m, int64_t n, int32_t head_dim,
@@ -456,7 +538,8 @@ int engram_shard_unpack(const uint16_t* rows, const int64_t* positions, int64_t 
   if (positions == nullptr || out == nullptr || (m > 0 && rows == nullptr)) return ENGRAM_ERR_INVALID;
   if (!aligned(positions, 8) || !aligned(out, 16) || (m > 0 && !aligned(rows, 16))) return ENGRAM_ERR_INVALID;
   if (n > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
-  return launch_rc(engram::launch_shard_unpack(rows, positions, m, n, head_dim, out, (cudaStream_t)stream));
+  return launched(launch_rc(engram::launch_shard_unpack(rows, positions, m, n, head_dim, out, (cudaStream_t)stream)),
+                  (cudaStream_t)stream, {span(out, (uint64_t)n * head_dim * 2)});
 }
 
 int engram_set_l2_fetch_granularity(int32_t bytes, int32_t* previous) {

@@ -42,6 +42,9 @@ struct CallArgs {
   int64_t L;                  // dense: tokens per row; packed: max_len (a longer sequence is skipped)
   int64_t total;              // packed: tokens in ids (T); dense: B * L
   int32_t B;
+  int32_t early;              // fused dense calls: 1 when the host found that none of this call's inputs (ids,
+                              // mask, start_pos, cache_rows, tables) is written by the previous kernel of this
+                              // library on the stream, so they may be read before pdl_wait()
   int32_t head_dim, block;
   int32_t scale_dtype;        // ENGRAM_SCALE_*: storage type of S
   const uint8_t* W[ENGRAM_MAX_LAYERS];

@@ -299,11 +299,12 @@ __device__ __forceinline__ void mod_column(const uint64_t* roll_s, const ColPara
 // start at element seq_off of ids / mask / hashes and use cache row b (or cache_rows[b]). Called by
 // every thread of the CTA (contains barriers). Fills rowidx (layer-major: [l][t][col]) when given,
 // and the optional int64 hash output. Returns whether the sequence's cache row and start position
-// fit the cache.
+// fit the cache. With `defer` it writes no global memory (no cache write, no hash output; rowidx is
+// filled): the caller writes them after pdl_wait() (write_deferred).
 __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a, unsigned char* smem,
                                           const SmemPlan& plan, const int tile, const int b, const int64_t seq_off,
                                           const int64_t Lb, const int64_t t0, const int ntok, const bool want_rowidx,
-                                          const bool staged, unsigned int* flags_s) {
+                                          const bool staged, unsigned int* flags_s, const bool defer = false) {
   const int N = sv.max_ngram, NL = sv.n_layers, C = sv.n_cols, H = sv.n_heads;
   const int NC = NL * C;
   ColParam* cols_s = reinterpret_cast<ColParam*>(smem + plan.cols_off);
@@ -352,7 +353,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
     for (int t = tid; t < ntok; t += nthr) {
       const int32_t cur = tok_s[t + N - 1];
       const int64_t pos = s_b + t0 + t;
-      if (in_bounds(pos >= 0 && pos < sv.max_seq_len, flags_s)) cache_row[pos] = cur;
+      if (!defer && in_bounds(pos >= 0 && pos < sv.max_seq_len, flags_s)) cache_row[pos] = cur;
       int64_t tok[ENGRAM_MAX_NGRAM];
       bool blocked = false;
 #pragma unroll
@@ -390,7 +391,7 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
       const int t1 = tid / NC;
       const ModWalk w{(t1 * NL + l) * (N - 1) + col / H, tstep * NL * (N - 1), (seq_off + t0 + t1) * NC + j,
                       (int64_t)tstep * NC, (l * ntok + t1) * C + col, tstep * C};
-      const bool out_h = a.hashes != nullptr;
+      const bool out_h = a.hashes != nullptr && !defer;
       if (!row_ok) {  // the row wrote nothing: its hash ids are -1
         ModWalk v = w;
         for (int t = t1; t < ntok; t += tstep, v.hi += v.hstep, v.xi += v.xstep) {
@@ -416,7 +417,8 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
         const ColParam cp = cols_s[j];
         h = floored_mod(roll_s[(t * NL + l) * (N - 1) + col / H], cp) + cp.offset;
       }
-      if (a.hashes != nullptr && in_bounds(seq_off + t0 + t < a.total, flags_s)) a.hashes[(seq_off + t0 + t) * NC + j] = h;
+      if (a.hashes != nullptr && !defer && in_bounds(seq_off + t0 + t < a.total, flags_s))
+        a.hashes[(seq_off + t0 + t) * NC + j] = h;
       if (want_rowidx) rowidx_s[(l * ntok + t) * C + col] = h;
     }
   }
@@ -487,6 +489,50 @@ __device__ bool packed_tile(const StateView& sv, const CallArgs& a, const int ti
 // Dense calls: grid = (ceil(L / tile), B), one CTA = `tile` consecutive tokens of sequence b. Packed
 // calls: a 1-D grid of floor(T / tile) + B CTAs mapped to (sequence, tile) pairs by packed_tile.
 // D = head_dim (compile time); G = D / 16 lanes per output row. Unused when GATHER is false.
+// The cache writes and hash-id stores of a tile whose hash phase ran with `defer` (before pdl_wait()):
+// the tokens are still in tok_s and the hash ids in rowidx_s.
+__device__ __forceinline__ void write_deferred(const StateView& sv, const CallArgs& a, const unsigned char* smem,
+                                               const SmemPlan& plan, const int b, const int64_t seq_off,
+                                               const int64_t t0, const int ntok, const bool row_ok,
+                                               unsigned int* flags_s) {
+  const int N = sv.max_ngram, C = sv.n_cols, NC = sv.n_layers * sv.n_cols;
+  const int32_t* tok_s = reinterpret_cast<const int32_t*>(smem + plan.tok_off);
+  const int64_t* rowidx_s = reinterpret_cast<const int64_t*>(smem + plan.rowidx_off);
+  if (row_ok) {
+    const int64_t s_b = (int64_t)a.start_pos[b];
+    const int64_t r_b = a.cache_rows != nullptr ? (int64_t)a.cache_rows[b] : (int64_t)b;
+    int32_t* cache_row = sv.cache + r_b * sv.max_seq_len;
+    for (int t = threadIdx.x; t < ntok; t += blockDim.x) {
+      const int64_t pos = s_b + t0 + t;
+      if (in_bounds(pos >= 0 && pos < sv.max_seq_len, flags_s)) cache_row[pos] = tok_s[t + N - 1];
+    }
+  }
+  if (a.hashes != nullptr) {  // rowidx holds the hash ids (-1 for a rejected row) layer-major
+    for (int e = threadIdx.x; e < ntok * NC; e += blockDim.x) {
+      const int t = e / NC;
+      const int j = e - t * NC;
+      const int l = j / C;
+      if (in_bounds(seq_off + t0 + t < a.total, flags_s))
+        a.hashes[(seq_off + t0 + t) * NC + j] = rowidx_s[(l * ntok + t) * C + (j - l * C)];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// fused kernel: hash a tile, then (GATHER) stream its rows through registers.
+// Dense calls: grid = (ceil(L / tile), B), one CTA = `tile` consecutive tokens of sequence b. Packed
+// calls: a 1-D grid of floor(T / tile) + B CTAs mapped to (sequence, tile) pairs by packed_tile.
+// D = head_dim (compile time); G = D / 16 lanes per output row. Unused when GATHER is false.
+//
+// Early reads (dense fused calls with a.early set): a launch overlaps the drain of the kernel before
+// it only as far as it reads nothing that kernel writes. The host sets a.early when this library's
+// previous launch on the stream writes none of the call's inputs (any other kind of producer is waited
+// for in full by the launch itself), so a CTA may then read ids, mask, start positions and the tables
+// before pdl_wait(): it hashes its tile and issues its first batch of row loads, and waits only before
+// its first store. A tile whose lookback reaches below the chunk (t0 < max_ngram - 1) reads the cache,
+// which the previous kernel may write, so it waits before hashing. Cache writes and hash-id stores are
+// deferred until after the wait. Every CTA waits before it exits and triggers the next launch only
+// after its wait, so a later kernel can never run ahead of a kernel two launches back.
 template <bool GATHER, int D, bool ONE, int SDT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateView sv, const CallArgs a, const int tile) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -497,8 +543,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
   // drains; packed calls learn their extents first (CTAs without tokens exit at once)
   const bool dense = a.cu_seqlens == nullptr;
   if (dense) stage_constants(sv, smem, plan);
-  pdl_wait();
-  pdl_trigger();
+  const bool early = GATHER && dense && a.early != 0;
+  bool waited = false;
+  auto wait_once = [&]() {
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+  };
+  if (!early) wait_once();
   const int64_t* rowidx_s = reinterpret_cast<const int64_t*>(smem + plan.rowidx_off);
   const int tid = threadIdx.x;
   int b;
@@ -511,11 +565,16 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
     Lb = a.L;
     t0 = (int64_t)blockIdx.x * tile;
   }
-  if (t0 >= Lb) return;
+  if (t0 >= Lb) {
+    wait_once();
+    return;
+  }
   const int ntok = (int)min((int64_t)tile, Lb - t0);
   if (tid == 0) flags_s = 0u;
+  if (early && t0 < sv.max_ngram - 1) wait_once();  // the lookback reads the cache below this chunk
+  const bool defer = !waited;
   __syncthreads();
-  hash_tile(sv, a, smem, plan, tile, b, seq_off, Lb, t0, ntok, GATHER, dense, &flags_s);
+  const bool row_ok = hash_tile(sv, a, smem, plan, tile, b, seq_off, Lb, t0, ntok, GATHER, dense, &flags_s, defer);
 
   if (GATHER) {
     __syncthreads();
@@ -548,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
           piece_load<D, ONE, SDT>(pc[k], a.W[l], a.S[l], a.rows[l], rowidx_s[l * rpl + r], u % G, blk_shift);
         }
       }
+      wait_once();  // the outputs may be the previous kernel's: no store before it has completed
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
         const int u = base + k * kThreads;
@@ -555,6 +615,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
       }
     }
   }
+  wait_once();
+  if (defer) write_deferred(sv, a, smem, plan, b, seq_off, t0, ntok, row_ok, &flags_s);
 
   __syncthreads();
   if (tid == 0 && flags_s != 0u) atomicOr(sv.status, flags_s);

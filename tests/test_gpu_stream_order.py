@@ -158,3 +158,37 @@ def test_explicit_side_stream_with_wrapper_temporaries(tiny):
         H.assert_bits_equal(H.bf16_bits(got_r[k]), H.oracle_lookup_rows(wl, 0, exp_h[:, :, 0, :]),
                             f"side-stream rows, step {k}")
     assert st.status() == 0
+
+
+def test_fused_call_whose_ids_the_previous_launch_wrote(tiny):
+    """A fused call may read its inputs before the kernel ahead of it completes only when this
+    library's previous launch on the stream does not write them. Here it does: call 1 writes its
+    int64 hash ids into H, and call 2, enqueued right behind it with nothing in between, takes H as its
+    token ids (values up to ~9,000 against a vocabulary of 1,000: most are flagged and treated as
+    masked, the rest map through token_map). H starts as -5 everywhere, so a call 2 that read H early
+    would see -5 ids and hash masked tokens instead. Repeated, with fresh sentinels, in both orders
+    of a large and a small call."""
+    wl, Ws, Ss = tiny
+    lay = wl.layout
+    rng = np.random.default_rng(23)
+    for B, L in ((4, 2048), (2, 96)):
+        C = lay.n_cols
+        st1, orc1 = H.make_state(wl, B, L), H.make_oracle(wl, B, L)
+        st2, orc2 = H.make_state(wl, B, L * C), H.make_oracle(wl, B, L * C)
+        ids1 = rng.integers(0, lay.raw_vocab, size=(B, L))
+        hbuf = torch.full((B, L, 1, C), -5, dtype=torch.int64, device="cuda")
+        out1 = [torch.empty((B, L, C, lay.head_dim), dtype=torch.bfloat16, device="cuda")]
+        out2 = [torch.empty((B, L * C, C, lay.head_dim), dtype=torch.bfloat16, device="cuda")]
+        h2 = torch.empty((B, L * C, 1, C), dtype=torch.int64, device="cuda")
+        ids1_d = H.to_dev(ids1)
+        torch.cuda.synchronize()
+        st1.hash_lookup(ids1_d, Ws, Ss, start_pos=0, out=out1, hashes=hbuf)
+        st2.hash_lookup(hbuf.view(B, L * C), Ws, Ss, start_pos=0, out=out2, hashes=h2)
+        torch.cuda.synchronize()
+        exp1, _ = orc1.hash(ids1, 0)
+        H.assert_bits_equal(hbuf.cpu().numpy(), exp1, "call 1 hash ids")
+        exp2, _ = orc2.hash(exp1.reshape(B, L * C), 0)
+        H.assert_bits_equal(h2.cpu().numpy(), exp2, "call 2 hash ids (its ids are call 1's output)")
+        H.assert_bits_equal(H.bf16_bits(out2[0]), H.oracle_lookup_rows(wl, 0, exp2[:, :, 0, :]), "call 2 rows")
+        st1.status()
+        st2.status()
