@@ -380,6 +380,21 @@ class Runner:
                 self.state.handle, i, self.starts[j % len(self.starts)], self.W, self.S, self.out, mask=m,
                 cu_seqlens=self.cu if self.varlen else None, max_len=self.L if self.varlen else None)
                 for j, (i, m) in enumerate(zip(self.ids, self.masks))]
+        # chunked steps: one prepared call per (id batch, chunk) with the chunk's start positions already
+        # on the device, so nothing but this library's kernels runs between two chunks (an int start
+        # position would put a fill kernel before every chunk and end the overlap of consecutive launches)
+        self.chunk_calls = None
+        if len(self.chunks) > 1:
+            chunk_starts = [torch.full((self.B,), c0, dtype=torch.int32, device=device) for c0, _ in self.chunks]
+            self.chunk_calls = []
+            for i, m in zip(self.ids, self.masks):
+                calls = []
+                for (c0, c1), sp in zip(self.chunks, chunk_starts):
+                    ii = i[:, c0:c1] if i[:, c0:c1].is_contiguous() else i[:, c0:c1].contiguous()
+                    mm = None if m is None else (m[:, c0:c1] if m[:, c0:c1].is_contiguous() else m[:, c0:c1].contiguous())
+                    calls.append(self.geng.PreparedHashLookup(self.state.handle, ii, sp, self.W, self.S, self.out,
+                                                              mask=mm))
+                self.chunk_calls.append(calls)
         sname = ["fp32", "bf16", "UE8M0", "E4M3"][lay.scale_dtype]
         self.scale_name = sname
         self.kernel_name = f"hash_kernel<GATHER=true, D={lay.head_dim}, {sname} scales> (hash + gather + dequant)"
@@ -389,6 +404,10 @@ class Runner:
         """Enqueue one step; returns the launches' (start, end) event pairs when timing."""
         if ids is None and mask is None and self.calls is not None:
             self.calls[k % len(self.calls)]()
+            return
+        if ids is None and mask is None and self.chunk_calls is not None:
+            for call in self.chunk_calls[k % len(self.chunk_calls)]:
+                call()
             return
         start = self.starts[k % len(self.starts)] if ids is None else self.start
         ids = self.ids[k % len(self.ids)] if ids is None else ids

@@ -323,7 +323,9 @@ def engram_hash_lookup(state: int, ids: torch.Tensor, start_pos, W: list, S: lis
                        out: list | None = None, hashes: torch.Tensor | None = None, stream=None,
                        cache_rows: torch.Tensor | None = None) -> list:
     """Hash + per-layer lookup in one launch. W/S: per-layer tables. Returns (or fills) the
-    per-layer bf16 outputs [B, L, C, D]."""
+    per-layer bf16 outputs [B, L, C, D]. An int start_pos costs a small fill kernel before the call;
+    in a loop of calls pass a device int32 [B] tensor (or use PreparedHashLookup): consecutive calls of
+    this library overlap their launches only when no other kernel or copy runs between them."""
     B, L = ids.shape
     lay = engram_state_layout(state)
     n = len(W)
