@@ -567,6 +567,36 @@ class Runner:
         return h2d, d2h
 
 
+def link_bandwidth(torch, runner, reps: int = 5):
+    """The CPU-GPU link alone, in the same run as the end-to-end leg: one step's output rows (device
+    to pinned host) and one step's ids (pinned host to device) copied with no kernel running, CUDA
+    events, best of `reps`. The end-to-end step cannot beat its device-to-host copy at this rate."""
+    out = runner.e2e_sets[0][3]
+    out_pinned = runner.e2e_sets[0][4]
+    d2h_bytes = sum(o.numel() * o.element_size() for o in out)
+    ids_dev, ids_host = runner.e2e_sets[0][0], runner.ids_pinned[0]
+    h2d_bytes = ids_dev.numel() * ids_dev.element_size()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best_d2h = best_h2d = float("inf")
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        a.record()
+        for o, h in zip(out, out_pinned):
+            h.copy_(o, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best_d2h = min(best_d2h, a.elapsed_time(b) / 1e3)
+        a.record()
+        ids_dev.copy_(ids_host, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best_h2d = min(best_h2d, a.elapsed_time(b) / 1e3)
+    return {"d2h_bytes": d2h_bytes, "d2h_ms": best_d2h * 1e3, "d2h_gbs": d2h_bytes / best_d2h / 1e9,
+            "h2d_bytes": h2d_bytes, "h2d_ms": best_h2d * 1e3, "h2d_gbs": h2d_bytes / best_h2d / 1e9,
+            "how": "the step's rows device->pinned host and its ids pinned host->device, no kernel running, "
+                   f"best of {reps}"}
+
+
 def time_region(torch, dist, dev_index, fn, steps, stream, per_launch_events=False, between=None):
     """Run `fn(k)` `steps` times between barriers and synchronisations; returns (total seconds, per-step
     seconds between the events around each `fn(k)`, or None) from CUDA events on `stream`.
@@ -856,6 +886,7 @@ def run_ours(args):
     e_total, _ = time_region(torch, dist, local, lambda k: runner.e2e_step(k, drain=k == Ke - 1), Ke, stream)
     e_total = max_over_ranks(dist, e_total, device)
     e_value = runner.tokens_per_step * Ke * world / e_total
+    link = link_bandwidth(torch, runner) if rank == 0 else None
     h2d, d2h = runner.e2e_bytes()
 
     lay = runner.lay
@@ -914,6 +945,7 @@ def run_ours(args):
                      "kernel": runner.kernel_name},
         "e2e": {"value": e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke, "ms_per_step": e_total / Ke * 1e3, "call": "engram_hash_lookup",
+                "link": link,
                 "copy_out": (f"pipelined: {len(runner.e2e_pieces)} calls on groups of batch rows, each group's rows "
                              "copied to the host on a second stream while the next group is computed; steps "
                              "alternate two sets of buffers, so a step's calls overlap the previous step's copies")
