@@ -497,7 +497,7 @@ int engram_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world
   if (n < 0 || rows < 0) return ENGRAM_ERR_INVALID;
   if (world < 1 || world > ENGRAM_MAX_SHARDS) return ENGRAM_ERR_UNSUPPORTED;
   if (n == 0) return ENGRAM_OK;
-  if (n > ((int64_t)1 << 40)) return ENGRAM_ERR_UNSUPPORTED;
+  if (n > INT32_MAX) return ENGRAM_ERR_UNSUPPORTED;  // bucket offsets are int32
   if (idx == nullptr || counts == nullptr || local_rows == nullptr || positions == nullptr || workspace == nullptr)
     return ENGRAM_ERR_INVALID;
   if (!aligned(idx, 8) || !aligned(counts, 8) || !aligned(local_rows, 8) || !aligned(positions, 8) ||

@@ -12,9 +12,10 @@
 //   shard_unpack scatters the rows received back (in the packed order) to their positions and writes
 //                +0 rows at the positions of the unowned indices, as the pages' masked rows.
 //
-// Design: pack is two passes over the indices (HBM-bound, 8 B read per index per pass, 16 B written):
-// a per-segment count, then a scatter that derives each segment's offsets from all the counts and
-// ranks elements inside a segment with warp ballots, so the order is deterministic. Unpack moves
+// Design: pack is two passes over the indices (8 B read per index per pass, 16 B written) around a
+// one-CTA scan: a per-segment count, the scan that turns the counts into each segment's start in
+// each bucket, then a scatter that ranks the elements of a segment with warp ballots, so the order is
+// deterministic. Unpack moves
 // 2 * head_dim bytes per row with 16-byte accesses.
 #include <cstdint>
 #include <mutex>
@@ -61,43 +62,71 @@ __global__ void __launch_bounds__(kPackThreads) shard_count_kernel(const int64_t
   for (int b = threadIdx.x; b < nb; b += blockDim.x) seg_counts[(int64_t)blockIdx.x * nb + b] = cnt[b];
 }
 
-// Writes every index of segment s to its bucket, in index order within the bucket.
+// One CTA: turns seg_counts[s][b] (the count of segment s in bucket b) into the position where segment
+// s's entries of bucket b start in the packed arrays (buckets one after the other, segments in order
+// inside a bucket), in place, and writes the bucket totals to counts. Offsets fit int32: n < 2^31.
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads) shard_scan_kernel(int32_t* __restrict__ seg_counts, int64_t n_seg,
+                                                                  int world, int64_t* __restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int32_t warp_sums[kScanThreads / 32];
+  __shared__ int32_t carry_s;
+  const int nb = world + 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t bucket_start = 0;  // entries of the buckets before b
+  for (int b = 0; b < nb; ++b) {
+    if (tid == 0) carry_s = bucket_start;
+    __syncthreads();
+    for (int64_t s0 = 0; s0 < n_seg; s0 += kScanThreads) {
+      const int64_t s = s0 + tid;
+      const int32_t c = s < n_seg ? seg_counts[s * nb + b] : 0;
+      // inclusive scan of c over the CTA: within the warp, then over the warps' sums
+      int32_t x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) warp_sums[warp] = x;
+      __syncthreads();
+      if (warp == 0) {
+        int32_t w = lane < kScanThreads / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+          if (lane >= o) w += y;
+        }
+        if (lane < kScanThreads / 32) warp_sums[lane] = w;  // inclusive over the warps
+      }
+      __syncthreads();
+      const int32_t before = carry_s + (warp > 0 ? warp_sums[warp - 1] : 0) + x - c;
+      if (s < n_seg) seg_counts[s * nb + b] = before;
+      __syncthreads();
+      if (tid == 0) carry_s += warp_sums[kScanThreads / 32 - 1];
+      __syncthreads();
+    }
+    const int32_t total = carry_s - bucket_start;
+    if (tid == 0) counts[b] = total;
+    bucket_start = carry_s;
+    __syncthreads();
+  }
+}
+
+// Writes every index of segment s to its bucket, in index order within the bucket, from the start
+// positions shard_scan_kernel left in seg_base.
 __global__ void __launch_bounds__(kPackThreads) shard_scatter_kernel(const int64_t* __restrict__ idx, int64_t n,
                                                                      int64_t rows, int64_t part, int world,
-                                                                     const int32_t* __restrict__ seg_counts,
-                                                                     int64_t n_seg, int64_t* __restrict__ counts,
+                                                                     const int32_t* __restrict__ seg_base,
                                                                      int64_t* __restrict__ local_rows,
                                                                      int64_t* __restrict__ positions) {
   pdl_wait();
   pdl_trigger();
-  __shared__ int64_t base[kMaxBuckets];                      // where this segment's part of bucket b starts
-  __shared__ unsigned long long before_s[kMaxBuckets];       // bucket b's elements in earlier segments
-  __shared__ unsigned long long total_s[kMaxBuckets];        // bucket b's elements in all segments
+  __shared__ int32_t base[kMaxBuckets];                      // where this segment's part of bucket b goes next
   __shared__ int warp_cnt[kPackThreads / 32][kMaxBuckets];   // this round's elements per (warp, bucket)
   const int nb = world + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x) before_s[b] = total_s[b] = 0ull;
-  __syncthreads();
-  // every thread sums a strided share of the segment counts, then adds its sums into shared memory
-  for (int b = 0; b < nb; ++b) {
-    unsigned long long before = 0, total = 0;
-    for (int64_t s = threadIdx.x; s < n_seg; s += blockDim.x) {
-      const unsigned long long c = (unsigned long long)seg_counts[s * nb + b];
-      if (s < (int64_t)blockIdx.x) before += c;
-      total += c;
-    }
-    if (total != 0ull) atomicAdd(&total_s[b], total);
-    if (before != 0ull) atomicAdd(&before_s[b], before);
-  }
-  __syncthreads();
-  if (threadIdx.x < nb) {
-    const int b = threadIdx.x;
-    int64_t earlier = 0;  // buckets are laid out one after the other: the totals of the buckets before b
-    for (int bb = 0; bb < b; ++bb) earlier += (int64_t)total_s[bb];
-    base[b] = earlier + (int64_t)before_s[b];
-    if (blockIdx.x == 0) counts[b] = (int64_t)total_s[b];
-  }
-  __syncthreads();
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) base[b] = seg_base[(int64_t)blockIdx.x * nb + b];
   const int64_t s0 = (int64_t)blockIdx.x * kSeg;
   const unsigned lt = (1u << lane) - 1u;
   int64_t vals[kPackPerThread];  // all of this thread's indices in flight at once
@@ -106,14 +135,12 @@ __global__ void __launch_bounds__(kPackThreads) shard_scatter_kernel(const int64
     const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
     vals[j] = i < n ? idx[i] : 0;
   }
-#pragma unroll 1
+  __syncthreads();
+#pragma unroll
   for (int j = 0; j < kPackPerThread; ++j) {
     const int64_t i = s0 + (int64_t)j * kPackThreads + threadIdx.x;
     const bool in = i < n;
-    int64_t v = 0;
-#pragma unroll
-    for (int jj = 0; jj < kPackPerThread; ++jj)
-      if (jj == j) v = vals[jj];  // a register, not a local-memory array: j is a loop variable
+    const int64_t v = vals[j];
     const int b = in ? bucket_of(v, rows, part, world) : -1;
     // rank of this element among the warp's elements of the same bucket
     int my_rank = 0;
@@ -124,7 +151,7 @@ __global__ void __launch_bounds__(kPackThreads) shard_scatter_kernel(const int64
     }
     __syncthreads();
     if (in) {
-      int64_t off = base[b] + my_rank;
+      int64_t off = (int64_t)base[b] + my_rank;
       for (int w = 0; w < warp; ++w) off += warp_cnt[w][b];
       local_rows[off] = b < world ? v - (int64_t)b * part : v;
       positions[off] = i;
@@ -166,9 +193,10 @@ cudaError_t launch_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32
   cudaError_t e = launch_pdl(shard_count_kernel, dim3((unsigned)n_seg), dim3(kPackThreads), 0, s, idx, n, rows,
                              part < 1 ? (int64_t)1 : part, (int)world, seg_counts);
   if (e != cudaSuccess) return e;
+  e = launch_pdl(shard_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, seg_counts, n_seg, (int)world, counts);
+  if (e != cudaSuccess) return e;
   return launch_pdl(shard_scatter_kernel, dim3((unsigned)n_seg), dim3(kPackThreads), 0, s, idx, n, rows,
-                    part < 1 ? (int64_t)1 : part, (int)world, (const int32_t*)seg_counts, n_seg, counts, local_rows,
-                    positions);
+                    part < 1 ? (int64_t)1 : part, (int)world, (const int32_t*)seg_counts, local_rows, positions);
 }
 
 cudaError_t launch_shard_unpack(const uint16_t* recv, const int64_t* positions, int64_t m, int64_t n,

@@ -322,7 +322,8 @@ int engram_device_status(engram_stream_t stream, uint32_t* flags, int clear);
  *   workspace   device memory of engram_shard_pack_workspace(n, world) bytes, 16-byte aligned; calls
  *               that use one workspace must not overlap on the GPU
  * n == 0 is a no-op (counts is not written).
- * Errors: _INVALID (null, misaligned, negative n or rows, workspace too small), _UNSUPPORTED (world), _CUDA.
+ * Errors: _INVALID (null, misaligned, negative n or rows, workspace too small), _UNSUPPORTED (world,
+ * n >= 2^31), _CUDA.
  */
 uint64_t engram_shard_pack_workspace(int64_t n, int32_t world);
 int engram_shard_pack(const int64_t* idx, int64_t n, int64_t rows, int32_t world, int64_t* counts,
