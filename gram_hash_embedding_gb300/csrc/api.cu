@@ -439,6 +439,18 @@ int engram_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K,
                   {span(out, (uint64_t)T * N * 2)});
 }
 
+int engram_project_withhold(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
+                            int32_t tile, engram_stream_t stream) {
+  if (T < 0 || tile < 0) return ENGRAM_ERR_INVALID;
+  if (K < 8 || K % 8 != 0 || N < 8 || N % 8 != 0 || N > INT32_MAX - 256 || T > INT32_MAX)
+    return ENGRAM_ERR_UNSUPPORTED;
+  if (T == 0) return ENGRAM_OK;
+  if (emb == nullptr || w == nullptr || out == nullptr || !aligned(emb, 16) || !aligned(w, 16) || !aligned(out, 16))
+    return ENGRAM_ERR_INVALID;
+  return launched(launch_rc(engram::launch_project(emb, w, T, K, N, out, (cudaStream_t)stream, tile)),
+                  (cudaStream_t)stream, {span(out, (uint64_t)T * N * 2)});
+}
+
 namespace {
 inline bool gate_shape_ok(int32_t hc, int32_t dim) {
   return (hc == 1 || hc == 2 || hc == 4 || hc == 8) && dim >= 256 && dim % 256 == 0 &&

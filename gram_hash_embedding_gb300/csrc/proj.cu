@@ -107,6 +107,10 @@ struct ProjParams {
   uint16_t* value;     // [T][dim]
   float* part;         // [ceil(T / kBM)][hc * dim / kBN][3][kBM]
   int32_t hc, dim;
+  // test hook (engram_project_withhold): the leader of every cluster does not signal the completion
+  // of its tile number `withhold` (counted from 0 per cluster), so that tile's epilogue waits in vain
+  // until its time limit; -1: every tile is signalled
+  int32_t withhold;
 };
 
 // tile index -> (tile row, column block): groups of `group` tile rows, column block outer, so the
@@ -358,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
     bool ok = true;
     const uint16_t pair_ctas = (uint16_t)(3u << lead);
-    for (int64_t tile = unit; ok && tile < p.n_tiles && !*abort; tile += n_units) {
+    int32_t local_tile = 0;
+    for (int64_t tile = unit; ok && tile < p.n_tiles && !*abort; tile += n_units, ++local_tile) {
       if (!tc::mbar_wait(acc_empty(acc), acc_phase ^ 1u, abort)) {
         raise_timeout(abort);
         break;
@@ -394,10 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // the tile's accumulators are complete once every MMA above is
-      if (PAIR)
-        tc::commit_pair_multicast(acc_full(acc), pair_ctas);
-      else
-        tc::commit(acc_full(acc));
+      if (local_tile != p.withhold) {
+        if (PAIR)
+          tc::commit_pair_multicast(acc_full(acc), pair_ctas);
+        else
+          tc::commit(acc_full(acc));
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -547,6 +554,7 @@ ProjParams base_params(int64_t T, int32_t K, int32_t N) {
   p.n_nblk = (N + kBN - 1) / kBN;
   p.n_ntile = (p.n_nblk + Cfg<kCS>::kNBlocks - 1) / Cfg<kCS>::kNBlocks;
   p.n_tiles = (int64_t)p.n_mtile * p.n_ntile;
+  p.withhold = -1;
   return p;
 }
 
@@ -598,9 +606,10 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
 }  // namespace
 
 cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
-                           cudaStream_t s) {
+                           cudaStream_t s, int32_t withhold) {
   ProjParams p = base_params(T, K, N);
   p.out = out;
+  p.withhold = withhold;
   return launch_proj<EPI_STORE>(emb, w, p, s);
 }
 

@@ -7,9 +7,9 @@
 
 namespace engram {
 
-// out[T][N] = bf16(emb[T][K] @ w[N][K]^T)
+// out[T][N] = bf16(emb[T][K] @ w[N][K]^T); withhold >= 0: the test hook of engram_project_withhold
 cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
-                           cudaStream_t s);
+                           cudaStream_t s, int32_t withhold = -1);
 
 // fp32 values of the partial-sum array of the fused gate projection for T tokens
 int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim);

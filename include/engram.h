@@ -263,6 +263,17 @@ int engram_gate(const uint16_t* x, const uint16_t* kv, const uint16_t* q_weight,
 int engram_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
                    engram_stream_t stream);
 
+/*
+ * Test hook of engram_project's failure path (no counterpart in the pages): the same call, except
+ * that in every cluster of CTAs the projection never signals that its tile number `tile` (counted
+ * from 0 per cluster) is complete. That tile's epilogue then waits until its one-second limit runs
+ * out, the kernel raises ENGRAM_STATUS_TIMEOUT (engram_device_status), stops, waits for its own
+ * copies and MMAs in flight, frees its tensor memory and ends instead of hanging; the output is
+ * undefined and the context stays usable. Errors: as engram_project, and _INVALID for tile < 0.
+ */
+int engram_project_withhold(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
+                            int32_t tile, engram_stream_t stream);
+
 /* Bytes of device workspace that engram_project_gate needs for T tokens (a multiple of 256). */
 uint64_t engram_project_gate_workspace(int64_t T, int32_t hc, int32_t dim);
 
