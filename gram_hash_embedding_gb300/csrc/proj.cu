@@ -5,19 +5,25 @@
 // keys are never written to memory (engram_project_gate).
 //
 // Design (GB300): a dense contraction (T x K x N = 65,536 x 3,072 x 25,600 per layer at the released
-// width), so it runs on the 5th-generation tensor cores. One persistent CTA per SM walks a list of
-// 128 x 256 output tiles. Its warps specialise:
-//   warp 0      one thread issues TMA loads of 128 x 64 (A = emb) and 256 x 64 (B = wkv) bf16 boxes,
-//               128-byte swizzled, into a 4-stage shared-memory ring (48 KB a stage);
-//   warp 1      allocates 512 columns of tensor memory (two 128 x 256 fp32 accumulators) and one of
-//               its threads issues tcgen05.mma (M 128, N 256, K 16; 4 per stage), committing each
-//               stage back to the loader and each finished tile to the epilogue;
-//   warps 2-5   the epilogue: each thread owns one row of the tile (one tensor-memory lane), reads
-//               its 256 fp32 accumulators 32 columns at a time, and either rounds them to bf16 and
-//               stores them, or (gate epilogue) turns a key tile into three partial sums per row.
+// width), so it runs on the 5th-generation tensor cores. A cluster of two CTAs on two SMs (a pair)
+// computes 256 x 256 output tiles with M = 256 MMAs issued by its leader (tcgen05.mma.cta_group::2):
+// each CTA holds its 128 rows of A and half of the B tile, and receives its 128 rows of the
+// accumulator in its own tensor memory. The 76 pairs are persistent and walk the tile list. In each
+// CTA the warps specialise:
+//   warp 0      one thread issues TMA loads (128-byte swizzle) of its 128 x 64 A box and 128 x 64 B
+//               box into a 6-stage ring of 32 KB stages, counted on the leader's barriers;
+//   warp 1      allocates 512 columns of tensor memory in both CTAs (two 128 x 256 fp32 accumulators);
+//               in the leader one thread issues the MMAs (M 256, N 256, K 16; 4 per stage) and commits
+//               each stage back to both loaders and each finished tile to both epilogues;
+//   warps 2-5   the epilogue: each thread owns one row (one tensor-memory lane), reads its 256 fp32
+//               accumulators 32 columns at a time and either rounds them to bf16 and stores them (a
+//               swizzled shared-memory chunk per warp, written out by a TMA store), or (gate epilogue)
+//               turns a key tile into three partial sums per row.
 // The two accumulators let the epilogue of tile i run while the tensor cores compute tile i+1.
-// Tiles are visited in groups of 16 row blocks, column block outer: the 152 tiles in flight at any
-// time share ~16 A blocks and ~10 B blocks, which stay in L2.
+// Tiles are visited in groups of 16 tile rows, column block outer, so the tiles in flight share a few
+// A and B blocks, which stay in L2. Built with ENGRAM_PROJ_CLUSTER=1 or 4 the same kernel runs one
+// CTA per tile (M = 128 MMAs) or two pairs side by side that share A by TMA multicast; both measured
+// no faster.
 //
 // Every wait is bounded (tc_ptx.cuh): a wait that runs out raises ENGRAM_STATUS_TIMEOUT in the
 // library's device status word, the CTA stops issuing work, waits for its copies and MMAs in
