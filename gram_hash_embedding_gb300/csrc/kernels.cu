@@ -304,8 +304,7 @@ __device__ __forceinline__ void mod_column(const uint64_t* roll_s, const ColPara
 __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a, unsigned char* smem,
                                           const SmemPlan& plan, const int tile, const int b, const int64_t seq_off,
                                           const int64_t Lb, const int64_t t0, const int ntok, const bool want_rowidx,
-                                          const bool staged, unsigned int* flags_s, const bool defer = false,
-                                          const int stage_part = 0) {
+                                          const bool staged, unsigned int* flags_s, const bool defer = false) {
   const int N = sv.max_ngram, NL = sv.n_layers, C = sv.n_cols, H = sv.n_heads;
   const int NC = NL * C;
   ColParam* cols_s = reinterpret_cast<ColParam*>(smem + plan.cols_off);
@@ -328,11 +327,8 @@ __device__ __forceinline__ bool hash_tile(const StateView& sv, const CallArgs& a
   //    In-chunk tokens come from ids (token_map, mask) and do not wait for the start position;
   //    earlier positions come from the cache, which this launch never writes below start_pos, so
   //    reads and writes are disjoint.
-  //    stage_part 1 stages only the in-chunk tokens, 2 only the earlier positions (the cache), 0 both:
-  //    a tile that reads its inputs early stages part 1 before pdl_wait() and part 2 after it.
   for (int j = tid; j < ntok + N - 1; j += nthr) {
     const int64_t t = t0 - (N - 1) + j;
-    if ((stage_part == 1 && t < 0) || (stage_part == 2 && t >= 0)) continue;
     int32_t c = dead;
     if (t >= 0) {
       if (in_bounds(seq_off + t >= 0 && seq_off + t < a.total, flags_s)) {
@@ -493,35 +489,6 @@ __device__ bool packed_tile(const StateView& sv, const CallArgs& a, const int ti
 // Dense calls: grid = (ceil(L / tile), B), one CTA = `tile` consecutive tokens of sequence b. Packed
 // calls: a 1-D grid of floor(T / tile) + B CTAs mapped to (sequence, tile) pairs by packed_tile.
 // D = head_dim (compile time); G = D / 16 lanes per output row. Unused when GATHER is false.
-// Step 1 of hash_tile for the in-chunk tokens only (positions t >= 0 of the tile's window): ids,
-// mask and token_map, which a call with early reads may read before pdl_wait(). The row checks raise
-// no flag here; hash_tile raises them after the wait.
-__device__ __forceinline__ void stage_tokens_early(const StateView& sv, const CallArgs& a, unsigned char* smem,
-                                                   const SmemPlan& plan, const int b, const int64_t seq_off,
-                                                   const int64_t Lb, const int64_t t0, const int ntok,
-                                                   unsigned int* flags_s) {
-  const int N = sv.max_ngram;
-  int32_t* tok_s = reinterpret_cast<int32_t*>(smem + plan.tok_off);
-  const int64_t s_b = (int64_t)a.start_pos[b];
-  const int64_t r_b = a.cache_rows != nullptr ? (int64_t)a.cache_rows[b] : (int64_t)b;
-  const bool row_ok = (r_b >= 0) && (r_b < sv.max_batch) && (s_b >= 0) && (s_b <= sv.max_seq_len - Lb);
-  for (int j = threadIdx.x; j < ntok + N - 1; j += blockDim.x) {
-    const int64_t t = t0 - (N - 1) + j;
-    if (t < 0) continue;
-    int32_t c = sv.dead;
-    if (in_bounds(seq_off + t >= 0 && seq_off + t < a.total, flags_s)) {
-      const int64_t id = a.ids[seq_off + t];
-      if (id < 0 || id >= sv.raw_vocab) {
-        if (row_ok) atomicOr(flags_s, ENGRAM_STATUS_BAD_ID);
-      } else {
-        c = sv.token_map[id];
-      }
-      if (a.mask != nullptr && a.mask[seq_off + t] == 0) c = sv.dead;
-    }
-    tok_s[j] = c;
-  }
-}
-
 // The cache writes and hash-id stores of a tile whose hash phase ran with `defer` (before pdl_wait()):
 // the tokens are still in tok_s and the hash ids in rowidx_s.
 __device__ __forceinline__ void write_deferred(const StateView& sv, const CallArgs& a, const unsigned char* smem,
@@ -604,20 +571,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) hash_kernel(const StateV
   }
   const int ntok = (int)min((int64_t)tile, Lb - t0);
   if (tid == 0) flags_s = 0u;
-  // A tile whose lookback reaches below the chunk reads the cache, which the previous kernel may write:
-  // with early reads it stages its own tokens (ids, mask, token_map) first, then waits, then reads the
-  // cache (stage_part 2); a decode step's tile is such a tile.
-  int stage_part = 0;
-  if (early && t0 < sv.max_ngram - 1) {
-    __syncthreads();
-    stage_tokens_early(sv, a, smem, plan, b, seq_off, Lb, t0, ntok, &flags_s);
-    wait_once();
-    stage_part = 2;
-  }
+  if (early && t0 < sv.max_ngram - 1) wait_once();  // the lookback reads the cache below this chunk
   const bool defer = !waited;
   __syncthreads();
-  const bool row_ok = hash_tile(sv, a, smem, plan, tile, b, seq_off, Lb, t0, ntok, GATHER, dense, &flags_s, defer,
-                                stage_part);
+  const bool row_ok = hash_tile(sv, a, smem, plan, tile, b, seq_off, Lb, t0, ntok, GATHER, dense, &flags_s, defer);
 
   if (GATHER) {
     __syncthreads();
