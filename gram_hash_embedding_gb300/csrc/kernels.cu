@@ -43,7 +43,7 @@ namespace {
 #define ENGRAM_FUSED_TILE 8
 #endif
 #ifndef ENGRAM_TARGET_CTAS
-#define ENGRAM_TARGET_CTAS 1216
+#define ENGRAM_TARGET_CTAS 608
 #endif
 #ifndef ENGRAM_HASH_TILE
 #define ENGRAM_HASH_TILE 32
@@ -59,7 +59,10 @@ constexpr int kFusedTile = ENGRAM_FUSED_TILE;      // largest tile (tokens per C
                                                    // tiles beat 16 at full scale (more, shorter CTAs keep more
                                                    // row loads in flight; the hash phase is the same per token)
 constexpr int kMinFusedTile = 4;                   // below 4 tokens the halo and hash phase dominate
-constexpr int kTargetCtas = ENGRAM_TARGET_CTAS;    // fused grid size the tile choice aims for (2 waves)
+constexpr int kTargetCtas = ENGRAM_TARGET_CTAS;    // fused grid size the tile choice aims for (one wave at 4 CTAs
+                                                   // per SM; consecutive launches overlap, so fewer, fuller CTAs
+                                                   // win: an 8K-token chunk takes 33.6 us at 8-token tiles against
+                                                   // 36.8 us at 4-token tiles aiming for 1216 CTAs, same box)
 constexpr int kHashTile = ENGRAM_HASH_TILE;        // tokens per CTA, hash-only kernel
 constexpr int kHashThreads = ENGRAM_HASH_THREADS;  // threads per CTA, hash-only kernel (<= kThreads); 96 keeps
                                                    // every thread busy in step 3 at 48 columns (2 tokens a pass)
