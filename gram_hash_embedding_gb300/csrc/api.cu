@@ -53,19 +53,35 @@ inline Span span(const void* p, uint64_t bytes) {
   return Span{lo, lo + (uintptr_t)bytes};
 }
 
+// The per-thread default stream is a different stream in every host thread, so its record is the
+// thread's own; cudaStreamLegacy and the null handle name the same (legacy) stream.
+thread_local std::vector<Span> t_per_thread_writes;
+thread_local bool t_per_thread_recorded = false;
+
+uintptr_t stream_key(cudaStream_t s) { return s == cudaStreamLegacy ? 0 : reinterpret_cast<uintptr_t>(s); }
+
 void record_writes(cudaStream_t s, std::vector<Span> writes) {
+  if (s == cudaStreamPerThread) {
+    t_per_thread_writes = std::move(writes);
+    t_per_thread_recorded = true;
+    return;
+  }
   std::lock_guard<std::mutex> lock(g_writes_mutex);
-  g_last_writes[reinterpret_cast<uintptr_t>(s)] = std::move(writes);
+  g_last_writes[stream_key(s)] = std::move(writes);
+}
+
+bool overlaps(const std::vector<Span>& writes, const std::vector<Span>& inputs) {
+  for (const Span& w : writes)
+    for (const Span& r : inputs)
+      if (r.lo < w.hi && w.lo < r.hi) return true;
+  return false;
 }
 
 bool untouched_by_last_launch(cudaStream_t s, const std::vector<Span>& inputs) {
+  if (s == cudaStreamPerThread) return !t_per_thread_recorded || !overlaps(t_per_thread_writes, inputs);
   std::lock_guard<std::mutex> lock(g_writes_mutex);
-  auto it = g_last_writes.find(reinterpret_cast<uintptr_t>(s));
-  if (it == g_last_writes.end()) return true;
-  for (const Span& w : it->second)
-    for (const Span& r : inputs)
-      if (r.lo < w.hi && w.lo < r.hi) return false;
-  return true;
+  auto it = g_last_writes.find(stream_key(s));
+  return it == g_last_writes.end() || !overlaps(it->second, inputs);
 }
 
 // After a launch path: record what it wrote on success; after a failure what ran is unknown, so the
