@@ -8,7 +8,6 @@
 
 namespace engram {
 namespace tc {
-
 // A wait that has not completed after this many nanoseconds of the global timer gives up. Real
 // waits in these kernels last microseconds; the limit only ends a kernel that would otherwise hang.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -177,13 +176,6 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-
-}  // namespace tc
-}  // namespace engram
-
-namespace engram {
-namespace tc {
-
 // ------------------------------------------------------------------------------------------ CTA pairs
 // A cluster of two CTAs on two SMs runs one tensor-core MMA of M = 256 together (cta_group::2):
 // rank 0 (the leader) issues it; each CTA supplies half of A and half of B from its own shared
@@ -253,13 +245,6 @@ __device__ __forceinline__ void commit_pair_multicast(uint32_t bar, uint16_t cta
                ::"r"(bar), "h"(cta_mask)
                : "memory");
 }
-
-}  // namespace tc
-}  // namespace engram
-
-namespace engram {
-namespace tc {
-
 // 2-D tiled load multicast to the CTAs of `cta_mask` (the same shared-memory offset in each); the
 // completion of each copy is counted on the mbarrier at offset `bar` of the leader of the
 // destination CTA's pair (`bar` a shared::cluster address of a pair leader)
@@ -271,13 +256,6 @@ __device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const v
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
       : "memory");
 }
-
-}  // namespace tc
-}  // namespace engram
-
-namespace engram {
-namespace tc {
-
 // ------------------------------------------------------------------------------------------ TMA stores
 // make this thread's generic-proxy shared-memory writes visible to the bulk copy engine
 __device__ __forceinline__ void fence_proxy_async_shared() {
