@@ -58,10 +58,12 @@ def parse_args(argv=None):
     p.add_argument("--block", action="store_true",
                    help="time the whole Engram block per step: hash + lookup, then per layer the wkv projection "
                         "and the gate, at the released width (dim 5120, 4 copies)")
-    p.add_argument("--proj", choices=["fused", "tcgen05", "cublas"], default="fused",
+    p.add_argument("--proj", choices=["fused", "lookahead", "tcgen05", "cublas"], default="fused",
                    help="--block: fused = engram_project_gate (tensor-core projection with the gate's sums in its "
-                        "epilogue, keys never written, then the gate's finishing pass); tcgen05 = engram_project "
-                        "then engram_gate; cublas = torch.matmul (cuBLAS) then engram_gate")
+                        "epilogue, keys never written, then the gate's finishing pass); lookahead = the hash alone, "
+                        "then per layer engram_lookup_project_gate (the lookup inside that projection, one tile "
+                        "group ahead); tcgen05 = engram_project then engram_gate; cublas = torch.matmul (cuBLAS) "
+                        "then engram_gate")
     p.add_argument("--shard", type=int, default=0, metavar="W",
                    help="time the device steps of the row-sharded lookup for W ranks on this GPU: engram_shard_pack "
                         "of the workload's layer-0 row ids and engram_shard_unpack of as many head_dim rows (the "
@@ -992,24 +994,42 @@ def run_block(args):
     qw = [torch.rand((hc, dim), generator=g).add_(0.5).to(torch.bfloat16).to(device) for _ in range(lay.n_layers)]
     kw = [torch.rand((hc, dim), generator=g).add_(0.5).to(torch.bfloat16).to(device) for _ in range(lay.n_layers)]
     x = torch.randn((T, hc, dim), generator=g).to(torch.bfloat16).to(device)
-    kv = None if args.proj == "fused" else torch.empty((T, dim * (hc + 1)), dtype=torch.bfloat16, device=device)
-    ws = (torch.empty(geng.engram_project_gate_workspace(T, hc, dim), dtype=torch.uint8, device=device)
-          if args.proj == "fused" else None)
+    lookahead = args.proj == "lookahead"
+    kv = (None if args.proj in ("fused", "lookahead")
+          else torch.empty((T, dim * (hc + 1)), dtype=torch.bfloat16, device=device))
+    ws = None
+    if args.proj == "fused":
+        ws = torch.empty(geng.engram_project_gate_workspace(T, hc, dim), dtype=torch.uint8, device=device)
+    elif lookahead:
+        ws = torch.empty(geng.engram_lookup_project_gate_workspace(T, lay.n_cols, lay.head_dim, hc, dim),
+                         dtype=torch.uint8, device=device)
+        runner.setup_mode("hash")  # the step hashes only; each layer's rows are looked up inside its projection
+        hashes = runner.hash_out.view(T, lay.n_layers, lay.n_cols)
     mask = None if runner.masks[0] is None else runner.masks[0].reshape(-1)
     stream = torch.cuda.current_stream(device)
     if args.proj == "fused":
         names = ["hash+lookup"] + [f"wkv+gate{l}" for l in range(lay.n_layers)]
+    elif lookahead:
+        names = ["hash"] + [f"lookup+wkv+gate{l}" for l in range(lay.n_layers)]
     else:
         names = ["hash+lookup"] + [f"{n}{l}" for l in range(lay.n_layers) for n in ("wkv", "gate")]
 
     def step(k, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        runner.step(k)
+        if lookahead:
+            runner.step_mode(k)
+        else:
+            runner.step(k)
         i = 1
         for l in range(lay.n_layers):
             if ev is not None:
                 ev[i].record(stream)
+            if lookahead:
+                geng.engram_lookup_project_gate(x, hashes[:, l, :], runner.W[l], runner.S[l], wkv[l], qw[l], kw[l],
+                                                lay.block, mask, workspace=ws, out=x)
+                i += 1
+                continue
             emb = runner.out[l].view(T, K)
             if args.proj == "fused":
                 geng.engram_project_gate(x, emb, wkv[l], qw[l], kw[l], mask, workspace=ws, out=x)
@@ -1049,17 +1069,24 @@ def run_block(args):
     gemm_flops = 2.0 * T * K * dim * (hc + 1)
     gate_bytes = T * 2.0 * dim * (3 * hc + 1)
     lookup_bytes = T * algo_bytes_per_token(lay)
-    roof = {"hash+lookup": {"bound": "hbm", "achieved": lookup_bytes / comp["hash+lookup"] / 1e3, "peak": peak_hbm,
-                            "unit": "GB/s"}}
+    if lookahead:  # the hash-only kernel: ids in, cache entries and int64 hash ids out
+        roof = {"hash": {"bound": "hbm", "achieved": T * runner.mode_bytes_per_token() / comp["hash"] / 1e3,
+                         "peak": peak_hbm, "unit": "GB/s"}}
+    else:
+        roof = {"hash+lookup": {"bound": "hbm", "achieved": lookup_bytes / comp["hash+lookup"] / 1e3,
+                                "peak": peak_hbm, "unit": "GB/s"}}
     proj_kernel = {"fused": "engram_project_gate: tcgen05 projection (CTA pairs) with the gate's sums in its "
                             "epilogue + the gate's finishing pass",
+                   "lookahead": "engram_lookup_project_gate: the lookup (warps of every CTA, one tile group ahead) "
+                                "inside the tcgen05 projection with the gate's sums in its epilogue + the gate's "
+                                "finishing pass",
                    "tcgen05": "engram_project: tcgen05 projection (CTA pairs)",
                    "cublas": "cuBLAS bf16 GEMM (library)"}[args.proj]
     for l in range(lay.n_layers):
-        if args.proj == "fused":
-            roof[f"wkv+gate{l}"] = {"bound": "tensor", "achieved": gemm_flops / comp[f"wkv+gate{l}"] / 1e6,
-                                    "peak": float(peaks["bf16_tflops_sustained"]), "unit": "TFLOP/s",
-                                    "kernel": proj_kernel}
+        if args.proj in ("fused", "lookahead"):
+            name = f"wkv+gate{l}" if args.proj == "fused" else f"lookup+wkv+gate{l}"
+            roof[name] = {"bound": "tensor", "achieved": gemm_flops / comp[name] / 1e6,
+                          "peak": float(peaks["bf16_tflops_sustained"]), "unit": "TFLOP/s", "kernel": proj_kernel}
             continue
         roof[f"wkv{l}"] = {"bound": "tensor", "achieved": gemm_flops / comp[f"wkv{l}"] / 1e6,
                            "peak": float(peaks["bf16_tflops_sustained"]), "unit": "TFLOP/s", "kernel": proj_kernel}
@@ -1078,7 +1105,8 @@ def run_block(args):
         "component_us": comp, "roofline": roof, "clocks": clocks.summary(),
         # ours per step: the fused hash + lookup, and per layer projection + finishing pass (fused), projection +
         # gate (tcgen05), or the gate alone (cublas: the projection is cuBLAS's)
-        "gpu_launches": K_steps * (runner.launches_per_step + lay.n_layers * (2 if args.proj != "cublas" else 1)),
+        "gpu_launches": K_steps * (runner.launches_per_step +
+                                   lay.n_layers * {"cublas": 1, "lookahead": 3}.get(args.proj, 2)),
     }
     print(json.dumps(line), flush=True)
 

@@ -30,7 +30,8 @@ __all__ = [
     "STATUS_BAD_ID", "STATUS_BAD_LENGTH", "STATUS_BAD_ROW", "STATUS_CHECK", "SCALE_F32", "SCALE_BF16", "SCALE_E8M0", "SCALE_E4M3",
     "library_path", "set_l2_fetch_granularity", "engram_project", "engram_project_gate",
     "engram_project_gate_workspace", "engram_device_status", "STATUS_TIMEOUT", "engram_shard_pack",
-    "engram_shard_unpack", "shard_part", "sharded_lookup", "dist_exchange",
+    "engram_shard_unpack", "shard_part", "sharded_lookup", "dist_exchange", "engram_lookup_project",
+    "engram_lookup_project_workspace", "engram_lookup_project_gate", "engram_lookup_project_gate_workspace",
 ]
 
 OK, ERR_INVALID, ERR_RANGE, ERR_CUDA, ERR_NOMEM, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5
@@ -60,6 +61,11 @@ class _Layout(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("max_seq_len", ctypes.c_int64), ("raw_vocab", ctypes.c_int64), ("dead", ctypes.c_int64),
                 ("pad_id", ctypes.c_int64), ("scale_dtype", ctypes.c_int32)]
+
+
+class _Table(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("S", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("head_dim", ctypes.c_int32), ("block", ctypes.c_int32), ("scale_dtype", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -95,6 +101,14 @@ def _lib():
         L.engram_project_gate.argtypes = [_P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, ctypes.c_float, _P,
                                           ctypes.c_uint64, _P, _P]
         L.engram_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+        L.engram_lookup_project_workspace.argtypes = [_I64, _I32, _I32]
+        L.engram_lookup_project_workspace.restype = ctypes.c_uint64
+        L.engram_lookup_project.argtypes = [_P, _I64, _I64, _I32, ctypes.POINTER(_Table), _P, _I32, _P,
+                                            ctypes.c_uint64, _P, _P]
+        L.engram_lookup_project_gate_workspace.argtypes = [_I64, _I32, _I32, _I32, _I32]
+        L.engram_lookup_project_gate_workspace.restype = ctypes.c_uint64
+        L.engram_lookup_project_gate.argtypes = [_P, _P, _I64, _I64, _I32, ctypes.POINTER(_Table), _P, _P, _P, _P,
+                                                 _I32, _I32, ctypes.c_float, _P, ctypes.c_uint64, _P, _P]
         L.engram_shard_pack_workspace.argtypes = [_I64, _I32]
         L.engram_shard_pack_workspace.restype = ctypes.c_uint64
         L.engram_shard_pack.argtypes = [_P, _I64, _I64, _I32, _P, _P, _P, _P, ctypes.c_uint64, _P]
@@ -105,7 +119,8 @@ def _lib():
         for name in ("engram_state_create", "engram_state_destroy", "engram_cache_reset", "engram_state_status",
                      "engram_hash", "engram_lookup", "engram_hash_lookup", "engram_state_layout",
                      "engram_hash_varlen", "engram_hash_lookup_varlen", "engram_gate", "engram_project",
-                     "engram_project_gate", "engram_device_status", "engram_shard_pack", "engram_shard_unpack"):
+                     "engram_project_gate", "engram_device_status", "engram_shard_pack", "engram_shard_unpack",
+                     "engram_lookup_project", "engram_lookup_project_gate"):
             getattr(L, name).restype = ctypes.c_int
         _lib_handle = L
     return _lib_handle
@@ -507,6 +522,111 @@ def engram_project_gate(x: torch.Tensor, emb: torch.Tensor, wkv: torch.Tensor, q
                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                       _dev(out, torch.bfloat16, "out"), _launch_stream(stream, temps)),
            "engram_project_gate")
+    return out
+
+
+def _table(W: torch.Tensor, S: torch.Tensor, block: int, scale_dtype=None) -> _Table:
+    sdt = _scale_dtype_of(S, scale_dtype)
+    rows, D = W.shape
+    if int(block) > 0 and D % int(block) == 0:
+        _size(S, rows * (D // int(block)), "S")
+    return _Table(_dev(W.view(torch.uint8), torch.uint8, "W"), _dev_scales(S, sdt), rows, D, int(block), sdt)
+
+
+def _hash_ids(idx: torch.Tensor):
+    """idx int64 [T, C] with unit stride along C (e.g. one layer of an engram_hash output viewed as
+    [T, n_layers, C][:, layer]): returns (pointer, row stride, T, C)."""
+    if not isinstance(idx, torch.Tensor) or not idx.is_cuda or idx.dtype != torch.int64:
+        raise TypeError("idx must be an int64 CUDA tensor")
+    if idx.dim() != 2 or (idx.shape[1] > 1 and idx.stride(1) != 1):
+        raise ValueError(f"idx must be [T, C] with unit stride along C, got shape {tuple(idx.shape)} "
+                         f"strides {idx.stride()}")
+    T, C = idx.shape
+    stride = idx.stride(0) if T > 1 else C
+    if stride < C:
+        raise ValueError("idx rows overlap")
+    return idx.data_ptr(), stride, T, C
+
+
+def _workspace(workspace, need: int, device, temps: list) -> tuple:
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        temps.append(workspace)
+    nbytes = workspace.numel() * workspace.element_size()
+    if nbytes < need:
+        raise ValueError(f"workspace holds {nbytes} bytes, need {need}")
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return workspace.data_ptr(), nbytes
+
+
+def engram_lookup_project_workspace(T: int, n_cols: int, head_dim: int) -> int:
+    """Bytes of workspace engram_lookup_project needs."""
+    return int(_lib().engram_lookup_project_workspace(int(T), int(n_cols), int(head_dim)))
+
+
+def engram_lookup_project(idx: torch.Tensor, W: torch.Tensor, S: torch.Tensor, wkv: torch.Tensor, block: int,
+                          out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None,
+                          scale_dtype: int | None = None) -> torch.Tensor:
+    """The lookup and the `wkv` projection in one kernel: idx int64 [T, C] hash ids of one layer (unit
+    stride along C); W, S that layer's table (as engram_lookup); wkv bf16 [N, C * head_dim].
+    Returns (or fills) bf16 [T, N], bit-identical to engram_project(engram_lookup(idx, W, S), wkv).
+    workspace: uint8 CUDA tensor of engram_lookup_project_workspace(T, C, head_dim) bytes (allocated
+    here when None)."""
+    ptr, stride, T, C = _hash_ids(idx)
+    tb = _table(W, S, block, scale_dtype)
+    N = wkv.shape[0]
+    _size(wkv, N * C * tb.head_dim, "wkv")
+    temps = []
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=idx.device)
+        temps.append(out)
+    _size(out, T * N, "out")
+    ws, nbytes = _workspace(workspace, engram_lookup_project_workspace(T, C, tb.head_dim), idx.device, temps)
+    _check(_lib().engram_lookup_project(ptr, stride, T, C, ctypes.byref(tb), _dev(wkv, torch.bfloat16, "wkv"), N,
+                                        ws, nbytes, _dev(out, torch.bfloat16, "out"), _launch_stream(stream, temps)),
+           "engram_lookup_project")
+    return out
+
+
+def engram_lookup_project_gate_workspace(T: int, n_cols: int, head_dim: int, hc: int, dim: int) -> int:
+    """Bytes of workspace engram_lookup_project_gate needs (0 for T == 0 or an unsupported shape)."""
+    return int(_lib().engram_lookup_project_gate_workspace(int(T), int(n_cols), int(head_dim), int(hc), int(dim)))
+
+
+def engram_lookup_project_gate(x: torch.Tensor, idx: torch.Tensor, W: torch.Tensor, S: torch.Tensor,
+                               wkv: torch.Tensor, q_weight: torch.Tensor, k_weight: torch.Tensor, block: int,
+                               mask: torch.Tensor | None = None, eps: float = 1e-20,
+                               workspace: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                               stream=None, scale_dtype: int | None = None) -> torch.Tensor:
+    """The whole Engram block of one layer from its hash ids: the lookup inside the `wkv` projection,
+    the gate's sums in its epilogue, then the gate. x bf16 [T, hc, dim]; idx int64 [T, C]; W, S the
+    layer's table; wkv bf16 [(hc+1)*dim, C * head_dim]; q_weight / k_weight bf16 [hc, dim]; mask [T]
+    bool or None. Returns (or fills; may be x) bf16 [T, hc, dim], bit-identical to
+    engram_project_gate(x, engram_lookup(idx, W, S).view(T, -1), wkv, ...)."""
+    ptr, stride, T, C = _hash_ids(idx)
+    tb = _table(W, S, block, scale_dtype)
+    hc, dim = x.shape[-2], x.shape[-1]
+    if x.numel() != T * hc * dim:
+        raise ValueError(f"x holds {x.numel()} values, expected T * hc * dim = {T * hc * dim}")
+    temps = []
+    if out is None:
+        out = torch.empty_like(x)
+        temps.append(out)
+    _size(wkv, (hc + 1) * dim * C * tb.head_dim, "wkv")
+    _size(q_weight, hc * dim, "q_weight")
+    _size(k_weight, hc * dim, "k_weight")
+    _size(mask, T, "mask")
+    _size(out, T * hc * dim, "out")
+    need = engram_lookup_project_gate_workspace(T, C, tb.head_dim, hc, dim)
+    ws, nbytes = _workspace(workspace, need, x.device, temps)
+    m = None if mask is None else _dev(_as_u8(mask), torch.uint8, "mask")
+    _check(_lib().engram_lookup_project_gate(_dev(x, torch.bfloat16, "x"), ptr, stride, T, C, ctypes.byref(tb),
+                                             _dev(wkv, torch.bfloat16, "wkv"),
+                                             _dev(q_weight, torch.bfloat16, "q_weight"),
+                                             _dev(k_weight, torch.bfloat16, "k_weight"), m, hc, dim, float(eps), ws,
+                                             nbytes, _dev(out, torch.bfloat16, "out"), _launch_stream(stream, temps)),
+           "engram_lookup_project_gate")
     return out
 
 

@@ -504,6 +504,105 @@ int engram_project_gate(const uint16_t* x, const uint16_t* emb, const uint16_t* 
                   {span(out, (uint64_t)T * hc * dim * 2), span(workspace, workspace_bytes)});
 }
 
+namespace {
+// workspace of the lookup-ahead projections: the looked-up rows, then the counters
+uint64_t lookup_rows_bytes(int64_t T, int32_t n_cols, int32_t head_dim) {
+  return round256((uint64_t)T * (uint64_t)n_cols * (uint64_t)head_dim * 2u);
+}
+uint64_t lookup_counter_bytes(int64_t T) { return round256((uint64_t)engram::lookup_ahead_counters(T) * 4u); }
+
+// common checks of engram_lookup_project(_gate) past T == 0; fills the lookup arguments
+int lookup_ahead_args(const int64_t* idx, int64_t idx_stride, int32_t n_cols, const engram_table* tb,
+                      void* workspace, engram::LookupArgs* la) {
+  if (idx == nullptr || !aligned(idx, 8) || idx_stride < n_cols || workspace == nullptr || !aligned(workspace, 256))
+    return ENGRAM_ERR_INVALID;
+  if (tb->rows > 0 && (tb->W == nullptr || tb->S == nullptr || !aligned(tb->W, 16) ||
+                       !aligned(tb->S, scale_bytes(tb->scale_dtype))))
+    return ENGRAM_ERR_INVALID;
+  la->idx = idx;
+  la->idx_stride = idx_stride;
+  la->n_cols = n_cols;
+  la->W = static_cast<const uint8_t*>(tb->W);
+  la->S = tb->S;
+  la->rows = tb->rows;
+  la->head_dim = tb->head_dim;
+  la->block = tb->block;
+  la->scale_dtype = tb->scale_dtype;
+  la->emb = static_cast<uint16_t*>(workspace);
+  return ENGRAM_OK;
+}
+
+// the shape checks that do not depend on pointers (T >= 0 checked by the caller)
+int lookup_ahead_shape(int64_t T, int32_t n_cols, const engram_table* tb) {
+  if (tb == nullptr || n_cols < 1 || tb->rows < 0) return ENGRAM_ERR_INVALID;
+  if (!head_dim_ok(tb->head_dim, tb->block) || !scale_dtype_ok(tb->scale_dtype) || T > INT32_MAX ||
+      (int64_t)n_cols * tb->head_dim > INT32_MAX - 256)
+    return ENGRAM_ERR_UNSUPPORTED;
+  return ENGRAM_OK;
+}
+}  // namespace
+
+uint64_t engram_lookup_project_workspace(int64_t T, int32_t n_cols, int32_t head_dim) {
+  if (T <= 0 || n_cols <= 0 || head_dim <= 0) return 0;
+  return lookup_rows_bytes(T, n_cols, head_dim) + lookup_counter_bytes(T);
+}
+
+int engram_lookup_project(const int64_t* idx, int64_t idx_stride, int64_t T, int32_t n_cols,
+                          const engram_table* table, const uint16_t* wkv, int32_t N, void* workspace,
+                          uint64_t workspace_bytes, uint16_t* out, engram_stream_t stream) {
+  if (T < 0) return ENGRAM_ERR_INVALID;
+  int rc = lookup_ahead_shape(T, n_cols, table);
+  if (rc != ENGRAM_OK) return rc;
+  if (N < 8 || N % 8 != 0 || N > INT32_MAX - 256) return ENGRAM_ERR_UNSUPPORTED;
+  if (T == 0) return ENGRAM_OK;
+  engram::LookupArgs la;
+  rc = lookup_ahead_args(idx, idx_stride, n_cols, table, workspace, &la);
+  if (rc != ENGRAM_OK) return rc;
+  if (wkv == nullptr || out == nullptr || !aligned(wkv, 16) || !aligned(out, 16)) return ENGRAM_ERR_INVALID;
+  if (workspace_bytes < engram_lookup_project_workspace(T, n_cols, table->head_dim)) return ENGRAM_ERR_INVALID;
+  la.counters = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(workspace) +
+                                                lookup_rows_bytes(T, n_cols, table->head_dim));
+  return launched(launch_rc(engram::launch_lookup_project(la, wkv, T, N, out, (cudaStream_t)stream)),
+                  (cudaStream_t)stream, {span(out, (uint64_t)T * N * 2), span(workspace, workspace_bytes)});
+}
+
+uint64_t engram_lookup_project_gate_workspace(int64_t T, int32_t n_cols, int32_t head_dim, int32_t hc, int32_t dim) {
+  const uint64_t rows = engram_lookup_project_workspace(T, n_cols, head_dim);
+  const uint64_t gate = engram_project_gate_workspace(T, hc, dim);
+  return rows == 0 || gate == 0 ? 0 : rows + gate;
+}
+
+int engram_lookup_project_gate(const uint16_t* x, const int64_t* idx, int64_t idx_stride, int64_t T, int32_t n_cols,
+                               const engram_table* table, const uint16_t* wkv, const uint16_t* q_weight,
+                               const uint16_t* k_weight, const uint8_t* mask, int32_t hc, int32_t dim, float eps,
+                               void* workspace, uint64_t workspace_bytes, uint16_t* out, engram_stream_t stream) {
+  if (T < 0) return ENGRAM_ERR_INVALID;
+  int rc = lookup_ahead_shape(T, n_cols, table);
+  if (rc != ENGRAM_OK) return rc;
+  if (!gate_shape_ok(hc, dim)) return ENGRAM_ERR_UNSUPPORTED;
+  if (T == 0) return ENGRAM_OK;
+  engram::LookupArgs la;
+  rc = lookup_ahead_args(idx, idx_stride, n_cols, table, workspace, &la);
+  if (rc != ENGRAM_OK) return rc;
+  if (x == nullptr || wkv == nullptr || q_weight == nullptr || k_weight == nullptr || out == nullptr)
+    return ENGRAM_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(wkv, 16) || !aligned(q_weight, 16) || !aligned(k_weight, 16) || !aligned(out, 16))
+    return ENGRAM_ERR_INVALID;
+  if (workspace_bytes < engram_lookup_project_gate_workspace(T, n_cols, table->head_dim, hc, dim))
+    return ENGRAM_ERR_INVALID;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const uint64_t rows_bytes = lookup_rows_bytes(T, n_cols, table->head_dim);
+  la.counters = reinterpret_cast<unsigned int*>(ws + rows_bytes);
+  uint8_t* gate_ws = ws + rows_bytes + lookup_counter_bytes(T);
+  uint16_t* value = reinterpret_cast<uint16_t*>(gate_ws);
+  float* part = reinterpret_cast<float*>(gate_ws + round256((uint64_t)T * dim * 2u));
+  cudaStream_t s = (cudaStream_t)stream;
+  rc = launch_rc(engram::launch_lookup_project_gate_sums(x, la, wkv, q_weight, k_weight, T, hc, dim, value, part, s));
+  if (rc != ENGRAM_OK) return launched(rc, s, {});
+  return launched(launch_rc(engram::launch_gate_finish(x, value, part, mask, T, hc, dim, eps, out, s)), s,
+                  {span(out, (uint64_t)T * hc * dim * 2), span(workspace, workspace_bytes)});
+}
+
 int engram_device_status(engram_stream_t stream, uint32_t* flags, int clear) {
   if (flags == nullptr) return ENGRAM_ERR_INVALID;
   unsigned int v = 0;

@@ -20,6 +20,9 @@
 //               swizzled shared-memory chunk per warp, written out by a TMA store), or (gate epilogue)
 //               turns a key tile into three partial sums per row.
 // The two accumulators let the epilogue of tile i run while the tensor cores compute tile i+1.
+// The lookup-ahead form (engram_lookup_project*) adds warps 6-9, which look the rows of A up from the
+// hash ids into a workspace one tile group ahead of the loads (see "lookup ahead" below); the loader
+// waits, once per group, until that group's rows are written.
 // Tiles are visited in groups of 16 tile rows, column block outer, so the tiles in flight share a few
 // A and B blocks, which stay in L2. Built with ENGRAM_PROJ_CLUSTER=1 or 4 the same kernel runs one
 // CTA per tile (M = 128 MMAs) or two pairs side by side that share A by TMA multicast; both measured
@@ -33,6 +36,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "dequant.cuh"
 #include "engram_internal.cuh"
 #include "proj.cuh"
 #include "tc_ptx.cuh"
@@ -51,6 +55,19 @@ constexpr int kUmmaK = 16;         // K of one tcgen05.mma (kind::f16)
 constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
+#ifndef ENGRAM_LOOKUP_WARPS
+#define ENGRAM_LOOKUP_WARPS 4
+#endif
+#ifndef ENGRAM_LOOKUP_BATCH
+#define ENGRAM_LOOKUP_BATCH 8
+#endif
+#ifndef ENGRAM_LOOKUP_CHUNK
+#define ENGRAM_LOOKUP_CHUNK 8
+#endif
+constexpr int kLookupWarps = ENGRAM_LOOKUP_WARPS;  // lookup ahead: warps 6, 7, ... look the rows of A up
+constexpr int kThreadsLookup = kThreads + 32 * kLookupWarps;
+constexpr int kChunkTokens = ENGRAM_LOOKUP_CHUNK;  // lookup ahead: tokens per chunk of work (all their columns)
+constexpr int kLookupBatch = ENGRAM_LOOKUP_BATCH;  // lookup ahead: 16-code pieces in flight per lane
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kEpiChunkBytes = 32 * 32 * 2;  // one epilogue warp's 32 rows x 32 columns of bf16
 #ifndef ENGRAM_PROJ_PAIR_STAGES
@@ -88,7 +105,8 @@ struct Cfg {
   static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
   static constexpr uint32_t kTmemSlotOff = kBarOff + 8 * kNumBars;  // tensor-memory base written by the alloc
   static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;          // set by a role whose wait ran out
-  static constexpr uint32_t kSmemBytes = kAbortOff + 4 + 1024;     // + slack to align the ring to 1024 bytes
+  static constexpr uint32_t kGroupOff = kAbortOff + 4;             // lookup ahead: the loader's tile group
+  static constexpr uint32_t kSmemBytes = kGroupOff + 4 + 1024;     // + slack to align the ring to 1024 bytes
 };
 
 enum Epilogue { EPI_STORE = 0, EPI_GATE = 1 };
@@ -117,6 +135,18 @@ struct ProjParams {
   // of its tile number `withhold` (counted from 0 per cluster), so that tile's epilogue waits in vain
   // until its time limit; -1: every tile is signalled
   int32_t withhold;
+  // Lookup ahead (engram_lookup_project*): A is the bf16 lookup of hash ids, written by this kernel's
+  // lookup warps into `emb` one tile group ahead of the loads that read it.
+  const int64_t* idx;       // token t's n_cols table row ids at idx[t * idx_stride + c]
+  int64_t idx_stride;
+  const uint8_t* W;         // fp8 E4M3 codes [rows][head_dim]
+  const void* S;            // scales [rows][head_dim / block], stored as scale_dtype
+  int64_t rows;
+  uint16_t* emb;            // [T][K] bf16, K = n_cols * head_dim: the looked-up rows (A of the projection)
+  unsigned int* counters;   // [0]: next chunk to take; [1 + g]: chunks of tile group g written
+  int64_t n_chunks;         // ceil(T / kChunkTokens)
+  int32_t group_tokens;     // tokens of one tile group
+  int32_t n_cols, head_dim, block, scale_dtype;
 };
 
 // tile index -> (tile row, column block): groups of `group` tile rows, column block outer, so the
@@ -252,8 +282,166 @@ __device__ __forceinline__ const uint16_t* h_row(const ProjParams& p, int64_t ro
   return p.x + (row * p.hc + i) * p.dim + (col0 - i * p.dim);
 }
 
-template <int EPI, int CS>
-__global__ void __launch_bounds__(kThreads, 1)
+// ------------------------------------------------------------------------------------------------
+// lookup ahead: warps 6-9 of every CTA look the rows of A up (engram-first/lookup page,
+// `ParallelEngramEmbedding.forward`, through the same dequantisation as engram_lookup) into the
+// workspace, one tile group ahead of the TMA loads that read them. The work is cut into chunks of
+// kChunkTokens tokens (all their columns), taken in token order from a global counter by whichever
+// warp is free, so no CTA waits on another one being resident. A warp takes a chunk of tile group g
+// only once its own CTA's loader has reached group g - 1, which keeps the looked-up rows of at most
+// two groups (8,192 tokens) ahead of the MMAs, in L2. The loader, before the first load of a tile
+// of group g, waits until all chunks of group g are written.
+
+__device__ __forceinline__ void st_v8(void* ptr, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
+// The row ids of one batch of units of a chunk: unit u = u0 + 32 i + lane is token t0 + tt[i],
+// column-and-piece cq[i] (column cq / pieces, piece cq % pieces); tt[i] = -1 past the chunk.
+__device__ __forceinline__ void lookup_ids(const ProjParams& p, int64_t t0, int u0, int n_units, int per_token,
+                                           int piece_shift, int lane, int64_t (&row)[kLookupBatch],
+                                           int (&tt)[kLookupBatch], int (&cq)[kLookupBatch]) {
+#pragma unroll
+  for (int i = 0; i < kLookupBatch; ++i) {
+    const int u = u0 + i * 32 + lane;
+    tt[i] = u < n_units ? u / per_token : -1;
+    cq[i] = u < n_units ? u - tt[i] * per_token : 0;
+    row[i] = u < n_units ? __ldg(p.idx + (t0 + tt[i]) * p.idx_stride + (cq[i] >> piece_shift)) : -1;
+  }
+}
+
+// Tokens [t0, t1), every column, into p.emb. Unit u is one 16-code piece (token t0 + u / per_token,
+// then column-and-piece u % per_token), so consecutive lanes read one row's codes contiguously and
+// write consecutive 32-byte pieces of the output. Each lane keeps kLookupBatch pieces in flight, and
+// the ids of the next batch are loaded while the current batch's codes and scales are on their way.
+// SDT (the scales' storage type) and ONE (a piece's 16 codes share one scale) are template
+// parameters: no branch may sit between a load and the end of the batch, since the copy that joins
+// two branches would wait for the loaded value and serialise the batch's loads.
+template <int SDT, bool ONE>
+__device__ __forceinline__ void lookup_chunk(const ProjParams& p, int64_t t0, int64_t t1, int lane) {
+  const int pieces = p.head_dim >> 4;
+  const int piece_shift = __ffs(pieces) - 1;
+  const int per_token = p.n_cols * pieces;
+  const int n_units = (int)(t1 - t0) * per_token;
+  const int64_t K = (int64_t)p.n_cols * p.head_dim;
+  const int64_t spr = p.head_dim / p.block;  // scales per table row
+  int64_t row[kLookupBatch];
+  int tt[kLookupBatch], cq[kLookupBatch];
+  lookup_ids(p, t0, 0, n_units, per_token, piece_shift, lane, row, tt, cq);
+#pragma unroll 1
+  for (int u0 = 0; u0 < n_units; u0 += 32 * kLookupBatch) {
+    uint4 code[kLookupBatch];
+    uint32_t s0[kLookupBatch], s1[kLookupBatch];
+    int tt_c[kLookupBatch], cq_c[kLookupBatch];
+    bool ok[kLookupBatch];
+#pragma unroll
+    for (int i = 0; i < kLookupBatch; ++i) {
+      code[i] = make_uint4(0u, 0u, 0u, 0u);
+      s0[i] = s1[i] = 0u;
+      ok[i] = row[i] >= 0 && row[i] < p.rows;
+      tt_c[i] = tt[i];
+      cq_c[i] = cq[i];
+      if (ok[i]) {
+        const int k0 = 16 * (cq[i] & (pieces - 1));
+        code[i] = ld_rows_v4(p.W + row[i] * p.head_dim + k0);
+        s0[i] = ld_scale_bits<SDT>(p.S, row[i] * spr + k0 / p.block);
+        if (!ONE) s1[i] = ld_scale_bits<SDT>(p.S, row[i] * spr + (k0 + 8) / p.block);
+      }
+    }
+    if (u0 + 32 * kLookupBatch < n_units)
+      lookup_ids(p, t0, u0 + 32 * kLookupBatch, n_units, per_token, piece_shift, lane, row, tt, cq);
+#pragma unroll
+    for (int i = 0; i < kLookupBatch; ++i) {
+      if (tt_c[i] < 0) continue;
+      uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;  // rows outside the table are +0
+      if (ok[i]) {
+        a = dequant8(make_uint2(code[i].x, code[i].y), widen_scale<SDT>(s0[i]));
+        b = dequant8(make_uint2(code[i].z, code[i].w), widen_scale<SDT>(ONE ? s0[i] : s1[i]));
+      }
+      st_v8(p.emb + (t0 + tt_c[i]) * K + 16 * (int64_t)cq_c[i], a, b);
+    }
+  }
+}
+
+template <int SDT>
+__device__ __forceinline__ void lookup_chunk_s(const ProjParams& p, int64_t t0, int64_t t1, int lane) {
+  if (p.block >= 16)
+    lookup_chunk<SDT, true>(p, t0, t1, lane);
+  else
+    lookup_chunk<SDT, false>(p, t0, t1, lane);
+}
+
+__device__ __forceinline__ void lookup_chunk_any(const ProjParams& p, int64_t t0, int64_t t1, int lane) {
+  switch (p.scale_dtype) {
+    case ENGRAM_SCALE_F32: lookup_chunk_s<ENGRAM_SCALE_F32>(p, t0, t1, lane); break;
+    case ENGRAM_SCALE_BF16: lookup_chunk_s<ENGRAM_SCALE_BF16>(p, t0, t1, lane); break;
+    case ENGRAM_SCALE_E8M0: lookup_chunk_s<ENGRAM_SCALE_E8M0>(p, t0, t1, lane); break;
+    default: lookup_chunk_s<ENGRAM_SCALE_E4M3>(p, t0, t1, lane); break;
+  }
+}
+
+// lane 0 of a lookup warp: wait until this CTA's loader has reached tile group `need` (or finished).
+// A group lasts hundreds of microseconds at the block's shapes, so the warp polls every few
+// microseconds: polling every 256 ns cost the projection about 1% (measured at 65,536 tokens).
+__device__ __forceinline__ bool pace_wait(const volatile int* cur_group, int32_t need, const volatile int* abort) {
+  const uint64_t t0 = tc::global_timer_ns();
+  while (*cur_group < need) {
+    if (*abort || tc::global_timer_ns() - t0 > tc::kWaitLimitNs) return false;
+    __nanosleep(4000);
+  }
+  return true;
+}
+
+// the loader: wait until `need` chunks of a tile group are written (acquire: their rows are visible)
+__device__ __forceinline__ bool ready_wait(const unsigned int* ctr, unsigned int need, const volatile int* abort) {
+  const uint64_t t0 = tc::global_timer_ns();
+  for (;;) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= need) return true;
+    if (*abort || tc::global_timer_ns() - t0 > tc::kWaitLimitNs) return false;
+    __nanosleep(128);
+  }
+}
+
+__device__ __forceinline__ void red_release_add(unsigned int* ctr, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
+// chunks of tile group g: [g * per_group, min(n_chunks, (g + 1) * per_group))
+__device__ __forceinline__ unsigned int group_chunks(const ProjParams& p, int32_t g) {
+  const int64_t per = p.group_tokens / kChunkTokens;
+  const int64_t c0 = (int64_t)g * per;
+  return (unsigned int)(min(p.n_chunks, c0 + per) - c0);
+}
+
+__device__ __forceinline__ void lookup_warp(const ProjParams& p, const volatile int* cur_group, volatile int* abort) {
+  const int lane = threadIdx.x & 31;
+  for (;;) {
+    unsigned int chunk = 0;
+    if (lane == 0) chunk = atomicAdd(&p.counters[0], 1u);
+    chunk = __shfl_sync(0xffffffffu, chunk, 0);
+    if ((int64_t)chunk >= p.n_chunks) break;
+    const int64_t t0 = (int64_t)chunk * kChunkTokens;
+    const int32_t g = (int32_t)(t0 / p.group_tokens);
+    int ok = 1;
+    if (lane == 0) {
+      ok = pace_wait(cur_group, g - 1, abort) ? 1 : 0;
+      if (!ok) raise_timeout(abort);
+    }
+    if (__shfl_sync(0xffffffffu, ok, 0) == 0) break;
+    lookup_chunk_any(p, t0, min(p.T, t0 + kChunkTokens), lane);
+    tc::fence_proxy_async_global();  // the rows are read next by TMA loads (the async proxy)
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_add(&p.counters[1 + g], 1u);
+  }
+}
+
+template <int EPI, int CS, bool LA>
+__global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const ProjParams p) {
   using C = Cfg<CS>;
@@ -263,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;  // the same offset in every CTA of a cluster
   uint8_t* gbase = smem_raw + (base - raw);
   volatile int* abort = reinterpret_cast<volatile int*>(gbase + C::kAbortOff);
+  volatile int* cur_group = reinterpret_cast<volatile int*>(gbase + C::kGroupOff);
   const uint32_t* tmem_slot = reinterpret_cast<const uint32_t*>(gbase + C::kTmemSlotOff);
   auto bar = [&](int i) { return base + C::kBarOff + 8u * (uint32_t)i; };
   auto full = [&](uint32_t s) { return bar((int)s); };
@@ -296,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc::mbar_init(drain, 1);
     *abort = 0;
+    *cur_group = 0;
     tc::fence_barrier_init();
     tc::tma_prefetch_descriptor(&tmA);
     tc::tma_prefetch_descriptor(&tmB);
@@ -322,9 +512,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- TMA loader (every CTA)
     int64_t issued = 0;
     uint32_t stage = 0, phase = 0;
+    int32_t ready_group = -1;
     for (int64_t tile = unit; tile < p.n_tiles && !*abort; tile += n_units) {
       int32_t mt, nt;
       tile_coords(p, C::kGroup, tile, mt, nt);
+      if (LA) {
+        // the rows of this tile's group must be looked up before the first load of A reads them
+        const int32_t g = (int32_t)(tile / ((int64_t)C::kGroup * p.n_ntile));
+        if (g != ready_group) {
+          *cur_group = g;  // this CTA's lookup warps may take chunks of group g + 1 from now on
+          if (!ready_wait(p.counters + 1 + g, group_chunks(p, g), abort)) {
+            raise_timeout(abort);
+            break;
+          }
+          tc::fence_proxy_async_global();
+          ready_group = g;
+        }
+      }
       const int32_t nb = nt * C::kNBlocks + (int32_t)pr;
       const int32_t arow0 = mt * C::kTileM + (int32_t)q * kBM + (int32_t)pr * C::kARows;
       const int32_t brow0 = nb * kBN + (int32_t)q * C::kBRows;
@@ -355,6 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (LA) *cur_group = 0x7fffffff;  // no more loads: the lookup warps take any chunk left
     // No copy may still be landing in shared memory when the CTA exits. A CTA of a pair counts its
     // loads on its leader's barriers, so it waits for the MMAs that read its last loads instead
     // (which implies they landed); a lone CTA waits for the loads themselves.
@@ -422,7 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     else
       tc::commit(drain);
     if (!tc::mbar_wait(drain, 0, nullptr)) atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
-  } else if (warp >= 2) {
+  } else if (LA && warp >= 6) {
+    // ---------------------------------------------------------------- lookup ahead (every CTA)
+    lookup_warp(p, cur_group, abort);
+  } else if (warp >= 2 && warp < 6) {
     // ---------------------------------------------------------------- epilogue (every CTA)
     const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
     const int r = quarter * 32 + lane;
@@ -566,7 +774,7 @@ ProjParams base_params(int64_t T, int32_t K, int32_t N) {
 
 // as many persistent clusters as can be resident at once, launched as a programmatic dependent like
 // every kernel of the library
-template <int EPI>
+template <int EPI, bool LA = false>
 cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
   using C = Cfg<kCS>;
   CUtensorMap ta, tb, to;
@@ -577,7 +785,7 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
       !make_map(&tb, w, (uint64_t)p.N, (uint64_t)p.K, (uint32_t)C::kBRows) ||
       !make_map(&to, optr, (uint64_t)p.T, ocols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto kern = proj_kernel<EPI, kCS>;
+  auto kern = proj_kernel<EPI, kCS, LA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -588,7 +796,7 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
   attr[1].val.clusterDim.x = kCS;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(LA ? kThreadsLookup : kThreads);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -609,7 +817,58 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, to, p);
 }
 
+// lookup ahead: the lookup arguments, the rows' workspace, and its counters zeroed on the stream
+cudaError_t lookup_ahead_params(ProjParams& p, const LookupArgs& la, cudaStream_t s) {
+  using C = Cfg<kCS>;
+  static_assert((C::kGroup * C::kTileM) % kChunkTokens == 0, "a chunk of lookup work lies in one tile group");
+  p.idx = la.idx;
+  p.idx_stride = la.idx_stride;
+  p.n_cols = la.n_cols;
+  p.W = la.W;
+  p.S = la.S;
+  p.rows = la.rows;
+  p.head_dim = la.head_dim;
+  p.block = la.block;
+  p.scale_dtype = la.scale_dtype;
+  p.emb = la.emb;
+  p.counters = la.counters;
+  p.n_chunks = (p.T + kChunkTokens - 1) / kChunkTokens;
+  p.group_tokens = C::kGroup * C::kTileM;
+  return launch_fill_i32(reinterpret_cast<int32_t*>(la.counters), lookup_ahead_counters(p.T), 0, s);
+}
+
 }  // namespace
+
+int64_t lookup_ahead_counters(int64_t T) {
+  using C = Cfg<kCS>;
+  const int64_t group_tokens = (int64_t)C::kGroup * C::kTileM;
+  return 1 + (T + group_tokens - 1) / group_tokens;
+}
+
+cudaError_t launch_lookup_project(const LookupArgs& la, const uint16_t* wkv, int64_t T, int32_t N, uint16_t* out,
+                                  cudaStream_t s) {
+  ProjParams p = base_params(T, la.n_cols * la.head_dim, N);
+  p.out = out;
+  cudaError_t e = lookup_ahead_params(p, la, s);
+  if (e != cudaSuccess) return e;
+  return launch_proj<EPI_STORE, true>(la.emb, wkv, p, s);
+}
+
+cudaError_t launch_lookup_project_gate_sums(const uint16_t* x, const LookupArgs& la, const uint16_t* wkv,
+                                            const uint16_t* qw, const uint16_t* kw, int64_t T, int32_t hc,
+                                            int32_t dim, uint16_t* value, float* part, cudaStream_t s) {
+  ProjParams p = base_params(T, la.n_cols * la.head_dim, (hc + 1) * dim);
+  p.x = x;
+  p.qw = qw;
+  p.kw = kw;
+  p.value = value;
+  p.part = part;
+  p.hc = hc;
+  p.dim = dim;
+  cudaError_t e = lookup_ahead_params(p, la, s);
+  if (e != cudaSuccess) return e;
+  return launch_proj<EPI_GATE, true>(la.emb, wkv, p, s);
+}
 
 cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
                            cudaStream_t s, int32_t withhold) {

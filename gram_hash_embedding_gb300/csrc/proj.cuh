@@ -19,6 +19,28 @@ cudaError_t launch_project_gate_sums(const uint16_t* x, const uint16_t* emb, con
                                      const uint16_t* kw, int64_t T, int32_t K, int32_t hc, int32_t dim,
                                      uint16_t* value, float* part, cudaStream_t s);
 
+// The projection with its A looked up inside the same kernel, one tile group ahead of the loads
+// (engram_lookup_project*): token t's row ids at idx[t * idx_stride + c], c < n_cols; A = emb
+// [T][n_cols * head_dim] bf16, a workspace written by the kernel; counters: lookup_ahead_counters(T)
+// words of workspace, zeroed by the launcher on the stream.
+struct LookupArgs {
+  const int64_t* idx;
+  int64_t idx_stride;
+  int32_t n_cols;
+  const uint8_t* W;
+  const void* S;
+  int64_t rows;
+  int32_t head_dim, block, scale_dtype;
+  uint16_t* emb;
+  unsigned int* counters;
+};
+int64_t lookup_ahead_counters(int64_t T);
+cudaError_t launch_lookup_project(const LookupArgs& la, const uint16_t* wkv, int64_t T, int32_t N, uint16_t* out,
+                                  cudaStream_t s);
+cudaError_t launch_lookup_project_gate_sums(const uint16_t* x, const LookupArgs& la, const uint16_t* wkv,
+                                            const uint16_t* qw, const uint16_t* kw, int64_t T, int32_t hc,
+                                            int32_t dim, uint16_t* value, float* part, cudaStream_t s);
+
 // the gate from the partial sums, out = bf16(h + gate * value)
 cudaError_t launch_gate_finish(const uint16_t* x, const uint16_t* value, const float* part, const uint8_t* mask,
                                int64_t T, int hc, int dim, float eps, uint16_t* out, cudaStream_t s);

@@ -258,6 +258,9 @@ __device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const v
 }
 // ------------------------------------------------------------------------------------------ TMA stores
 // make this thread's generic-proxy shared-memory writes visible to the bulk copy engine
+// order this thread's generic-proxy global writes before later async-proxy (TMA) reads of them
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -303,6 +303,70 @@ int engram_project_gate(const uint16_t* x, const uint16_t* emb, const uint16_t* 
                         const uint16_t* k_weight, const uint8_t* mask, int64_t T, int32_t K, int32_t hc, int32_t dim,
                         float eps, void* workspace, uint64_t workspace_bytes, uint16_t* out, engram_stream_t stream);
 
+/*
+ * One layer's table, as engram_lookup takes it: fp8 E4M3 codes W [rows][head_dim] (16-byte
+ * aligned), scales S [rows][head_dim / block] stored as scale_dtype (ENGRAM_SCALE_*; aligned to
+ * their size). rows == 0 is an empty table (every row +0; W and S may then be NULL).
+ */
+typedef struct engram_table {
+  const void* W;
+  const void* S;
+  int64_t rows;
+  int32_t head_dim;
+  int32_t block;
+  int32_t scale_dtype;
+} engram_table;
+
+/* Bytes of device workspace that engram_lookup_project needs (a multiple of 256; 0 for T <= 0 or
+ * n_cols * head_dim <= 0): the looked-up bf16 rows [T][n_cols * head_dim] and a few counters. */
+uint64_t engram_lookup_project_workspace(int64_t T, int32_t n_cols, int32_t head_dim);
+
+/*
+ * The lookup and the `wkv` projection after it in one kernel (blocks/stack-hashes page,
+ * `Engram.forward`: kv = wkv(embed(hash ids) flattened over the hash columns); the embedding is
+ * `ParallelEngramEmbedding.forward` of the engram-first/lookup page):
+ *   emb[t][c * head_dim + k] = the bf16 row of engram_lookup for table row idx[t * idx_stride + c]
+ *   out[t][n] = bf16_rne( sum_k emb[t][k] * wkv[n][k] )        (fp32 accumulation)
+ * equal bit for bit to engram_lookup followed by engram_project. Warps of every CTA of the projection
+ * look the rows up into the workspace one tile group (4,096 tokens) ahead of the tensor-core loads
+ * that read them, which read them back from L2; only the first group's lookup runs before the first
+ * MMA. On GB300 this is as fast as the two calls at 65,536 tokens and 2% slower at 16,384 (the lookup
+ * inside the contraction still costs the tensor cores about its own time). Inputs written by an
+ * earlier launch on the stream are read after it completes.
+ *   idx         device int64: token t's n_cols row ids at idx[t * idx_stride + c] (8-byte aligned;
+ *               idx_stride >= n_cols), e.g. one layer's slice of engram_hash's output (stride
+ *               n_layers * C); ids outside [0, rows) give +0 rows
+ *   table       host pointer to the layer's table; head_dim and block as engram_lookup
+ *   wkv         device bf16 [N][n_cols * head_dim]; out  device bf16 [T][N], written
+ *   workspace   device memory of engram_lookup_project_workspace(T, n_cols, head_dim) bytes, 256-byte
+ *               aligned, owned by the caller; calls that use one workspace must not overlap on the GPU
+ * N a multiple of 8, N >= 8. T == 0 is a no-op. A wait that does not end (a lookup warp or load that
+ * stops progressing) raises ENGRAM_STATUS_TIMEOUT (engram_device_status) after one second instead of
+ * hanging. Errors: _INVALID (null, misaligned, idx_stride < n_cols, workspace too small), _UNSUPPORTED
+ * (head_dim, block, scale_dtype as engram_lookup; N; T >= 2^31), _CUDA.
+ */
+int engram_lookup_project(const int64_t* idx, int64_t idx_stride, int64_t T, int32_t n_cols,
+                          const engram_table* table, const uint16_t* wkv, int32_t N, void* workspace,
+                          uint64_t workspace_bytes, uint16_t* out, engram_stream_t stream);
+
+/* Bytes of device workspace that engram_lookup_project_gate needs (a multiple of 256). */
+uint64_t engram_lookup_project_gate_workspace(int64_t T, int32_t n_cols, int32_t head_dim, int32_t hc, int32_t dim);
+
+/*
+ * The whole Engram block for one layer from its hash ids (blocks/stack-hashes page, `Engram.forward`):
+ * the lookup of engram_lookup_project inside the projection of engram_project_gate, whose epilogue
+ * turns the key tiles into the gate's partial sums, then the gate's finishing pass:
+ *   out[t][i] = bf16_rne(h + gate * value),  h = x[t][i]
+ * equal bit for bit to engram_lookup, then engram_project_gate. Arguments as engram_lookup_project and
+ * engram_project_gate (wkv [(hc + 1) * dim][n_cols * head_dim]; x, out [T][hc][dim]; out may be x);
+ * workspace of engram_lookup_project_gate_workspace(T, n_cols, head_dim, hc, dim) bytes.
+ * Errors: as engram_lookup_project, and _UNSUPPORTED for hc or dim as engram_project_gate.
+ */
+int engram_lookup_project_gate(const uint16_t* x, const int64_t* idx, int64_t idx_stride, int64_t T, int32_t n_cols,
+                               const engram_table* table, const uint16_t* wkv, const uint16_t* q_weight,
+                               const uint16_t* k_weight, const uint8_t* mask, int32_t hc, int32_t dim, float eps,
+                               void* workspace, uint64_t workspace_bytes, uint16_t* out, engram_stream_t stream);
+
 /* Read the status flags of the kernels that have no state object (ENGRAM_STATUS_TIMEOUT) for the
  * current device into *flags, ordered after the work already on `stream` (synchronises it); clears
  * them in the same atomic step when `clear` is non-zero. The pages have no counterpart: it reports

@@ -150,6 +150,49 @@ def test_projection_checks_need_no_gpu(lib):
     assert lib.engram_project_gate(a, a, a, a, a, None, 0, 64, 4, 256, 1e-20, None, 0, a, None) == geng.OK
 
 
+def test_lookup_projection_checks_need_no_gpu(lib):
+    """engram_lookup_project(_gate): shapes, pointers and the workspace are checked before any launch."""
+    P = ctypes.c_void_p
+    L = geng._lib()  # the binding's argtypes, with the table struct
+    a = P(4096)  # never dereferenced
+    tb = geng._Table(4096, 4096, 100, 128, 128, geng.SCALE_F32)
+    need = L.engram_lookup_project_workspace(300, 24, 128)
+    # the looked-up rows (T x n_cols x head_dim bf16), then 1 + ceil(T / 4096) counters, each part 256-byte rounded
+    assert need == (300 * 24 * 128 * 2 + 255) // 256 * 256 + 256
+    assert L.engram_lookup_project_workspace(4097, 24, 128) == 4097 * 24 * 128 * 2 + 256
+    assert L.engram_lookup_project_workspace(0, 24, 128) == 0
+    ok = dict(idx=a, stride=24, T=300, C=24, wkv=a, N=256, ws=a, nbytes=need, out=a)
+
+    def call(**kw):
+        v = {**ok, **kw}
+        return L.engram_lookup_project(v["idx"], v["stride"], v["T"], v["C"], ctypes.byref(kw.get("tb", tb)), v["wkv"],
+                                       v["N"], v["ws"], v["nbytes"], v["out"], None)
+    assert call(T=0) == geng.OK
+    assert call(T=-1) == geng.ERR_INVALID
+    assert call(stride=23) == geng.ERR_INVALID          # rows of ids overlap
+    assert call(nbytes=need - 1) == geng.ERR_INVALID    # workspace too small
+    assert call(ws=P(4096 + 64)) == geng.ERR_INVALID    # workspace not 256-byte aligned
+    assert call(idx=P(4100)) == geng.ERR_INVALID        # ids not 8-byte aligned
+    assert call(out=None) == geng.ERR_INVALID
+    assert call(N=4) == geng.ERR_UNSUPPORTED
+    assert call(T=1 << 31) == geng.ERR_UNSUPPORTED
+    assert call(tb=geng._Table(4096, 4096, 100, 128, 48, geng.SCALE_F32)) == geng.ERR_UNSUPPORTED  # block
+    assert call(tb=geng._Table(4096, 4096, 100, 96, 32, geng.SCALE_F32)) == geng.ERR_UNSUPPORTED   # head_dim
+    assert call(tb=geng._Table(4096, 4096, 100, 128, 128, 7)) == geng.ERR_UNSUPPORTED              # scale type
+    assert call(tb=geng._Table(4098, 4096, 100, 128, 128, geng.SCALE_F32)) == geng.ERR_INVALID     # W misaligned
+    assert call(tb=geng._Table(4096, 4096, -1, 128, 128, geng.SCALE_F32)) == geng.ERR_INVALID
+    assert L.engram_lookup_project(a, 24, 8, 24, None, a, 256, a, need, a, None) == geng.ERR_INVALID  # no table
+    gneed = L.engram_lookup_project_gate_workspace(300, 24, 128, 4, 256)
+    assert gneed == need + L.engram_project_gate_workspace(300, 4, 256)
+    assert L.engram_lookup_project_gate_workspace(300, 24, 128, 3, 256) == 0
+    g = lambda hc, dim, nbytes, T=300: L.engram_lookup_project_gate(a, a, 24, T, 24, ctypes.byref(tb), a, a, a, None,
+                                                                    hc, dim, 1e-20, a, nbytes, a, None)
+    assert g(3, 256, gneed) == geng.ERR_UNSUPPORTED
+    assert g(4, 200, gneed) == geng.ERR_UNSUPPORTED
+    assert g(4, 256, gneed - 1) == geng.ERR_INVALID
+    assert g(4, 256, gneed, T=0) == geng.OK
+
+
 def test_shard_checks_need_no_gpu(lib):
     P = ctypes.c_void_p
     lib.engram_shard_pack_workspace.argtypes = [ctypes.c_int64, ctypes.c_int32]
