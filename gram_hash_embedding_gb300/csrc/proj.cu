@@ -10,10 +10,11 @@
 // each CTA holds its 128 rows of A and half of the B tile, and receives its 128 rows of the
 // accumulator in its own tensor memory. The 76 pairs are persistent and walk the tile list. In each
 // CTA the warps specialise:
-//   warp 0      one thread issues TMA loads (128-byte swizzle) of its 128 x 64 A box and 128 x 64 B
-//               box into a 6-stage ring of 32 KB stages, counted on the leader's barriers;
+//   warp 0      one thread issues TMA loads (128-byte swizzle) of its 128 x 128 A block and 128 x 128
+//               B block (two 64-column boxes each) into a 3-stage ring of 64 KB stages, counted on the
+//               leader's barriers;
 //   warp 1      allocates 512 columns of tensor memory in both CTAs (two 128 x 256 fp32 accumulators);
-//               in the leader one thread issues the MMAs (M 256, N 256, K 16; 4 per stage) and commits
+//               in the leader one thread issues the MMAs (M 256, N 256, K 16; 8 per stage) and commits
 //               each stage back to both loaders and each finished tile to both epilogues;
 //   warps 2-5   the epilogue: each thread owns one row (one tensor-memory lane), reads its 256 fp32
 //               accumulators 32 columns at a time and either rounds them to bf16 and stores them (a
@@ -50,7 +51,15 @@ namespace {
 
 constexpr int kBM = 128;           // tile rows of one CTA (tokens)
 constexpr int kBN = 256;           // tile columns (output features)
-constexpr int kBK = 64;            // K per stage: 64 bf16 = one 128-byte swizzle row
+#ifndef ENGRAM_PROJ_KATOMS
+// 128-byte swizzle atoms (64 bf16 of K each) per stage. Two atoms (8 MMAs per stage wait and commit)
+// measured 1% faster than one with the store epilogue and 5.5% faster with the gate epilogue (single
+// calls interleaved, 16,384 and 65,536 tokens); three atoms (two stages) were slower.
+#define ENGRAM_PROJ_KATOMS 2
+#endif
+constexpr int kAtomK = 64;                        // K of one 128-byte swizzle row: 64 bf16
+constexpr int kKAtoms = ENGRAM_PROJ_KATOMS;
+constexpr int kBK = kAtomK * kKAtoms;             // K per stage
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma (kind::f16)
 constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
 constexpr int kTmemCols = 2 * kAccCols;
@@ -69,28 +78,31 @@ constexpr int kThreadsLookup = kThreads + 32 * kLookupWarps;
 constexpr int kChunkTokens = ENGRAM_LOOKUP_CHUNK;  // lookup ahead: tokens per chunk of work (all their columns)
 constexpr int kLookupBatch = ENGRAM_LOOKUP_BATCH;  // lookup ahead: 16-code pieces in flight per lane
 constexpr uint32_t kABytes = kBM * kBK * 2;
+constexpr uint32_t kAAtomBytes = kBM * kAtomK * 2;  // one atom of the A block: 128 rows of 128 bytes
 constexpr uint32_t kEpiChunkBytes = 32 * 32 * 2;  // one epilogue warp's 32 rows x 32 columns of bf16
 #ifndef ENGRAM_PROJ_PAIR_STAGES
-#define ENGRAM_PROJ_PAIR_STAGES 6  // stages of 32 KB in the ring of a CTA of a pair
+#define ENGRAM_PROJ_PAIR_STAGES 3  // stages of 64 KB (two atoms of K) in the ring of a CTA of a pair
 #endif
 #ifndef ENGRAM_PROJ_GROUP
 #define ENGRAM_PROJ_GROUP 16  // 256-row blocks per tile group (16 measured ahead of 4, 8 and 32)
 #endif
 
-// CS = 1: one CTA computes a 128 x 256 tile with M = 128 MMAs (4 stages of A + all of B, 48 KB).
+// Sizes below are per 64-column atom of K; a stage holds kKAtoms of them.
+// CS = 1: one CTA computes a 128 x 256 tile with M = 128 MMAs (A + all of B, 48 KB per atom).
 // CS = 2: a cluster of two CTAs (a pair) computes a 256 x 256 tile with M = 256 pair MMAs issued by
-// the leader; each CTA loads its own 128 rows of A and its half (128 rows) of B, so a stage is 32 KB
-// and the ring holds 6 of them: each SM reads 2/3 of the bytes per MMA from L2 that a lone CTA does.
+// the leader; each CTA loads its own 128 rows of A and its half (128 rows) of B, 32 KB per atom, so
+// each SM reads 2/3 of the bytes per MMA from L2 that a lone CTA does.
 // CS = 4: two pairs side by side along N compute a 256 x 512 tile and share A: each CTA loads 64 of
 // its 128 A rows and multicasts them to the CTA at the same place in the other pair, so L2 serves
 // 3/4 of the bytes per MMA of a pair. Four-CTA clusters fill 144 of the 152 SMs.
 template <int CS>
 struct Cfg {
   static constexpr bool kPairs = CS >= 2;
-  static constexpr int kStages = kPairs ? ENGRAM_PROJ_PAIR_STAGES : 4;
+  static constexpr int kStages = kPairs ? ENGRAM_PROJ_PAIR_STAGES : 4 / kKAtoms;
   static constexpr int kBRows = kPairs ? kBN / 2 : kBN;        // rows of the B tile this CTA loads
   static constexpr int kARows = CS == 4 ? kBM / 2 : kBM;        // rows of A this CTA loads per stage
   static constexpr uint32_t kBBytes = kBRows * kBK * 2;
+  static constexpr uint32_t kBAtomBytes = kBRows * kAtomK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTxBytes = kPairs ? 2 * kStageBytes : kStageBytes;  // per stage, both CTAs of a pair
   static constexpr int kTileM = kPairs ? 2 * kBM : kBM;        // rows of one cluster tile
@@ -107,6 +119,7 @@ struct Cfg {
   static constexpr uint32_t kAbortOff = kTmemSlotOff + 4;          // set by a role whose wait ran out
   static constexpr uint32_t kGroupOff = kAbortOff + 4;             // lookup ahead: the loader's tile group
   static constexpr uint32_t kSmemBytes = kGroupOff + 4 + 1024;     // + slack to align the ring to 1024 bytes
+  static_assert(kSmemBytes <= 232448, "the stage ring must fit in a CTA's shared memory");
 };
 
 enum Epilogue { EPI_STORE = 0, EPI_GATE = 1 };
@@ -537,20 +550,29 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
           raise_timeout(abort);
           break;
         }
+        // one box per 128-byte swizzle atom of K: atom j of A at a_dst + j * kAAtomBytes, of B after A
         const uint32_t a_dst = base + stage * C::kStageBytes;
         if (PAIR) {
           const uint32_t fb = tc::map_to_rank(full(stage), lead);
           if (leader) tc::mbar_arrive_expect_tx(full(stage), C::kTxBytes);
-          if (CS == 4)  // this CTA's half of its A block, to itself and its counterpart in the other pair
-            tc::tma_load_2d_pair_multicast(a_dst + pr * (C::kARows * kBK * 2), &tmA, fb, kb * kBK, arow0,
-                                           (uint16_t)((1u << q) | (1u << (q + 2))));
-          else
-            tc::tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, arow0);
-          tc::tma_load_2d_pair(a_dst + kABytes, &tmB, fb, kb * kBK, brow0);
+#pragma unroll
+          for (int j = 0; j < kKAtoms; ++j) {
+            const int x = kb * kBK + j * kAtomK;
+            if (CS == 4)  // this CTA's half of its A block, to itself and its counterpart in the other pair
+              tc::tma_load_2d_pair_multicast(a_dst + j * kAAtomBytes + pr * (C::kARows * kAtomK * 2), &tmA, fb, x,
+                                             arow0, (uint16_t)((1u << q) | (1u << (q + 2))));
+            else
+              tc::tma_load_2d_pair(a_dst + j * kAAtomBytes, &tmA, fb, x, arow0);
+            tc::tma_load_2d_pair(a_dst + kABytes + j * C::kBAtomBytes, &tmB, fb, x, brow0);
+          }
         } else {
           tc::mbar_arrive_expect_tx(full(stage), C::kTxBytes);
-          tc::tma_load_2d(a_dst, &tmA, full(stage), kb * kBK, arow0);
-          tc::tma_load_2d(a_dst + kABytes, &tmB, full(stage), kb * kBK, brow0);
+#pragma unroll
+          for (int j = 0; j < kKAtoms; ++j) {
+            const int x = kb * kBK + j * kAtomK;
+            tc::tma_load_2d(a_dst + j * kAAtomBytes, &tmA, full(stage), x, arow0);
+            tc::tma_load_2d(a_dst + kABytes + j * C::kBAtomBytes, &tmB, full(stage), x, brow0);
+          }
         }
         ++issued;
         if (++stage == C::kStages) {
@@ -591,8 +613,10 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
         const uint32_t a0 = base + stage * C::kStageBytes, b0 = a0 + kABytes;
 #pragma unroll
         for (int k = 0; k < kBK / kUmmaK; ++k) {
-          const uint64_t ad = tc::sw128_kmajor_desc(a0 + 2 * kUmmaK * k);
-          const uint64_t bd = tc::sw128_kmajor_desc(b0 + 2 * kUmmaK * k);
+          constexpr int kPerAtom = kAtomK / kUmmaK;  // MMAs per swizzle atom of K
+          const uint32_t off = 2 * kUmmaK * (k % kPerAtom);
+          const uint64_t ad = tc::sw128_kmajor_desc(a0 + (k / kPerAtom) * kAAtomBytes + off);
+          const uint64_t bd = tc::sw128_kmajor_desc(b0 + (k / kPerAtom) * C::kBAtomBytes + off);
           if (PAIR)
             tc::mma_bf16_pair(d, ad, bd, C::kIdesc, (kb | k) != 0 ? 1u : 0u);
           else
@@ -737,7 +761,7 @@ EncodeTiledFn encode_fn() {
 // swizzling (reads past the matrix, ragged rows or K, are filled with zeros), outputs written from
 // 64-byte swizzled staging chunks (writes past the matrix are dropped)
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-              uint32_t box_cols = kBK, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
+              uint32_t box_cols = kAtomK, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t dims[2] = {cols, rows};
