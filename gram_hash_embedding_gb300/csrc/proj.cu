@@ -53,8 +53,8 @@ constexpr int kBM = 128;           // tile rows of one CTA (tokens)
 constexpr int kBN = 256;           // tile columns (output features)
 #ifndef ENGRAM_PROJ_KATOMS
 // 128-byte swizzle atoms (64 bf16 of K each) per stage. Two atoms (8 MMAs per stage wait and commit)
-// measured 1% faster than one with the store epilogue and 5.5% faster with the gate epilogue (single
-// calls interleaved, 16,384 and 65,536 tokens); three atoms (two stages) were slower.
+// measured as fast as one with the store epilogue and 2.4-4.0% faster with the gate epilogue (steady
+// state under the power cap, 16,384 and 65,536 tokens); three atoms (two stages) were slower.
 #define ENGRAM_PROJ_KATOMS 2
 #endif
 constexpr int kAtomK = 64;                        // K of one 128-byte swizzle row: 64 bf16
