@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "engram_internal.cuh"
+#include "gate_math.cuh"
 #include "proj.cuh"
 
 namespace engram {
@@ -42,12 +43,6 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
-}
-
-__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
 }
 
 // L2 eviction policies for the loads below (createpolicy: the whole access gets the priority)
@@ -136,13 +131,7 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS) gate_ker
       b += red[3 * tid + 1][w];
       c += red[3 * tid + 2][w];
     }
-    const float rd = 1.0f / (float)dim;
-    const float rstd = (1.0f / sqrtf(a * rd + eps)) * (1.0f / sqrtf(b * rd + eps));
-    const float dot = c * rstd * inv_sqrt_dim;
-    const float z = copysignf(sqrtf(fmaxf(fabsf(dot), 1e-6f)), dot);
-    float g = 1.0f / (1.0f + expf(-z));
-    if (mask != nullptr && mask[t] == 0) g = 0.f;
-    gate_s[tid] = g;
+    gate_s[tid] = gate_of_sums(a, b, c, 1.0f / (float)dim, eps, inv_sqrt_dim, mask == nullptr || mask[t] != 0);
   }
   __syncthreads();
   // out = h + gate * value (the value row is shared by the HC copies)
@@ -155,13 +144,7 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS) gate_ker
     for (int i = 0; i < HC; ++i) {
       float h[8];
       bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v, stream), h);  // last use
-      const float g = gate_s[i];
-      uint4 o;
-      o.x = f32x2_to_bf16x2(h[0] + g * val[0], h[1] + g * val[1]);
-      o.y = f32x2_to_bf16x2(h[2] + g * val[2], h[3] + g * val[3]);
-      o.z = f32x2_to_bf16x2(h[4] + g * val[4], h[5] + g * val[5]);
-      o.w = f32x2_to_bf16x2(h[6] + g * val[6], h[7] + g * val[7]);
-      *reinterpret_cast<uint4*>(ot + (int64_t)i * dim + 8 * v) = o;
+      *reinterpret_cast<uint4*>(ot + (int64_t)i * dim + 8 * v) = gate_mix8(h, val, gate_s[i]);
     }
   }
 }
@@ -203,13 +186,8 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS)
   }
   __syncthreads();
   if (tid < HC) {
-    const float rd = 1.0f / (float)dim;
-    const float rstd = (1.0f / sqrtf(red[3 * tid] * rd + eps)) * (1.0f / sqrtf(red[3 * tid + 1] * rd + eps));
-    const float dot = red[3 * tid + 2] * rstd * inv_sqrt_dim;
-    const float z = copysignf(sqrtf(fmaxf(fabsf(dot), 1e-6f)), dot);
-    float g = 1.0f / (1.0f + expf(-z));
-    if (mask != nullptr && mask[t] == 0) g = 0.f;
-    gate_s[tid] = g;
+    gate_s[tid] = gate_of_sums(red[3 * tid], red[3 * tid + 1], red[3 * tid + 2], 1.0f / (float)dim, eps,
+                               inv_sqrt_dim, mask == nullptr || mask[t] != 0);
   }
   __syncthreads();
   const uint64_t stream = l2_evict_first();
@@ -223,13 +201,7 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS)
     for (int i = 0; i < HC; ++i) {
       float h[8];
       bf16x8_to_f32(ld16(xt + (int64_t)i * dim + 8 * v, stream), h);
-      const float g = gate_s[i];
-      uint4 o;
-      o.x = f32x2_to_bf16x2(h[0] + g * val[0], h[1] + g * val[1]);
-      o.y = f32x2_to_bf16x2(h[2] + g * val[2], h[3] + g * val[3]);
-      o.z = f32x2_to_bf16x2(h[4] + g * val[4], h[5] + g * val[5]);
-      o.w = f32x2_to_bf16x2(h[6] + g * val[6], h[7] + g * val[7]);
-      *reinterpret_cast<uint4*>(ot + (int64_t)i * dim + 8 * v) = o;
+      *reinterpret_cast<uint4*>(ot + (int64_t)i * dim + 8 * v) = gate_mix8(h, val, gate_s[i]);
     }
   }
 }
