@@ -330,9 +330,9 @@ uint64_t engram_lookup_project_workspace(int64_t T, int32_t n_cols, int32_t head
  * equal bit for bit to engram_lookup followed by engram_project. Warps of every CTA of the projection
  * look the rows up into the workspace one tile group (4,096 tokens) ahead of the tensor-core loads
  * that read them, which read them back from L2; only the first group's lookup runs before the first
- * MMA. On GB300 this is as fast as the two calls at 65,536 tokens and 2% slower at 16,384 (the lookup
- * inside the contraction still costs the tensor cores about its own time). Inputs written by an
- * earlier launch on the stream are read after it completes.
+ * MMA. On GB300, in steady state, this is 0.5% faster than the two calls at 65,536 tokens and 0.4%
+ * slower at 16,384 (the lookup inside the contraction still costs the tensor cores about its own
+ * time). Inputs written by an earlier launch on the stream are read after it completes.
  *   idx         device int64: token t's n_cols row ids at idx[t * idx_stride + c] (8-byte aligned;
  *               idx_stride >= n_cols), e.g. one layer's slice of engram_hash's output (stride
  *               n_layers * C); ids outside [0, rows) give +0 rows
