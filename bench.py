@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fused_profile_case_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "gram_hash_embedding_gb300", "csrc", f) for f in
-                  ("kernels.cu", "engram_internal.cuh")]
+                  ("kernels.cu", "engram_internal.cuh", "dequant.cuh")]
 
 
 def parse_args(argv=None):
