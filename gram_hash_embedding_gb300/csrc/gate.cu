@@ -160,9 +160,9 @@ cudaError_t launch_gate_hc(const uint16_t* x, const uint16_t* kv, const uint16_t
 }
 
 // The gate's second half after engram_project_gate's projection: the projection epilogue left, for
-// every row block of 128 tokens and every key tile u (256 columns of copy u / tpc), the per-token sums
-// of h^2, key^2 and h*q_weight*k_weight*key over the tile at part[block][u][0..2][token % 128]. One CTA
-// per token adds them up per copy (tpc tiles each), forms the hc gates exactly as gate_kernel does,
+// every row block of 128 tokens and every key tile u (project_tile_cols(T) columns of copy u / tpc), the
+// per-token sums of h^2, key^2 and h*q_weight*k_weight*key over the tile at part[block][u][0..2][token %
+// 128]. One CTA per token adds them up per copy (tpc tiles each), forms the hc gates exactly as gate_kernel does,
 // and writes out = bf16(h + gate * value) from the value rows the projection stored.
 template <int HC>
 __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS)
@@ -213,7 +213,7 @@ cudaError_t launch_gate_finish_hc(const uint16_t* x, const uint16_t* value, cons
   threads = threads < 32 ? 32 : (threads > kGateThreads ? kGateThreads : ((threads + 31) / 32) * 32);
   const float inv_sqrt_dim = (float)(1.0 / sqrt((double)dim));
   return launch_pdl(gate_finish_kernel<HC>, dim3((unsigned)T), dim3(threads), 0, s, x, value, part, mask, dim,
-                    dim / 256, eps, inv_sqrt_dim, out);
+                    (int)(dim / project_tile_cols(T)), eps, inv_sqrt_dim, out);
 }
 
 }  // namespace

@@ -50,7 +50,7 @@ __device__ unsigned int g_device_status;
 namespace {
 
 constexpr int kBM = 128;           // tile rows of one CTA (tokens)
-constexpr int kBN = 256;           // tile columns (output features)
+constexpr int kBN = 256;           // widest tile (output features); calls with few row tiles use 128 (see bn_for)
 #ifndef ENGRAM_PROJ_KATOMS
 // 128-byte swizzle atoms (64 bf16 of K each) per stage. Two atoms (8 MMAs per stage wait and commit)
 // measured as fast as one with the store epilogue and 2.4-4.0% faster with the gate epilogue (steady
@@ -61,8 +61,6 @@ constexpr int kAtomK = 64;                        // K of one 128-byte swizzle r
 constexpr int kKAtoms = ENGRAM_PROJ_KATOMS;
 constexpr int kBK = kAtomK * kKAtoms;             // K per stage
 constexpr int kUmmaK = 16;         // K of one tcgen05.mma (kind::f16)
-constexpr int kAccCols = kBN;      // fp32 accumulator columns per tile
-constexpr int kTmemCols = 2 * kAccCols;
 constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
 #ifndef ENGRAM_LOOKUP_WARPS
 #define ENGRAM_LOOKUP_WARPS 4
@@ -95,20 +93,25 @@ constexpr uint32_t kEpiChunkBytes = 32 * 32 * 2;  // one epilogue warp's 32 rows
 // CS = 4: two pairs side by side along N compute a 256 x 512 tile and share A: each CTA loads 64 of
 // its 128 A rows and multicasts them to the CTA at the same place in the other pair, so L2 serves
 // 3/4 of the bytes per MMA of a pair. Four-CTA clusters fill 144 of the 152 SMs.
-template <int CS>
+// BN: tile columns (256, or 128 for calls with few row tiles); the ring keeps the bytes of
+// ENGRAM_PROJ_PAIR_STAGES stages of the 256-column form, so narrower tiles get more stages.
+template <int CS, int BN = kBN>
 struct Cfg {
   static constexpr bool kPairs = CS >= 2;
-  static constexpr int kStages = kPairs ? ENGRAM_PROJ_PAIR_STAGES : 4 / kKAtoms;
-  static constexpr int kBRows = kPairs ? kBN / 2 : kBN;        // rows of the B tile this CTA loads
+  static constexpr int kAccCols = BN;                          // fp32 accumulator columns per tile
+  static constexpr int kTmemCols = 2 * BN;                     // two accumulators
+  static constexpr int kBRows = kPairs ? BN / 2 : BN;          // rows of the B tile this CTA loads
   static constexpr int kARows = CS == 4 ? kBM / 2 : kBM;        // rows of A this CTA loads per stage
   static constexpr uint32_t kBBytes = kBRows * kBK * 2;
   static constexpr uint32_t kBAtomBytes = kBRows * kAtomK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = kPairs ? (int)(ENGRAM_PROJ_PAIR_STAGES * (kABytes + (kBM * kBK * 2)) / kStageBytes)
+                                        : 4 / kKAtoms;
   static constexpr uint32_t kTxBytes = kPairs ? 2 * kStageBytes : kStageBytes;  // per stage, both CTAs of a pair
   static constexpr int kTileM = kPairs ? 2 * kBM : kBM;        // rows of one cluster tile
   static constexpr int kNBlocks = CS == 4 ? 2 : 1;             // 256-column blocks of one cluster tile
   static constexpr int kGroup = (kPairs ? 1 : 2) * ENGRAM_PROJ_GROUP;  // tile rows per group (256-row units)
-  static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kBN);
+  static constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, BN);
   // shared memory: the stage ring (1024-byte aligned), then barriers and two words
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
   static constexpr uint32_t kEpiOff = kRingBytes;  // output staging: 2 chunks of 32 x 32 bf16 per epilogue warp
@@ -130,19 +133,20 @@ struct ProjParams {
   int32_t N;        // rows of wkv = output columns
   int32_t num_kb;   // ceil(K / kBK)
   int32_t n_mtile;  // ceil(T / cluster tile rows)
-  int32_t n_nblk;   // ceil(N / kBN)
+  int32_t bn;       // tile columns: 256, or 128 (project_tile_cols)
+  int32_t n_nblk;   // ceil(N / bn)
   int32_t n_ntile;  // ceil(n_nblk / 256-column blocks per cluster tile)
   int64_t n_tiles;
   // EPI_STORE: out [T][N] bf16
   uint16_t* out;
-  // EPI_GATE: N = (hc + 1) * dim, dim a multiple of kBN. Key tiles (columns < hc * dim) produce the
+  // EPI_GATE: N = (hc + 1) * dim, dim a multiple of 256. Key tiles (columns < hc * dim) produce the
   // partial sums sum(h^2), sum(k^2), sum(h * q_weight * k_weight * k) of every row over their 256
   // columns into part[m_blk][n_blk][3][kBM]; value tiles store bf16 rows into value [T][dim].
   const uint16_t* x;   // [T][hc][dim] residual copies (h)
   const uint16_t* qw;  // [hc][dim]
   const uint16_t* kw;  // [hc][dim]
   uint16_t* value;     // [T][dim]
-  float* part;         // [ceil(T / kBM)][hc * dim / kBN][3][kBM]
+  float* part;         // [ceil(T / kBM)][hc * dim / bn][3][kBM]
   int32_t hc, dim;
   // test hook (engram_project_withhold): the leader of every cluster does not signal the completion
   // of its tile number `withhold` (counted from 0 per cluster), so that tile's epilogue waits in vain
@@ -218,11 +222,12 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
 // one TMA copy. Two chunks per warp alternate; a chunk is rewritten only after the copy issued from it
 // two chunks earlier has read it. Whole 128-byte lines reach L2 instead of a 16-byte piece of each of
 // 32 rows per store instruction, which costs less power (the projection runs at the power limit).
+template <int COLS>
 __device__ __forceinline__ void store_tile_rows_tma(uint32_t taddr, const void* tmap, uint32_t stage_base, int x0,
                                                     int32_t y0) {
   const int lane = threadIdx.x & 31;
 #pragma unroll 1
-  for (int c = 0; c < kAccCols / 32; ++c) {
+  for (int c = 0; c < COLS / 32; ++c) {
     float v[32];
     tc::tmem_load_32cols(taddr + 32 * c, v);
     const uint32_t chunk = stage_base + (uint32_t)(c & 1) * kEpiChunkBytes;
@@ -250,9 +255,10 @@ __device__ __forceinline__ void load_h_chunk(uint4 (&d)[4], const uint16_t* hrow
   for (int g = 0; g < 4; ++g) d[g] = hrow != nullptr ? ld_nc_v4(hrow + 32 * c + 8 * g) : make_uint4(0u, 0u, 0u, 0u);
 }
 
+template <int COLS>
 __device__ __forceinline__ void gate_tile_row(uint32_t taddr, const uint16_t* hrow, const uint16_t* qrow,
                                               const uint16_t* wrow, float (&sums)[3]) {
-  constexpr int kChunks = kAccCols / 32;
+  constexpr int kChunks = COLS / 32;
   float sh = 0.f, sk = 0.f, sd = 0.f;
   uint4 h0[4], h1[4], h2[4];
   load_h_chunk(h0, hrow, 0);
@@ -453,11 +459,11 @@ __device__ __forceinline__ void lookup_warp(const ProjParams& p, const volatile 
   }
 }
 
-template <int EPI, int CS, bool LA>
+template <int EPI, int CS, bool LA, int BN>
 __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, const ProjParams p) {
-  using C = Cfg<CS>;
+  using C = Cfg<CS, BN>;
   constexpr bool PAIR = C::kPairs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
@@ -509,10 +515,10 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
   if (CS > 1) tc::cluster_sync();  // every CTA's barriers exist before anyone signals them
   if (warp == 1) {
     if (PAIR) {
-      tc::tmem_alloc_pair(base + C::kTmemSlotOff, kTmemCols);
+      tc::tmem_alloc_pair(base + C::kTmemSlotOff, C::kTmemCols);
       tc::tmem_relinquish_alloc_permit_pair();
     } else {
-      tc::tmem_alloc(base + C::kTmemSlotOff, kTmemCols);
+      tc::tmem_alloc(base + C::kTmemSlotOff, C::kTmemCols);
       tc::tmem_relinquish_alloc_permit();
     }
   }
@@ -544,7 +550,7 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
       }
       const int32_t nb = nt * C::kNBlocks + (int32_t)pr;
       const int32_t arow0 = mt * C::kTileM + (int32_t)q * kBM + (int32_t)pr * C::kARows;
-      const int32_t brow0 = nb * kBN + (int32_t)q * C::kBRows;
+      const int32_t brow0 = nb * BN + (int32_t)q * C::kBRows;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (!tc::mbar_wait(empty(stage), phase ^ 1u, abort)) {
           raise_timeout(abort);
@@ -602,7 +608,7 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
         break;
       }
       tc::fence_after_thread_sync();
-      const uint32_t d = tmem_base + acc * kAccCols;
+      const uint32_t d = tmem_base + acc * C::kAccCols;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (!tc::mbar_wait(full(stage), phase, abort)) {
           raise_timeout(abort);
@@ -664,10 +670,10 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
       if (EPI != EPI_GATE || t >= p.n_tiles) return;
       int32_t pm, pn;
       tile_coords(p, C::kGroup, t, pm, pn);
-      const int col = (pn * C::kNBlocks + (int)pr) * kBN;
+      const int col = (pn * C::kNBlocks + (int)pr) * BN;
       if (col >= p.N) return;
       const uint16_t* hr = h_row(p, ((int64_t)pm * (C::kTileM / kBM) + q) * kBM + r, col);
-      if (hr != nullptr) tc::prefetch_l2_bulk(hr, kBN * 2);
+      if (hr != nullptr) tc::prefetch_l2_bulk(hr, BN * 2);
     };
     prefetch_h(unit);
     for (int64_t tile = unit; tile < p.n_tiles; tile += n_units) {
@@ -678,24 +684,24 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
       prefetch_h(tile + n_units);
       const int64_t mb = (int64_t)mt * (C::kTileM / kBM) + q;  // this CTA's block of 128 rows
       const int64_t row = mb * kBM + r;
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * kAccCols;
-      const int col0 = (nt * C::kNBlocks + (int)pr) * kBN;  // a pair past the last column block stores nothing
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::kAccCols;
+      const int col0 = (nt * C::kNBlocks + (int)pr) * BN;  // a pair past the last column block stores nothing
       const uint32_t stage_base = base + C::kEpiOff + (uint32_t)quarter * 2u * kEpiChunkBytes;
       const int32_t y0 = (int32_t)(mb * kBM) + quarter * 32;  // TMA stores skip rows past T
       if (EPI == EPI_STORE) {
-        if (col0 < p.N) store_tile_rows_tma(taddr, &tmO, stage_base, col0, y0);
+        if (col0 < p.N) store_tile_rows_tma<BN>(taddr, &tmO, stage_base, col0, y0);
       } else if (col0 < p.N) {
         const int key_cols = p.hc * p.dim;
         if (col0 < key_cols) {
           const int i = col0 / p.dim, j0 = col0 - i * p.dim;
           float sums[3];
-          gate_tile_row(taddr, h_row(p, row, col0), p.qw + i * p.dim + j0, p.kw + i * p.dim + j0, sums);
-          float* dst = p.part + (mb * (key_cols / kBN) + col0 / kBN) * 3 * kBM + r;
+          gate_tile_row<BN>(taddr, h_row(p, row, col0), p.qw + i * p.dim + j0, p.kw + i * p.dim + j0, sums);
+          float* dst = p.part + (mb * (key_cols / BN) + col0 / BN) * 3 * kBM + r;
           dst[0] = sums[0];
           dst[kBM] = sums[1];
           dst[2 * kBM] = sums[2];
         } else {
-          store_tile_rows_tma(taddr, &tmO, stage_base, col0 - key_cols, y0);
+          store_tile_rows_tma<BN>(taddr, &tmO, stage_base, col0 - key_cols, y0);
         }
       }
       tc::fence_before_thread_sync();
@@ -723,9 +729,9 @@ __global__ void __launch_bounds__(LA ? kThreadsLookup : kThreads, 1)
     __syncwarp();
     tc::fence_after_thread_sync();
     if (PAIR)
-      tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+      tc::tmem_dealloc_pair(tmem_base, C::kTmemCols);
     else
-      tc::tmem_dealloc(tmem_base, kTmemCols);
+      tc::tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 
@@ -789,7 +795,8 @@ ProjParams base_params(int64_t T, int32_t K, int32_t N) {
   p.N = N;
   p.num_kb = (K + kBK - 1) / kBK;
   p.n_mtile = (int32_t)((T + Cfg<kCS>::kTileM - 1) / Cfg<kCS>::kTileM);
-  p.n_nblk = (N + kBN - 1) / kBN;
+  p.bn = (int32_t)project_tile_cols(T);
+  p.n_nblk = (N + p.bn - 1) / p.bn;
   p.n_ntile = (p.n_nblk + Cfg<kCS>::kNBlocks - 1) / Cfg<kCS>::kNBlocks;
   p.n_tiles = (int64_t)p.n_mtile * p.n_ntile;
   p.withhold = -1;
@@ -798,9 +805,9 @@ ProjParams base_params(int64_t T, int32_t K, int32_t N) {
 
 // as many persistent clusters as can be resident at once, launched as a programmatic dependent like
 // every kernel of the library
-template <int EPI, bool LA = false>
-cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
-  using C = Cfg<kCS>;
+template <int EPI, bool LA, int BN>
+cudaError_t launch_proj_bn(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
+  using C = Cfg<kCS, BN>;
   CUtensorMap ta, tb, to;
   // the output tensor: out [T][N], or the value rows [T][dim] of the gate epilogue
   const uint16_t* optr = EPI == EPI_STORE ? p.out : p.value;
@@ -809,7 +816,7 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
       !make_map(&tb, w, (uint64_t)p.N, (uint64_t)p.K, (uint32_t)C::kBRows) ||
       !make_map(&to, optr, (uint64_t)p.T, ocols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
-  auto kern = proj_kernel<EPI, kCS, LA>;
+  auto kern = proj_kernel<EPI, kCS, LA, BN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -839,6 +846,11 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
   const int64_t n = p.n_tiles < units ? p.n_tiles : units;
   cfg.gridDim = dim3((unsigned)(n * kCS));
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, to, p);
+}
+
+template <int EPI, bool LA = false>
+cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams& p, cudaStream_t s) {
+  return p.bn == 128 ? launch_proj_bn<EPI, LA, 128>(emb, w, p, s) : launch_proj_bn<EPI, LA, 256>(emb, w, p, s);
 }
 
 // lookup ahead: the lookup arguments, the rows' workspace, and its counters zeroed on the stream
@@ -902,10 +914,20 @@ cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, in
   return launch_proj<EPI_STORE>(emb, w, p, s);
 }
 
+#ifndef ENGRAM_PROJ_NARROW_T
+#define ENGRAM_PROJ_NARROW_T 256  // calls of at most this many tokens use 128-column tiles
+#endif
+// 128-column tiles for calls of one row tile: a decode batch's projection (T = 256, N = 25,600) has
+// only 100 tiles of 256 columns for 76 pairs, a full wave and a third; 200 narrower tiles fill the
+// waves better: 38.9 against 41.2 us per call. Every tile re-reads its rows of A from L2, and narrow
+// tiles read A twice as often per MMA, so from 512 tokens on the wider tiles win (57.9 against 68.7 us
+// at 512 tokens, even at 1,024). Each output sums its K terms in the same order either way: the same bits.
+int64_t project_tile_cols(int64_t T) { return T <= ENGRAM_PROJ_NARROW_T ? 128 : 256; }
+
 int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim) {
   // whole (cluster) tiles: the second CTA of a pair's last tile writes its block even past T
   const int64_t tiles = (T + Cfg<kCS>::kTileM - 1) / Cfg<kCS>::kTileM;
-  return tiles * (Cfg<kCS>::kTileM / kBM) * (int64_t)(hc * dim / kBN) * 3 * kBM;
+  return tiles * (Cfg<kCS>::kTileM / kBM) * (int64_t)(hc * dim / project_tile_cols(T)) * 3 * kBM;
 }
 
 cudaError_t launch_project_gate_sums(const uint16_t* x, const uint16_t* emb, const uint16_t* wkv, const uint16_t* qw,

@@ -11,6 +11,10 @@ namespace engram {
 cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, int32_t K, int32_t N, uint16_t* out,
                            cudaStream_t s, int32_t withhold = -1);
 
+// columns of the projection's output tiles for a call of T tokens (128 or 256); the gate's partial
+// sums come one set per tile
+int64_t project_tile_cols(int64_t T);
+
 // fp32 values of the partial-sum array of the fused gate projection for T tokens
 int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim);
 

@@ -136,9 +136,12 @@ def test_projection_checks_need_no_gpu(lib):
     assert lib.engram_project(None, a, 5, 64, 64, a, None) == geng.ERR_INVALID
     assert lib.engram_project(P(4098), a, 5, 64, 64, a, None) == geng.ERR_INVALID  # misaligned
     # workspace: value rows (T x dim bf16) + 3 partial sums per (128-token block, key tile, token)
-    # partial sums are kept for whole 256-row tiles (a pair of 128-row blocks)
-    assert lib.engram_project_gate_workspace(128, 4, 256) == 128 * 256 * 2 + 2 * 4 * 3 * 128 * 4
-    assert lib.engram_project_gate_workspace(129, 4, 5120) == (129 * 5120 * 2 + 255) // 256 * 256 + 2 * 80 * 3 * 128 * 4
+    # partial sums are kept for whole 256-row tiles (a pair of 128-row blocks); key tiles are 128
+    # columns wide for calls of at most 256 tokens, 256 columns wide above
+    assert lib.engram_project_gate_workspace(128, 4, 256) == 128 * 256 * 2 + 2 * 8 * 3 * 128 * 4
+    assert lib.engram_project_gate_workspace(129, 4, 5120) == (129 * 5120 * 2 + 255) // 256 * 256 + 2 * 160 * 3 * 128 * 4
+    assert lib.engram_project_gate_workspace(257, 4, 5120) == \
+        (257 * 5120 * 2 + 255) // 256 * 256 + 2 * 2 * 80 * 3 * 128 * 4
     assert lib.engram_project_gate_workspace(0, 4, 256) == 0
     assert lib.engram_project_gate_workspace(8, 3, 256) == 0 and lib.engram_project_gate_workspace(8, 4, 200) == 0
     need = lib.engram_project_gate_workspace(8, 4, 256)
