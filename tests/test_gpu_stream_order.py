@@ -192,3 +192,40 @@ def test_fused_call_whose_ids_the_previous_launch_wrote(tiny):
         H.assert_bits_equal(H.bf16_bits(out2[0]), H.oracle_lookup_rows(wl, 0, exp2[:, :, 0, :]), "call 2 rows")
         st1.status()
         st2.status()
+
+
+def test_packed_call_whose_ids_the_previous_launch_wrote(tiny):
+    """The same for a packed (continuous batching) call: call 1 writes its int64 hash ids into H, and
+    a packed call enqueued right behind it takes H, flattened, as the token ids of sequences of ragged
+    lengths (one of them empty), each at start position 0, so most of its tiles are past the cache
+    halo. Packed calls read nothing before the kernel ahead of them completes; H starts as -5
+    everywhere, so a call that did would hash masked tokens instead."""
+    wl, Ws, Ss = tiny
+    lay = wl.layout
+    rng = np.random.default_rng(29)
+    C = lay.n_cols
+    B1, L1 = 2, 512
+    lens = np.array([700, 0, 13, 300, 1], dtype=np.int64)
+    T = int(lens.sum())
+    assert T <= B1 * L1 * C
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    B2 = lens.size
+    st1, orc1 = H.make_state(wl, B1, L1), H.make_oracle(wl, B1, L1)
+    st2, orc2 = H.make_state(wl, B2, int(lens.max())), H.make_oracle(wl, B2, int(lens.max()))
+    ids1 = rng.integers(0, lay.raw_vocab, size=(B1, L1))
+    hbuf = torch.full((B1, L1, 1, C), -5, dtype=torch.int64, device="cuda")
+    out1 = [torch.empty((B1, L1, C, lay.head_dim), dtype=torch.bfloat16, device="cuda")]
+    h2 = torch.empty((T, 1, C), dtype=torch.int64, device="cuda")
+    out2 = [torch.empty((T, C, lay.head_dim), dtype=torch.bfloat16, device="cuda")]
+    cu_d, starts_d = H.to_dev(cu), H.to_dev(np.zeros(B2, dtype=np.int32))
+    torch.cuda.synchronize()
+    st1.hash_lookup(H.to_dev(ids1), Ws, Ss, start_pos=0, out=out1, hashes=hbuf)
+    st2.hash_lookup_varlen(hbuf.view(-1)[:T], cu_d, starts_d, Ws, Ss, out=out2, hashes=h2, max_len=int(lens.max()))
+    torch.cuda.synchronize()
+    exp1, _ = orc1.hash(ids1, 0)
+    H.assert_bits_equal(hbuf.cpu().numpy(), exp1, "call 1 hash ids")
+    exp2, _ = orc2.hash_varlen(exp1.reshape(-1)[:T], cu, np.zeros(B2, dtype=np.int64))
+    H.assert_bits_equal(h2.cpu().numpy(), exp2, "packed call 2 hash ids (its ids are call 1's output)")
+    H.assert_bits_equal(H.bf16_bits(out2[0]), H.oracle_lookup_rows(wl, 0, exp2[:, 0, :]), "packed call 2 rows")
+    st1.status()
+    st2.status()
