@@ -14,6 +14,7 @@
 // keys pushed a third of h out of L2 before its second read (1.73 GB of DRAM reads instead of
 // 1.51 GB at 16,384 tokens; 1.62 ms instead of 1.43 ms at 65,536). The page's PyTorch code instead
 // makes ~15 full passes over fp32 temporaries.
+#include <algorithm>
 #include <cstdint>
 
 #include "engram_internal.cuh"
@@ -162,28 +163,41 @@ cudaError_t launch_gate_hc(const uint16_t* x, const uint16_t* kv, const uint16_t
 // The gate's second half after engram_project_gate's projection: the projection epilogue left, for
 // every row block of 128 tokens and every key tile u (project_tile_cols(T) columns of copy u / tpc), the
 // per-token sums of h^2, key^2 and h*q_weight*k_weight*key over the tile at part[block][u][0..2][token %
-// 128]. One CTA per token adds them up per copy (tpc tiles each), forms the hc gates exactly as gate_kernel does,
-// and writes out = bf16(h + gate * value) from the value rows the projection stored.
+// 128]. A CTA per token (and, for calls of few tokens, per chunk of nvec_chunk 8-value columns) adds
+// them up per copy, forms the hc gates exactly as gate_kernel does, and writes out = bf16(h + gate *
+// value) for its columns from the value rows the projection stored. The sums are staged in shared
+// memory by all threads, kFinishStage tiles at a time, and then added by thread (copy i, quantity q)
+// in tile order: one round trip of loads per kFinishStage tiles instead of one per few tiles.
+constexpr int kFinishStage = 32;
+
 template <int HC>
 __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS)
     gate_finish_kernel(const uint16_t* x, const uint16_t* __restrict__ value, const float* __restrict__ part,
                        const uint8_t* __restrict__ mask, const int dim, const int tpc, const float eps,
-                       const float inv_sqrt_dim, uint16_t* out) {
+                       const float inv_sqrt_dim, const int nvec_chunk, uint16_t* out) {
   pdl_wait();
   pdl_trigger();
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int nvec = dim >> 3;
+  __shared__ float ps[3 * kGateMaxCopies * kFinishStage];
   __shared__ float red[3 * kGateMaxCopies];
   __shared__ float gate_s[kGateMaxCopies];
-  if (tid < 3 * HC) {  // thread (copy i, quantity q) sums its copy's tpc tiles
-    const int i = tid / 3, q = tid - 3 * (tid / 3);
-    const float* pt = part + ((t >> 7) * (int64_t)(HC * tpc) * 3 + q) * 128 + (t & 127);
-    float a = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < tpc; ++j) a += pt[(int64_t)(i * tpc + j) * 3 * 128];
-    red[tid] = a;
+  const float* pt = part + (t >> 7) * (int64_t)(HC * tpc) * 3 * 128 + (t & 127);
+  float a = 0.f;
+  for (int j0 = 0; j0 < tpc; j0 += kFinishStage) {
+    const int nj = min(kFinishStage, tpc - j0);
+    for (int e = tid; e < 3 * HC * nj; e += nthr) {  // e = (copy i, quantity q) * nj + tile j
+      const int iq = e / nj, j = e - iq * nj;
+      const int i = iq / 3, q = iq - 3 * i;
+      ps[e] = pt[((int64_t)(i * tpc + j0 + j) * 3 + q) * 128];
+    }
+    __syncthreads();
+    if (tid < 3 * HC)
+      for (int j = 0; j < nj; ++j) a += ps[tid * nj + j];
+    __syncthreads();
   }
+  if (tid < 3 * HC) red[tid] = a;
   __syncthreads();
   if (tid < HC) {
     gate_s[tid] = gate_of_sums(red[3 * tid], red[3 * tid + 1], red[3 * tid + 2], 1.0f / (float)dim, eps,
@@ -194,7 +208,8 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS)
   const uint16_t* xt = x + t * (int64_t)HC * dim;
   const uint16_t* vt = value + t * (int64_t)dim;
   uint16_t* ot = out + t * (int64_t)HC * dim;
-  for (int v = tid; v < nvec; v += nthr) {
+  const int v1 = min(nvec, (int)(blockIdx.y + 1) * nvec_chunk);
+  for (int v = (int)blockIdx.y * nvec_chunk + tid; v < v1; v += nthr) {
     float val[8];
     bf16x8_to_f32(ld16(vt + 8 * v, stream), val);
 #pragma unroll
@@ -206,14 +221,23 @@ __global__ void __launch_bounds__(kGateThreads, ENGRAM_GATE_MIN_BLOCKS)
   }
 }
 
+#ifndef ENGRAM_FINISH_TARGET_CTAS
+#define ENGRAM_FINISH_TARGET_CTAS 1216  // 8 CTAs on each of the 152 SMs
+#endif
+
 template <int HC>
 cudaError_t launch_gate_finish_hc(const uint16_t* x, const uint16_t* value, const float* part, const uint8_t* mask,
                                   int64_t T, int dim, float eps, uint16_t* out, cudaStream_t s) {
   int threads = dim / 8;
   threads = threads < 32 ? 32 : (threads > kGateThreads ? kGateThreads : ((threads + 31) / 32) * 32);
   const float inv_sqrt_dim = (float)(1.0 / sqrt((double)dim));
-  return launch_pdl(gate_finish_kernel<HC>, dim3((unsigned)T), dim3(threads), 0, s, x, value, part, mask, dim,
-                    (int)(dim / project_tile_cols(T)), eps, inv_sqrt_dim, out);
+  // calls of few tokens split each token's columns over several CTAs (at least `threads` vectors each)
+  const int nvec = dim / 8;
+  const int64_t want = (ENGRAM_FINISH_TARGET_CTAS + T - 1) / T;
+  const int chunks = (int)std::max<int64_t>(1, std::min<int64_t>(want, nvec / threads));
+  const int nvec_chunk = (nvec + chunks - 1) / chunks;
+  return launch_pdl(gate_finish_kernel<HC>, dim3((unsigned)T, (unsigned)chunks), dim3(threads), 0, s, x, value, part,
+                    mask, dim, (int)(dim / project_tile_cols(T)), eps, inv_sqrt_dim, nvec_chunk, out);
 }
 
 }  // namespace
