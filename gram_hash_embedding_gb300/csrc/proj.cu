@@ -69,11 +69,11 @@ constexpr int kThreads = 192;      // 6 warps: loader, MMA, 4 epilogue
 #define ENGRAM_LOOKUP_BATCH 8
 #endif
 #ifndef ENGRAM_LOOKUP_CHUNK
-#define ENGRAM_LOOKUP_CHUNK 8
+#define ENGRAM_LOOKUP_CHUNK 8  // largest chunk; smaller calls take smaller chunks (lookup_chunk_tokens)
 #endif
 constexpr int kLookupWarps = ENGRAM_LOOKUP_WARPS;  // lookup ahead: warps 6, 7, ... look the rows of A up
 constexpr int kThreadsLookup = kThreads + 32 * kLookupWarps;
-constexpr int kChunkTokens = ENGRAM_LOOKUP_CHUNK;  // lookup ahead: tokens per chunk of work (all their columns)
+constexpr int kChunkTokens = ENGRAM_LOOKUP_CHUNK;  // lookup ahead: most tokens per chunk of work (all columns)
 constexpr int kLookupBatch = ENGRAM_LOOKUP_BATCH;  // lookup ahead: 16-code pieces in flight per lane
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kAAtomBytes = kBM * kAtomK * 2;  // one atom of the A block: 128 rows of 128 bytes
@@ -161,7 +161,8 @@ struct ProjParams {
   int64_t rows;
   uint16_t* emb;            // [T][K] bf16, K = n_cols * head_dim: the looked-up rows (A of the projection)
   unsigned int* counters;   // [0]: next chunk to take; [1 + g]: chunks of tile group g written
-  int64_t n_chunks;         // ceil(T / kChunkTokens)
+  int32_t chunk_tokens;     // tokens per chunk of lookup work: a power of two up to kChunkTokens
+  int64_t n_chunks;         // ceil(T / chunk_tokens)
   int32_t group_tokens;     // tokens of one tile group
   int32_t n_cols, head_dim, block, scale_dtype;
 };
@@ -305,8 +306,9 @@ __device__ __forceinline__ const uint16_t* h_row(const ProjParams& p, int64_t ro
 // lookup ahead: warps 6-9 of every CTA look the rows of A up (engram-first/lookup page,
 // `ParallelEngramEmbedding.forward`, through the same dequantisation as engram_lookup) into the
 // workspace, one tile group ahead of the TMA loads that read them. The work is cut into chunks of
-// kChunkTokens tokens (all their columns), taken in token order from a global counter by whichever
-// warp is free, so no CTA waits on another one being resident. A warp takes a chunk of tile group g
+// up to kChunkTokens tokens (all their columns; fewer in calls too small to give every lookup warp a
+// chunk of that size), taken in token order from a global counter by whichever warp is free, so no
+// CTA waits on another one being resident. A warp takes a chunk of tile group g
 // only once its own CTA's loader has reached group g - 1, which keeps the looked-up rows of at most
 // two groups (8,192 tokens) ahead of the MMAs, in L2. The loader, before the first load of a tile
 // of group g, waits until all chunks of group g are written.
@@ -431,7 +433,7 @@ __device__ __forceinline__ void red_release_add(unsigned int* ctr, unsigned int 
 
 // chunks of tile group g: [g * per_group, min(n_chunks, (g + 1) * per_group))
 __device__ __forceinline__ unsigned int group_chunks(const ProjParams& p, int32_t g) {
-  const int64_t per = p.group_tokens / kChunkTokens;
+  const int64_t per = p.group_tokens / p.chunk_tokens;
   const int64_t c0 = (int64_t)g * per;
   return (unsigned int)(min(p.n_chunks, c0 + per) - c0);
 }
@@ -443,7 +445,7 @@ __device__ __forceinline__ void lookup_warp(const ProjParams& p, const volatile 
     if (lane == 0) chunk = atomicAdd(&p.counters[0], 1u);
     chunk = __shfl_sync(0xffffffffu, chunk, 0);
     if ((int64_t)chunk >= p.n_chunks) break;
-    const int64_t t0 = (int64_t)chunk * kChunkTokens;
+    const int64_t t0 = (int64_t)chunk * p.chunk_tokens;
     const int32_t g = (int32_t)(t0 / p.group_tokens);
     int ok = 1;
     if (lane == 0) {
@@ -451,7 +453,7 @@ __device__ __forceinline__ void lookup_warp(const ProjParams& p, const volatile 
       if (!ok) raise_timeout(abort);
     }
     if (__shfl_sync(0xffffffffu, ok, 0) == 0) break;
-    lookup_chunk_any(p, t0, min(p.T, t0 + kChunkTokens), lane);
+    lookup_chunk_any(p, t0, min(p.T, t0 + (int64_t)p.chunk_tokens), lane);
     tc::fence_proxy_async_global();  // the rows are read next by TMA loads (the async proxy)
     __threadfence();
     __syncwarp();
@@ -857,6 +859,13 @@ cudaError_t launch_proj(const uint16_t* emb, const uint16_t* w, const ProjParams
 cudaError_t lookup_ahead_params(ProjParams& p, const LookupArgs& la, cudaStream_t s) {
   using C = Cfg<kCS>;
   static_assert((C::kGroup * C::kTileM) % kChunkTokens == 0, "a chunk of lookup work lies in one tile group");
+  // chunks of up to kChunkTokens tokens, smaller when the call has fewer tokens than the lookup warps
+  // could take in chunks of that size (a 256-token call: 1-token chunks, 256 of them); powers of two,
+  // so a chunk never straddles a tile group
+  int32_t ct = kChunkTokens;
+  const int64_t warps = 152 * kLookupWarps;
+  while (ct > 1 && p.T < (int64_t)ct * warps) ct >>= 1;
+  p.chunk_tokens = ct;
   p.idx = la.idx;
   p.idx_stride = la.idx_stride;
   p.n_cols = la.n_cols;
@@ -868,7 +877,7 @@ cudaError_t lookup_ahead_params(ProjParams& p, const LookupArgs& la, cudaStream_
   p.scale_dtype = la.scale_dtype;
   p.emb = la.emb;
   p.counters = la.counters;
-  p.n_chunks = (p.T + kChunkTokens - 1) / kChunkTokens;
+  p.n_chunks = (p.T + ct - 1) / ct;
   p.group_tokens = C::kGroup * C::kTileM;
   return launch_fill_i32(reinterpret_cast<int32_t*>(la.counters), lookup_ahead_counters(p.T), 0, s);
 }
