@@ -1,7 +1,8 @@
 /*
  * A plain C client of libengram: no Python, no torch. It reads a tiny layout and its inputs from
- * raw files, creates a state, runs the fused hash + lookup and the standalone lookup through the
- * C ABI (include/engram.h) with buffers from cudaMalloc, and writes the results back as raw files.
+ * raw files, creates a state, runs the fused hash + lookup, the standalone lookup and the lookup
+ * inside the wkv projection through the C ABI (include/engram.h) with buffers from cudaMalloc, and
+ * writes the results back as raw files.
  * tests/test_gpu_c_client.py builds and runs it and compares the results with the oracle.
  *
  * usage: engram_client DIR   (DIR holds the inputs listed in main() and receives the outputs)
@@ -109,6 +110,30 @@ int main(int argc, char** argv) {
   CK(cudaMalloc((void**)&d_rows0, out_bytes));
   EK(engram_lookup((const int64_t*)d_idx0, n_idx, (const uint8_t*)d_W, d_S, rows, lay.head_dim, lay.block,
                    ENGRAM_SCALE_F32, d_rows0, NULL));
+  /* the lookup inside the wkv projection, on layer 0's slice of the hash ids (row stride n_layers * C) */
+  size_t n_wkv;
+  const uint16_t* wkv = (const uint16_t*)slurp(dir, "wkv.bin", &n_wkv);
+  const int64_t K = C * lay.head_dim;
+  const int32_t N = (int32_t)(n_wkv / 2 / (size_t)K);
+  void* d_wkv = to_dev(wkv, n_wkv);
+  if (!d_wkv) { fprintf(stderr, "device copy failed\n"); return 3; }
+  engram_table tb;
+  tb.W = d_W;
+  tb.S = d_S;
+  tb.rows = rows;
+  tb.head_dim = lay.head_dim;
+  tb.block = lay.block;
+  tb.scale_dtype = ENGRAM_SCALE_F32;
+  const uint64_t ws_bytes = engram_lookup_project_workspace((int64_t)B * L, (int32_t)C, lay.head_dim);
+  void* d_ws = NULL;
+  CK(cudaMalloc(&d_ws, ws_bytes));
+  const size_t kv_bytes = (size_t)B * L * N * 2;
+  uint16_t* d_kv = NULL;
+  CK(cudaMalloc((void**)&d_kv, kv_bytes));
+  EK(engram_lookup_project((const int64_t*)d_hash, (int64_t)lay.n_layers * C, (int64_t)B * L, (int32_t)C, &tb,
+                           (const uint16_t*)d_wkv, N, d_ws, ws_bytes, d_kv, NULL));
+  uint32_t dflags = 1;
+  EK(engram_device_status(NULL, &dflags, 1));
   uint32_t flags = 0;
   EK(engram_state_status(st, NULL, &flags, 1));
   CK(cudaDeviceSynchronize());
@@ -123,6 +148,10 @@ int main(int argc, char** argv) {
   CK(cudaMemcpy(h_out, d_rows0, out_bytes, cudaMemcpyDeviceToHost));
   spit(dir, "lookup0.out", h_out, out_bytes);
   spit(dir, "status.out", &flags, sizeof flags);
+  void* h_kv = malloc(kv_bytes);
+  CK(cudaMemcpy(h_kv, d_kv, kv_bytes, cudaMemcpyDeviceToHost));
+  spit(dir, "kv0.out", h_kv, kv_bytes);
+  spit(dir, "device_status.out", &dflags, sizeof dflags);
   EK(engram_state_destroy(st));
   printf("ok\n");
   return 0;

@@ -1,6 +1,7 @@
 """The C ABI from a plain C program (no Python or torch in the loop): tests/c_client/engram_client.c
 is compiled with gcc against include/engram.h, libengram.so and the CUDA runtime, run on a tiny
-workload, and its hash ids and bf16 rows are compared with the oracle (GPU only)."""
+workload, and its hash ids, bf16 rows and the lookup inside the projection are compared with the
+oracle (GPU only)."""
 import os
 import subprocess
 
@@ -43,6 +44,11 @@ def test_plain_c_client(tmp_path):
     start.tofile(d / "start.bin")
     W.tofile(d / "W.bin")
     S.tofile(d / "S.bin")
+    K, N = lay.n_cols * lay.head_dim, 64
+    rng = np.random.default_rng(6)
+    wkv = (rng.standard_normal((N, K)) * K ** -0.5).astype(np.float32)
+    wkv_bits = (wkv.view(np.uint32) >> 16).astype(np.uint16)  # truncated to bf16: any bf16 weights will do
+    wkv_bits.tofile(d / "wkv.bin")
     r = subprocess.run([str(exe), str(d)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr
     C = lay.n_cols
@@ -55,3 +61,12 @@ def test_plain_c_client(tmp_path):
     assert np.array_equal(np.fromfile(d / "rows0.out", dtype=np.uint16).reshape(exp_rows.shape), exp_rows)
     assert np.array_equal(np.fromfile(d / "lookup0.out", dtype=np.uint16).reshape(exp_rows.shape), exp_rows)
     assert int(np.fromfile(d / "status.out", dtype=np.uint32)[0]) == 0
+    # the lookup inside the projection against the oracle chain (tolerance of tests/test_gpu_project.py)
+    assert int(np.fromfile(d / "device_status.out", dtype=np.uint32)[0]) == 0
+    got = np.fromfile(d / "kv0.out", dtype=np.uint16).reshape(B * L, N)
+    emb = exp_rows.reshape(B * L, K)
+    exp = oracle.engram_linear(emb, wkv_bits)
+    e64, g64 = oracle.bf16_bits_to_f64(exp), oracle.bf16_bits_to_f64(got)
+    abs_sum = np.abs(oracle.bf16_bits_to_f64(emb)) @ np.abs(oracle.bf16_bits_to_f64(wkv_bits)).T
+    tol = 2.0 ** -7 * (1 + 2.0 ** -7) * np.abs(e64) + 2.0 * (K - 1) * 2.0 ** -23 * abs_sum + 2.0 ** -133
+    assert not (np.abs(g64 - e64) > tol).any()
