@@ -860,10 +860,14 @@ cudaError_t lookup_ahead_params(ProjParams& p, const LookupArgs& la, cudaStream_
   using C = Cfg<kCS>;
   static_assert((C::kGroup * C::kTileM) % kChunkTokens == 0, "a chunk of lookup work lies in one tile group");
   // chunks of up to kChunkTokens tokens, smaller when the call has fewer tokens than the lookup warps
-  // could take in chunks of that size (a 256-token call: 1-token chunks, 256 of them); powers of two,
-  // so a chunk never straddles a tile group
+  // could take in chunks of that size (a 256-token call on 152 SMs: 1-token chunks, 256 of them);
+  // powers of two, so a chunk never straddles a tile group
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   int32_t ct = kChunkTokens;
-  const int64_t warps = 152 * kLookupWarps;
+  const int64_t warps = (int64_t)sms * kLookupWarps;  // one CTA per SM
   while (ct > 1 && p.T < (int64_t)ct * warps) ct >>= 1;
   p.chunk_tokens = ct;
   p.idx = la.idx;
