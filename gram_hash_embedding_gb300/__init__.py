@@ -8,10 +8,16 @@ fallback: if the library is missing, every call raises.
 Functions carry the C names: :func:`engram_state_create`,
 :func:`engram_state_destroy`, :func:`engram_cache_reset`,
 :func:`engram_state_status`, :func:`engram_hash`, :func:`engram_lookup`,
-:func:`engram_hash_lookup`. :class:`EngramHash` bundles a state with them.
+:func:`engram_hash_lookup` (and their packed forms), the Engram block after
+the lookup (:func:`engram_project`, :func:`engram_gate`,
+:func:`engram_project_gate`, and with the lookup inside the projection
+:func:`engram_lookup_project`, :func:`engram_lookup_project_gate`), and the
+row-sharded lookup's two ends (:func:`engram_shard_pack`,
+:func:`engram_shard_unpack`). :class:`EngramHash` bundles a state with them.
 
 Method: the "DeepSeek V4.1" pages -- blocks/stack-hashes page (the n-gram hash
-``forward``) and engram-first/lookup page (``ParallelEngramEmbedding.forward``).
+``forward``, ``Engram.forward``) and engram-first/lookup page
+(``ParallelEngramEmbedding.forward``).
 """
 from __future__ import annotations
 

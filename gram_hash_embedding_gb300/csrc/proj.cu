@@ -50,7 +50,7 @@ __device__ unsigned int g_device_status;
 namespace {
 
 constexpr int kBM = 128;           // tile rows of one CTA (tokens)
-constexpr int kBN = 256;           // widest tile (output features); calls with few row tiles use 128 (see bn_for)
+constexpr int kBN = 256;           // widest tile (output features); calls of one row tile use 128 (project_tile_cols)
 #ifndef ENGRAM_PROJ_KATOMS
 // 128-byte swizzle atoms (64 bf16 of K each) per stage. Two atoms (8 MMAs per stage wait and commit)
 // measured as fast as one with the store epilogue and 2.4-4.0% faster with the gate epilogue (steady
