@@ -932,9 +932,10 @@ cudaError_t launch_project(const uint16_t* emb, const uint16_t* w, int64_t T, in
 #endif
 // 128-column tiles for calls of one row tile: a decode batch's projection (T = 256, N = 25,600) has
 // only 100 tiles of 256 columns for 76 pairs, a full wave and a third; 200 narrower tiles fill the
-// waves better: 38.9 against 41.2 us per call. Every tile re-reads its rows of A from L2, and narrow
-// tiles read A twice as often per MMA, so from 512 tokens on the wider tiles win (57.9 against 68.7 us
-// at 512 tokens, even at 1,024). Each output sums its K terms in the same order either way: the same bits.
+// waves better: 38.9 against 41.2 us per call. From 512 tokens on the waves are as full either way and
+// the wider tiles win (57.9 against 68.7 us at 512 tokens, even at 1,024): a narrow tile does half the
+// work per MMA and per stage wait and re-reads its rows of A twice as often. Each output sums its K
+// terms in the same order either way: the same bits.
 int64_t project_tile_cols(int64_t T) { return T <= ENGRAM_PROJ_NARROW_T ? 128 : 256; }
 
 int64_t project_gate_partials(int64_t T, int32_t hc, int32_t dim) {
