@@ -120,6 +120,23 @@ def test_binding_checks_sizes_before_any_pointer():
         geng.engram_gate(x, torch.zeros((3, 5 * 64), dtype=torch.bfloat16), w, w, mask=torch.ones(4, dtype=torch.bool))
 
 
+def test_lookup_projection_binding_checks_need_no_gpu():
+    """engram_lookup_project(_gate): the hash ids must be an int64 CUDA tensor [T, C] with unit stride
+    along C; the binding refuses anything else before taking a pointer."""
+    import torch
+
+    W = torch.zeros((4, 128), dtype=torch.uint8)
+    S = torch.zeros((4, 1), dtype=torch.float32)
+    wkv = torch.zeros((64, 2 * 128), dtype=torch.bfloat16)
+    with pytest.raises(TypeError, match="int64 CUDA"):
+        geng.engram_lookup_project(torch.zeros((8, 2), dtype=torch.int64), W, S, wkv, 128)  # a CPU tensor
+    with pytest.raises(TypeError, match="int64 CUDA"):
+        geng.engram_lookup_project(torch.zeros((8, 2), dtype=torch.int32), W, S, wkv, 128)
+    x = torch.zeros((8, 4, 256), dtype=torch.bfloat16)
+    with pytest.raises(TypeError, match="int64 CUDA"):
+        geng.engram_lookup_project_gate(x, torch.zeros((8, 2), dtype=torch.int64), W, S, wkv, wkv, wkv, 128)
+
+
 def test_projection_checks_need_no_gpu(lib):
     P = ctypes.c_void_p
     lib.engram_project.argtypes = [P, P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, P, P]
