@@ -593,6 +593,8 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const int64_t* __restr
 }
 
 __global__ void fill_i32_kernel(int32_t* p, int64_t n, int32_t v) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = v;
 }
@@ -662,8 +664,7 @@ cudaError_t launch_fill_i32(int32_t* p, int64_t n, int32_t value, cudaStream_t s
   if (n <= 0) return cudaSuccess;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 152 * 8) blocks = 152 * 8;
-  fill_i32_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, n, value);
-  return cudaGetLastError();
+  return launch_pdl(fill_i32_kernel, dim3((unsigned)blocks), dim3(256), 0, s, p, n, value);
 }
 
 cudaError_t launch_hash(const StateView& sv, const CallArgs& a, cudaStream_t s) {
