@@ -70,7 +70,7 @@ def parse_args(argv=None):
                         "exchange between ranks is the caller's all-to-all and is not timed here)")
     p.add_argument("--graph", action="store_true",
                    help="capture the steps in a CUDA graph and replay it (removes host launch overhead; for the "
-                        "small decode / chunk launches)")
+                        "small decode / chunk launches, and for --block steps of a few hundred tokens)")
     p.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
                    help="L2 between timed steps: flush = write 256 MB before every step and time the kernels "
                         "alone; auto (default) = flush when the steps' rows fit in L2 (decode) and launches are "
@@ -1063,6 +1063,29 @@ def run_block(args):
     clocks.stop()
     total = t0.elapsed_time(t1) / 1e3
     comp = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) * 1e3 for i, n in enumerate(names)}
+    eager_ms = total / K_steps * 1e3
+    if args.graph:
+        # the same steps captured in one CUDA graph and replayed back to back: no host launch gaps
+        # (the per-component times above stay those of the eager pass, whose events split the step)
+        per_graph = 16
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for k in range(per_graph):
+                step(k)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        replays = max(1, -(-K_steps // per_graph))
+        clocks = ClockSampler(local)
+        clocks.start()
+        t0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        clocks.stop()
+        K_steps = replays * per_graph
+        total = t0.elapsed_time(t1) / 1e3
     peak_hbm, _ = measured_peaks()
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         peaks = json.load(f)
@@ -1101,7 +1124,10 @@ def run_block(args):
         "config": {"workload": runner.wl.name, "dim": dim, "hc_mult": hc, "wkv": [dim * (hc + 1), K],
                    "projection": args.proj,
                    "l2_fetch_granularity": (f"{args.l2_fetch} B (context default {l2_default} B)" if args.l2_fetch
-                                            else "context default")},
+                                            else "context default"),
+                   "launch": ("CUDA graph replay (16 steps per graph); component times from an eager pass"
+                              if args.graph else "eager launches from Python")},
+        "eager_ms_per_step": eager_ms,
         "component_us": comp, "roofline": roof, "clocks": clocks.summary(),
         # ours per step: the fused hash + lookup, and per layer projection + finishing pass (fused), projection +
         # gate (tcgen05), or the gate alone (cublas: the projection is cuBLAS's)
