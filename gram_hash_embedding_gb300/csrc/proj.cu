@@ -184,7 +184,7 @@ __device__ __forceinline__ void raise_timeout(volatile int* abort) {
   atomicOr(&g_device_status, (unsigned)ENGRAM_STATUS_TIMEOUT);
 }
 
-// lane 0 waits, the warp follows its verdict (keeps the warp converged for .sync.aligned tcgen05 ops)
+// lane 0 waits, the warp follows its result (keeps the warp converged for .sync.aligned tcgen05 ops)
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) {

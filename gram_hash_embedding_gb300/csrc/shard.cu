@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kPackThreads) shard_scatter_kernel(const int64
   pdl_wait();
   pdl_trigger();
   __shared__ int32_t base[kMaxBuckets];                      // where this segment's part of bucket b goes next
-  __shared__ int warp_cnt[kPackThreads / 32][kMaxBuckets];   // this round's elements per (warp, bucket)
+  __shared__ int warp_cnt[kPackThreads / 32][kMaxBuckets];   // this pass's elements per (warp, bucket)
   const int nb = world + 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int b = threadIdx.x; b < nb; b += blockDim.x) base[b] = seg_base[(int64_t)blockIdx.x * nb + b];
